@@ -1,0 +1,241 @@
+/*
+ * mlora.h -- C ABI of libmlora.so: one multi-tenant LoRA training step
+ * (forward_backward + optim_step) over a mixed batch whose tokens belong to
+ * many LoRA adapters that share one frozen base, on one sm_103a GPU.
+ *
+ * The model.  A token embedding E [V x d]; L residual blocks
+ *     u = W1 h + gamma_a B1_a (A1_a h),   act = silu(u),
+ *     h <- h + W2 act + gamma_a B2_a (A2_a act)
+ * with W1 [f x d], W2 [d x f] frozen and shared, and per adapter a and layer
+ * l the trainable factors A1 [r x d], B1 [f x r], A2 [r x f], B2 [d x r],
+ * gamma_a = alpha_a / r_a (Deep Dive - Tinker, "LoRA is the adaptation
+ * boundary": W' = W + gamma B A); then an untied LM head Wout [V x d] and the
+ * target-token logprob l_t = z[y_t] - logsumexp(z), z = Wout h (Tinker API
+ * Implementation on TPUs, section 10.3-10.4: the [tokens x vocab] logits are
+ * never stored; the backward recomputes them chunk by chunk).
+ *
+ * Conventions for every entry point:
+ *  - Return value: MLORA_OK (0) or a negative MLORA_E_* code; the message of
+ *    the last failure on the calling thread is mlora_last_error().
+ *  - "device" pointers are CUDA device memory of the current device; "host"
+ *    pointers are ordinary host memory.  The caller owns every buffer it
+ *    passes; the library owns every buffer it allocates (freed by
+ *    mlora_destroy).  The library never keeps a caller pointer after a call
+ *    returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is queued asynchronously on it; calls on one handle must
+ *    be serialised by the caller (one training client, ordered requests:
+ *    Deep Dive - Tinker, "optim_step advances adapter state").
+ *  - Errors found on the device (token id >= V, target >= V, adapter id >=
+ *    n_adapters) never trap: the kernels skip the offending token, write NaN
+ *    as its logprob, and raise a status bit that mlora_check_status() reports
+ *    as MLORA_E_RANGE.  A device wait that exceeds its bound sets
+ *    MLORA_E_TIMEOUT the same way.
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Routing tile height: every adapter's segment of the sorted token matrix is
+ * padded to a multiple of this many rows, so that no GEMM row tile mixes two
+ * adapters (tinker-ticks, "How the SGMV kernel works": segment indices over
+ * the flattened tokens). */
+#define MLORA_TILE_M 128
+/* Largest supported LoRA rank; ranks must also be multiples of 4. */
+#define MLORA_MAX_RANK 64
+
+enum {
+    MLORA_OK = 0,
+    MLORA_E_ARG = -1,      /* invalid argument or configuration              */
+    MLORA_E_RANGE = -2,    /* device saw an id out of range (token/adapter)  */
+    MLORA_E_CUDA = -3,     /* a CUDA runtime call failed                     */
+    MLORA_E_NOMEM = -4,    /* device allocation failed                       */
+    MLORA_E_TIMEOUT = -5,  /* a bounded device wait gave up                  */
+    MLORA_E_IO = -6,       /* file write failed (save_state)                 */
+    MLORA_E_UNSUPPORTED = -7 /* no sm_103a device / feature missing          */
+};
+
+typedef enum { MLORA_BF16 = 0, MLORA_FP32 = 1 } mlora_dtype;
+
+/* Loss kinds (Deep Dive - Tinker, "The RL datum shape"); every loss is a sum
+ * over tokens with no normalisation.
+ *   CROSS_ENTROPY        L = -sum_t w_t l_t
+ *   IMPORTANCE_SAMPLING  L = -sum_t r_t A_t,             r_t = exp(l_t - s_t)
+ *   PPO                  L = -sum_t min(r_t A_t, clip(r_t, 1-eps, 1+eps) A_t)
+ * A token whose inputs, logprob or ratio are not finite contributes neither
+ * value nor gradient (Tinker API Implementation on TPUs, section 12). */
+typedef enum {
+    MLORA_CROSS_ENTROPY = 0,
+    MLORA_IMPORTANCE_SAMPLING = 1,
+    MLORA_PPO = 2
+} mlora_loss;
+
+/* Selector for mlora_read_adapter / mlora_write_adapter.  Shapes (row-major,
+ * fp32): A1 [r x d], B1 [f x r], A2 [r x f], B2 [d x r].  GRAD_* are the
+ * accumulated gradients, M_* / V_* the Adam moments. */
+typedef enum {
+    MLORA_A1 = 0, MLORA_B1 = 1, MLORA_A2 = 2, MLORA_B2 = 3,
+    MLORA_GRAD_A1 = 4, MLORA_GRAD_B1 = 5, MLORA_GRAD_A2 = 6, MLORA_GRAD_B2 = 7,
+    MLORA_M_A1 = 8, MLORA_M_B1 = 9, MLORA_M_A2 = 10, MLORA_M_B2 = 11,
+    MLORA_V_A1 = 12, MLORA_V_B1 = 13, MLORA_V_A2 = 14, MLORA_V_B2 = 15
+} mlora_tensor;
+
+typedef struct mlora mlora_t;
+
+typedef struct {
+    int32_t vocab;         /* V                                              */
+    int32_t d_model;       /* d, multiple of 64                              */
+    int32_t d_ffn;         /* f, multiple of 64                              */
+    int32_t n_layers;      /* L >= 1                                         */
+    int32_t dtype;         /* mlora_dtype of the frozen base and activations */
+    int32_t n_adapters;    /* 1 .. 1024                                      */
+    const int32_t* ranks;  /* host [n_adapters]; 1..MLORA_MAX_RANK, % 4 == 0 */
+    const float* alphas;   /* host [n_adapters]; gamma_a = alphas[a]/ranks[a] */
+    int64_t max_tokens;    /* largest n_tokens any call will pass (>= 1)     */
+} mlora_config;
+
+/* Initial values, all DEVICE pointers, read once by mlora_create and copied
+ * into library-owned memory.  Base tensors hold `dtype` elements (bf16 as
+ * raw 16-bit patterns).  Adapter arrays are HOST arrays of n_adapters *
+ * n_layers device pointers to fp32 tensors, indexed [a * n_layers + l]; a NULL
+ * array or a NULL entry initialises that tensor to zero. */
+typedef struct {
+    const void* E;                 /* [V x d]                  */
+    const void* const* W1;         /* host [n_layers] -> [f x d] */
+    const void* const* W2;         /* host [n_layers] -> [d x f] */
+    const void* Wout;              /* [V x d]                  */
+    const float* const* A1;
+    const float* const* B1;
+    const float* const* A2;
+    const float* const* B2;
+} mlora_init;
+
+/* A flattened token batch: DEVICE int32 arrays of length n_tokens.  Token t
+ * has input id tokens[t], target id targets[t] (the next token of its
+ * sequence) and adapter adapter_ids[t]. */
+typedef struct {
+    int64_t n_tokens;              /* 0 .. max_tokens */
+    const int32_t* tokens;
+    const int32_t* targets;
+    const int32_t* adapter_ids;
+} mlora_batch;
+
+/* Per-token loss inputs, DEVICE fp32 arrays of length n_tokens (those the
+ * loss kind does not read may be NULL). */
+typedef struct {
+    const float* weights;           /* CROSS_ENTROPY: w_t                 */
+    const float* advantages;        /* IMPORTANCE_SAMPLING / PPO: A_t      */
+    const float* sampler_logprobs;  /* IMPORTANCE_SAMPLING / PPO: s_t      */
+    float clip_eps;                 /* PPO clip range eps                 */
+} mlora_loss_inputs;
+
+/* Adam hyper-parameters (Deep Dive - Tinker, "optim_step advances adapter
+ * state": AdamW-equivalent, default weight decay 0).  Update per element:
+ *   m = b1 m + (1-b1) G;  v = b2 v + (1-b2) G^2;  t = t + 1
+ *   p = p - lr * ( (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps) + wd * p ) */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} mlora_adam;
+
+/* Create a handle: validates the config, allocates all device memory for up
+ * to max_tokens tokens, copies the base and the initial adapters, zeroes
+ * gradients and moments, sets every adapter's step count to 0.  Synchronous.
+ * Errors: E_ARG (bad config/NULL), E_NOMEM, E_CUDA, E_UNSUPPORTED (a BF16
+ * handle needs an sm_103 device). */
+int mlora_create(const mlora_config* cfg, const mlora_init* init, mlora_t** out);
+
+/* Free everything the handle owns (synchronises the device first). */
+int mlora_destroy(mlora_t* h);
+
+/* Target-token logprobs of every token (no gradient, no state change).
+ * logprobs_out: DEVICE fp32 [n_tokens], caller-owned. */
+int mlora_forward(mlora_t* h, const mlora_batch* b, float* logprobs_out, void* stream);
+
+/* Forward, loss and adapter-only backward.  Gradients ACCUMULATE into the
+ * handle's per-adapter buffers until mlora_optim_step consumes them; every
+ * adapter with at least one token is marked as touched.
+ * logprobs_out: DEVICE fp32 [n_tokens] (may be NULL).
+ * loss_out: DEVICE fp64 [n_adapters] (may be NULL): loss summed over each
+ * adapter's tokens of this call. */
+int mlora_forward_backward(mlora_t* h, const mlora_batch* b, int32_t loss_kind,
+                           const mlora_loss_inputs* li, float* logprobs_out,
+                           double* loss_out, void* stream);
+
+/* Backpropagate the surrogate sum_t g_t l_t with the caller's
+ * g_t = dC/dl_t (Deep Dive - Tinker, "The RL datum shape"; the Telegram note
+ * on forward_backward_custom: the server re-runs the forward and backprops
+ * sum(logprobs * dLoss/dLogprobs)).  dloss_dlogprobs: DEVICE fp32 [n_tokens].
+ * Outputs and accumulation as mlora_forward_backward (loss_out receives
+ * sum_t g_t l_t per adapter). */
+int mlora_forward_backward_custom(mlora_t* h, const mlora_batch* b,
+                                  const float* dloss_dlogprobs, float* logprobs_out,
+                                  double* loss_out, void* stream);
+
+/* One Adam step per selected adapter, consuming (and zeroing) its gradient.
+ * adapters: HOST int32 [n] of adapter ids, or NULL to select every adapter
+ * touched since the previous optim_step.  An adapter whose accumulated
+ * gradient holds a non-finite value keeps its weights, moments and step
+ * count; its gradient is still consumed and skipped_out[a] is set to 1
+ * (Tinker API Implementation on TPUs, section 12: non-finite optimizer
+ * updates are skipped).  skipped_out: DEVICE int32 [n_adapters] (may be
+ * NULL), 0 for every adapter not skipped. */
+int mlora_optim_step(mlora_t* h, const mlora_adam* p, const int32_t* adapters,
+                     int32_t n, int32_t* skipped_out, void* stream);
+
+/* Write a checkpoint of every adapter (weights and Adam state) to `path`.
+ * Synchronises `stream`.  Format, little-endian: 8-byte magic "MLORASTA",
+ * u32 version = 1, u32 n_adapters, u32 n_layers, u32 d_model, u32 d_ffn,
+ * u32 0; then per adapter: u32 rank, f32 alpha, u64 step count, followed by
+ * the weights, the first moments and the second moments, each as, for every
+ * layer, A1, B1, A2, B2 in fp32 row-major.  (Deep Dive - Tinker, "save_state
+ * creates a recovery point".)  Errors: E_IO, E_CUDA. */
+int mlora_save_state(mlora_t* h, const char* path, void* stream);
+
+/* Copy one fp32 adapter tensor (see mlora_tensor) of adapter `adapter`,
+ * layer `layer` into dst (DEVICE, caller-owned, shape as documented there).
+ * Test and inspection hook. */
+int mlora_read_adapter(mlora_t* h, int32_t adapter, int32_t layer, int32_t which,
+                       float* dst, void* stream);
+
+/* Overwrite a weight tensor (MLORA_A1..MLORA_B2 only) from src (DEVICE fp32)
+ * and refresh its bf16 copy used by the GEMMs. */
+int mlora_write_adapter(mlora_t* h, int32_t adapter, int32_t layer, int32_t which,
+                        const float* src, void* stream);
+
+/* Step counts: HOST int64 [n_adapters] out (synchronises `stream`). */
+int mlora_get_steps(mlora_t* h, int64_t* steps_out, void* stream);
+
+/* The routing that forward / forward_backward use, exposed for checking:
+ * adapter_ids: DEVICE int32 [n]; outputs are DEVICE int32:
+ *   perm[n]              stable order of token positions grouped by adapter
+ *   seg_off[n_adapters+1] exclusive prefix of per-adapter token counts
+ *   pad_off[n_adapters+1] the same with each segment padded to MLORA_TILE_M
+ *   tile_ad[n / MLORA_TILE_M + n_adapters + 1] adapter of each padded row
+ *                        tile, -1 after the last tile
+ * Ids out of range are left out and raise MLORA_E_RANGE on check_status. */
+int mlora_get_routing(mlora_t* h, const int32_t* adapter_ids, int64_t n, int32_t* perm,
+                      int32_t* seg_off, int32_t* pad_off, int32_t* tile_ad, void* stream);
+
+/* Synchronise `stream`, then return and clear the device status word:
+ * MLORA_OK, MLORA_E_RANGE or MLORA_E_TIMEOUT. */
+int mlora_check_status(mlora_t* h, void* stream);
+
+/* Number of kernels this handle has launched so far. */
+int64_t mlora_kernel_launches(const mlora_t* h);
+
+/* Bytes of device memory the handle owns. */
+int64_t mlora_device_bytes(const mlora_t* h);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* mlora_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLORA_H */

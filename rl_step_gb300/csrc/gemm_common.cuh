@@ -1,0 +1,274 @@
+// GEMM problem description and fused epilogues shared by the two GEMM
+// engines of libmlora: the tcgen05/TMEM/TMA engine (bf16) and the FFMA engine
+// (fp32 base).  Both call the same epilogue on the same unit of work: one
+// output row and 32 consecutive output columns held by one thread.
+#pragma once
+
+#include "common.cuh"
+
+namespace mlk {
+
+// One operand of C[m][n] = sum_k A[m][k] B[n][k].
+// Element (mn, k) of adapter a sits in the stored row-major matrix at
+//   K-major  (mn_major == 0): row = a*ad_rows + mn + row_shift, col = k
+//   MN-major (mn_major == 1): row = a*ad_rows + k  + row_shift, col = mn
+// and reads as zero outside [0, rows) x [0, cols).
+struct GemmOperand {
+    const void* ptr = nullptr;
+    int64_t ld = 0;          // elements between consecutive stored rows
+    int64_t rows = 0, cols = 0;
+    int mn_major = 0;
+    int64_t ad_rows = 0;     // per-adapter row stride (0: shared by all adapters)
+    int64_t row_shift = 0;
+};
+
+enum EpiKind : int {
+    EPI_SILU = 0,     // out0 = u = acc ; out1 = silu(acc)                     (T)
+    EPI_RESID = 1,    // f32 += acc ; out0 = T(f32)                             (residual h / dh)
+    EPI_STORE2 = 2,   // f32 = acc ; out0 = T(acc)                              (dh of the LM head)
+    EPI_DSILU = 3,    // out0 = T(acc * silu'(aux))                             (du)
+    EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
+    EPI_LMFWD = 5,    // per row: online max / sum-exp over cols < V, target z  (LM head)
+    EPI_LMDZ = 6,     // out0 = T(g (onehot(y) - exp(acc - lse)))               (LM head backward)
+    EPI_GRAD = 7      // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
+};
+
+struct EpiParams {
+    int kind = 0;
+    void* out0 = nullptr;
+    void* out1 = nullptr;
+    int64_t ld0 = 0, ld1 = 0;
+    float* f32 = nullptr;
+    int64_t ldf = 0;
+    const void* aux = nullptr;
+    int64_t ld_aux = 0;
+    const float* gamma = nullptr;   // per adapter
+    // LM head
+    float2* part = nullptr;         // [rows][n_ntiles] (running max, sum exp)
+    float* zt = nullptr;            // target logit per row
+    const int* tgt = nullptr;       // target id per padded row (-1: none)
+    int n_ntiles = 0;
+    int V = 0, Vpad = 0;
+    const float* g = nullptr;       // dL/dl per padded row
+    const float* lse = nullptr;     // logsumexp per padded row
+    int64_t out_row_shift = 0;      // output row = row + out_row_shift (chunk buffers)
+    // adapter gradients
+    float* grad = nullptr;
+    const int64_t* grad_off = nullptr;  // per adapter element offset of this tensor
+    const int* ranks = nullptr;
+    int grad_trans = 0;             // 0: grad[m*r + n]; 1: grad[n*M + m]
+    int grad_M = 0;
+    int* nonfinite = nullptr;       // per adapter flag
+};
+
+struct GemmParams {
+    int M = 0, N = 0, K = 0, Kx = 0;
+    GemmOperand A, B, Ax, Bx;
+    // dense mode: rows are padded token rows in 128-row tiles
+    const int* mtiles_dev = nullptr;  // valid global m-tiles (nullptr: ceil(M/128))
+    int mt_base = 0, mt_count = 0;    // this launch: global m-tiles [mt_base, mt_base+mt_count)
+    const int* tile_ad = nullptr;     // adapter per global m-tile
+    // grouped mode: M = output rows, K runs over one chunk of one adapter's tokens
+    int grouped = 0;
+    const int4* chunks = nullptr;     // (adapter, k0, klen, 0)
+    const int* nchunks_dev = nullptr;
+    int max_chunks = 0;
+    int group_m = 8;                  // raster band height (m-tiles) for L2 reuse
+    EpiParams ep;
+};
+
+// ----------------------------------------------------------------------------
+// vector stores of 32 consecutive values
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T> __device__ __forceinline__ void store32(T* dst, const float* v);
+
+template <> __device__ __forceinline__ void store32<bf16>(bf16* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        d4[q] = w;
+    }
+}
+
+template <> __device__ __forceinline__ void store32<float>(float* dst, const float* v) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+template <typename T> __device__ __forceinline__ void load32(const T* src, float* v);
+
+template <> __device__ __forceinline__ void load32<bf16>(const bf16* src, float* v) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w = s4[q];
+        uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 p = *reinterpret_cast<__nv_bfloat162*>(&ws[e]);
+            float2 f = __bfloat1622float2(p);
+            v[8 * q + 2 * e] = f.x;
+            v[8 * q + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+template <> __device__ __forceinline__ void load32<float>(const float* src, float* v) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 f = s4[q];
+        v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// epilogue: per thread, one row and 32 consecutive columns at a time
+// ----------------------------------------------------------------------------
+struct EpiRowState {
+    float m, s, zt;
+    int found;
+};
+
+__device__ __forceinline__ void epi_row_begin(EpiRowState& st) {
+    st.m = -INFINITY;
+    st.s = 0.f;
+    st.zt = 0.f;
+    st.found = 0;
+}
+
+// acc holds C[row][col0 .. col0+31].  `row` is the global output row (padded
+// token row in dense mode, output-feature row in grouped mode).
+template <typename T>
+__device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int col0, int adapter,
+                                          float* acc, EpiRowState& st) {
+    const float LOG2E = 1.4426950408889634f;
+    switch (ep.kind) {
+    case EPI_SILU: {
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = acc[j] * sigmoidf_(acc[j]);
+        store32<T>(reinterpret_cast<T*>(ep.out1) + row * ep.ld1 + col0, a);
+    } break;
+    case EPI_RESID: {
+        float* hp = ep.f32 + row * ep.ldf + col0;
+        float h[32];
+        load32<float>(hp, h);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j] += acc[j];
+        store32<float>(hp, h);
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, h);
+    } break;
+    case EPI_STORE2: {
+        store32<float>(ep.f32 + row * ep.ldf + col0, acc);
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+    } break;
+    case EPI_DSILU: {
+        float u[32];
+        load32<T>(reinterpret_cast<const T*>(ep.aux) + row * ep.ld_aux + col0, u);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float s = sigmoidf_(u[j]);
+            u[j] = acc[j] * (s * (1.f + u[j] * (1.f - s)));
+        }
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, u);
+    } break;
+    case EPI_SHRINK: {
+        float gm = ep.gamma[adapter];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] *= gm;
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+    } break;
+    case EPI_LMFWD: {
+        int t = ep.tgt[row];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            bool ok = (col0 + j) < ep.V;
+            cm = fmaxf(cm, ok ? acc[j] : -INFINITY);
+            if (col0 + j == t) { st.zt = acc[j]; st.found = 1; }
+        }
+        float mn = fmaxf(st.m, cm);
+        if (mn > -INFINITY) {
+            float sc = exp2f((st.m - mn) * LOG2E);
+            float sum = 0.f;
+            float mb = mn * LOG2E;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                sum += ((col0 + j) < ep.V) ? exp2f(fmaf(acc[j], LOG2E, -mb)) : 0.f;
+            st.s = st.s * sc + sum;
+            st.m = mn;
+        }
+    } break;
+    case EPI_LMDZ: {
+        if (col0 >= ep.Vpad) break;
+        float gr = ep.g[row];
+        float d[32];
+        if (gr == 0.f) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] = 0.f;
+        } else {
+            int t = ep.tgt[row];
+            float lb = ep.lse[row] * LOG2E;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                int c = col0 + j;
+                float p = exp2f(fmaf(acc[j], LOG2E, -lb));
+                float v = gr * ((c == t ? 1.f : 0.f) - p);
+                d[j] = c < ep.V ? v : 0.f;
+            }
+        }
+        store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, d);
+    } break;
+    case EPI_GRAD: {
+        int r = ep.ranks[adapter];
+        float* base = ep.grad + ep.grad_off[adapter];
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            int c = col0 + j;
+            if (c < r) {
+                float v = acc[j];
+                bad |= !isfinite(v);
+                int64_t off = ep.grad_trans ? (int64_t)c * ep.grad_M + row : row * (int64_t)r + c;
+                atomicAdd(base + off, v);
+            }
+        }
+        if (bad) ep.nonfinite[adapter] = 1;
+    } break;
+    default: break;
+    }
+}
+
+__device__ __forceinline__ void epi_row_end(const EpiParams& ep, int64_t row, int ntile,
+                                            const EpiRowState& st) {
+    if (ep.kind == EPI_LMFWD) {
+        ep.part[row * ep.n_ntiles + ntile] = make_float2(st.m, st.s);
+        if (st.found) ep.zt[row] = st.zt;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// tile bookkeeping shared by both engines
+// ----------------------------------------------------------------------------
+struct TileInfo {
+    int mt;        // global m-tile (dense) or m-tile inside the chunk (grouped)
+    int nt;        // n-tile
+    int adapter;
+    int k0, klen;  // contraction range of the main operands
+    int valid;
+};
+
+}  // namespace mlk

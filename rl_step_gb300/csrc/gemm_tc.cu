@@ -1,0 +1,528 @@
+// Tensor-core GEMM engine for sm_103a: C = A B^T (+ Ax Bx^T) on tcgen05 with
+// TMEM accumulators, operands staged in shared memory by TMA, and the fused
+// epilogues of gemm_common.cuh.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0      TMA producer (one elected thread) filling an S-stage ring of
+//               128x64 A tiles and BNx64 B tiles (bf16, 128-byte swizzle)
+//   warp 1      TMEM allocator and MMA issuer (one elected thread):
+//               tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16, into
+//               one of two TMEM accumulators (2 x BN fp32 columns)
+//   warps 2-5   epilogue: tcgen05.ld 32x32b.x32 of the finished accumulator,
+//               one output row per thread, 32 columns at a time, while the
+//               MMA warp already fills the other accumulator
+// Tiles are scheduled statically (tile = blockIdx.x + i * gridDim.x) in
+// bands of group_m row tiles, so CTAs running together share B tiles in L2.
+// The adapter of a row tile (routing guarantees one per tile) selects the
+// per-adapter rows of B / Bx: the SGMV shrink and expand of tinker-ticks
+// ("How the SGMV kernel works") become one extra K block of the base GEMM.
+//
+// Every wait on an mbarrier is bounded (about 4 s of %globaltimer); on
+// expiry the CTA raises the timeout status bit, stops issuing work, drains
+// its own copies and MMAs (again bounded), frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace mlk {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                     // bf16 elements = 128 bytes per row
+constexpr uint64_t TIMEOUT_NS = 4000000000ull;
+constexpr int NUM_THREADS = 192;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; false on timeout/abort.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > TIMEOUT_NS) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2).
+//   K-major tile: rows of 64 bf16 (128 B), 8-row groups 1024 B apart (SBO).
+//   MN-major tile: 64-element MN blocks LBO bytes apart, 8-row K groups
+//   1024 B apart (SBO).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;   // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M=128, N=n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+struct TcMaps {
+    CUtensorMap A, B, Ax, Bx;
+};
+
+struct TileCoord {
+    int valid;
+    int mt;       // global m-tile (dense) / m-tile in the chunk (grouped)
+    int nt;
+    int adapter;
+    int k0;       // first contraction index of the main operands
+    int nkb;      // main K blocks
+    int nkbx;     // extension K blocks
+};
+
+template <int BN>
+__device__ __forceinline__ int total_tiles(const GemmParams& p) {
+    const int n_nt = (p.N + BN - 1) / BN;
+    if (!p.grouped) {
+        int nmt = p.mtiles_dev ? *p.mtiles_dev : (p.M + BM - 1) / BM;
+        int cnt = nmt - p.mt_base;
+        if (cnt > p.mt_count) cnt = p.mt_count;
+        if (cnt < 0) cnt = 0;
+        return cnt * n_nt;
+    }
+    const int mtiles = (p.M + BM - 1) / BM;
+    int nch = *p.nchunks_dev;
+    if (nch > p.max_chunks) nch = p.max_chunks;
+    return nch * mtiles * n_nt;
+}
+
+template <int BN>
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int t) {
+    TileCoord c;
+    const int n_nt = (p.N + BN - 1) / BN;
+    c.valid = 1;
+    if (!p.grouped) {
+        int nmt = p.mtiles_dev ? *p.mtiles_dev : (p.M + BM - 1) / BM;
+        int cnt = nmt - p.mt_base;
+        if (cnt > p.mt_count) cnt = p.mt_count;
+        const int G = p.group_m > 0 ? p.group_m : 1;
+        const int band = t / (G * n_nt);
+        const int r = t - band * G * n_nt;
+        int bm = cnt - band * G;
+        if (bm > G) bm = G;
+        const int ml = band * G + r % bm;
+        c.mt = p.mt_base + ml;
+        c.nt = r / bm;
+        c.adapter = p.tile_ad ? p.tile_ad[c.mt] : 0;
+        if (c.adapter < 0) c.adapter = 0;
+        c.k0 = 0;
+        c.nkb = (p.K + BK - 1) / BK;
+        c.nkbx = (p.Kx + BK - 1) / BK;
+    } else {
+        const int mtiles = (p.M + BM - 1) / BM;
+        const int per_chunk = mtiles * n_nt;
+        const int ci = t / per_chunk;
+        const int r = t - ci * per_chunk;
+        c.mt = r % mtiles;
+        c.nt = r / mtiles;
+        const int4 ch = p.chunks[ci];
+        c.adapter = ch.x;
+        c.k0 = ch.y;
+        c.nkb = (ch.z + BK - 1) / BK;
+        c.nkbx = 0;
+    }
+    return c;
+}
+
+template <int BN, int STAGES>
+struct SmemLayout {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = TILES_BYTES;                 // full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;        // tmem base, abort flag
+    static constexpr int TOTAL = MISC_OFF + 16 + 1024;          // + alignment slack
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status) {
+    using SL = SmemLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + SL::BAR_OFF;
+    const uint32_t bar_empty = bar_full + STAGES * 8;
+    const uint32_t bar_tfull = bar_empty + STAGES * 8;
+    const uint32_t bar_tempty = bar_tfull + 2 * 8;
+    const uint32_t bar_drain = bar_tempty + 2 * 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC_OFF + 4);
+    constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, 4);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tma_prefetch_desc(&maps.A);
+        tma_prefetch_desc(&maps.B);
+        if (p.Kx > 0) {
+            tma_prefetch_desc(&maps.Ax);
+            tma_prefetch_desc(&maps.Bx);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int ntiles = total_tiles<BN>(p);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileCoord c = tile_coord<BN>(p, t);
+                const int m0 = c.mt * BM;
+                const int n0 = c.nt * BN;
+                const int nall = c.nkb + c.nkbx;
+                for (int kb = 0; kb < nall; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+                    mbar_expect_tx(fb, SL::STAGE_BYTES);
+                    const bool ext = kb >= c.nkb;
+                    const GemmOperand& A = ext ? p.Ax : p.A;
+                    const GemmOperand& B = ext ? p.Bx : p.B;
+                    const CUtensorMap* mA = ext ? &maps.Ax : &maps.A;
+                    const CUtensorMap* mB = ext ? &maps.Bx : &maps.B;
+                    const int k = ext ? (kb - c.nkb) * BK : c.k0 + kb * BK;
+                    if (!A.mn_major) {
+                        tma_load_2d(sa, mA, fb, k, (int)(m0 + A.row_shift));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BM / 64; ++i)
+                            tma_load_2d(sa + i * 8192, mA, fb, m0 + 64 * i, (int)(k + A.row_shift));
+                    }
+                    const int brow = (int)((int64_t)c.adapter * B.ad_rows + B.row_shift);
+                    if (!B.mn_major) {
+                        tma_load_2d(sb, mB, fb, k, brow + n0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_2d(sb + i * 8192, mB, fb, n0 + 64 * i, brow + k);
+                    }
+                    issued[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                atomicOr(status, ST_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // our copies must have landed before the CTA may exit
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s] >= 0) {
+                    int dummy = 0;
+                    if (!mbar_wait(bar_full + 8 * s, (uint32_t)issued[s], (volatile int*)&dummy)) {
+                        atomicOr(status, ST_TIMEOUT);
+                    }
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major);
+            const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major);
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileCoord c = tile_coord<BN>(p, t);
+                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const int nall = c.nkb + c.nkbx;
+                for (int kb = 0; kb < nall; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const bool ext = kb >= c.nkb;
+                    const int a_mn = ext ? p.Ax.mn_major : p.A.mn_major;
+                    const int b_mn = ext ? p.Bx.mn_major : p.B.mn_major;
+                    const uint32_t idesc = ext ? id_ext : id_main;
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = a_mn ? sdesc(sa + kk * 2048, 8192, 1024)
+                                                 : sdesc(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 8192, 1024)
+                                                 : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar_empty + 8 * stage);     // frees the stage when the MMAs finish
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(bar_tfull + 8 * acc);           // accumulator ready
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (!ok) {
+                atomicOr(status, ST_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // drain: every MMA issued by this thread completes before TMEM is freed
+            umma_commit(bar_drain);
+            int dummy = 0;
+            if (!mbar_wait(bar_drain, 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const TileCoord c = tile_coord<BN>(p, t);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+                break;
+            }
+            tc_fence_after();
+            const int64_t row = (int64_t)c.mt * BM + 32 * q + lane;
+            const bool row_ok = !p.grouped || row < p.M;
+            EpiRowState st;
+            epi_row_begin(st);
+            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ch * 32, r);
+                tmem_ld_wait();
+                const int col0 = c.nt * BN + ch * 32;
+                if (row_ok && col0 < p.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    epi_chunk<bf16>(p.ep, row, col0, c.adapter, v, st);
+                }
+            }
+            if (row_ok) epi_row_end(p.ep, row, c.nt, st);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---- host ------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encode() {
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+bool encode_2d(CUtensorMap* m, const GemmOperand& op, uint32_t box_cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)op.cols, (cuuint64_t)op.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)op.ld * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.ptr), dims, strides,
+                          box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool operand_ok(const GemmOperand& op) {
+    // TMA: 16-byte aligned base, row pitch a multiple of 16 bytes.
+    return op.ptr && (reinterpret_cast<uintptr_t>(op.ptr) % 16 == 0) && (op.ld % 8 == 0) && op.rows > 0 &&
+           op.cols > 0 && op.rows < (1LL << 31) && op.cols < (1LL << 31);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
+    using SL = SmemLayout<BN, STAGES>;
+    TcMaps maps;
+    auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
+        if (!operand_ok(op)) return false;
+        if (op.mn_major) return encode_2d(m, op, 64, 64);
+        return encode_2d(m, op, 64, (uint32_t)rows_mn);
+    };
+    if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN)) return cudaErrorInvalidValue;
+    if (p.Kx > 0) {
+        if (p.Kx % BK || !enc(&maps.Ax, p.Ax, BM) || !enc(&maps.Bx, p.Bx, BN)) return cudaErrorInvalidValue;
+    } else {
+        maps.Ax = maps.A;
+        maps.Bx = maps.B;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int n_nt = (p.N + BN - 1) / BN;
+    int64_t upper = p.grouped ? (int64_t)p.max_chunks * ((p.M + BM - 1) / BM) * n_nt
+                              : (int64_t)p.mt_count * n_nt;
+    if (upper <= 0) return cudaSuccess;
+    int grid = (int)(upper < num_sms ? upper : num_sms);
+    tc_gemm_kernel<BN, STAGES><<<grid, NUM_THREADS, SL::TOTAL, s>>>(maps, p, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_engine_available() { return get_encode(); }
+
+cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
+    if (!get_encode()) return cudaErrorNotSupported;
+    if (p.N <= 64) return launch_bn<64, 8>(p, s, num_sms, status);
+    return launch_bn<256, 4>(p, s, num_sms, status);
+}
+
+}  // namespace mlk

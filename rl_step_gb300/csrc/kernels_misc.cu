@@ -1,0 +1,382 @@
+// Bandwidth-bound kernels of the step: embedding gather, the LM-head partial
+// combine fused with the loss epilogue, the per-adapter loss reduction, and
+// the fused Adam update.
+#include <math.h>
+
+#include "internal.h"
+
+namespace mlk {
+
+// ----------------------------------------------------------------------------
+// embedding: h0[p] = E[x_{perm[p]}] in padded order; padding rows are zero.
+// One warp per row, 16-byte accesses.
+// ----------------------------------------------------------------------------
+template <typename T>
+__global__ void embed_kernel(const int* __restrict__ perm_pad, const int* __restrict__ meta,
+                             const int* __restrict__ tokens, const int* __restrict__ targets,
+                             const T* __restrict__ E, int V, int d, T* __restrict__ hb,
+                             float* __restrict__ h32, int* __restrict__ tgt_pad, int* status) {
+    const int rows = meta[0] * TILE_M;
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < rows; p += gridDim.x * wpb) {
+        int t = perm_pad[p];
+        int x = -1;
+        if (t >= 0) {
+            x = tokens[t];
+            int y = targets[t];
+            if (x < 0 || x >= V) { if (lane == 0) raise_status(status, ST_RANGE); x = -1; y = -1; }
+            if (y < 0 || y >= V) { if (lane == 0) raise_status(status, ST_RANGE); y = -1; }
+            if (lane == 0) tgt_pad[p] = y;
+        } else if (lane == 0) {
+            tgt_pad[p] = -1;
+        }
+        constexpr int VEC = 16 / sizeof(T);   // elements per 16 bytes
+        for (int c = lane * VEC; c < d; c += 32 * VEC) {
+            float v[VEC];
+            if (x >= 0) {
+                uint4 raw = *reinterpret_cast<const uint4*>(E + (int64_t)x * d + c);
+                if constexpr (sizeof(T) == 2) {
+                    const bf16* b = reinterpret_cast<const bf16*>(&raw);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[e] = __bfloat162float(b[e]);
+                } else {
+                    const float* f = reinterpret_cast<const float*>(&raw);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[e] = f[e];
+                }
+                *reinterpret_cast<uint4*>(hb + (int64_t)p * d + c) = raw;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[e] = 0.f;
+                *reinterpret_cast<uint4*>(hb + (int64_t)p * d + c) = make_uint4(0, 0, 0, 0);
+            }
+            float* hp = h32 + (int64_t)p * d + c;
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4)
+                *reinterpret_cast<float4*>(hp + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+    }
+}
+
+template <typename T>
+void launch_embed(const int* perm_pad, const int* meta, int max_rows, const int* tokens,
+                  const int* targets, const T* E, int V, int d, T* hb, float* h32, int* tgt_pad,
+                  int* status, cudaStream_t s) {
+    int blocks = (max_rows + 7) / 8;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    embed_kernel<T><<<blocks, 256, 0, s>>>(perm_pad, meta, tokens, targets, E, V, d, hb, h32,
+                                           tgt_pad, status);
+}
+template void launch_embed<float>(const int*, const int*, int, const int*, const int*, const float*,
+                                  int, int, float*, float*, int*, int*, cudaStream_t);
+template void launch_embed<bf16>(const int*, const int*, int, const int*, const int*, const bf16*,
+                                 int, int, bf16*, float*, int*, int*, cudaStream_t);
+
+// ----------------------------------------------------------------------------
+// LM-head combine + loss epilogue.
+// For padded row p: lse = M + log sum_j s_j exp(m_j - M) over the per-tile
+// partials (m_j, s_j); l = z[y] - lse (Tinker API Implementation on TPUs,
+// section 10.3: the target logprob is a gather minus a logsumexp).  Then the
+// per-token loss value and g = dL/dl (Deep Dive - Tinker, "The RL datum
+// shape"; custom: g is the caller's dC/dl), with non-finite inputs contained
+// (Tinker API Implementation on TPUs, section 12).  One CTA per 128-row tile;
+// the tile's loss sum (fp64) goes to loss_tile for a deterministic
+// per-adapter reduction.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void token_loss_dev(int kind, float ell, int t, const LossArgs& la,
+                                               double& val, float& g) {
+    val = 0.0;
+    g = 0.f;
+    if (kind < 0) return;
+    bool ok = isfinite(ell);
+    if (kind == 0) {
+        float w = la.w[t];
+        ok = ok && isfinite(w);
+        if (ok) { val = -(double)w * ell; g = -w; }
+    } else if (kind == 1 || kind == 2) {
+        float A = la.adv[t], sl = la.slp[t];
+        ok = ok && isfinite(A) && isfinite(sl);
+        if (ok) {
+            float r = expf(ell - sl);
+            ok = isfinite(r);
+            if (ok) {
+                float un = r * A;
+                if (kind == 1) {
+                    val = -(double)un;
+                    g = -un;
+                } else {
+                    float rc = fminf(fmaxf(r, 1.f - la.clip), 1.f + la.clip);
+                    float cl = rc * A;
+                    val = -(double)fminf(un, cl);
+                    g = (un <= cl) ? -un : 0.f;
+                }
+                ok = isfinite(val) && isfinite(g);
+            }
+        }
+    } else {
+        float c = la.dl[t];
+        ok = ok && isfinite(c);
+        if (ok) { val = (double)c * ell; g = c; }
+    }
+    if (!ok) { val = 0.0; g = 0.f; }
+}
+
+__global__ void __launch_bounds__(128) combine_loss_kernel(
+    LossArgs la, const float2* __restrict__ part, int n_nt, const float* __restrict__ zt,
+    const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
+    float* logprobs_out, float* lse_out, float* g_out, double* loss_tile) {
+    const int mt = blockIdx.x;
+    if (mt >= meta[0]) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ double s_red[4];
+    double wsum = 0.0;
+    for (int i = 0; i < 32; ++i) {
+        const int64_t p = (int64_t)mt * TILE_M + warp * 32 + i;
+        const float2* pr = part + p * n_nt;
+        float M = -INFINITY;
+        for (int j = lane; j < n_nt; j += 32) M = fmaxf(M, pr[j].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float S = 0.f;
+        for (int j = lane; j < n_nt; j += 32) {
+            float2 q = pr[j];
+            S += q.y * expf(q.x - M);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (lane == 0) {
+            int t = perm_pad[p];
+            float g = 0.f, lse = 0.f;
+            if (t >= 0) {
+                int y = tgt_pad[p];
+                float ell;
+                if (y >= 0) {
+                    lse = M + logf(S);
+                    ell = zt[p] - lse;
+                } else {
+                    ell = __int_as_float(0x7fc00000);   // NaN: invalid target
+                }
+                double val;
+                token_loss_dev(la.kind, ell, t, la, val, g);
+                if (y < 0) g = 0.f, val = 0.0;
+                wsum += val;
+                if (logprobs_out) logprobs_out[t] = ell;
+            }
+            lse_out[p] = lse;
+            g_out[p] = g;
+        }
+    }
+    if (lane == 0) s_red[warp] = wsum;
+    __syncthreads();
+    if (threadIdx.x == 0) loss_tile[mt] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+}
+
+void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, const float* zt,
+                         const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
+                         float* logprobs_out, float* lse, float* g, double* loss_tile,
+                         cudaStream_t s) {
+    if (max_tiles <= 0) return;
+    combine_loss_kernel<<<max_tiles, 128, 0, s>>>(la, part, n_nt, zt, perm_pad, tgt_pad, meta,
+                                                  logprobs_out, lse, g, loss_tile);
+}
+
+// Per-adapter loss: sum of its tiles' partial sums, in tile order.
+__global__ void loss_reduce_kernel(const double* loss_tile, const int* pad_off, int n_ad,
+                                   double* loss_out) {
+    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n_ad; a += gridDim.x * blockDim.x) {
+        double s = 0.0;
+        for (int j = pad_off[a] / TILE_M; j < pad_off[a + 1] / TILE_M; ++j) s += loss_tile[j];
+        loss_out[a] = s;
+    }
+}
+
+void launch_loss_reduce(const double* loss_tile, const int* pad_off, int n_ad, double* loss_out,
+                        cudaStream_t s) {
+    loss_reduce_kernel<<<(n_ad + 127) / 128, 128, 0, s>>>(loss_tile, pad_off, n_ad, loss_out);
+}
+
+// ----------------------------------------------------------------------------
+// Adam.  Parameters of adapter a occupy [ad_off[a], ad_off[a+1]) of the fp32
+// buffers P, G, M, V; inside, layer l holds A1 [r x d], B1 [f x r], A2 [r x f],
+// B2 [d x r].  The same element is mirrored into the padded-rank copies used
+// by the GEMMs:  A1 -> A1s[l][(a*RP + j)*d + i],  B1 -> B1s[l][(a*f + i)*RP + j],
+//                A2 -> A2s[l][(a*RP + j)*f + i],  B2 -> B2s[l][(a*d + i)*RP + j].
+// ----------------------------------------------------------------------------
+__global__ void adam_prep_kernel(int n_ad, const int* sel_mask, int* touched, int* nonfinite,
+                                 int64_t* step, float beta1, float beta2, AdamTab* tab,
+                                 int* skipped_out) {
+    for (int a = threadIdx.x; a < n_ad; a += blockDim.x) {
+        bool sel = sel_mask ? (sel_mask[a] != 0) : (touched[a] != 0);
+        AdamTab e;
+        e.mode = 0;
+        e.c1 = e.c2 = 0.f;
+        int skipped = 0;
+        if (sel) {
+            if (nonfinite[a]) {
+                e.mode = 2;
+                skipped = 1;
+            } else {
+                int64_t t = step[a] + 1;
+                step[a] = t;
+                e.mode = 1;
+                e.c1 = (float)(1.0 / (1.0 - pow((double)beta1, (double)t)));
+                e.c2 = (float)(1.0 / (1.0 - pow((double)beta2, (double)t)));
+            }
+            touched[a] = 0;
+            nonfinite[a] = 0;
+        }
+        tab[a] = e;
+        if (skipped_out) skipped_out[a] = skipped;
+    }
+}
+
+void launch_adam_prep(int n_ad, const int* sel_mask, int* touched, int* nonfinite, int64_t* step,
+                      float beta1, float beta2, AdamTab* tab, int* skipped_out, cudaStream_t s) {
+    adam_prep_kernel<<<1, 1024, 0, s>>>(n_ad, sel_mask, touched, nonfinite, step, beta1, beta2, tab,
+                                        skipped_out);
+}
+
+__device__ __forceinline__ int find_adapter(const int64_t* off, int n_ad, int64_t i) {
+    int lo = 0, hi = n_ad - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// element index (inside adapter a) -> padded copy pointer offset
+template <typename T>
+__device__ __forceinline__ T* shadow_ptr(const ShadowMap& sh, int a, int r, int d, int f, int64_t rel) {
+    const int64_t per_layer = 2LL * r * (d + f);
+    const int l = (int)(rel / per_layer);
+    int64_t q = rel - (int64_t)l * per_layer;
+    const int64_t nA1 = (int64_t)r * d, nB1 = (int64_t)f * r, nA2 = (int64_t)r * f;
+    if (q < nA1) {
+        int64_t j = q / d, i = q % d;
+        return reinterpret_cast<T*>(sh.A1[l]) + ((int64_t)a * RP + j) * d + i;
+    }
+    q -= nA1;
+    if (q < nB1) {
+        int64_t i = q / r, j = q % r;
+        return reinterpret_cast<T*>(sh.B1[l]) + ((int64_t)a * f + i) * RP + j;
+    }
+    q -= nB1;
+    if (q < nA2) {
+        int64_t j = q / f, i = q % f;
+        return reinterpret_cast<T*>(sh.A2[l]) + ((int64_t)a * RP + j) * f + i;
+    }
+    q -= nA2;
+    int64_t i = q / r, j = q % r;
+    return reinterpret_cast<T*>(sh.B2[l]) + ((int64_t)a * d + i) * RP + j;
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+    *reinterpret_cast<float4*>(dst) = v;
+}
+template <> __device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
+    uint2 w;
+    w.x = pack_bf16x2(v.x, v.y);
+    w.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst) = w;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) adam_kernel(int n_ad, const int64_t* __restrict__ ad_off,
+                                                   const int* __restrict__ ranks, int d, int f,
+                                                   int64_t total4, const AdamTab* __restrict__ tab,
+                                                   float4* P, float4* G, float4* M, float4* Vm,
+                                                   float lr, float b1, float b2, float eps, float wd,
+                                                   ShadowMap sh) {
+    __shared__ int64_t s_off[1025];
+    for (int a = threadIdx.x; a <= n_ad; a += blockDim.x) s_off[a] = ad_off[a];
+    __syncthreads();
+    for (int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i4 < total4;
+         i4 += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = i4 * 4;
+        const int a = find_adapter(s_off, n_ad, i);
+        const AdamTab e = tab[a];
+        if (e.mode == 0) continue;
+        if (e.mode == 2) {
+            G[i4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
+        float4 g = G[i4], p = P[i4], m = M[i4], v = Vm[i4];
+        float gv[4] = {g.x, g.y, g.z, g.w};
+        float pv[4] = {p.x, p.y, p.z, p.w};
+        float mv[4] = {m.x, m.y, m.z, m.w};
+        float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            mv[q] = b1 * mv[q] + (1.f - b1) * gv[q];
+            vv[q] = b2 * vv[q] + (1.f - b2) * gv[q] * gv[q];
+            float mh = mv[q] * e.c1;
+            float vh = vv[q] * e.c2;
+            pv[q] = pv[q] - lr * (mh / (sqrtf(vh) + eps) + wd * pv[q]);
+        }
+        float4 pn = make_float4(pv[0], pv[1], pv[2], pv[3]);
+        P[i4] = pn;
+        M[i4] = make_float4(mv[0], mv[1], mv[2], mv[3]);
+        Vm[i4] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        G[i4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        store4<T>(shadow_ptr<T>(sh, a, ranks[a], d, f, i - s_off[a]), pn);
+    }
+}
+
+template <typename T>
+void launch_adam(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d, int f, int64_t total,
+                 const AdamTab* tab, float* P, float* G, float* M, float* Vm, float lr, float beta1,
+                 float beta2, float eps, float wd, const ShadowMap& sh, cudaStream_t s) {
+    (void)L;
+    int64_t total4 = total / 4;
+    int blocks = (int)((total4 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    adam_kernel<T><<<blocks, 256, 0, s>>>(n_ad, ad_off, ranks, d, f, total4, tab,
+                                          reinterpret_cast<float4*>(P), reinterpret_cast<float4*>(G),
+                                          reinterpret_cast<float4*>(M), reinterpret_cast<float4*>(Vm),
+                                          lr, beta1, beta2, eps, wd, sh);
+}
+template void launch_adam<float>(int, const int64_t*, const int*, int, int, int, int64_t,
+                                 const AdamTab*, float*, float*, float*, float*, float, float, float,
+                                 float, float, const ShadowMap&, cudaStream_t);
+template void launch_adam<bf16>(int, const int64_t*, const int*, int, int, int, int64_t,
+                                const AdamTab*, float*, float*, float*, float*, float, float, float,
+                                float, float, const ShadowMap&, cudaStream_t);
+
+template <typename T>
+__global__ void shadow_sync_kernel(int n_ad, const int64_t* __restrict__ ad_off,
+                                   const int* __restrict__ ranks, int d, int f, int64_t total4,
+                                   const float4* __restrict__ P, ShadowMap sh) {
+    __shared__ int64_t s_off[1025];
+    for (int a = threadIdx.x; a <= n_ad; a += blockDim.x) s_off[a] = ad_off[a];
+    __syncthreads();
+    for (int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i4 < total4;
+         i4 += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = i4 * 4;
+        const int a = find_adapter(s_off, n_ad, i);
+        store4<T>(shadow_ptr<T>(sh, a, ranks[a], d, f, i - s_off[a]), P[i4]);
+    }
+}
+
+template <typename T>
+void launch_shadow_sync(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d, int f,
+                        int64_t total, const float* P, const ShadowMap& sh, cudaStream_t s) {
+    (void)L;
+    int64_t total4 = total / 4;
+    int blocks = (int)((total4 + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    shadow_sync_kernel<T><<<blocks, 256, 0, s>>>(n_ad, ad_off, ranks, d, f, total4,
+                                                 reinterpret_cast<const float4*>(P), sh);
+}
+template void launch_shadow_sync<float>(int, const int64_t*, const int*, int, int, int, int64_t,
+                                        const float*, const ShadowMap&, cudaStream_t);
+template void launch_shadow_sync<bf16>(int, const int64_t*, const int*, int, int, int, int64_t,
+                                       const float*, const ShadowMap&, cudaStream_t);
+
+}  // namespace mlk

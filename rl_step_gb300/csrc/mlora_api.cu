@@ -1,0 +1,774 @@
+// C ABI of libmlora (include/mlora.h) and the host-side launch sequence of
+// one training step.  Every step of the computation runs in this library's
+// kernels on the caller's stream; the host only validates arguments, builds
+// launch descriptors and queues work.
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cmath>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace mlk;
+
+// ----------------------------------------------------------------------------
+// errors
+// ----------------------------------------------------------------------------
+static thread_local std::string g_last_error;
+
+static int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+#define CUDA_TRY(expr)                                                                   \
+    do {                                                                                 \
+        cudaError_t _e = (expr);                                                         \
+        if (_e != cudaSuccess)                                                           \
+            return fail(MLORA_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(_e));  \
+    } while (0)
+
+// ----------------------------------------------------------------------------
+// handle
+// ----------------------------------------------------------------------------
+struct mlora {
+    int V = 0, d = 0, f = 0, L = 0, dtype = 0, n_ad = 0;
+    int64_t max_tokens = 0;
+    int max_pad = 0, max_tiles = 0, max_chunks = 0, max_blocks = 0;
+    int Vpad = 0;
+    int num_sms = 0;
+    int use_tc = 0;
+    size_t esize = 2;
+    std::vector<int> ranks;
+    std::vector<float> alphas;
+    std::vector<void*> allocs;
+    int64_t bytes = 0;
+    int64_t launches = 0;
+
+    // frozen base
+    void* E = nullptr;
+    void* Wout = nullptr;
+    std::vector<void*> W1, W2;
+    // adapters
+    int64_t n_params = 0;
+    std::vector<int64_t> ad_off_h;      // [n_ad + 1]
+    float *P = nullptr, *G = nullptr, *M = nullptr, *Vm = nullptr;
+    int64_t* ad_off = nullptr;
+    int* ranks_d = nullptr;
+    float* gamma_d = nullptr;
+    int64_t* grad_off = nullptr;        // [(l*4 + k) * n_ad + a]
+    int64_t* step = nullptr;
+    int *touched = nullptr, *nonfinite = nullptr, *sel_mask = nullptr;
+    AdamTab* adam_tab = nullptr;
+    ShadowMap shadow;                   // padded-rank copies per layer (dtype)
+    // routing
+    RouteBufs rb;
+    // activations (dtype unless noted)
+    std::vector<void*> hb, ub, actb, v1s, v2s;
+    float* h32 = nullptr;
+    float* dh32 = nullptr;
+    void *dhb = nullptr, *dub = nullptr, *w1s = nullptr, *w2s = nullptr;
+    // LM head
+    int lm_bn = 32, n_nt = 0, nc_tiles = 0;
+    float2* part = nullptr;
+    float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
+    int* tgt_pad = nullptr;
+    void* dz = nullptr;
+    double* loss_tile = nullptr;
+    int* status = nullptr;
+};
+
+static int dalloc(mlora_t* h, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return fail(MLORA_E_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    h->allocs.push_back(*p);
+    h->bytes += (int64_t)bytes;
+    return MLORA_OK;
+}
+
+template <typename P>
+static int dalloc_t(mlora_t* h, P** p, size_t count) {
+    void* q = nullptr;
+    int rc = dalloc(h, &q, count * sizeof(P));
+    *p = reinterpret_cast<P*>(q);
+    return rc;
+}
+
+static void free_all(mlora_t* h) {
+    for (void* p : h->allocs) cudaFree(p);
+    h->allocs.clear();
+}
+
+static inline int64_t tensor_size(int k, int r, int d, int f) {
+    switch (k) {
+    case 0: return (int64_t)r * d;   // A1
+    case 1: return (int64_t)f * r;   // B1
+    case 2: return (int64_t)r * f;   // A2
+    default: return (int64_t)d * r;  // B2
+    }
+}
+
+static inline int64_t tensor_off(const mlora_t* h, int a, int l, int k) {
+    int r = h->ranks[a];
+    int64_t off = h->ad_off_h[a] + (int64_t)l * 2 * r * (h->d + h->f);
+    for (int q = 0; q < k; ++q) off += tensor_size(q, r, h->d, h->f);
+    return off;
+}
+
+// padded-row upper bound for a batch of n tokens
+static inline int pad_rows_for(const mlora_t* h, int64_t n) {
+    int64_t busy = n < h->n_ad ? n : h->n_ad;
+    int64_t rows = n + (int64_t)(TILE_M - 1) * busy;
+    return (int)((rows + TILE_M - 1) / TILE_M * TILE_M);
+}
+
+extern "C" const char* mlora_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int64_t mlora_kernel_launches(const mlora_t* h) { return h ? h->launches : 0; }
+
+extern "C" int64_t mlora_device_bytes(const mlora_t* h) { return h ? h->bytes : 0; }
+
+// ----------------------------------------------------------------------------
+// create / destroy
+// ----------------------------------------------------------------------------
+extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlora_t** out) {
+    if (!cfg || !init || !out) return fail(MLORA_E_ARG, "NULL argument");
+    *out = nullptr;
+    if (cfg->vocab < 1 || cfg->d_model < 64 || cfg->d_model % 64 || cfg->d_ffn < 64 ||
+        cfg->d_ffn % 64 || cfg->n_layers < 1 || cfg->n_layers > 64)
+        return fail(MLORA_E_ARG, "bad model shape (V=%d d=%d f=%d L=%d): d and f must be "
+                    "multiples of 64, 1 <= L <= 64", cfg->vocab, cfg->d_model, cfg->d_ffn,
+                    cfg->n_layers);
+    if (cfg->dtype != MLORA_BF16 && cfg->dtype != MLORA_FP32)
+        return fail(MLORA_E_ARG, "bad dtype %d", cfg->dtype);
+    if (cfg->n_adapters < 1 || cfg->n_adapters > 1024 || !cfg->ranks || !cfg->alphas)
+        return fail(MLORA_E_ARG, "n_adapters must be 1..1024 with ranks and alphas");
+    if (cfg->max_tokens < 1 || cfg->max_tokens > (1LL << 26))
+        return fail(MLORA_E_ARG, "max_tokens out of range");
+    for (int a = 0; a < cfg->n_adapters; ++a) {
+        int r = cfg->ranks[a];
+        if (r < 1 || r > MLORA_MAX_RANK || r % 4)
+            return fail(MLORA_E_ARG, "adapter %d: rank %d must be in 4..%d and a multiple of 4", a, r,
+                        MLORA_MAX_RANK);
+        if (!std::isfinite(cfg->alphas[a])) return fail(MLORA_E_ARG, "adapter %d: alpha not finite", a);
+    }
+    if (!init->E || !init->Wout || !init->W1 || !init->W2) return fail(MLORA_E_ARG, "NULL base weight");
+    for (int l = 0; l < cfg->n_layers; ++l)
+        if (!init->W1[l] || !init->W2[l]) return fail(MLORA_E_ARG, "NULL W1/W2 for layer %d", l);
+
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+
+    mlora_t* h = new mlora();
+    h->V = cfg->vocab; h->d = cfg->d_model; h->f = cfg->d_ffn; h->L = cfg->n_layers;
+    h->dtype = cfg->dtype; h->n_ad = cfg->n_adapters; h->max_tokens = cfg->max_tokens;
+    h->num_sms = prop.multiProcessorCount;
+    h->esize = cfg->dtype == MLORA_BF16 ? 2 : 4;
+    h->ranks.assign(cfg->ranks, cfg->ranks + cfg->n_adapters);
+    h->alphas.assign(cfg->alphas, cfg->alphas + cfg->n_adapters);
+    h->use_tc = (cfg->dtype == MLORA_BF16) && prop.major == 10 && getenv("MLORA_ENABLE_TC") != nullptr &&
+                tc_engine_available();
+    h->Vpad = (h->V + 63) / 64 * 64;
+    h->lm_bn = h->use_tc ? 256 : 32;
+    h->n_nt = (h->V + h->lm_bn - 1) / h->lm_bn;
+
+    const int n_ad = h->n_ad, L = h->L, d = h->d, f = h->f, V = h->V;
+    const size_t es = h->esize;
+    h->max_pad = pad_rows_for(h, h->max_tokens);
+    h->max_tiles = h->max_pad / TILE_M;
+    h->max_chunks = h->max_pad / GRAD_CHUNK + n_ad + 1;
+    h->max_blocks = (int)((h->max_tokens + ROUTE_BLOCK - 1) / ROUTE_BLOCK);
+    const int64_t MP = h->max_pad;
+
+    int rc = MLORA_OK;
+#define ALLOC(ptr, count) do { if ((rc = dalloc_t(h, &(ptr), (size_t)(count))) != MLORA_OK) goto fail_out; } while (0)
+#define ALLOCB(ptr, bytes) do { if ((rc = dalloc(h, &(ptr), (size_t)(bytes))) != MLORA_OK) goto fail_out; } while (0)
+    {
+        // base
+        ALLOCB(h->E, (size_t)V * d * es);
+        ALLOCB(h->Wout, (size_t)V * d * es);
+        h->W1.resize(L); h->W2.resize(L);
+        for (int l = 0; l < L; ++l) {
+            ALLOCB(h->W1[l], (size_t)f * d * es);
+            ALLOCB(h->W2[l], (size_t)d * f * es);
+        }
+        // adapters
+        h->ad_off_h.resize(n_ad + 1);
+        h->ad_off_h[0] = 0;
+        for (int a = 0; a < n_ad; ++a)
+            h->ad_off_h[a + 1] = h->ad_off_h[a] + (int64_t)L * 2 * h->ranks[a] * (d + f);
+        h->n_params = h->ad_off_h[n_ad];
+        ALLOC(h->P, h->n_params); ALLOC(h->G, h->n_params);
+        ALLOC(h->M, h->n_params); ALLOC(h->Vm, h->n_params);
+        ALLOC(h->ad_off, n_ad + 1);
+        ALLOC(h->ranks_d, n_ad);
+        ALLOC(h->gamma_d, n_ad);
+        ALLOC(h->grad_off, (size_t)L * 4 * n_ad);
+        ALLOC(h->step, n_ad);
+        ALLOC(h->touched, n_ad);
+        ALLOC(h->nonfinite, n_ad);
+        ALLOC(h->sel_mask, n_ad);
+        ALLOC(h->adam_tab, n_ad);
+        memset(&h->shadow, 0, sizeof(h->shadow));
+        for (int l = 0; l < L; ++l) {
+            ALLOCB(h->shadow.A1[l], (size_t)n_ad * RP * d * es);
+            ALLOCB(h->shadow.B1[l], (size_t)n_ad * f * RP * es);
+            ALLOCB(h->shadow.A2[l], (size_t)n_ad * RP * f * es);
+            ALLOCB(h->shadow.B2[l], (size_t)n_ad * d * RP * es);
+        }
+        // routing
+        ALLOC(h->rb.blk_cnt, (size_t)(h->max_blocks > 0 ? h->max_blocks : 1) * n_ad);
+        ALLOC(h->rb.perm_pad, MP);
+        ALLOC(h->rb.inv, h->max_tokens);
+        ALLOC(h->rb.seg_off, n_ad + 1);
+        ALLOC(h->rb.pad_off, n_ad + 1);
+        ALLOC(h->rb.tile_ad, h->max_tiles);
+        ALLOC(h->rb.meta, 4);
+        ALLOC(h->rb.chunks, h->max_chunks);
+        h->rb.max_pad = h->max_pad; h->rb.max_tiles = h->max_tiles; h->rb.max_chunks = h->max_chunks;
+        // activations
+        h->hb.resize(L + 1); h->ub.resize(L); h->actb.resize(L); h->v1s.resize(L); h->v2s.resize(L);
+        for (int l = 0; l <= L; ++l) ALLOCB(h->hb[l], (size_t)MP * d * es);
+        for (int l = 0; l < L; ++l) {
+            ALLOCB(h->ub[l], (size_t)MP * f * es);
+            ALLOCB(h->actb[l], (size_t)MP * f * es);
+            ALLOCB(h->v1s[l], (size_t)MP * RP * es);
+            ALLOCB(h->v2s[l], (size_t)MP * RP * es);
+        }
+        ALLOC(h->h32, (size_t)MP * d);
+        ALLOC(h->dh32, (size_t)MP * d);
+        ALLOCB(h->dhb, (size_t)MP * d * es);
+        ALLOCB(h->dub, (size_t)MP * f * es);
+        ALLOCB(h->w1s, (size_t)MP * RP * es);
+        ALLOCB(h->w2s, (size_t)MP * RP * es);
+        // LM head: partials, per-row scalars, and the bounded dz chunk buffer
+        ALLOC(h->part, (size_t)MP * h->n_nt);
+        ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
+        ALLOC(h->tgt_pad, MP);
+        h->nc_tiles = h->max_tiles < 64 ? h->max_tiles : 64;   // 8192-row chunks
+        ALLOCB(h->dz, (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
+        ALLOC(h->loss_tile, h->max_tiles);
+        ALLOC(h->status, 1);
+    }
+#undef ALLOC
+#undef ALLOCB
+    {
+        cudaStream_t s = 0;
+        // copy the base
+        CUDA_TRY(cudaMemcpyAsync(h->E, init->E, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
+        CUDA_TRY(cudaMemcpyAsync(h->Wout, init->Wout, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
+        for (int l = 0; l < L; ++l) {
+            CUDA_TRY(cudaMemcpyAsync(h->W1[l], init->W1[l], (size_t)f * d * es, cudaMemcpyDeviceToDevice, s));
+            CUDA_TRY(cudaMemcpyAsync(h->W2[l], init->W2[l], (size_t)d * f * es, cudaMemcpyDeviceToDevice, s));
+        }
+        // adapters
+        CUDA_TRY(cudaMemsetAsync(h->P, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY(cudaMemsetAsync(h->G, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY(cudaMemsetAsync(h->M, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY(cudaMemsetAsync(h->Vm, 0, sizeof(float) * h->n_params, s));
+        const float* const* src[4] = {init->A1, init->B1, init->A2, init->B2};
+        for (int a = 0; a < n_ad; ++a)
+            for (int l = 0; l < L; ++l)
+                for (int k = 0; k < 4; ++k) {
+                    const float* p = src[k] ? src[k][a * L + l] : nullptr;
+                    if (p)
+                        CUDA_TRY(cudaMemcpyAsync(h->P + tensor_off(h, a, l, k), p,
+                                                 sizeof(float) * tensor_size(k, h->ranks[a], d, f),
+                                                 cudaMemcpyDeviceToDevice, s));
+                }
+        for (int l = 0; l < L; ++l) {
+            CUDA_TRY(cudaMemsetAsync(h->shadow.A1[l], 0, (size_t)n_ad * RP * d * es, s));
+            CUDA_TRY(cudaMemsetAsync(h->shadow.B1[l], 0, (size_t)n_ad * f * RP * es, s));
+            CUDA_TRY(cudaMemsetAsync(h->shadow.A2[l], 0, (size_t)n_ad * RP * f * es, s));
+            CUDA_TRY(cudaMemsetAsync(h->shadow.B2[l], 0, (size_t)n_ad * d * RP * es, s));
+        }
+        std::vector<float> gam(n_ad);
+        for (int a = 0; a < n_ad; ++a) gam[a] = h->alphas[a] / (float)h->ranks[a];
+        std::vector<int64_t> goff((size_t)L * 4 * n_ad);
+        for (int l = 0; l < L; ++l)
+            for (int k = 0; k < 4; ++k)
+                for (int a = 0; a < n_ad; ++a) goff[((size_t)l * 4 + k) * n_ad + a] = tensor_off(h, a, l, k);
+        CUDA_TRY(cudaMemcpy(h->ad_off, h->ad_off_h.data(), sizeof(int64_t) * (n_ad + 1), cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(h->ranks_d, h->ranks.data(), sizeof(int) * n_ad, cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(h->gamma_d, gam.data(), sizeof(float) * n_ad, cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(h->grad_off, goff.data(), sizeof(int64_t) * goff.size(), cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemset(h->step, 0, sizeof(int64_t) * n_ad));
+        CUDA_TRY(cudaMemset(h->touched, 0, sizeof(int) * n_ad));
+        CUDA_TRY(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
+        CUDA_TRY(cudaMemset(h->status, 0, sizeof(int)));
+        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float2) * (size_t)MP * h->n_nt));
+        if (h->dtype == MLORA_BF16)
+            launch_shadow_sync<bf16>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
+        else
+            launch_shadow_sync<float>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
+        ++h->launches;
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(cudaDeviceSynchronize());
+    }
+    *out = h;
+    return MLORA_OK;
+fail_out:
+    free_all(h);
+    delete h;
+    return rc;
+}
+
+extern "C" int mlora_destroy(mlora_t* h) {
+    if (!h) return MLORA_OK;
+    cudaDeviceSynchronize();
+    free_all(h);
+    delete h;
+    return MLORA_OK;
+}
+
+// ----------------------------------------------------------------------------
+// GEMM descriptor helpers
+// ----------------------------------------------------------------------------
+static GemmOperand op_kmajor(const void* p, int64_t rows, int64_t cols, int64_t ad_rows = 0,
+                             int64_t shift = 0) {
+    GemmOperand o;
+    o.ptr = p; o.ld = cols; o.rows = rows; o.cols = cols; o.mn_major = 0; o.ad_rows = ad_rows;
+    o.row_shift = shift;
+    return o;
+}
+static GemmOperand op_mnmajor(const void* p, int64_t rows, int64_t cols, int64_t ad_rows = 0) {
+    GemmOperand o;
+    o.ptr = p; o.ld = cols; o.rows = rows; o.cols = cols; o.mn_major = 1; o.ad_rows = ad_rows;
+    return o;
+}
+
+template <typename T>
+static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s) {
+    if (h->use_tc) {
+        cudaError_t e = launch_tc_gemm(p, s, h->num_sms, h->status);
+        if (e != cudaSuccess) return fail(MLORA_E_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(e));
+    } else {
+        launch_simt_gemm<T>(p, s);
+    }
+    ++h->launches;
+    return MLORA_OK;
+}
+
+// dense GEMM over the padded token rows of the current batch
+static GemmParams dense_params(mlora_t* h, int mt_upper, int N, int K) {
+    GemmParams p;
+    p.M = mt_upper * TILE_M;
+    p.N = N; p.K = K; p.Kx = 0;
+    p.mtiles_dev = h->rb.meta;
+    p.mt_base = 0; p.mt_count = mt_upper;
+    p.tile_ad = h->rb.tile_ad;
+    return p;
+}
+
+// per-adapter reduction over token rows: grad[a] (+)= X_seg^T Y_seg
+static GemmParams grad_params(mlora_t* h, int mp, int Dout, const void* X, const void* Y, int l, int k,
+                              int trans) {
+    GemmParams p;
+    p.M = Dout; p.N = RP; p.K = 0;
+    p.grouped = 1;
+    p.chunks = h->rb.chunks;
+    p.nchunks_dev = h->rb.meta + 1;
+    p.max_chunks = mp / GRAD_CHUNK + (mp / TILE_M < h->n_ad ? mp / TILE_M : h->n_ad) + 1;
+    if (p.max_chunks > h->max_chunks) p.max_chunks = h->max_chunks;
+    p.A = op_mnmajor(X, h->max_pad, Dout);
+    p.B = op_mnmajor(Y, h->max_pad, RP);
+    p.ep.kind = EPI_GRAD;
+    p.ep.grad = h->G;
+    p.ep.grad_off = h->grad_off + ((size_t)l * 4 + k) * h->n_ad;
+    p.ep.ranks = h->ranks_d;
+    p.ep.grad_trans = trans;
+    p.ep.grad_M = Dout;
+    p.ep.nonfinite = h->nonfinite;
+    return p;
+}
+
+// ----------------------------------------------------------------------------
+// one step
+// ----------------------------------------------------------------------------
+template <typename T>
+static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float* logprobs_out,
+                     double* loss_out, bool backward, cudaStream_t s) {
+    const int64_t N = b->n_tokens;
+    const int n_ad = h->n_ad, L = h->L, d = h->d, f = h->f, V = h->V;
+    const int64_t MP = h->max_pad;
+    const int mp = pad_rows_for(h, N);
+    const int mt_upper = mp / TILE_M;
+    int rc;
+
+    if (logprobs_out && N > 0) CUDA_TRY(cudaMemsetAsync(logprobs_out, 0xff, sizeof(float) * N, s));
+    if (N == 0) {
+        if (loss_out) CUDA_TRY(cudaMemsetAsync(loss_out, 0, sizeof(double) * n_ad, s));
+        return MLORA_OK;
+    }
+    // a1 routing
+    launch_routing(b->adapter_ids, N, n_ad, h->rb, backward ? h->touched : nullptr, h->status, s,
+                   &h->launches);
+    // a2 embedding
+    launch_embed<T>(h->rb.perm_pad, h->rb.meta, mp, b->tokens, b->targets,
+                    reinterpret_cast<const T*>(h->E), V, d, reinterpret_cast<T*>(h->hb[0]), h->h32,
+                    h->tgt_pad, h->status, s);
+    ++h->launches;
+
+    // a3-a5 layers
+    for (int l = 0; l < L; ++l) {
+        {   // v1s = gamma * A1_a h
+            GemmParams p = dense_params(h, mt_upper, RP, d);
+            p.A = op_kmajor(h->hb[l], MP, d);
+            p.B = op_kmajor(h->shadow.A1[l], (int64_t)n_ad * RP, d, RP);
+            p.ep.kind = EPI_SHRINK; p.ep.out0 = h->v1s[l]; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // u = W1 h + B1_a v1s ; act = silu(u)
+            GemmParams p = dense_params(h, mt_upper, f, d);
+            p.A = op_kmajor(h->hb[l], MP, d);
+            p.B = op_kmajor(h->W1[l], f, d);
+            p.Kx = RP;
+            p.Ax = op_kmajor(h->v1s[l], MP, RP);
+            p.Bx = op_kmajor(h->shadow.B1[l], (int64_t)n_ad * f, RP, f);
+            p.ep.kind = EPI_SILU; p.ep.out0 = h->ub[l]; p.ep.ld0 = f; p.ep.out1 = h->actb[l]; p.ep.ld1 = f;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // v2s = gamma * A2_a act
+            GemmParams p = dense_params(h, mt_upper, RP, f);
+            p.A = op_kmajor(h->actb[l], MP, f);
+            p.B = op_kmajor(h->shadow.A2[l], (int64_t)n_ad * RP, f, RP);
+            p.ep.kind = EPI_SHRINK; p.ep.out0 = h->v2s[l]; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // h += W2 act + B2_a v2s
+            GemmParams p = dense_params(h, mt_upper, d, f);
+            p.A = op_kmajor(h->actb[l], MP, f);
+            p.B = op_kmajor(h->W2[l], d, f);
+            p.Kx = RP;
+            p.Ax = op_kmajor(h->v2s[l], MP, RP);
+            p.Bx = op_kmajor(h->shadow.B2[l], (int64_t)n_ad * d, RP, d);
+            p.ep.kind = EPI_RESID; p.ep.f32 = h->h32; p.ep.ldf = d; p.ep.out0 = h->hb[l + 1]; p.ep.ld0 = d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+    }
+    // a6 LM head: per-tile (max, sum exp) and the target logit
+    {
+        GemmParams p = dense_params(h, mt_upper, V, d);
+        p.A = op_kmajor(h->hb[L], MP, d);
+        p.B = op_kmajor(h->Wout, V, d);
+        p.group_m = 64;
+        p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
+        p.ep.n_ntiles = h->n_nt; p.ep.V = V; p.ep.Vpad = h->Vpad;
+        if ((rc = run_gemm<T>(h, p, s))) return rc;
+    }
+    // a7 combine + loss epilogue
+    launch_combine_loss(la, h->part, h->n_nt, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
+                        logprobs_out, h->lse, h->gvec, h->loss_tile, s);
+    ++h->launches;
+    if (loss_out) {
+        launch_loss_reduce(h->loss_tile, h->rb.pad_off, n_ad, loss_out, s);
+        ++h->launches;
+    }
+    if (!backward) return MLORA_OK;
+
+    // a8 LM head backward, chunk by chunk: recompute z, dz = g (onehot - softmax), dh = dz Wout
+    for (int c0 = 0; c0 < mt_upper; c0 += h->nc_tiles) {
+        int cnt = mt_upper - c0 < h->nc_tiles ? mt_upper - c0 : h->nc_tiles;
+        {
+            GemmParams p = dense_params(h, mt_upper, V, d);
+            p.mt_base = c0; p.mt_count = cnt;
+            p.A = op_kmajor(h->hb[L], MP, d);
+            p.B = op_kmajor(h->Wout, V, d);
+            p.group_m = 64;
+            p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
+            p.ep.tgt = h->tgt_pad; p.ep.V = V; p.ep.Vpad = h->Vpad;
+            p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {
+            GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
+            p.mt_base = c0; p.mt_count = cnt;
+            p.A = op_kmajor(h->dz, (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
+            p.B = op_mnmajor(h->Wout, V, d);
+            p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+    }
+    // a9-a11 layers in reverse
+    for (int l = L - 1; l >= 0; --l) {
+        {   // w2s = gamma * B2_a^T dh
+            GemmParams p = dense_params(h, mt_upper, RP, d);
+            p.A = op_kmajor(h->dhb, MP, d);
+            p.B = op_mnmajor(h->shadow.B2[l], (int64_t)n_ad * d, RP, d);
+            p.ep.kind = EPI_SHRINK; p.ep.out0 = h->w2s; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // du = (W2^T dh + A2_a^T w2s) * silu'(u)
+            GemmParams p = dense_params(h, mt_upper, f, d);
+            p.A = op_kmajor(h->dhb, MP, d);
+            p.B = op_mnmajor(h->W2[l], d, f);
+            p.Kx = RP;
+            p.Ax = op_kmajor(h->w2s, MP, RP);
+            p.Bx = op_mnmajor(h->shadow.A2[l], (int64_t)n_ad * RP, f, RP);
+            p.ep.kind = EPI_DSILU; p.ep.aux = h->ub[l]; p.ep.ld_aux = f; p.ep.out0 = h->dub; p.ep.ld0 = f;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // dB2_a += dh^T v2s   [d x r]
+            GemmParams p = grad_params(h, mp, d, h->dhb, h->v2s[l], l, 3, 0);
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // dA2_a += w2s^T act  [r x f], computed as act^T w2s
+            GemmParams p = grad_params(h, mp, f, h->actb[l], h->w2s, l, 2, 1);
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // w1s = gamma * B1_a^T du
+            GemmParams p = dense_params(h, mt_upper, RP, f);
+            p.A = op_kmajor(h->dub, MP, f);
+            p.B = op_mnmajor(h->shadow.B1[l], (int64_t)n_ad * f, RP, f);
+            p.ep.kind = EPI_SHRINK; p.ep.out0 = h->w1s; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // dh += W1^T du + A1_a^T w1s
+            GemmParams p = dense_params(h, mt_upper, d, f);
+            p.A = op_kmajor(h->dub, MP, f);
+            p.B = op_mnmajor(h->W1[l], f, d);
+            p.Kx = RP;
+            p.Ax = op_kmajor(h->w1s, MP, RP);
+            p.Bx = op_mnmajor(h->shadow.A1[l], (int64_t)n_ad * RP, d, RP);
+            p.ep.kind = EPI_RESID; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // dB1_a += du^T v1s   [f x r]
+            GemmParams p = grad_params(h, mp, f, h->dub, h->v1s[l], l, 1, 0);
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+        {   // dA1_a += w1s^T h    [r x d], computed as h^T w1s
+            GemmParams p = grad_params(h, mp, d, h->hb[l], h->w1s, l, 0, 1);
+            if ((rc = run_gemm<T>(h, p, s))) return rc;
+        }
+    }
+    return MLORA_OK;
+}
+
+static int check_batch(mlora_t* h, const mlora_batch* b) {
+    if (!h || !b) return fail(MLORA_E_ARG, "NULL handle or batch");
+    if (b->n_tokens < 0 || b->n_tokens > h->max_tokens)
+        return fail(MLORA_E_ARG, "n_tokens %lld outside 0..max_tokens (%lld)", (long long)b->n_tokens,
+                    (long long)h->max_tokens);
+    if (b->n_tokens > 0 && (!b->tokens || !b->targets || !b->adapter_ids))
+        return fail(MLORA_E_ARG, "NULL token array");
+    return MLORA_OK;
+}
+
+static int dispatch_step(mlora_t* h, const mlora_batch* b, const LossArgs& la, float* lp,
+                         double* loss, bool bwd, void* stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = h->dtype == MLORA_BF16 ? step_impl<bf16>(h, b, la, lp, loss, bwd, s)
+                                    : step_impl<float>(h, b, la, lp, loss, bwd, s);
+    if (rc) return rc;
+    CUDA_TRY(cudaGetLastError());
+    return MLORA_OK;
+}
+
+extern "C" int mlora_forward(mlora_t* h, const mlora_batch* b, float* logprobs_out, void* stream) {
+    int rc = check_batch(h, b);
+    if (rc) return rc;
+    if (!logprobs_out && b->n_tokens > 0) return fail(MLORA_E_ARG, "NULL logprobs_out");
+    LossArgs la{-1, nullptr, nullptr, nullptr, 0.f, nullptr};
+    return dispatch_step(h, b, la, logprobs_out, nullptr, false, stream);
+}
+
+extern "C" int mlora_forward_backward(mlora_t* h, const mlora_batch* b, int32_t loss_kind,
+                                      const mlora_loss_inputs* li, float* logprobs_out,
+                                      double* loss_out, void* stream) {
+    int rc = check_batch(h, b);
+    if (rc) return rc;
+    if (!li) return fail(MLORA_E_ARG, "NULL loss inputs");
+    LossArgs la{loss_kind, li->weights, li->advantages, li->sampler_logprobs, li->clip_eps, nullptr};
+    if (b->n_tokens > 0) {
+        if (loss_kind == MLORA_CROSS_ENTROPY) {
+            if (!li->weights) return fail(MLORA_E_ARG, "cross_entropy needs weights");
+        } else if (loss_kind == MLORA_IMPORTANCE_SAMPLING || loss_kind == MLORA_PPO) {
+            if (!li->advantages || !li->sampler_logprobs)
+                return fail(MLORA_E_ARG, "importance_sampling / ppo need advantages and sampler_logprobs");
+            if (loss_kind == MLORA_PPO && !(li->clip_eps >= 0.f && li->clip_eps < 1.f))
+                return fail(MLORA_E_ARG, "ppo clip_eps must be in [0, 1)");
+        } else {
+            return fail(MLORA_E_ARG, "unknown loss kind %d", loss_kind);
+        }
+    }
+    return dispatch_step(h, b, la, logprobs_out, loss_out, true, stream);
+}
+
+extern "C" int mlora_forward_backward_custom(mlora_t* h, const mlora_batch* b,
+                                             const float* dloss_dlogprobs, float* logprobs_out,
+                                             double* loss_out, void* stream) {
+    int rc = check_batch(h, b);
+    if (rc) return rc;
+    if (!dloss_dlogprobs && b->n_tokens > 0) return fail(MLORA_E_ARG, "NULL dloss_dlogprobs");
+    LossArgs la{3, nullptr, nullptr, nullptr, 0.f, dloss_dlogprobs};
+    return dispatch_step(h, b, la, logprobs_out, loss_out, true, stream);
+}
+
+extern "C" int mlora_optim_step(mlora_t* h, const mlora_adam* p, const int32_t* adapters, int32_t n,
+                                int32_t* skipped_out, void* stream) {
+    if (!h || !p) return fail(MLORA_E_ARG, "NULL handle or adam params");
+    if (!(p->lr >= 0.f) || !(p->beta1 >= 0.f && p->beta1 < 1.f) || !(p->beta2 >= 0.f && p->beta2 < 1.f) ||
+        !(p->eps > 0.f) || !std::isfinite(p->weight_decay))
+        return fail(MLORA_E_ARG, "bad Adam hyper-parameters");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int* sel = nullptr;
+    if (adapters) {
+        if (n < 0) return fail(MLORA_E_ARG, "negative adapter count");
+        std::vector<int> mask(h->n_ad, 0);
+        for (int i = 0; i < n; ++i) {
+            if (adapters[i] < 0 || adapters[i] >= h->n_ad) return fail(MLORA_E_ARG, "adapter id %d out of range", adapters[i]);
+            mask[adapters[i]] = 1;
+        }
+        CUDA_TRY(cudaMemcpyAsync(h->sel_mask, mask.data(), sizeof(int) * h->n_ad, cudaMemcpyHostToDevice, s));
+        CUDA_TRY(cudaStreamSynchronize(s));   // the host vector goes out of scope
+        sel = h->sel_mask;
+    }
+    launch_adam_prep(h->n_ad, sel, h->touched, h->nonfinite, h->step, p->beta1, p->beta2, h->adam_tab,
+                     skipped_out, s);
+    ++h->launches;
+    if (h->dtype == MLORA_BF16)
+        launch_adam<bf16>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->adam_tab, h->P,
+                          h->G, h->M, h->Vm, p->lr, p->beta1, p->beta2, p->eps, p->weight_decay, h->shadow, s);
+    else
+        launch_adam<float>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->adam_tab, h->P,
+                           h->G, h->M, h->Vm, p->lr, p->beta1, p->beta2, p->eps, p->weight_decay, h->shadow, s);
+    ++h->launches;
+    CUDA_TRY(cudaGetLastError());
+    return MLORA_OK;
+}
+
+// ----------------------------------------------------------------------------
+// inspection hooks, checkpoint, status
+// ----------------------------------------------------------------------------
+static int tensor_ptr(mlora_t* h, int a, int l, int which, float** ptr, int64_t* count) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    if (a < 0 || a >= h->n_ad || l < 0 || l >= h->L || which < 0 || which > 15)
+        return fail(MLORA_E_ARG, "adapter/layer/tensor selector out of range");
+    int k = which & 3;
+    float* bufs[4] = {h->P, h->G, h->M, h->Vm};
+    *ptr = bufs[which >> 2] + tensor_off(h, a, l, k);
+    *count = tensor_size(k, h->ranks[a], h->d, h->f);
+    return MLORA_OK;
+}
+
+extern "C" int mlora_read_adapter(mlora_t* h, int32_t adapter, int32_t layer, int32_t which, float* dst,
+                                  void* stream) {
+    float* src;
+    int64_t cnt;
+    int rc = tensor_ptr(h, adapter, layer, which, &src, &cnt);
+    if (rc) return rc;
+    if (!dst) return fail(MLORA_E_ARG, "NULL dst");
+    CUDA_TRY(cudaMemcpyAsync(dst, src, sizeof(float) * cnt, cudaMemcpyDeviceToDevice,
+                             reinterpret_cast<cudaStream_t>(stream)));
+    return MLORA_OK;
+}
+
+extern "C" int mlora_write_adapter(mlora_t* h, int32_t adapter, int32_t layer, int32_t which,
+                                   const float* src, void* stream) {
+    if (which < 0 || which > 3) return fail(MLORA_E_ARG, "only weight tensors can be written");
+    float* dst;
+    int64_t cnt;
+    int rc = tensor_ptr(h, adapter, layer, which, &dst, &cnt);
+    if (rc) return rc;
+    if (!src) return fail(MLORA_E_ARG, "NULL src");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaMemcpyAsync(dst, src, sizeof(float) * cnt, cudaMemcpyDeviceToDevice, s));
+    if (h->dtype == MLORA_BF16)
+        launch_shadow_sync<bf16>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->P, h->shadow, s);
+    else
+        launch_shadow_sync<float>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->P, h->shadow, s);
+    ++h->launches;
+    CUDA_TRY(cudaGetLastError());
+    return MLORA_OK;
+}
+
+extern "C" int mlora_get_steps(mlora_t* h, int64_t* steps_out, void* stream) {
+    if (!h || !steps_out) return fail(MLORA_E_ARG, "NULL argument");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaMemcpyAsync(steps_out, h->step, sizeof(int64_t) * h->n_ad, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return MLORA_OK;
+}
+
+extern "C" int mlora_get_routing(mlora_t* h, const int32_t* adapter_ids, int64_t n, int32_t* perm,
+                                 int32_t* seg_off, int32_t* pad_off, int32_t* tile_ad, void* stream) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    if (n < 0 || n > h->max_tokens) return fail(MLORA_E_ARG, "n outside 0..max_tokens");
+    if ((n > 0 && (!adapter_ids || !perm)) || !seg_off || !pad_off || !tile_ad)
+        return fail(MLORA_E_ARG, "NULL output");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    launch_routing(adapter_ids, n, h->n_ad, h->rb, nullptr, h->status, s, &h->launches);
+    if (n > 0) launch_compact_perm(h->rb, h->n_ad, perm, s, &h->launches);
+    CUDA_TRY(cudaMemcpyAsync(seg_off, h->rb.seg_off, sizeof(int) * (h->n_ad + 1), cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(pad_off, h->rb.pad_off, sizeof(int) * (h->n_ad + 1), cudaMemcpyDeviceToDevice, s));
+    int ntile_out = (int)(n / TILE_M) + h->n_ad + 1;
+    int ncopy = ntile_out < h->max_tiles ? ntile_out : h->max_tiles;
+    CUDA_TRY(cudaMemcpyAsync(tile_ad, h->rb.tile_ad, sizeof(int) * ncopy, cudaMemcpyDeviceToDevice, s));
+    if (ntile_out > ncopy) CUDA_TRY(cudaMemsetAsync(tile_ad + ncopy, 0xff, sizeof(int) * (ntile_out - ncopy), s));
+    CUDA_TRY(cudaGetLastError());
+    return MLORA_OK;
+}
+
+extern "C" int mlora_check_status(mlora_t* h, void* stream) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaStreamSynchronize(s));
+    int st = 0;
+    CUDA_TRY(cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemset(h->status, 0, sizeof(int)));
+    if (st & ST_TIMEOUT) return fail(MLORA_E_TIMEOUT, "a bounded device wait gave up");
+    if (st & ST_RANGE) return fail(MLORA_E_RANGE, "a token, target or adapter id was out of range");
+    return MLORA_OK;
+}
+
+extern "C" int mlora_save_state(mlora_t* h, const char* path, void* stream) {
+    if (!h || !path) return fail(MLORA_E_ARG, "NULL argument");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaStreamSynchronize(s));
+    std::vector<float> P(h->n_params), M(h->n_params), Vv(h->n_params);
+    std::vector<int64_t> steps(h->n_ad);
+    CUDA_TRY(cudaMemcpy(P.data(), h->P, sizeof(float) * h->n_params, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(M.data(), h->M, sizeof(float) * h->n_params, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(Vv.data(), h->Vm, sizeof(float) * h->n_params, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(steps.data(), h->step, sizeof(int64_t) * h->n_ad, cudaMemcpyDeviceToHost));
+    FILE* fh = fopen(path, "wb");
+    if (!fh) return fail(MLORA_E_IO, "cannot open %s for writing", path);
+    bool ok = true;
+    auto put = [&](const void* p, size_t n) { ok = ok && fwrite(p, 1, n, fh) == n; };
+    // The format is little-endian; both supported hosts (x86-64, aarch64) are.
+    put("MLORASTA", 8);
+    uint32_t hdr[6] = {1u, (uint32_t)h->n_ad, (uint32_t)h->L, (uint32_t)h->d, (uint32_t)h->f, 0u};
+    put(hdr, sizeof(hdr));
+    for (int a = 0; a < h->n_ad; ++a) {
+        uint32_t r = (uint32_t)h->ranks[a];
+        float al = h->alphas[a];
+        uint64_t st = (uint64_t)steps[a];
+        put(&r, 4); put(&al, 4); put(&st, 8);
+        const std::vector<float>* grp[3] = {&P, &M, &Vv};
+        for (int g = 0; g < 3; ++g)
+            for (int l = 0; l < h->L; ++l)
+                for (int k = 0; k < 4; ++k)
+                    put(grp[g]->data() + tensor_off(h, a, l, k),
+                        sizeof(float) * tensor_size(k, h->ranks[a], h->d, h->f));
+    }
+    ok = (fclose(fh) == 0) && ok;
+    if (!ok) return fail(MLORA_E_IO, "write to %s failed", path);
+    return MLORA_OK;
+}
