@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark: trained tokens/s of one forward_backward + optim_step.
+
+A step is one pass of the whole hot path over one synthetic batch: routing,
+embedding, L LoRA-MLP blocks, LM head with the loss epilogue, the backward
+(LM head by recompute, the blocks in reverse, per-adapter gradient GEMMs) and
+the per-adapter Adam update.  Default workload: Qwen3-8B widths (V=151936,
+d=4096, f=12288, L=4), 32 rank-32 adapters with Zipf(1.1) traffic, 65,536
+tokens in sequences of 512-2048 tokens, PPO clip 0.2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is device-timed throughput with the
+inputs resident in HBM (CUDA events on the launch stream, max over ranks);
+`e2e` is the same metric through the C-ABI with host buffers, the copies
+inside the timed region.  `roofline` reports the tcgen05 GEMM kernel family
+(algorithmic FLOPs only, timed live by per-launch CUDA events), `kernels` the
+per-class breakdown, `cpu_baseline` the CPU oracle on a bounded sample.
+`--impl reference` times the CPU oracle itself (the reference arm).
+With N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU: the path has no cross-replica exchange in this
+build, so scaling is weak and no collective touches the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TC_CLASSES = ("w1_fwd", "w2_fwd", "lm_fwd", "lm_dz", "lm_dh", "w2_bwd", "w1_bwd")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen3_8b_ppo", choices=wl.CONFIG_NAMES)
+    ap.add_argument("--tokens", type=int, default=None, help="override the batch size (tokens)")
+    ap.add_argument("--cpu-sample", type=int, default=256,
+                    help="tokens of the oracle's bounded CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+def flop_model(cfg, b):
+    """Algorithmic FLOPs of one step, per kernel family (no recompute, no padding)."""
+    d, f, L, V = cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.vocab
+    N = len(b["tokens"])
+    ranks = np.array(cfg.ranks)[b["adapter_ids"]]
+    sr = float(ranks.sum())                         # sum over tokens of r
+    base = 8.0 * N * d * f * L
+    lora_ext = 4.0 * sr * (d + f) * L               # expand in fwd + dgrad through A in bwd
+    lm = 4.0 * N * V * d                            # LM head forward + dh
+    small = 8.0 * sr * (d + f) * L                  # shrinks (fwd+bwd) and dA/dB reductions
+    return {"tc256": base + lora_ext + lm, "tc64": small, "total": base + lora_ext + lm + small,
+            "mean_rank": sr / max(1, N)}
+
+
+def adam_bytes(cfg, b):
+    present = np.unique(b["adapter_ids"])
+    n = sum(cfg.n_layers * 2 * cfg.ranks[a] * (cfg.d_model + cfg.d_ffn) for a in present)
+    return 28.0 * n, n
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import rl_step_gb300 as m
+    from rl_step_gb300 import _build
+
+    _build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = wl.get_config(args.config)
+    N_req = args.tokens or cfg.n_tokens
+    b = wl.make_batch(cfg, N_req)
+    N = len(b["tokens"])
+    base = wl.make_base_weights(cfg)
+    ad = wl.make_adapters(cfg)
+
+    def T(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(x).to(dev)
+
+    h = m.mlora_create(cfg.vocab, cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.dtype, cfg.ranks,
+                       cfg.alphas, N, T(base["E"]), [T(w) for w in base["W1"]],
+                       [T(w) for w in base["W2"]], T(base["Wout"]),
+                       *[[[T(x) for x in row] for row in ad[k]] for k in ("A1", "B1", "A2", "B2")])
+    torch.cuda.synchronize()
+    tok, tgt, ids = T(b["tokens"]), T(b["targets"]), T(b["adapter_ids"])
+    stream = torch.cuda.current_stream()
+    kind = cfg.loss
+    # sampler logprobs of the policy-gradient losses: the current policy's
+    # logprobs (one untimed forward) plus the workload's noise
+    s_dev = None
+    if kind in ("importance_sampling", "ppo"):
+        ell = m.mlora_forward(h, tok, tgt, ids)
+        s_dev = (ell + T(b["sampler_noise"])).contiguous()
+    w_dev, a_dev, g_dev = T(b["weights"]), T(b["advantages"]), T(b["dloss"])
+    lp_out = torch.empty(N, dtype=torch.float32, device=dev)
+    loss_out = torch.empty(cfg.n_adapters, dtype=torch.float64, device=dev)
+    skipped = torch.empty(cfg.n_adapters, dtype=torch.int32, device=dev)
+
+    def step(tk=tok, tg=tgt, ai=ids, w=w_dev, av=a_dev, sl=s_dev, gd=g_dev):
+        if kind == "custom":
+            m.mlora_forward_backward_custom(h, tk, tg, ai, gd, logprobs_out=lp_out, loss_out=loss_out)
+        else:
+            m.mlora_forward_backward(h, tk, tg, ai, kind, weights=w, advantages=av,
+                                     sampler_logprobs=sl, clip_eps=cfg.clip_eps,
+                                     logprobs_out=lp_out, loss_out=loss_out)
+        m.mlora_optim_step(h, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
+                           weight_decay=cfg.weight_decay, skipped_out=skipped)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = m.mlora_check_status(h)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # ---- device-timed region ------------------------------------------------
+    m.mlora_profile_read(h, reset=True)
+    m.mlora_profile_enable(h, True)
+    launches0 = h.kernel_launches
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    m.mlora_profile_enable(h, False)
+    launches = h.kernel_launches - launches0
+    prof = m.mlora_profile_read(h, reset=True)
+    ms = e0.elapsed_time(e1)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    status = m.mlora_check_status(h)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    # ---- end-to-end through host buffers -------------------------------------
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+        hs = {"tok": pin(b["tokens"]), "tgt": pin(b["targets"]), "ids": pin(b["adapter_ids"])}
+        dev_bufs = {k: torch.empty_like(v, device=dev) for k, v in hs.items()}
+        loss_in = {}
+        if kind == "cross_entropy":
+            loss_in["w"] = pin(b["weights"])
+        elif kind == "custom":
+            loss_in["g"] = pin(b["dloss"])
+        else:
+            loss_in["av"] = pin(b["advantages"])
+            loss_in["sl"] = s_dev.cpu().pin_memory()
+        dev_loss = {k: torch.empty_like(v, device=dev) for k, v in loss_in.items()}
+        lp_host = torch.empty(N, dtype=torch.float32).pin_memory()
+        loss_host = torch.empty(cfg.n_adapters, dtype=torch.float64).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in list(hs.values()) + list(loss_in.values()))
+        d2h = lp_host.numel() * 4 + loss_host.numel() * 8
+
+        def e2e_step():
+            for k, v in hs.items():
+                dev_bufs[k].copy_(v, non_blocking=True)
+            for k, v in loss_in.items():
+                dev_loss[k].copy_(v, non_blocking=True)
+            step(dev_bufs["tok"], dev_bufs["tgt"], dev_bufs["ids"], dev_loss.get("w", w_dev),
+                 dev_loss.get("av", a_dev), dev_loss.get("sl", s_dev), dev_loss.get("g", g_dev))
+            lp_host.copy_(lp_out, non_blocking=True)
+            loss_host.copy_(loss_out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": N * args.steps * world / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": 1e3 * t_e2e / args.steps}
+
+    # ---- derived numbers -----------------------------------------------------
+    peaks, peak_src = load_peaks()
+    fl = flop_model(cfg, b)
+    K = args.steps
+    tc_ms = sum(prof[c][0] for c in TC_CLASSES)
+    tc_launch = sum(prof[c][1] for c in TC_CLASSES)
+    achieved = fl["tc256"] * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    step_ms = ms_max / K
+    adam_b, n_ad_params = adam_bytes(cfg, b)
+    kernels = {c: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for c, v in prof.items()
+               if v[1] > 0}
+    if prof["adam"][0] > 0:
+        kernels["adam"]["achieved_gbs"] = adam_b * K / (prof["adam"][0] * 1e-3) / 1e9
+        kernels["adam"]["frac_of_hbm"] = kernels["adam"]["achieved_gbs"] / peaks["hbm_gbs"]
+    out = {
+        "metric": "trained tokens/sec per forward_backward+optim_step",
+        "value": N * K * world / (ms_max * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded), random-init weights",
+        "config": {"workload": cfg.description, "name": cfg.name, "tokens_per_gpu": N,
+                   "adapters": cfg.n_adapters, "loss": cfg.loss,
+                   "l2": "inputs larger than L2 (frozen base %.1f GB)" %
+                         ((2 * cfg.vocab * cfg.d_model + 2 * cfg.n_layers * cfg.d_model * cfg.d_ffn)
+                          * (2 if cfg.dtype == "bf16" else 4) / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "tflops_algorithmic": fl["total"] * K * world / (ms_max * 1e-3) / 1e12,
+        "frac_of_bf16_peak": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "roofline": {"kernel": "tc_gemm_kernel<256,4> (all base and LM-head GEMMs)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak_tc,
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
+                     "frac": (achieved / peak_tc) if achieved else None, "traffic": None,
+                     "launches_per_step": tc_launch / K},
+        "kernels": kernels,
+        "clocks": clk,
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+    }
+    return out, (cfg, base, ad, b)
+
+
+def oracle_sample_rate(cfg, base, ad, b, n_sample, s_full=None):
+    """Time the oracle's step on the first n_sample tokens; returns (tokens/s, seconds)."""
+    import oracle
+    o = oracle.Oracle(base, ad, cfg.ranks, cfg.alphas)
+    sl = slice(0, n_sample)
+    tok, tgt, ids = b["tokens"][sl], b["targets"][sl], b["adapter_ids"][sl]
+    kw = {}
+    if cfg.loss == "cross_entropy":
+        kw["weights"] = b["weights"][sl]
+    elif cfg.loss in ("importance_sampling", "ppo"):
+        ell = o.forward(tok, tgt, ids) if s_full is None else s_full[sl]
+        kw = {"advantages": b["advantages"][sl], "sampler_logprobs": ell + b["sampler_noise"][sl],
+              "clip_eps": cfg.clip_eps}
+    t0 = time.perf_counter()
+    if cfg.loss == "custom":
+        o.forward_backward_custom(tok, tgt, ids, b["dloss"][sl])
+    else:
+        o.forward_backward(tok, tgt, ids, cfg.loss, **kw)
+    o.optim_step(lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
+                 weight_decay=cfg.weight_decay)
+    dt = time.perf_counter() - t0
+    return n_sample / dt, dt
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed as it stands, on a bounded
+    sample of the same workload per step."""
+    cfg = wl.get_config(args.config)
+    b = wl.make_batch(cfg, args.tokens or cfg.n_tokens)
+    base = wl.make_base_weights(cfg)
+    ad = wl.make_adapters(cfg)
+    n = min(64, len(b["tokens"]))
+    for _ in range(args.warmup):
+        oracle_sample_rate(cfg, base, ad, b, n)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample_rate(cfg, base, ad, b, n)[1]
+    value = n * args.steps / total
+    return {
+        "metric": "trained tokens/sec per forward_backward+optim_step", "impl": "reference",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded), random-init weights",
+        "config": {"workload": cfg.description, "name": cfg.name,
+                   "tokens_per_step": n, "sample": f"first {n} tokens of the batch per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"{n} tokens per step at full widths (numpy fp64)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    out, ctx = run_ours(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cfg, base, ad, b = ctx
+        n = min(args.cpu_sample, len(b["tokens"]))
+        rate, dt = oracle_sample_rate(cfg, base, ad, b, n)
+        out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores(),
+                               "kind": "oracle",
+                               "sample": f"first {n} tokens of the batch, forward_backward + "
+                                         f"optim_step at full widths (numpy fp64, {dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

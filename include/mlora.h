@@ -226,6 +226,23 @@ int mlora_get_routing(mlora_t* h, const int32_t* adapter_ids, int64_t n, int32_t
  * MLORA_OK, MLORA_E_RANGE or MLORA_E_TIMEOUT. */
 int mlora_check_status(mlora_t* h, void* stream);
 
+/* Per-kernel-class timing for measurement.  While enabled, the library
+ * brackets each of its kernel launches with CUDA events recorded on the
+ * launch stream and tags it with one of the MLORA_PROF_* classes below.
+ * mlora_profile_read synchronises those events and returns, per class, the
+ * accumulated milliseconds and launch counts since the last reset
+ * (ms_out / launches_out: HOST arrays of MLORA_PROF_CLASSES entries).
+ * Enabling costs two event records per launch. */
+enum {
+    MLORA_PROF_ROUTING = 0, MLORA_PROF_EMBED = 1, MLORA_PROF_SHRINK = 2,
+    MLORA_PROF_W1_FWD = 3, MLORA_PROF_W2_FWD = 4, MLORA_PROF_LM_FWD = 5,
+    MLORA_PROF_LOSS = 6, MLORA_PROF_LM_DZ = 7, MLORA_PROF_LM_DH = 8,
+    MLORA_PROF_W2_BWD = 9, MLORA_PROF_W1_BWD = 10, MLORA_PROF_GRAD = 11,
+    MLORA_PROF_ADAM = 12, MLORA_PROF_OTHER = 13, MLORA_PROF_CLASSES = 14
+};
+int mlora_profile_enable(mlora_t* h, int32_t on);
+int mlora_profile_read(mlora_t* h, double* ms_out, int64_t* launches_out, int32_t reset);
+
 /* Number of kernels this handle has launched so far. */
 int64_t mlora_kernel_launches(const mlora_t* h);
 

@@ -29,7 +29,8 @@ __all__ = [
     "mlora_create", "mlora_destroy", "mlora_forward", "mlora_forward_backward",
     "mlora_forward_backward_custom", "mlora_optim_step", "mlora_save_state",
     "mlora_read_adapter", "mlora_write_adapter", "mlora_get_steps", "mlora_get_routing",
-    "mlora_check_status", "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
+    "mlora_check_status", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
+    "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlora.so")
@@ -39,6 +40,8 @@ LOSS_KINDS = {"cross_entropy": 0, "importance_sampling": 1, "ppo": 2}
 TENSOR_IDS = {n: i for i, n in enumerate(
     ["A1", "B1", "A2", "B2", "gA1", "gB1", "gA2", "gB2",
      "mA1", "mB1", "mA2", "mB2", "vA1", "vB1", "vA2", "vB2"])}
+PROF_CLASSES = ["routing", "embed", "shrink", "w1_fwd", "w2_fwd", "lm_fwd", "loss", "lm_dz",
+                "lm_dh", "w2_bwd", "w1_bwd", "grad", "adam", "other"]
 _ERRORS = {-1: "E_ARG", -2: "E_RANGE", -3: "E_CUDA", -4: "E_NOMEM", -5: "E_TIMEOUT",
            -6: "E_IO", -7: "E_UNSUPPORTED"}
 
@@ -94,6 +97,8 @@ _SIGNATURES = {
     "mlora_get_routing": (c_int32, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p]),
     "mlora_check_status": (c_int32, [c_void_p, c_void_p]),
+    "mlora_profile_enable": (c_int32, [c_void_p, c_int32]),
+    "mlora_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_kernel_launches": (c_int64, [c_void_p]),
     "mlora_device_bytes": (c_int64, [c_void_p]),
     "mlora_last_error": (c_char_p, []),
@@ -304,3 +309,16 @@ def mlora_get_routing(h: Handle, adapter_ids, stream=None):
 def mlora_check_status(h: Handle, stream=None) -> int:
     """Synchronise and return the device status code (0, -2 E_RANGE, -5 E_TIMEOUT)."""
     return int(_lib.mlora_check_status(h.ptr, _stream(stream)))
+
+
+def mlora_profile_enable(h: Handle, on: bool = True):
+    _check(_lib.mlora_profile_enable(h.ptr, 1 if on else 0))
+
+
+def mlora_profile_read(h: Handle, reset: bool = True) -> dict:
+    """{class: (milliseconds, launches)} accumulated since the last reset."""
+    n = len(PROF_CLASSES)
+    ms = (c_double * n)()
+    cnt = (c_int64 * n)()
+    _check(_lib.mlora_profile_read(h.ptr, ms, cnt, 1 if reset else 0))
+    return {PROF_CLASSES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}

@@ -85,6 +85,39 @@ struct mlora {
     void* dz = nullptr;
     double* loss_tile = nullptr;
     int* status = nullptr;
+    // measurement: events around launches
+    bool prof = false;
+    std::vector<cudaEvent_t> ev;      // pairs (start, stop)
+    std::vector<int> ev_cls;
+    size_t ev_used = 0;
+    double prof_ms[MLORA_PROF_CLASSES] = {0};
+    int64_t prof_n[MLORA_PROF_CLASSES] = {0};
+};
+
+// Brackets one launch with events when profiling is on.
+struct ProfScope {
+    mlora_t* h;
+    cudaStream_t s;
+    int cls;
+    size_t slot = (size_t)-1;
+    ProfScope(mlora_t* h_, cudaStream_t s_, int cls_) : h(h_), s(s_), cls(cls_) {
+        if (!h->prof) return;
+        if (h->ev_used * 2 + 2 > h->ev.size()) {
+            for (int i = 0; i < 64; ++i) {
+                cudaEvent_t e;
+                if (cudaEventCreate(&e) != cudaSuccess) return;
+                h->ev.push_back(e);
+            }
+            h->ev_cls.resize(h->ev.size() / 2);
+        }
+        slot = h->ev_used++;
+        cudaEventRecord(h->ev[2 * slot], s);
+    }
+    ~ProfScope() {
+        if (slot == (size_t)-1) return;
+        cudaEventRecord(h->ev[2 * slot + 1], s);
+        h->ev_cls[slot] = cls;
+    }
 };
 
 static int dalloc(mlora_t* h, void** p, size_t bytes) {
@@ -111,6 +144,8 @@ static int dalloc_t(mlora_t* h, P** p, size_t count) {
 static void free_all(mlora_t* h) {
     for (void* p : h->allocs) cudaFree(p);
     h->allocs.clear();
+    for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
+    h->ev.clear();
 }
 
 static inline int64_t tensor_size(int k, int r, int d, int f) {
@@ -182,8 +217,13 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
     h->esize = cfg->dtype == MLORA_BF16 ? 2 : 4;
     h->ranks.assign(cfg->ranks, cfg->ranks + cfg->n_adapters);
     h->alphas.assign(cfg->alphas, cfg->alphas + cfg->n_adapters);
-    h->use_tc = (cfg->dtype == MLORA_BF16) && prop.major == 10 && getenv("MLORA_ENABLE_TC") != nullptr &&
-                tc_engine_available();
+    // bf16 runs on the tcgen05 engine only (sm_100 family); fp32 on the FFMA engine.
+    h->use_tc = cfg->dtype == MLORA_BF16;
+    if (h->use_tc && (prop.major != 10 || !tc_engine_available())) {
+        delete h;
+        return fail(MLORA_E_UNSUPPORTED, "a bf16 handle needs an sm_100-family GPU with TMA "
+                    "(found compute capability %d.%d)", prop.major, prop.minor);
+    }
     h->Vpad = (h->V + 63) / 64 * 64;
     h->lm_bn = h->use_tc ? 256 : 32;
     h->n_nt = (h->V + h->lm_bn - 1) / h->lm_bn;
@@ -263,6 +303,10 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOC(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 64 ? h->max_tiles : 64;   // 8192-row chunks
         ALLOCB(h->dz, (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
+        if (cudaMemset(h->dz, 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
+            rc = fail(MLORA_E_CUDA, "cudaMemset of the dz chunk buffer failed");
+            goto fail_out;
+        }
         ALLOC(h->loss_tile, h->max_tiles);
         ALLOC(h->status, 1);
     }
@@ -354,7 +398,8 @@ static GemmOperand op_mnmajor(const void* p, int64_t rows, int64_t cols, int64_t
 }
 
 template <typename T>
-static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s) {
+static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s, int cls) {
+    ProfScope ps(h, s, cls);
     if (h->use_tc) {
         cudaError_t e = launch_tc_gemm(p, s, h->num_sms, h->status);
         if (e != cudaSuccess) return fail(MLORA_E_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(e));
@@ -417,13 +462,19 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         return MLORA_OK;
     }
     // a1 routing
-    launch_routing(b->adapter_ids, N, n_ad, h->rb, backward ? h->touched : nullptr, h->status, s,
-                   &h->launches);
+    {
+        ProfScope ps(h, s, MLORA_PROF_ROUTING);
+        launch_routing(b->adapter_ids, N, n_ad, h->rb, backward ? h->touched : nullptr, h->status, s,
+                       &h->launches);
+    }
     // a2 embedding
-    launch_embed<T>(h->rb.perm_pad, h->rb.meta, mp, b->tokens, b->targets,
-                    reinterpret_cast<const T*>(h->E), V, d, reinterpret_cast<T*>(h->hb[0]), h->h32,
-                    h->tgt_pad, h->status, s);
-    ++h->launches;
+    {
+        ProfScope ps(h, s, MLORA_PROF_EMBED);
+        launch_embed<T>(h->rb.perm_pad, h->rb.meta, mp, b->tokens, b->targets,
+                        reinterpret_cast<const T*>(h->E), V, d, reinterpret_cast<T*>(h->hb[0]), h->h32,
+                        h->tgt_pad, h->status, s);
+        ++h->launches;
+    }
 
     // a3-a5 layers
     for (int l = 0; l < L; ++l) {
@@ -432,7 +483,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.A = op_kmajor(h->hb[l], MP, d);
             p.B = op_kmajor(h->shadow.A1[l], (int64_t)n_ad * RP, d, RP);
             p.ep.kind = EPI_SHRINK; p.ep.out0 = h->v1s[l]; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // u = W1 h + B1_a v1s ; act = silu(u)
             GemmParams p = dense_params(h, mt_upper, f, d);
@@ -442,14 +493,14 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->v1s[l], MP, RP);
             p.Bx = op_kmajor(h->shadow.B1[l], (int64_t)n_ad * f, RP, f);
             p.ep.kind = EPI_SILU; p.ep.out0 = h->ub[l]; p.ep.ld0 = f; p.ep.out1 = h->actb[l]; p.ep.ld1 = f;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // v2s = gamma * A2_a act
             GemmParams p = dense_params(h, mt_upper, RP, f);
             p.A = op_kmajor(h->actb[l], MP, f);
             p.B = op_kmajor(h->shadow.A2[l], (int64_t)n_ad * RP, f, RP);
             p.ep.kind = EPI_SHRINK; p.ep.out0 = h->v2s[l]; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // h += W2 act + B2_a v2s
             GemmParams p = dense_params(h, mt_upper, d, f);
@@ -459,7 +510,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->v2s[l], MP, RP);
             p.Bx = op_kmajor(h->shadow.B2[l], (int64_t)n_ad * d, RP, d);
             p.ep.kind = EPI_RESID; p.ep.f32 = h->h32; p.ep.ldf = d; p.ep.out0 = h->hb[l + 1]; p.ep.ld0 = d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
     }
     // a6 LM head: per-tile (max, sum exp) and the target logit
@@ -470,13 +521,17 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         p.group_m = 64;
         p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
         p.ep.n_ntiles = h->n_nt; p.ep.V = V; p.ep.Vpad = h->Vpad;
-        if ((rc = run_gemm<T>(h, p, s))) return rc;
+        if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
     }
     // a7 combine + loss epilogue
-    launch_combine_loss(la, h->part, h->n_nt, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
-                        logprobs_out, h->lse, h->gvec, h->loss_tile, s);
-    ++h->launches;
+    {
+        ProfScope ps(h, s, MLORA_PROF_LOSS);
+        launch_combine_loss(la, h->part, h->n_nt, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
+                            logprobs_out, h->lse, h->gvec, h->loss_tile, s);
+        ++h->launches;
+    }
     if (loss_out) {
+        ProfScope ps(h, s, MLORA_PROF_OTHER);
         launch_loss_reduce(h->loss_tile, h->rb.pad_off, n_ad, loss_out, s);
         ++h->launches;
     }
@@ -486,7 +541,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     for (int c0 = 0; c0 < mt_upper; c0 += h->nc_tiles) {
         int cnt = mt_upper - c0 < h->nc_tiles ? mt_upper - c0 : h->nc_tiles;
         {
-            GemmParams p = dense_params(h, mt_upper, V, d);
+            GemmParams p = dense_params(h, mt_upper, h->Vpad, d);
             p.mt_base = c0; p.mt_count = cnt;
             p.A = op_kmajor(h->hb[L], MP, d);
             p.B = op_kmajor(h->Wout, V, d);
@@ -494,7 +549,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
             p.ep.tgt = h->tgt_pad; p.ep.V = V; p.ep.Vpad = h->Vpad;
             p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
         }
         {
             GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
@@ -502,7 +557,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.A = op_kmajor(h->dz, (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
             p.B = op_mnmajor(h->Wout, V, d);
             p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH))) return rc;
         }
     }
     // a9-a11 layers in reverse
@@ -512,7 +567,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.A = op_kmajor(h->dhb, MP, d);
             p.B = op_mnmajor(h->shadow.B2[l], (int64_t)n_ad * d, RP, d);
             p.ep.kind = EPI_SHRINK; p.ep.out0 = h->w2s; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // du = (W2^T dh + A2_a^T w2s) * silu'(u)
             GemmParams p = dense_params(h, mt_upper, f, d);
@@ -522,22 +577,22 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->w2s, MP, RP);
             p.Bx = op_mnmajor(h->shadow.A2[l], (int64_t)n_ad * RP, f, RP);
             p.ep.kind = EPI_DSILU; p.ep.aux = h->ub[l]; p.ep.ld_aux = f; p.ep.out0 = h->dub; p.ep.ld0 = f;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W2_BWD))) return rc;
         }
         {   // dB2_a += dh^T v2s   [d x r]
             GemmParams p = grad_params(h, mp, d, h->dhb, h->v2s[l], l, 3, 0);
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // dA2_a += w2s^T act  [r x f], computed as act^T w2s
             GemmParams p = grad_params(h, mp, f, h->actb[l], h->w2s, l, 2, 1);
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_GRAD))) return rc;
         }
         {   // w1s = gamma * B1_a^T du
             GemmParams p = dense_params(h, mt_upper, RP, f);
             p.A = op_kmajor(h->dub, MP, f);
             p.B = op_mnmajor(h->shadow.B1[l], (int64_t)n_ad * f, RP, f);
             p.ep.kind = EPI_SHRINK; p.ep.out0 = h->w1s; p.ep.ld0 = RP; p.ep.gamma = h->gamma_d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // dh += W1^T du + A1_a^T w1s
             GemmParams p = dense_params(h, mt_upper, d, f);
@@ -547,15 +602,15 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->w1s, MP, RP);
             p.Bx = op_mnmajor(h->shadow.A1[l], (int64_t)n_ad * RP, d, RP);
             p.ep.kind = EPI_RESID; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W1_BWD))) return rc;
         }
         {   // dB1_a += du^T v1s   [f x r]
             GemmParams p = grad_params(h, mp, f, h->dub, h->v1s[l], l, 1, 0);
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
         }
         {   // dA1_a += w1s^T h    [r x d], computed as h^T w1s
             GemmParams p = grad_params(h, mp, d, h->hb[l], h->w1s, l, 0, 1);
-            if ((rc = run_gemm<T>(h, p, s))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_GRAD))) return rc;
         }
     }
     return MLORA_OK;
@@ -640,9 +695,13 @@ extern "C" int mlora_optim_step(mlora_t* h, const mlora_adam* p, const int32_t* 
         CUDA_TRY(cudaStreamSynchronize(s));   // the host vector goes out of scope
         sel = h->sel_mask;
     }
-    launch_adam_prep(h->n_ad, sel, h->touched, h->nonfinite, h->step, p->beta1, p->beta2, h->adam_tab,
-                     skipped_out, s);
-    ++h->launches;
+    {
+        ProfScope ps(h, s, MLORA_PROF_OTHER);
+        launch_adam_prep(h->n_ad, sel, h->touched, h->nonfinite, h->step, p->beta1, p->beta2, h->adam_tab,
+                         skipped_out, s);
+        ++h->launches;
+    }
+    ProfScope ps_adam(h, s, MLORA_PROF_ADAM);
     if (h->dtype == MLORA_BF16)
         launch_adam<bf16>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->adam_tab, h->P,
                           h->G, h->M, h->Vm, p->lr, p->beta1, p->beta2, p->eps, p->weight_decay, h->shadow, s);
@@ -770,5 +829,31 @@ extern "C" int mlora_save_state(mlora_t* h, const char* path, void* stream) {
     }
     ok = (fclose(fh) == 0) && ok;
     if (!ok) return fail(MLORA_E_IO, "write to %s failed", path);
+    return MLORA_OK;
+}
+
+extern "C" int mlora_profile_enable(mlora_t* h, int32_t on) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    h->prof = on != 0;
+    return MLORA_OK;
+}
+
+extern "C" int mlora_profile_read(mlora_t* h, double* ms_out, int64_t* launches_out, int32_t reset) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    for (size_t i = 0; i < h->ev_used; ++i) {
+        CUDA_TRY(cudaEventSynchronize(h->ev[2 * i + 1]));
+        float ms = 0.f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]));
+        int c = h->ev_cls[i];
+        if (c < 0 || c >= MLORA_PROF_CLASSES) c = MLORA_PROF_OTHER;
+        h->prof_ms[c] += ms;
+        h->prof_n[c] += 1;
+    }
+    h->ev_used = 0;
+    for (int c = 0; c < MLORA_PROF_CLASSES; ++c) {
+        if (ms_out) ms_out[c] = h->prof_ms[c];
+        if (launches_out) launches_out[c] = h->prof_n[c];
+        if (reset) { h->prof_ms[c] = 0.0; h->prof_n[c] = 0; }
+    }
     return MLORA_OK;
 }
