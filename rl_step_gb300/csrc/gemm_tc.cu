@@ -146,6 +146,67 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- CTA pairs (cta_group::2) ------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same smem offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// TMA load whose completion is counted on the leader CTA's barrier (cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on the barrier at this smem offset in both CTAs of the pair when the MMAs finish
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2).
 //   K-major tile: rows of 64 bf16 (128 B), 8-row groups 1024 B apart (SBO).
 //   MN-major tile: 64-element MN blocks LBO bytes apart, 8-row K groups
@@ -160,10 +221,10 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M=128, N=n.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n, int a_mn, int b_mn) {
+// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, M=m, N=n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, int a_mn, int b_mn, int m = BM) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 struct TcMaps {
@@ -449,6 +510,265 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---- CTA-pair kernel: 256 x BN tiles with tcgen05.mma.cta_group::2 ---------
+//
+// A cluster of two CTAs on two SMs computes one 256-row x BN tile.  Each CTA
+// stages its own 128 rows of A and half of the B tile (BN/2 rows); the MMA
+// issued by the leader (cluster rank 0) reads both CTAs' shared memory and
+// writes rows 0-127 of the accumulator into the leader's TMEM and rows
+// 128-255 into the peer's.  Both CTAs' TMA loads complete on the leader's
+// "full" barrier; the leader's MMA commits arrive on the "empty" and "tmem
+// full" barriers of both CTAs (multicast); both CTAs' epilogue warps release
+// the accumulator on the leader's "tmem empty" barrier.  Used for GEMMs whose
+// B operand is shared by all rows (the LM head); the per-adapter GEMMs keep
+// the single-CTA kernel.
+template <int BN, int STAGES, int NUM_ACC>
+struct SmemLayoutPair {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = (BN / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = TILES_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int TOTAL = MISC_OFF + 16 + 1024;
+};
+
+struct PairCoord {
+    int mt;       // first global m-tile of the pair
+    int nt;
+    int k0, nkb;
+};
+
+template <int BN>
+__device__ __forceinline__ int pair_mcount(const GemmParams& p) {
+    int nmt = p.mtiles_dev ? *p.mtiles_dev : (p.M + BM - 1) / BM;
+    int cnt = nmt - p.mt_base;
+    if (cnt > p.mt_count) cnt = p.mt_count;
+    return cnt < 0 ? 0 : cnt;
+}
+
+template <int BN>
+__device__ __forceinline__ PairCoord pair_coord(const GemmParams& p, int t, int cnt) {
+    PairCoord c;
+    const int n_nt = (p.N + BN - 1) / BN;
+    const int pairs = (cnt + 1) / 2;
+    int G = p.group_m / 2;
+    if (G < 1) G = 1;
+    const int band = t / (G * n_nt);
+    const int r = t - band * G * n_nt;
+    int bm = pairs - band * G;
+    if (bm > G) bm = G;
+    c.mt = p.mt_base + 2 * (band * G + r % bm);
+    c.nt = r / bm;
+    c.k0 = 0;
+    c.nkb = (p.K + BK - 1) / BK;
+    return c;
+}
+
+template <int BN, int STAGES, int NUM_ACC>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + SL::BAR_OFF;
+    const uint32_t bar_empty = bar_full + STAGES * 8;
+    const uint32_t bar_tfull = bar_empty + STAGES * 8;
+    const uint32_t bar_tempty = bar_tfull + NUM_ACC * 8;
+    const uint32_t bar_drain = bar_tempty + NUM_ACC * 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC_OFF + 4);
+    constexpr uint32_t TMEM_COLS = NUM_ACC * BN;
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < NUM_ACC; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, 8);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tma_prefetch_desc(&maps.A);
+        tma_prefetch_desc(&maps.B);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (dbg && threadIdx.x == 0) dbg[blockIdx.x] = (int)tmem_base;
+
+    const int cnt = pair_mcount<BN>(p);
+    const int n_nt = (p.N + BN - 1) / BN;
+    const int ntiles = ((cnt + 1) / 2) * n_nt;
+    const int cid = blockIdx.x >> 1;
+    const int ncl = gridDim.x >> 1;
+    const uint32_t full_leader = map_to_rank(bar_full, 0);
+    const uint32_t tempty_leader = map_to_rank(bar_tempty, 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producers (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+            bool ok = true;
+            for (int t = cid; t < ntiles && ok; t += ncl) {
+                const PairCoord c = pair_coord<BN>(p, t, cnt);
+                const int m0 = (c.mt + (int)rank) * BM;
+                const int n0 = c.nt * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < c.nkb; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
+                    const uint32_t fb = full_leader + 8 * stage;
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+                    const int k = c.k0 + kb * BK;
+                    if (!p.A.mn_major) {
+                        tma_load_2d_pair(sa, &maps.A, fb, k, (int)(m0 + p.A.row_shift));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BM / 64; ++i)
+                            tma_load_2d_pair(sa + i * 8192, &maps.A, fb, m0 + 64 * i, (int)(k + p.A.row_shift));
+                    }
+                    const int brow = (int)p.B.row_shift;
+                    if (!p.B.mn_major) {
+                        tma_load_2d_pair(sb, &maps.B, fb, k, brow + n0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BN / 128; ++i)
+                            tma_load_2d_pair(sb + i * 8192, &maps.B, fb, n0 + 64 * i, brow + k);
+                    }
+                    issued[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                atomicOr(status, ST_TIMEOUT);
+                *abort_flag = 1;
+            }
+            if (leader) {
+                // the pair's copies of every issued stage have landed (counted here)
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued[s] >= 0) {
+                        int dummy = 0;
+                        if (!mbar_wait(bar_full + 8 * s, (uint32_t)issued[s], (volatile int*)&dummy))
+                            atomicOr(status, ST_TIMEOUT);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA (leader)
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
+            for (int t = cid; t < ntiles && ok; t += ncl) {
+                const PairCoord c = pair_coord<BN>(p, t, cnt);
+                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < c.nkb; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = p.A.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
+                                                         : sdesc(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = p.B.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
+                                                         : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(bar_empty + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(bar_tfull + 8 * acc);
+                if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (!ok) {
+                atomicOr(status, ST_TIMEOUT);
+                *abort_flag = 1;
+            }
+            umma_commit_pair(bar_drain);
+            int dummy = 0;
+            if (!mbar_wait(bar_drain, 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = cid; t < ntiles; t += ncl) {
+            const PairCoord c = pair_coord<BN>(p, t, cnt);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+                break;
+            }
+            tc_fence_after();
+            const int my_mt = c.mt + (int)rank;
+            const bool tile_ok = (my_mt - p.mt_base) < cnt;
+            const int64_t row = (int64_t)my_mt * BM + 32 * q + lane;
+            EpiRowState st;
+            epi_row_begin(st);
+            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ch * 32, r);
+                tmem_ld_wait();
+                const int col0 = c.nt * BN + ch * 32;
+                if (tile_ok && col0 < p.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    epi_chunk<bf16>(p.ep, row, col0, 0, v, st);
+                }
+            }
+            if (tile_ok) epi_row_end(p.ep, row, c.nt, st);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(bar_tempty + 8 * acc);
+                else mbar_arrive_cluster(tempty_leader + 8 * acc);
+            }
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
 // ---- host ------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -515,13 +835,67 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
     return cudaGetLastError();
 }
 
+template <int BN, int STAGES, int NUM_ACC>
+cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status, int* dbg) {
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC>;
+    TcMaps maps;
+    auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
+        if (!operand_ok(op)) return false;
+        if (op.mn_major) return encode_2d(m, op, 64, 64);
+        return encode_2d(m, op, 64, (uint32_t)rows_mn);
+    };
+    if (p.grouped || p.Kx > 0 || p.B.ad_rows != 0) return cudaErrorInvalidValue;
+    if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN / 2)) return cudaErrorInvalidValue;
+    maps.Ax = maps.A;
+    maps.Bx = maps.B;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int n_nt = (p.N + BN - 1) / BN;
+    const int64_t upper = (int64_t)((p.mt_count + 1) / 2) * n_nt;
+    if (upper <= 0) return cudaSuccess;
+    int nclusters = num_sms / 2;
+    if (upper < nclusters) nclusters = (int)upper;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * nclusters, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SL::TOTAL;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>, maps, p, status, dbg);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+// CTA-pair variants (exposed for the engine's own checks): acc_buffers = 1 or 2.
+cudaError_t launch_tc_gemm_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status,
+                                int acc_buffers, int* dbg) {
+    if (!get_encode()) return cudaErrorNotSupported;
+    if (p.N < 256) return cudaErrorInvalidValue;
+    if (acc_buffers == 1) return launch_pair<256, 6, 1>(p, s, num_sms, status, dbg);
+    return launch_pair<256, 6, 2>(p, s, num_sms, status, dbg);
+}
 
 bool tc_engine_available() { return get_encode(); }
 
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
     if (!get_encode()) return cudaErrorNotSupported;
     if (p.N <= 64) return launch_bn<64, 8>(p, s, num_sms, status);
+    // B shared by every row and no K extension: 256 x 256 tiles on CTA pairs
+    if (!p.grouped && p.Kx == 0 && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256)
+        return launch_pair<256, 6, 2>(p, s, num_sms, status, nullptr);
     return launch_bn<256, 4>(p, s, num_sms, status);
 }
 

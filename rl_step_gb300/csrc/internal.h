@@ -13,6 +13,9 @@ template <typename T> void launch_simt_gemm(const GemmParams& p, cudaStream_t s)
 // tcgen05 engine (bf16 only).  Returns cudaSuccess or the first error.
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status);
 bool tc_engine_available();
+// CTA-pair (cta_group::2) variant for GEMMs whose B is shared by all rows.
+cudaError_t launch_tc_gemm_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status,
+                                int acc_buffers, int* dbg);
 
 // ---- routing ----------------------------------------------------------------
 struct RouteBufs {
@@ -76,5 +79,8 @@ void launch_adam(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d
 template <typename T>
 void launch_shadow_sync(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d, int f,
                         int64_t total, const float* P, const ShadowMap& sh, cudaStream_t s);
+
+template <typename T>
+void launch_transpose(const T* in, T* out, int rows, int cols, cudaStream_t s);
 
 }  // namespace mlk

@@ -379,4 +379,31 @@ template void launch_shadow_sync<float>(int, const int64_t*, const int*, int, in
 template void launch_shadow_sync<bf16>(int, const int64_t*, const int*, int, int, int, int64_t,
                                        const float*, const ShadowMap&, cudaStream_t);
 
+// ----------------------------------------------------------------------------
+// out[c][r] = in[r][c] for a rows x cols matrix (32 x 32 tiles through smem).
+// Used once at create to give the backward GEMMs K-major copies of W1, W2.
+// ----------------------------------------------------------------------------
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int rows, int cols) {
+    __shared__ T tile[32][33];
+    const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        int r = by + i, c = bx + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = in[(int64_t)r * cols + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        int c = bx + i, r = by + threadIdx.x;
+        if (c < cols && r < rows) out[(int64_t)c * rows + r] = tile[threadIdx.x][i];
+    }
+}
+
+template <typename T>
+void launch_transpose(const T* in, T* out, int rows, int cols, cudaStream_t s) {
+    dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+    transpose_kernel<T><<<grid, dim3(32, 8), 0, s>>>(in, out, rows, cols);
+}
+template void launch_transpose<float>(const float*, float*, int, int, cudaStream_t);
+template void launch_transpose<bf16>(const bf16*, bf16*, int, int, cudaStream_t);
+
 }  // namespace mlk

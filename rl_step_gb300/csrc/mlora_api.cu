@@ -58,6 +58,7 @@ struct mlora {
     void* E = nullptr;
     void* Wout = nullptr;
     std::vector<void*> W1, W2;
+    std::vector<void*> W1T, W2T;        // K-major copies for the backward GEMMs
     // adapters
     int64_t n_params = 0;
     std::vector<int64_t> ad_off_h;      // [n_ad + 1]
@@ -243,10 +244,12 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         // base
         ALLOCB(h->E, (size_t)V * d * es);
         ALLOCB(h->Wout, (size_t)V * d * es);
-        h->W1.resize(L); h->W2.resize(L);
+        h->W1.resize(L); h->W2.resize(L); h->W1T.resize(L); h->W2T.resize(L);
         for (int l = 0; l < L; ++l) {
             ALLOCB(h->W1[l], (size_t)f * d * es);
             ALLOCB(h->W2[l], (size_t)d * f * es);
+            ALLOCB(h->W1T[l], (size_t)d * f * es);
+            ALLOCB(h->W2T[l], (size_t)f * d * es);
         }
         // adapters
         h->ad_off_h.resize(n_ad + 1);
@@ -320,6 +323,14 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         for (int l = 0; l < L; ++l) {
             CUDA_TRY(cudaMemcpyAsync(h->W1[l], init->W1[l], (size_t)f * d * es, cudaMemcpyDeviceToDevice, s));
             CUDA_TRY(cudaMemcpyAsync(h->W2[l], init->W2[l], (size_t)d * f * es, cudaMemcpyDeviceToDevice, s));
+            if (h->dtype == MLORA_BF16) {
+                launch_transpose<bf16>(reinterpret_cast<const bf16*>(h->W1[l]), reinterpret_cast<bf16*>(h->W1T[l]), f, d, s);
+                launch_transpose<bf16>(reinterpret_cast<const bf16*>(h->W2[l]), reinterpret_cast<bf16*>(h->W2T[l]), d, f, s);
+            } else {
+                launch_transpose<float>(reinterpret_cast<const float*>(h->W1[l]), reinterpret_cast<float*>(h->W1T[l]), f, d, s);
+                launch_transpose<float>(reinterpret_cast<const float*>(h->W2[l]), reinterpret_cast<float*>(h->W2T[l]), d, f, s);
+            }
+            h->launches += 2;
         }
         // adapters
         CUDA_TRY(cudaMemsetAsync(h->P, 0, sizeof(float) * h->n_params, s));
@@ -493,7 +504,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->v1s[l], MP, RP);
             p.Bx = op_kmajor(h->shadow.B1[l], (int64_t)n_ad * f, RP, f);
             p.ep.kind = EPI_SILU; p.ep.out0 = h->ub[l]; p.ep.ld0 = f; p.ep.out1 = h->actb[l]; p.ep.ld1 = f;
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W1_FWD))) return rc;
         }
         {   // v2s = gamma * A2_a act
             GemmParams p = dense_params(h, mt_upper, RP, f);
@@ -510,7 +521,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.Ax = op_kmajor(h->v2s[l], MP, RP);
             p.Bx = op_kmajor(h->shadow.B2[l], (int64_t)n_ad * d, RP, d);
             p.ep.kind = EPI_RESID; p.ep.f32 = h->h32; p.ep.ldf = d; p.ep.out0 = h->hb[l + 1]; p.ep.ld0 = d;
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W2_FWD))) return rc;
         }
     }
     // a6 LM head: per-tile (max, sum exp) and the target logit
@@ -572,7 +583,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         {   // du = (W2^T dh + A2_a^T w2s) * silu'(u)
             GemmParams p = dense_params(h, mt_upper, f, d);
             p.A = op_kmajor(h->dhb, MP, d);
-            p.B = op_mnmajor(h->W2[l], d, f);
+            p.B = op_kmajor(h->W2T[l], f, d);
             p.Kx = RP;
             p.Ax = op_kmajor(h->w2s, MP, RP);
             p.Bx = op_mnmajor(h->shadow.A2[l], (int64_t)n_ad * RP, f, RP);
@@ -581,7 +592,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         }
         {   // dB2_a += dh^T v2s   [d x r]
             GemmParams p = grad_params(h, mp, d, h->dhb, h->v2s[l], l, 3, 0);
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_GRAD))) return rc;
         }
         {   // dA2_a += w2s^T act  [r x f], computed as act^T w2s
             GemmParams p = grad_params(h, mp, f, h->actb[l], h->w2s, l, 2, 1);
@@ -597,7 +608,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         {   // dh += W1^T du + A1_a^T w1s
             GemmParams p = dense_params(h, mt_upper, d, f);
             p.A = op_kmajor(h->dub, MP, f);
-            p.B = op_mnmajor(h->W1[l], f, d);
+            p.B = op_kmajor(h->W1T[l], d, f);
             p.Kx = RP;
             p.Ax = op_kmajor(h->w1s, MP, RP);
             p.Bx = op_mnmajor(h->shadow.A1[l], (int64_t)n_ad * RP, d, RP);
@@ -606,7 +617,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         }
         {   // dB1_a += du^T v1s   [f x r]
             GemmParams p = grad_params(h, mp, f, h->dub, h->v1s[l], l, 1, 0);
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_SHRINK))) return rc;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_GRAD))) return rc;
         }
         {   // dA1_a += w1s^T h    [r x d], computed as h^T w1s
             GemmParams p = grad_params(h, mp, d, h->hb[l], h->w1s, l, 0, 1);
