@@ -222,6 +222,30 @@ int mlora_get_steps(mlora_t* h, int64_t* steps_out, void* stream);
 int mlora_get_routing(mlora_t* h, const int32_t* adapter_ids, int64_t n, int32_t* perm,
                       int32_t* seg_off, int32_t* pad_off, int32_t* tile_ad, void* stream);
 
+/* Routing without allocation.  The same stable grouping as
+ * mlora_get_routing (same outputs, same layout, same -1 tail of tile_ad), but
+ * with no handle and no device allocation of any kind: for callers that
+ * cannot call cudaMalloc -- their device memory is owned by another
+ * allocator, or their loop must not pay for cudaMalloc's possible device
+ * synchronisation.  The pages have no counterpart of this entry point; it
+ * exists for such embedders.
+ *   adapter_ids: DEVICE int32 [n]; n <= MLORA_NOALLOC_MAX_TOKENS
+ *   n_adapters:  1 .. MLORA_NOALLOC_MAX_ADAPTERS
+ *   perm, seg_off, pad_off, tile_ad: DEVICE int32 outputs sized as for
+ *   mlora_get_routing.
+ * Scratch lives in a fixed array inside the library (about 0.6 MB per GPU,
+ * held until the process exits).  The first call on a device resolves that
+ * array's device address (cudaGetSymbolAddress) with the device current.
+ * All calls share the array: calls whose GPU work may overlap race and must
+ * be ordered by the caller.  Ids out of range are left out, as in
+ * mlora_get_routing, but are not reported (there is no handle status word).
+ * Errors: E_ARG for sizes beyond the limits or NULL pointers, E_CUDA. */
+#define MLORA_NOALLOC_MAX_TOKENS 65536
+#define MLORA_NOALLOC_MAX_ADAPTERS 128
+int mlora_routing_noalloc(const int32_t* adapter_ids, int64_t n, int32_t n_adapters,
+                          int32_t* perm, int32_t* seg_off, int32_t* pad_off, int32_t* tile_ad,
+                          void* stream);
+
 /* Synchronise `stream`, then return and clear the device status word:
  * MLORA_OK, MLORA_E_RANGE or MLORA_E_TIMEOUT. */
 int mlora_check_status(mlora_t* h, void* stream);

@@ -29,7 +29,7 @@ __all__ = [
     "mlora_create", "mlora_destroy", "mlora_forward", "mlora_forward_backward",
     "mlora_forward_backward_custom", "mlora_optim_step", "mlora_save_state",
     "mlora_read_adapter", "mlora_write_adapter", "mlora_get_steps", "mlora_get_routing",
-    "mlora_check_status", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
+    "mlora_check_status", "mlora_routing_noalloc", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
     "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
 ]
 
@@ -97,6 +97,8 @@ _SIGNATURES = {
     "mlora_get_routing": (c_int32, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p]),
     "mlora_check_status": (c_int32, [c_void_p, c_void_p]),
+    "mlora_routing_noalloc": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p]),
     "mlora_profile_enable": (c_int32, [c_void_p, c_int32]),
     "mlora_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_kernel_launches": (c_int64, [c_void_p]),
@@ -303,6 +305,27 @@ def mlora_get_routing(h: Handle, adapter_ids, stream=None):
     tiles = torch.empty(n // TILE_M + h.n_adapters + 1, dtype=torch.int32, device=dev)
     _check(_lib.mlora_get_routing(h.ptr, _ptr(adapter_ids), n, _ptr(perm), _ptr(seg), _ptr(pad),
                                   _ptr(tiles), _stream(stream)))
+    return perm[:n], seg, pad, tiles
+
+
+def mlora_routing_noalloc(adapter_ids, n_adapters: int, stream=None):
+    """Routing with no handle and no device allocation by the library.
+
+    For callers that cannot call cudaMalloc; the library keeps its scratch in
+    a fixed device array.  The output tensors here are allocated by torch on
+    the caller's side.  Returns (perm, seg_off, pad_off, tile_ad) like
+    mlora_get_routing.
+    """
+    import torch
+    load_library()
+    n = int(adapter_ids.numel())
+    dev = adapter_ids.device
+    perm = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+    seg = torch.empty(n_adapters + 1, dtype=torch.int32, device=dev)
+    pad = torch.empty(n_adapters + 1, dtype=torch.int32, device=dev)
+    tiles = torch.empty(n // TILE_M + n_adapters + 1, dtype=torch.int32, device=dev)
+    _check(_lib.mlora_routing_noalloc(_ptr(adapter_ids), n, n_adapters, _ptr(perm), _ptr(seg),
+                                      _ptr(pad), _ptr(tiles), _stream(stream)))
     return perm[:n], seg, pad, tiles
 
 

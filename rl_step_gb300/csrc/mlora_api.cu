@@ -174,6 +174,13 @@ static inline int pad_rows_for(const mlora_t* h, int64_t n) {
 
 extern "C" const char* mlora_last_error(void) { return g_last_error.c_str(); }
 
+// Lets other translation units of the library report a failure through
+// mlora_last_error().
+int mlk_report_error(int code, const char* msg) {
+    g_last_error = msg;
+    return code;
+}
+
 extern "C" int64_t mlora_kernel_launches(const mlora_t* h) { return h ? h->launches : 0; }
 
 extern "C" int64_t mlora_device_bytes(const mlora_t* h) { return h ? h->bytes : 0; }

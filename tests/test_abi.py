@@ -47,6 +47,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
+def test_library_has_no_unresolved_internal_symbols(lib):
+    import rl_step_gb300
+    out = subprocess.run(["nm", "-D", "--undefined-only", rl_step_gb300.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    bad = [ln for ln in out.splitlines() if "mlk" in ln or "mlora" in ln]
+    assert not bad, bad
+
+
 def test_argument_errors_need_no_gpu(lib):
     import ctypes
     import rl_step_gb300 as m
