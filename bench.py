@@ -151,6 +151,21 @@ def adam_bytes(cfg, b):
     return 28.0 * n, n
 
 
+def padded_rows(cfg, b):
+    counts = np.bincount(b["adapter_ids"], minlength=cfg.n_adapters)
+    return int(((counts + 127) // 128 * 128).sum())
+
+
+def loss_epilogue_bytes(cfg, b, bn=256):
+    """Bytes the loss epilogue must move: per padded row the vocabulary-tile
+    partials (max, sum exp) and five scalars; per token its loss inputs and
+    the logprob it returns."""
+    n_nt = (cfg.vocab + bn - 1) // bn
+    rows = padded_rows(cfg, b)
+    per_tok_in = {"cross_entropy": 4, "importance_sampling": 8, "ppo": 8, "custom": 4}[cfg.loss]
+    return rows * (8.0 * n_nt + 20.0) + len(b["tokens"]) * (per_tok_in + 4.0)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -324,6 +339,12 @@ def run_ours(args, rank, world):
     if prof["adam"][0] > 0:
         kernels["adam"]["achieved_gbs"] = adam_b * K / (prof["adam"][0] * 1e-3) / 1e9
         kernels["adam"]["frac_of_hbm"] = kernels["adam"]["achieved_gbs"] / peaks["hbm_gbs"]
+        kernels["adam"]["bytes_per_step"] = adam_b
+    if prof["loss"][0] > 0:
+        lb = loss_epilogue_bytes(cfg, b)
+        kernels["loss"]["achieved_gbs"] = lb * K / (prof["loss"][0] * 1e-3) / 1e9
+        kernels["loss"]["frac_of_hbm"] = kernels["loss"]["achieved_gbs"] / peaks["hbm_gbs"]
+        kernels["loss"]["bytes_per_step"] = lb
     out = {
         "metric": "trained tokens/sec per forward_backward+optim_step",
         "value": N * K * world / (ms_max * 1e-3),
@@ -361,10 +382,13 @@ def run_ours(args, rank, world):
     return out, (cfg, base, ad, b)
 
 
-def oracle_sample_rate(cfg, base, ad, b, n_sample, s_full=None):
-    """Time the oracle's step on the first n_sample tokens; returns (tokens/s, seconds)."""
+def make_oracle(cfg, base, ad):
     import oracle
-    o = oracle.Oracle(base, ad, cfg.ranks, cfg.alphas)
+    return oracle.Oracle(base, ad, cfg.ranks, cfg.alphas)
+
+
+def oracle_sample_rate(cfg, o, b, n_sample, s_full=None):
+    """Time the oracle's step on the first n_sample tokens; returns (tokens/s, seconds)."""
     sl = slice(0, n_sample)
     tok, tgt, ids = b["tokens"][sl], b["targets"][sl], b["adapter_ids"][sl]
     kw = {}
@@ -400,11 +424,12 @@ def run_reference(args):
     base = wl.make_base_weights(cfg)
     ad = wl.make_adapters(cfg)
     n = min(64, len(b["tokens"]))
+    o = make_oracle(cfg, base, ad)
     for _ in range(args.warmup):
-        oracle_sample_rate(cfg, base, ad, b, n)
+        oracle_sample_rate(cfg, o, b, n)
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_sample_rate(cfg, base, ad, b, n)[1]
+        total += oracle_sample_rate(cfg, o, b, n)[1]
     value = n * args.steps / total
     return {
         "metric": "trained tokens/sec per forward_backward+optim_step", "impl": "reference",
@@ -438,7 +463,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cfg, base, ad, b = ctx
         n = min(args.cpu_sample, len(b["tokens"]))
-        rate, dt = oracle_sample_rate(cfg, base, ad, b, n)
+        rate, dt = oracle_sample_rate(cfg, make_oracle(cfg, base, ad), b, n)
         out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores(),
                                "kind": "oracle",
                                "sample": f"first {n} tokens of the batch, forward_backward + "

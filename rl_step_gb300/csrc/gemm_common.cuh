@@ -44,10 +44,10 @@ struct EpiParams {
     int64_t ld_aux = 0;
     const float* gamma = nullptr;   // per adapter
     // LM head
-    float2* part = nullptr;         // [rows][n_ntiles] (running max, sum exp)
+    float2* part = nullptr;         // [rows][part_ld] (running max, sum exp) per n-tile
     float* zt = nullptr;            // target logit per row
     const int* tgt = nullptr;       // target id per padded row (-1: none)
-    int n_ntiles = 0;
+    int part_ld = 0;                // pitch of a row of partials (even)
     int V = 0, Vpad = 0;
     const float* g = nullptr;       // dL/dl per padded row
     const float* lse = nullptr;     // logsumexp per padded row
@@ -255,7 +255,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
 __device__ __forceinline__ void epi_row_end(const EpiParams& ep, int64_t row, int ntile,
                                             const EpiRowState& st) {
     if (ep.kind == EPI_LMFWD) {
-        ep.part[row * ep.n_ntiles + ntile] = make_float2(st.m, st.s);
+        ep.part[row * ep.part_ld + ntile] = make_float2(st.m, st.s);
         if (st.found) ep.zt[row] = st.zt;
     }
 }

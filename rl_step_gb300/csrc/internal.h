@@ -51,7 +51,7 @@ struct LossArgs {
     float clip;
     const float* dl;
 };
-void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, const float* zt,
+void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, int part_ld, const float* zt,
                          const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
                          float* logprobs_out, float* lse, float* g, double* loss_tile,
                          cudaStream_t s);

@@ -123,40 +123,59 @@ __device__ __forceinline__ void token_loss_dev(int kind, float ell, int t, const
     if (!ok) { val = 0.0; g = 0.f; }
 }
 
-__global__ void __launch_bounds__(128) combine_loss_kernel(
-    LossArgs la, const float2* __restrict__ part, int n_nt, const float* __restrict__ zt,
+// (m, s) <- combination of two (max, sum exp(z - max)) partials
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    const float M = fmaxf(m, m2);
+    if (M == -INFINITY) return;
+    s = s * __expf(m - M) + s2 * __expf(m2 - M);
+    m = M;
+}
+
+// One CTA (8 warps) per 128-row tile; each warp combines 16 rows, one row at
+// a time: every lane folds its strided share of the row's partials into a
+// running (max, sum) pair with 16-byte loads, then the warp merges the lanes.
+// part_ld (even) is the pitch of a row of partials, n_nt the number used.
+__global__ void __launch_bounds__(256) combine_loss_kernel(
+    LossArgs la, const float2* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
     const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
     float* logprobs_out, float* lse_out, float* g_out, double* loss_tile) {
     const int mt = blockIdx.x;
     if (mt >= meta[0]) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __shared__ double s_red[4];
+    __shared__ double s_red[8];
     double wsum = 0.0;
-    for (int i = 0; i < 32; ++i) {
-        const int64_t p = (int64_t)mt * TILE_M + warp * 32 + i;
-        const float2* pr = part + p * n_nt;
-        float M = -INFINITY;
-        for (int j = lane; j < n_nt; j += 32) M = fmaxf(M, pr[j].x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float S = 0.f;
-        for (int j = lane; j < n_nt; j += 32) {
-            float2 q = pr[j];
-            S += q.y * expf(q.x - M);
+    const int npair = n_nt >> 1;
+    for (int i = 0; i < 16; ++i) {
+        const int64_t p = (int64_t)mt * TILE_M + warp * 16 + i;
+        const float4* pr = reinterpret_cast<const float4*>(part + p * part_ld);
+        float m = -INFINITY, sum = 0.f;
+#pragma unroll 4
+        for (int j = lane; j < npair; j += 32) {
+            const float4 q = pr[j];
+            lse_merge(m, sum, q.x, q.y);
+            lse_merge(m, sum, q.z, q.w);
+        }
+        if ((n_nt & 1) && lane == 0) {
+            const float2 q = part[p * part_ld + n_nt - 1];
+            lse_merge(m, sum, q.x, q.y);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+            lse_merge(m, sum, m2, s2);
+        }
         if (lane == 0) {
-            int t = perm_pad[p];
+            const int t = perm_pad[p];
             float g = 0.f, lse = 0.f;
             if (t >= 0) {
-                int y = tgt_pad[p];
+                const int y = tgt_pad[p];
                 float ell;
                 if (y >= 0) {
-                    lse = M + logf(S);
+                    lse = m + __logf(sum);
                     ell = zt[p] - lse;
                 } else {
-                    ell = __int_as_float(0x7fc00000);   // NaN: invalid target
+                    ell = __int_as_float(0x7fc00000);   // NaN: invalid token or target
                 }
                 double val;
                 token_loss_dev(la.kind, ell, t, la, val, g);
@@ -170,15 +189,19 @@ __global__ void __launch_bounds__(128) combine_loss_kernel(
     }
     if (lane == 0) s_red[warp] = wsum;
     __syncthreads();
-    if (threadIdx.x == 0) loss_tile[mt] = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 8; ++w) t += s_red[w];
+        loss_tile[mt] = t;
+    }
 }
 
-void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, const float* zt,
+void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, int part_ld, const float* zt,
                          const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
                          float* logprobs_out, float* lse, float* g, double* loss_tile,
                          cudaStream_t s) {
     if (max_tiles <= 0) return;
-    combine_loss_kernel<<<max_tiles, 128, 0, s>>>(la, part, n_nt, zt, perm_pad, tgt_pad, meta,
+    combine_loss_kernel<<<max_tiles, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad, tgt_pad, meta,
                                                   logprobs_out, lse, g, loss_tile);
 }
 

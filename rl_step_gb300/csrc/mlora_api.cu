@@ -79,7 +79,7 @@ struct mlora {
     float* dh32 = nullptr;
     void *dhb = nullptr, *dub = nullptr, *w1s = nullptr, *w2s = nullptr;
     // LM head
-    int lm_bn = 32, n_nt = 0, nc_tiles = 0;
+    int lm_bn = 32, n_nt = 0, part_ld = 0, nc_tiles = 0;
     float2* part = nullptr;
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
@@ -235,6 +235,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
     h->Vpad = (h->V + 63) / 64 * 64;
     h->lm_bn = h->use_tc ? 256 : 32;
     h->n_nt = (h->V + h->lm_bn - 1) / h->lm_bn;
+    h->part_ld = (h->n_nt + 1) & ~1;   // even pitch: 16-byte aligned rows of partials
 
     const int n_ad = h->n_ad, L = h->L, d = h->d, f = h->f, V = h->V;
     const size_t es = h->esize;
@@ -308,7 +309,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOCB(h->w1s, (size_t)MP * RP * es);
         ALLOCB(h->w2s, (size_t)MP * RP * es);
         // LM head: partials, per-row scalars, and the bounded dz chunk buffer
-        ALLOC(h->part, (size_t)MP * h->n_nt);
+        ALLOC(h->part, (size_t)MP * h->part_ld);
         ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
         ALLOC(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 64 ? h->max_tiles : 64;   // 8192-row chunks
@@ -374,7 +375,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         CUDA_TRY(cudaMemset(h->touched, 0, sizeof(int) * n_ad));
         CUDA_TRY(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
         CUDA_TRY(cudaMemset(h->status, 0, sizeof(int)));
-        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float2) * (size_t)MP * h->n_nt));
+        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float2) * (size_t)MP * h->part_ld));
         if (h->dtype == MLORA_BF16)
             launch_shadow_sync<bf16>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
         else
@@ -538,13 +539,13 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         p.B = op_kmajor(h->Wout, V, d);
         p.group_m = 64;
         p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
-        p.ep.n_ntiles = h->n_nt; p.ep.V = V; p.ep.Vpad = h->Vpad;
+        p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
         if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
     }
     // a7 combine + loss epilogue
     {
         ProfScope ps(h, s, MLORA_PROF_LOSS);
-        launch_combine_loss(la, h->part, h->n_nt, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
+        launch_combine_loss(la, h->part, h->n_nt, h->part_ld, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
                             logprobs_out, h->lse, h->gvec, h->loss_tile, s);
         ++h->launches;
     }

@@ -1,0 +1,125 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (one handle sized to the whole batch, every token through
+every kernel).
+
+The oracle cannot run 65k-262k tokens at full widths, so the loss inputs are
+zeroed outside a sampled token set S (a few hundred tokens covering every
+adapter present, sequence starts and ends, and row-tile boundaries).  Tokens
+are independent and adapters isolated, so the GPU's full-size gradient must
+equal the oracle's gradient over S alone, and the post-Adam weights of the
+adapters in S must match too; logprobs are compared on S.  Tolerances as in
+test_gpu_parity.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _gpu_util import create_handle, dev, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["qwen3_4b_is", "qwen3_8b_ppo", "many_tenant_ce", "long_custom"]
+N_SAMPLE = 384
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _sample(b, rng, n_sample):
+    """Token positions spread over adapters, sequence edges and 128-row tiles."""
+    N = len(b["tokens"])
+    pick = set()
+    starts = np.concatenate([[0], np.cumsum(b["seq_lens"])[:-1]])
+    ends = starts + b["seq_lens"] - 1
+    for s0, e0 in zip(starts, ends):
+        pick.update([int(s0), int(e0)])
+    ids = b["adapter_ids"]
+    for a in np.unique(ids):
+        rows = np.nonzero(ids == a)[0]
+        pick.update(int(x) for x in rows[[0, -1]])
+        for k in (127, 128, 255, 256):                 # around the routing tile edges
+            if k < len(rows):
+                pick.add(int(rows[k]))
+    pick = sorted(pick)
+    if len(pick) > n_sample:
+        pick = sorted(rng.choice(pick, n_sample, replace=False).tolist())
+    rest = np.setdiff1d(np.arange(N), pick)
+    extra = rng.choice(rest, max(0, n_sample - len(pick)), replace=False)
+    return np.array(sorted(set(pick) | set(int(x) for x in extra)), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity(name):
+    import rl_step_gb300 as m
+    cfg = wl.get_config(name)
+    b = wl.make_batch(cfg)
+    N = len(b["tokens"])
+    assert N == cfg.n_tokens
+    base = wl.make_base_weights(cfg)
+    ad = wl.make_adapters(cfg)
+    o = oracle.Oracle(base, ad, cfg.ranks, cfg.alphas)
+    rng = np.random.Generator(np.random.PCG64([31, N]))
+    S = _sample(b, rng, N_SAMPLE)
+    mask = np.zeros(N, bool)
+    mask[S] = True
+    sub = {k: b[k][S] for k in ("tokens", "targets", "adapter_ids")}
+    ell_S = o.forward(sub["tokens"], sub["targets"], sub["adapter_ids"])
+
+    # loss inputs: the workload's values on S, zero elsewhere
+    w = np.where(mask, b["weights"], 0).astype(np.float32)
+    A = np.where(mask, b["advantages"], 0).astype(np.float32)
+    g = np.where(mask, b["dloss"], 0).astype(np.float32)
+    s = np.full(N, -np.log(cfg.vocab), np.float64) + b["sampler_noise"]
+    s[S] = ell_S + b["sampler_noise"][S]
+    s = s.astype(np.float32)
+
+    h = create_handle(cfg, base, ad, N)
+    tok, tgt, ids = dev(b["tokens"]), dev(b["targets"]), dev(b["adapter_ids"])
+    if cfg.loss == "custom":
+        lp, _ = m.mlora_forward_backward_custom(h, tok, tgt, ids, dev(g))
+        ref = o.forward_backward_custom(sub["tokens"], sub["targets"], sub["adapter_ids"], g[S])
+    elif cfg.loss == "cross_entropy":
+        lp, _ = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, weights=dev(w))
+        ref = o.forward_backward(sub["tokens"], sub["targets"], sub["adapter_ids"], cfg.loss,
+                                 weights=w[S])
+    else:
+        lp, _ = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, advantages=dev(A),
+                                         sampler_logprobs=dev(s), clip_eps=cfg.clip_eps)
+        ref = o.forward_backward(sub["tokens"], sub["targets"], sub["adapter_ids"], cfg.loss,
+                                 advantages=A[S], sampler_logprobs=s[S].astype(np.float64),
+                                 clip_eps=cfg.clip_eps)
+    assert m.mlora_check_status(h) == 0
+    lp = lp.cpu().numpy()
+    assert np.isfinite(lp).all()
+    lp_err = float(np.max(np.abs(lp[S] - ref["logprobs"])))
+    present = np.unique(sub["adapter_ids"])
+    worst = 0.0
+    for a in present:
+        for l in range(cfg.n_layers):
+            for k in oracle.TENSORS:
+                x = m.mlora_read_adapter(h, int(a), l, "g" + k).cpu().numpy()
+                worst = max(worst, rel_fro(x, o.G[k][a][l]))
+    # adapters with no token in S received no gradient at all
+    others = [a for a in np.unique(b["adapter_ids"]) if a not in set(present.tolist())]
+    for a in others[:4]:
+        assert not m.mlora_read_adapter(h, int(a), 0, "gA1").cpu().numpy().any()
+    m.mlora_optim_step(h, lr=cfg.lr, adapters=[int(a) for a in present])
+    o.optim_step(lr=cfg.lr, adapters=[int(a) for a in present])
+    p_worst = 0.0
+    for a in present:
+        for l in range(cfg.n_layers):
+            for k in oracle.TENSORS:
+                x = m.mlora_read_adapter(h, int(a), l, k).cpu().numpy()
+                p_worst = max(p_worst, rel_fro(x, o.P[k][a][l]))
+    print(f"\n[{name} full N={N}, |S|={len(S)}, adapters in S={len(present)}] logprob max|err|="
+          f"{lp_err:.3e}; grad rel Fro max={worst:.3e}; post-Adam rel Fro max={p_worst:.3e}")
+    assert lp_err <= 2e-2
+    assert worst <= 1e-2
+    assert p_worst <= 1e-2
