@@ -227,6 +227,79 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n, int a_mn, int b_mn, int
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// TMA loads of one stage's A tile (ROWS x 64, K-major box or two MN-major
+// boxes) and B tile (ROWS x 64).  `pair` loads complete on the leader CTA's
+// barrier (bar is then a shared::cluster address).
+template <int ROWS>
+__device__ __forceinline__ void load_tile_a(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            const GemmOperand& op, int m0, int k, int arow, bool pair) {
+    if (!op.mn_major) {
+        if (pair) tma_load_2d_pair(dst, map, bar, k, arow);
+        else tma_load_2d(dst, map, bar, k, arow);
+    } else {
+#pragma unroll
+        for (int i = 0; i < ROWS / 64; ++i) {
+            if (pair) tma_load_2d_pair(dst + i * 8192, map, bar, m0 + 64 * i, (int)(k + op.row_shift));
+            else tma_load_2d(dst + i * 8192, map, bar, m0 + 64 * i, (int)(k + op.row_shift));
+        }
+    }
+}
+
+template <int ROWS>
+__device__ __forceinline__ void load_tile_b(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            const GemmOperand& op, int n0, int k, int adapter, bool pair) {
+    const int brow = (int)((int64_t)adapter * op.ad_rows + op.row_shift);
+    if (!op.mn_major) {
+        if (pair) tma_load_2d_pair(dst, map, bar, k, brow + n0);
+        else tma_load_2d(dst, map, bar, k, brow + n0);
+    } else {
+#pragma unroll
+        for (int i = 0; i < ROWS / 64; ++i) {
+            if (pair) tma_load_2d_pair(dst + i * 8192, map, bar, n0 + 64 * i, brow + k);
+            else tma_load_2d(dst + i * 8192, map, bar, n0 + 64 * i, brow + k);
+        }
+    }
+}
+
+// Epilogue of one finished accumulator for one thread's row: BN columns in
+// chunks of 32.  The TMEM read of chunk c+1 is issued before chunk c is
+// processed, so the load latency overlaps the epilogue arithmetic.
+template <int BN>
+__device__ __forceinline__ void epilogue_row(const GemmParams& p, uint32_t tbase, int64_t row, bool row_ok,
+                                             int col_base, int adapter, int nt) {
+    static_assert((BN / 32) % 2 == 0, "chunks are processed in pairs");
+    EpiRowState st;
+    epi_row_begin(st);
+    uint32_t ra[32], rb[32];
+    tmem_ld32(tbase, ra);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ch += 2) {
+        tmem_ld_wait();
+        tmem_ld32(tbase + (ch + 1) * 32, rb);
+        {
+            const int col0 = col_base + ch * 32;
+            if (row_ok && col0 < p.N) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
+                epi_chunk<bf16>(p.ep, row, col0, adapter, v, st);
+            }
+        }
+        tmem_ld_wait();
+        if (ch + 2 < BN / 32) tmem_ld32(tbase + (ch + 2) * 32, ra);
+        {
+            const int col0 = col_base + (ch + 1) * 32;
+            if (row_ok && col0 < p.N) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rb[j]);
+                epi_chunk<bf16>(p.ep, row, col0, adapter, v, st);
+            }
+        }
+    }
+    if (row_ok) epi_row_end(p.ep, row, nt, st);
+}
+
 struct TcMaps {
     CUtensorMap A, B, Ax, Bx;
 };
@@ -369,34 +442,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const TileCoord c = tile_coord<BN>(p, t);
                 const int m0 = c.mt * BM;
                 const int n0 = c.nt * BN;
-                const int nall = c.nkb + c.nkbx;
-                for (int kb = 0; kb < nall; ++kb) {
+                for (int kb = 0; kb < c.nkb && ok; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
                     mbar_expect_tx(fb, SL::STAGE_BYTES);
-                    const bool ext = kb >= c.nkb;
-                    const GemmOperand& A = ext ? p.Ax : p.A;
-                    const GemmOperand& B = ext ? p.Bx : p.B;
-                    const CUtensorMap* mA = ext ? &maps.Ax : &maps.A;
-                    const CUtensorMap* mB = ext ? &maps.Bx : &maps.B;
-                    const int k = ext ? (kb - c.nkb) * BK : c.k0 + kb * BK;
-                    if (!A.mn_major) {
-                        tma_load_2d(sa, mA, fb, k, (int)(m0 + A.row_shift));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < BM / 64; ++i)
-                            tma_load_2d(sa + i * 8192, mA, fb, m0 + 64 * i, (int)(k + A.row_shift));
-                    }
-                    const int brow = (int)((int64_t)c.adapter * B.ad_rows + B.row_shift);
-                    if (!B.mn_major) {
-                        tma_load_2d(sb, mB, fb, k, brow + n0);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tma_load_2d(sb + i * 8192, mB, fb, n0 + 64 * i, brow + k);
-                    }
+                    const int k = c.k0 + kb * BK;
+                    load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), false);
+                    load_tile_b<BN>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, c.adapter, false);
+                    issued[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                for (int kb = 0; kb < c.nkbx && ok; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    mbar_expect_tx(fb, SL::STAGE_BYTES);
+                    const int k = kb * BK;
+                    load_tile_a<BM>(sa, &maps.Ax, fb, p.Ax, m0, k, (int)(m0 + p.Ax.row_shift), false);
+                    load_tile_b<BN>(sa + SL::A_BYTES, &maps.Bx, fb, p.Bx, n0, k, c.adapter, false);
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -429,25 +493,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const int nall = c.nkb + c.nkbx;
-                for (int kb = 0; kb < nall; ++kb) {
+                for (int kb = 0; kb < c.nkb; ++kb) {
                     if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const bool ext = kb >= c.nkb;
-                    const int a_mn = ext ? p.Ax.mn_major : p.A.mn_major;
-                    const int b_mn = ext ? p.Bx.mn_major : p.B.mn_major;
-                    const uint32_t idesc = ext ? id_ext : id_main;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
                     const uint32_t sb = sa + SL::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = a_mn ? sdesc(sa + kk * 2048, 8192, 1024)
-                                                 : sdesc(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 8192, 1024)
-                                                 : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t ad = p.A.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
+                                                         : sdesc(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = p.B.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
+                                                         : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, id_main, (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_empty + 8 * stage);     // frees the stage when the MMAs finish
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                for (int kb = 0; kb < c.nkbx && ok; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = p.Ax.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
+                                                          : sdesc(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = p.Bx.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
+                                                          : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, id_ext, (c.nkb > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -480,23 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int64_t row = (int64_t)c.mt * BM + 32 * q + lane;
             const bool row_ok = !p.grouped || row < p.M;
-            EpiRowState st;
-            epi_row_begin(st);
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tbase + ch * 32, r);
-                tmem_ld_wait();
-                const int col0 = c.nt * BN + ch * 32;
-                if (row_ok && col0 < p.N) {
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi_chunk<bf16>(p.ep, row, col0, c.adapter, v, st);
-                }
-            }
-            if (row_ok) epi_row_end(p.ep, row, c.nt, st);
+            epilogue_row<BN>(p, tbase, row, row_ok, c.nt * BN, c.adapter, c.nt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
@@ -538,6 +598,9 @@ struct PairCoord {
     int mt;       // first global m-tile of the pair
     int nt;
     int k0, nkb;
+    int a0, a1;   // adapters of the pair's two row tiles
+    int nkbx;     // extension K blocks per adapter
+    int next;     // extension stages: nkbx, or 2 * nkbx when a0 != a1
 };
 
 template <int BN>
@@ -563,6 +626,15 @@ __device__ __forceinline__ PairCoord pair_coord(const GemmParams& p, int t, int 
     c.nt = r / bm;
     c.k0 = 0;
     c.nkb = (p.K + BK - 1) / BK;
+    c.a0 = c.a1 = 0;
+    if (p.tile_ad) {
+        c.a0 = p.tile_ad[c.mt];
+        c.a1 = (c.mt + 1 - p.mt_base) < cnt ? p.tile_ad[c.mt + 1] : c.a0;
+        if (c.a0 < 0) c.a0 = 0;
+        if (c.a1 < 0) c.a1 = c.a0;
+    }
+    c.nkbx = (p.Kx + BK - 1) / BK;
+    c.next = (c.a0 == c.a1) ? c.nkbx : 2 * c.nkbx;
     return c;
 }
 
@@ -603,6 +675,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tma_prefetch_desc(&maps.A);
         tma_prefetch_desc(&maps.B);
+        if (p.Kx > 0) {
+            tma_prefetch_desc(&maps.Ax);
+            tma_prefetch_desc(&maps.Bx);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -635,28 +711,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 const int m0 = (c.mt + (int)rank) * BM;
                 const int n0 = c.nt * BN + (int)rank * (BN / 2);
-                for (int kb = 0; kb < c.nkb; ++kb) {
+                for (int kb = 0; kb < c.nkb && ok; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
                     const uint32_t fb = full_leader + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
                     const int k = c.k0 + kb * BK;
-                    if (!p.A.mn_major) {
-                        tma_load_2d_pair(sa, &maps.A, fb, k, (int)(m0 + p.A.row_shift));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < BM / 64; ++i)
-                            tma_load_2d_pair(sa + i * 8192, &maps.A, fb, m0 + 64 * i, (int)(k + p.A.row_shift));
+                    load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), true);
+                    load_tile_b<BN / 2>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, 0, true);
+                    issued[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                // K extension: with two adapters in the pair, stage `half` multiplies
+                // adapter a_half's factor with only that half's rows (the other CTA
+                // loads zeros, read out of bounds)
+                for (int e = 0; e < c.next && ok; ++e) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
+                    const uint32_t fb = full_leader + 8 * stage;
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const int half = e / c.nkbx;
+                    const int k = (e - half * c.nkbx) * BK;
+                    int adapter = c.a0;
+                    int arow = (int)(m0 + p.Ax.row_shift);
+                    if (c.a0 != c.a1) {
+                        adapter = half ? c.a1 : c.a0;
+                        if ((int)rank != half) arow = -BM;
                     }
-                    const int brow = (int)p.B.row_shift;
-                    if (!p.B.mn_major) {
-                        tma_load_2d_pair(sb, &maps.B, fb, k, brow + n0);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < BN / 128; ++i)
-                            tma_load_2d_pair(sb + i * 8192, &maps.B, fb, n0 + 64 * i, brow + k);
-                    }
+                    load_tile_a<BM>(sa, &maps.Ax, fb, p.Ax, m0, k, arow, true);
+                    load_tile_b<BN / 2>(sa + SL::A_BYTES, &maps.Bx, fb, p.Bx, n0, k, adapter, true);
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -683,12 +766,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
+            const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
+            const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major, 2 * BM);
             for (int t = cid; t < ntiles && ok; t += ncl) {
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const int nall = c.nkb + c.next;
                 for (int kb = 0; kb < c.nkb; ++kb) {
                     if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
@@ -700,7 +785,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                          : sdesc(sa + kk * 32, 16, 1024);
                         const uint64_t bd = p.B.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
                                                          : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_pair(d_tmem, ad, bd, id_main, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(bar_empty + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                for (int kb = c.nkb; kb < nall && ok; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
+                    const uint32_t sb = sa + SL::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);     // Ax is K-major
+                        const uint64_t bd = p.Bx.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
+                                                          : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16_pair(d_tmem, ad, bd, id_ext, 1u);
                     }
                     umma_commit_pair_mc(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -735,23 +835,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int my_mt = c.mt + (int)rank;
             const bool tile_ok = (my_mt - p.mt_base) < cnt;
             const int64_t row = (int64_t)my_mt * BM + 32 * q + lane;
-            EpiRowState st;
-            epi_row_begin(st);
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tbase + ch * 32, r);
-                tmem_ld_wait();
-                const int col0 = c.nt * BN + ch * 32;
-                if (tile_ok && col0 < p.N) {
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi_chunk<bf16>(p.ep, row, col0, 0, v, st);
-                }
-            }
-            if (tile_ok) epi_row_end(p.ep, row, c.nt, st);
+            epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -844,10 +929,15 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         if (op.mn_major) return encode_2d(m, op, 64, 64);
         return encode_2d(m, op, 64, (uint32_t)rows_mn);
     };
-    if (p.grouped || p.Kx > 0 || p.B.ad_rows != 0) return cudaErrorInvalidValue;
+    if (p.grouped || p.B.ad_rows != 0 || p.A.mn_major) return cudaErrorInvalidValue;
     if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN / 2)) return cudaErrorInvalidValue;
-    maps.Ax = maps.A;
-    maps.Bx = maps.B;
+    if (p.Kx > 0) {
+        if (p.Kx % BK || p.Ax.mn_major || !enc(&maps.Ax, p.Ax, BM) || !enc(&maps.Bx, p.Bx, BN / 2))
+            return cudaErrorInvalidValue;
+    } else {
+        maps.Ax = maps.A;
+        maps.Bx = maps.B;
+    }
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>,
@@ -893,8 +983,9 @@ bool tc_engine_available() { return get_encode(); }
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
     if (!get_encode()) return cudaErrorNotSupported;
     if (p.N <= 64) return launch_bn<64, 8>(p, s, num_sms, status);
-    // B shared by every row and no K extension: 256 x 256 tiles on CTA pairs
-    if (!p.grouped && p.Kx == 0 && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256)
+    // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
+    // K extension, if any, is split per row half inside the kernel)
+    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256)
         return launch_pair<256, 6, 2>(p, s, num_sms, status, nullptr);
     return launch_bn<256, 4>(p, s, num_sms, status);
 }

@@ -43,6 +43,8 @@ void launch_embed(const int* perm_pad, const int* meta, int max_rows, const int*
                   const int* targets, const T* E, int V, int d, T* hb, float* h32, int* tgt_pad,
                   int* status, cudaStream_t s);
 
+constexpr int COMBINE_SPLIT = 4;    // CTAs per 128-row tile in the LM-head combine
+
 struct LossArgs {
     int kind;                 // -1 forward only, 0 CE, 1 IS, 2 PPO, 3 custom
     const float* w;

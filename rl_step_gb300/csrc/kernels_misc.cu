@@ -131,29 +131,42 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     m = M;
 }
 
-// One CTA (8 warps) per 128-row tile; each warp combines 16 rows, one row at
-// a time: every lane folds its strided share of the row's partials into a
-// running (max, sum) pair with 16-byte loads, then the warp merges the lanes.
-// part_ld (even) is the pitch of a row of partials, n_nt the number used.
+// COMBINE_SPLIT CTAs (8 warps each) per 128-row tile; each warp combines
+// 128 / (8 * COMBINE_SPLIT) rows, one at a time: every lane issues up to
+// eight 16-byte loads of the row's partials before folding them into a
+// running (max, sum) pair, then the warp merges its lanes.  part_ld (even)
+// is the pitch of a row of partials, n_nt the number in use.  Each CTA's
+// loss sum goes to loss_part[tile * COMBINE_SPLIT + sub] for a deterministic
+// per-adapter reduction.
+constexpr int COMBINE_ROWS_PER_WARP = TILE_M / (8 * COMBINE_SPLIT);
+
 __global__ void __launch_bounds__(256) combine_loss_kernel(
     LossArgs la, const float2* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
     const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
-    float* logprobs_out, float* lse_out, float* g_out, double* loss_tile) {
-    const int mt = blockIdx.x;
+    float* logprobs_out, float* lse_out, float* g_out, double* loss_part) {
+    const int mt = blockIdx.x / COMBINE_SPLIT;
+    const int sub = blockIdx.x % COMBINE_SPLIT;
     if (mt >= meta[0]) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ double s_red[8];
     double wsum = 0.0;
     const int npair = n_nt >> 1;
-    for (int i = 0; i < 16; ++i) {
-        const int64_t p = (int64_t)mt * TILE_M + warp * 16 + i;
+    for (int i = 0; i < COMBINE_ROWS_PER_WARP; ++i) {
+        const int64_t p = (int64_t)mt * TILE_M + (sub * 8 + warp) * COMBINE_ROWS_PER_WARP + i;
         const float4* pr = reinterpret_cast<const float4*>(part + p * part_ld);
         float m = -INFINITY, sum = 0.f;
-#pragma unroll 4
-        for (int j = lane; j < npair; j += 32) {
-            const float4 q = pr[j];
-            lse_merge(m, sum, q.x, q.y);
-            lse_merge(m, sum, q.z, q.w);
+        for (int j0 = lane; j0 < npair; j0 += 32 * 8) {
+            float4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + 32 * u;
+                q[u] = j < npair ? pr[j] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                lse_merge(m, sum, q[u].x, q[u].y);
+                lse_merge(m, sum, q[u].z, q[u].w);
+            }
         }
         if ((n_nt & 1) && lane == 0) {
             const float2 q = part[p * part_ld + n_nt - 1];
@@ -192,25 +205,27 @@ __global__ void __launch_bounds__(256) combine_loss_kernel(
     if (threadIdx.x == 0) {
         double t = 0.0;
         for (int w = 0; w < 8; ++w) t += s_red[w];
-        loss_tile[mt] = t;
+        loss_part[blockIdx.x] = t;
     }
 }
 
 void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, int part_ld, const float* zt,
                          const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
-                         float* logprobs_out, float* lse, float* g, double* loss_tile,
+                         float* logprobs_out, float* lse, float* g, double* loss_part,
                          cudaStream_t s) {
     if (max_tiles <= 0) return;
-    combine_loss_kernel<<<max_tiles, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad, tgt_pad, meta,
-                                                  logprobs_out, lse, g, loss_tile);
+    combine_loss_kernel<<<max_tiles * COMBINE_SPLIT, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad,
+                                                                  tgt_pad, meta, logprobs_out, lse, g,
+                                                                  loss_part);
 }
 
-// Per-adapter loss: sum of its tiles' partial sums, in tile order.
-__global__ void loss_reduce_kernel(const double* loss_tile, const int* pad_off, int n_ad,
+// Per-adapter loss: sum of its tiles' partial sums, in a fixed order.
+__global__ void loss_reduce_kernel(const double* loss_part, const int* pad_off, int n_ad,
                                    double* loss_out) {
     for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n_ad; a += gridDim.x * blockDim.x) {
         double s = 0.0;
-        for (int j = pad_off[a] / TILE_M; j < pad_off[a + 1] / TILE_M; ++j) s += loss_tile[j];
+        for (int j = pad_off[a] / TILE_M * COMBINE_SPLIT; j < pad_off[a + 1] / TILE_M * COMBINE_SPLIT; ++j)
+            s += loss_part[j];
         loss_out[a] = s;
     }
 }

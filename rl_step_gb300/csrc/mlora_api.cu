@@ -318,7 +318,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
             rc = fail(MLORA_E_CUDA, "cudaMemset of the dz chunk buffer failed");
             goto fail_out;
         }
-        ALLOC(h->loss_tile, h->max_tiles);
+        ALLOC(h->loss_tile, (size_t)h->max_tiles * COMBINE_SPLIT);   // per (tile, combine CTA)
         ALLOC(h->status, 1);
     }
 #undef ALLOC
