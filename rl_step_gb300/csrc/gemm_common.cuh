@@ -74,6 +74,7 @@ struct GemmParams {
     const int* nchunks_dev = nullptr;
     int max_chunks = 0;
     int group_m = 8;                  // raster band height (m-tiles) for L2 reuse
+    int* tile_counter = nullptr;      // device int, tile scheduler of the CTA-pair kernel
     EpiParams ep;
 };
 

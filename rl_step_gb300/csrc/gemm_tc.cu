@@ -588,9 +588,11 @@ struct SmemLayoutPair {
     static constexpr int B_BYTES = (BN / 2) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int SCHED = 4;                     // tile-index ring depth
     static constexpr int BAR_OFF = TILES_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1;
-    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * SCHED;
+    static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int MISC_OFF = SLOT_OFF + SCHED * 4;
     static constexpr int TOTAL = MISC_OFF + 16 + 1024;
 };
 
@@ -638,10 +640,59 @@ __device__ __forceinline__ PairCoord pair_coord(const GemmParams& p, int t, int 
     return c;
 }
 
+// Tile scheduling: the leader's producer thread takes pair-tile indices from
+// a global counter (atomicAdd), so the tiles in flight on the GPU stay
+// consecutive and the band raster keeps its L2 reuse (a static per-cluster
+// list lets clusters drift apart over thousands of tiles).  Each index is
+// published through a small ring in both CTAs' shared memory; the peer's
+// producer, the leader's MMA thread and all eight epilogue warps take it
+// from there and release the slot on the leader's "sched empty" barrier.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > TIMEOUT_NS) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Take the next tile index from ring slot `slot` (phase `ph`) and release the
+// slot on the leader's barrier.  Returns false on timeout; t = -1 ends the work.
+__device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_leader, const volatile int* slots,
+                                           int& slot, uint32_t& ph, bool leader, volatile int* abort_flag,
+                                           int& t) {
+    if (!mbar_wait_cluster(bar_sfull + 8 * slot, ph, abort_flag)) return false;
+    t = slots[slot];
+    if (leader) mbar_arrive(sempty_leader + 8 * slot);
+    else mbar_arrive_cluster(sempty_leader + 8 * slot);
+    if (++slot == 4) { slot = 0; ph ^= 1u; }
+    return true;
+}
+
 template <int BN, int STAGES, int NUM_ACC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
     using SL = SmemLayoutPair<BN, STAGES, NUM_ACC>;
+    static_assert(SL::SCHED == 4, "sched_take assumes a 4-slot ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -650,6 +701,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_tfull = bar_empty + STAGES * 8;
     const uint32_t bar_tempty = bar_tfull + NUM_ACC * 8;
     const uint32_t bar_drain = bar_tempty + NUM_ACC * 8;
+    const uint32_t bar_sfull = bar_drain + 8;
+    const uint32_t bar_sempty = bar_sfull + SL::SCHED * 8;
+    volatile int* slots = reinterpret_cast<volatile int*>(smem + SL::SLOT_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC_OFF + 4);
     constexpr uint32_t TMEM_COLS = NUM_ACC * BN;
@@ -670,6 +724,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar_tempty + 8 * b, 8);
         }
         mbar_init(bar_drain, 1);
+        for (int s = 0; s < SL::SCHED; ++s) {
+            mbar_init(bar_sfull + 8 * s, 1);
+            mbar_init(bar_sempty + 8 * s, 10);   // peer producer, leader MMA, 8 epilogue warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -694,10 +752,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int cnt = pair_mcount<BN>(p);
     const int n_nt = (p.N + BN - 1) / BN;
     const int ntiles = ((cnt + 1) / 2) * n_nt;
-    const int cid = blockIdx.x >> 1;
-    const int ncl = gridDim.x >> 1;
     const uint32_t full_leader = map_to_rank(bar_full, 0);
     const uint32_t tempty_leader = map_to_rank(bar_tempty, 0);
+    const uint32_t sempty_leader = map_to_rank(bar_sempty, 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producers (both CTAs)
@@ -707,7 +764,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int issued[STAGES];
             for (int s = 0; s < STAGES; ++s) issued[s] = -1;
             bool ok = true;
-            for (int t = cid; t < ntiles && ok; t += ncl) {
+            int sslot = 0;
+            uint32_t sph = 0;
+            const uint32_t sfull_peer = map_to_rank(bar_sfull, 1);
+            const uint32_t slot_peer = map_to_rank(smem_u32(const_cast<int*>(slots)), 1);
+            for (;;) {
+                int t;
+                if (leader) {
+                    // scheduler: next pair tile, published to both CTAs
+                    t = atomicAdd(p.tile_counter, 1);
+                    if (t >= ntiles) t = -1;
+                    if (!mbar_wait(bar_sempty + 8 * sslot, sph ^ 1u, abort_flag)) { ok = false; break; }
+                    slots[sslot] = t;
+                    st_shared_cluster(slot_peer + 4 * sslot, t);
+                    mbar_arrive(bar_sfull + 8 * sslot);
+                    mbar_arrive_cluster(sfull_peer + 8 * sslot);
+                    if (++sslot == SL::SCHED) { sslot = 0; sph ^= 1u; }
+                } else {
+                    if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, false, abort_flag, t)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (t < 0) break;
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 const int m0 = (c.mt + (int)rank) * BM;
                 const int n0 = c.nt * BN + (int)rank * (BN / 2);
@@ -743,6 +822,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (!ok) break;
             }
             if (!ok) {
                 atomicOr(status, ST_TIMEOUT);
@@ -766,9 +846,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            int sslot = 0;
+            uint32_t sph = 0;
             const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
             const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major, 2 * BM);
-            for (int t = cid; t < ntiles && ok; t += ncl) {
+            for (;;) {
+                int t;
+                if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, true, abort_flag, t)) {
+                    ok = false;
+                    break;
+                }
+                if (t < 0) break;
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -822,9 +910,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = cid; t < ntiles; t += ncl) {
-            const PairCoord c = pair_coord<BN>(p, t, cnt);
+        int sslot = 0;
+        uint32_t sph = 0;
+        for (;;) {
+            int t = -1;
             bool ok = true;
+            if (lane == 0) ok = sched_take(bar_sfull, sempty_leader, slots, sslot, sph, leader, abort_flag, t);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            sslot = __shfl_sync(0xffffffffu, sslot, 0);
+            sph = __shfl_sync(0xffffffffu, sph, 0);
+            if (!ok) {
+                if (lane == 0) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+                break;
+            }
+            if (t < 0) break;
+            const PairCoord c = pair_coord<BN>(p, t, cnt);
             if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
@@ -929,7 +1030,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         if (op.mn_major) return encode_2d(m, op, 64, 64);
         return encode_2d(m, op, 64, (uint32_t)rows_mn);
     };
-    if (p.grouped || p.B.ad_rows != 0 || p.A.mn_major) return cudaErrorInvalidValue;
+    if (p.grouped || p.B.ad_rows != 0 || p.A.mn_major || !p.tile_counter) return cudaErrorInvalidValue;
     if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN / 2)) return cudaErrorInvalidValue;
     if (p.Kx > 0) {
         if (p.Kx % BK || p.Ax.mn_major || !enc(&maps.Ax, p.Ax, BM) || !enc(&maps.Bx, p.Bx, BN / 2))
@@ -962,7 +1063,9 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>, maps, p, status, dbg);
+    cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);   // fresh tile counter
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>, maps, p, status, dbg);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -985,7 +1088,7 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
     if (p.N <= 64) return launch_bn<64, 8>(p, s, num_sms, status);
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
-    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256)
+    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
         return launch_pair<256, 6, 2>(p, s, num_sms, status, nullptr);
     return launch_bn<256, 4>(p, s, num_sms, status);
 }

@@ -86,6 +86,7 @@ struct mlora {
     void* dz = nullptr;
     double* loss_tile = nullptr;
     int* status = nullptr;
+    int* tile_counter = nullptr;        // GEMM tile scheduler (reset before each launch)
     // measurement: events around launches
     bool prof = false;
     std::vector<cudaEvent_t> ev;      // pairs (start, stop)
@@ -320,6 +321,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         }
         ALLOC(h->loss_tile, (size_t)h->max_tiles * COMBINE_SPLIT);   // per (tile, combine CTA)
         ALLOC(h->status, 1);
+        ALLOC(h->tile_counter, 1);
     }
 #undef ALLOC
 #undef ALLOCB
@@ -419,6 +421,7 @@ static GemmOperand op_mnmajor(const void* p, int64_t rows, int64_t cols, int64_t
 template <typename T>
 static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s, int cls) {
     ProfScope ps(h, s, cls);
+    p.tile_counter = h->tile_counter;
     if (h->use_tc) {
         cudaError_t e = launch_tc_gemm(p, s, h->num_sms, h->status);
         if (e != cudaSuccess) return fail(MLORA_E_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(e));
@@ -537,7 +540,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         GemmParams p = dense_params(h, mt_upper, V, d);
         p.A = op_kmajor(h->hb[L], MP, d);
         p.B = op_kmajor(h->Wout, V, d);
-        p.group_m = 64;
+        p.group_m = 32;
         p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
         p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
         if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
@@ -564,7 +567,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.mt_base = c0; p.mt_count = cnt;
             p.A = op_kmajor(h->hb[L], MP, d);
             p.B = op_kmajor(h->Wout, V, d);
-            p.group_m = 64;
+            p.group_m = 32;
             p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
             p.ep.tgt = h->tgt_pad; p.ep.V = V; p.ep.Vpad = h->Vpad;
             p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
