@@ -151,6 +151,36 @@ def adam_bytes(cfg, b):
     return 28.0 * n, n
 
 
+KERNEL_SOURCES = ("gemm_tc.cu", "gemm_common.cuh", "mlora_api.cu", "kernels_misc.cu")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources that determine the GEMM kernels and their launches."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "rl_step_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def committed_traffic(workload: str, kernel: str, launches: int):
+    """Per-launch DRAM bytes of `kernel` from the committed full-size ncu
+    summary, or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    k = rec.get("kernels", {}).get(kernel)
+    if not k or k.get("launches_per_step") != launches:
+        return None
+    return k.get("dram_bytes_per_launch")
+
+
 def padded_rows(cfg, b):
     counts = np.bincount(b["adapter_ids"], minlength=cfg.n_adapters)
     return int(((counts + 127) // 128 * 128).sum())
@@ -158,12 +188,12 @@ def padded_rows(cfg, b):
 
 def loss_epilogue_bytes(cfg, b, bn=256):
     """Bytes the loss epilogue must move: per padded row the vocabulary-tile
-    partials (max, sum exp) and five scalars; per token its loss inputs and
-    the logprob it returns."""
+    log-sum-exp partials (4 B each) and five scalars; per token its loss
+    inputs and the logprob it returns."""
     n_nt = (cfg.vocab + bn - 1) // bn
     rows = padded_rows(cfg, b)
     per_tok_in = {"cross_entropy": 4, "importance_sampling": 8, "ppo": 8, "custom": 4}[cfg.loss]
-    return rows * (8.0 * n_nt + 20.0) + len(b["tokens"]) * (per_tok_in + 4.0)
+    return rows * (4.0 * n_nt + 20.0) + len(b["tokens"]) * (per_tok_in + 4.0)
 
 
 def run_ours(args, rank, world):
@@ -261,11 +291,7 @@ def run_ours(args, rank, world):
     launches = h.kernel_launches - launches0
     prof = m.mlora_profile_read(h, reset=True)
     ms = e0.elapsed_time(e1)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     status = m.mlora_check_status(h)
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
@@ -307,12 +333,8 @@ def run_ours(args, rank, world):
         for _ in range(args.steps):
             e2e_step()
         torch.cuda.synchronize()
-        t_e2e = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": N * args.steps * world / t_e2e, "unit": "tokens/s",
+        t_e2e = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": job_throughput(N, args.steps, world, 1e3 * t_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
@@ -320,18 +342,18 @@ def run_ours(args, rank, world):
     peaks, peak_src = load_peaks()
     fl = flop_model(cfg, b)
     K = args.steps
-    # dominant kernel: the CTA-pair tcgen05 GEMM carrying the LM head (forward,
-    # recomputed logits + dz, dh).  Algorithmic FLOPs credit 2NVd for the
-    # forward and 2NVd for dh; the recompute pass is executed work only.
-    lm_ms = sum(prof[c][0] for c in ("lm_fwd", "lm_dz", "lm_dh"))
-    lm_launch = sum(prof[c][1] for c in ("lm_fwd", "lm_dz", "lm_dh"))
-    lm_alg = 4.0 * N * cfg.vocab * cfg.d_model
-    lm_exec = 6.0 * N * cfg.vocab * cfg.d_model
-    achieved = lm_alg * K / (lm_ms * 1e-3) / 1e12 if lm_ms > 0 else None
-    executed = lm_exec * K / (lm_ms * 1e-3) / 1e12 if lm_ms > 0 else None
-    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # dominant kernel: the CTA-pair tcgen05 GEMM, which carries every base and
+    # LM-head GEMM (35 launches per step at L=4).  Algorithmic FLOPs credit the
+    # base and LoRA-extension GEMMs, the LM-head forward and dh; the recomputed
+    # logits (dz pass) and padding rows are executed work only.
     tc_ms = sum(prof[c][0] for c in TC_CLASSES)
-    family = fl["tc256"] * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    tc_launch = sum(prof[c][1] for c in TC_CLASSES)
+    achieved = fl["tc256"] * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    rows = padded_rows(cfg, b)
+    exec_flops = (fl["tc256"] * rows / max(1, N)) + 2.0 * rows * cfg.vocab * cfg.d_model
+    executed = exec_flops * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
+    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    traffic = committed_traffic(cfg.name, "tc_gemm_pair_kernel", int(round(tc_launch / K)))
     step_ms = ms_max / K
     adam_b, n_ad_params = adam_bytes(cfg, b)
     kernels = {c: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for c, v in prof.items()
@@ -347,7 +369,7 @@ def run_ours(args, rank, world):
         kernels["loss"]["bytes_per_step"] = lb
     out = {
         "metric": "trained tokens/sec per forward_backward+optim_step",
-        "value": N * K * world / (ms_max * 1e-3),
+        "value": job_throughput(N, K, world, ms_max),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -366,20 +388,36 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world}"},
         "tflops_algorithmic": fl["total"] * K * world / (ms_max * 1e-3) / 1e12,
         "frac_of_bf16_peak": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-        "roofline": {"kernel": "tc_gemm_pair_kernel<256,6,2> (LM head: forward, recompute+dz, dh)",
+        "roofline": {"kernel": "tc_gemm_pair_kernel<256,6,2> (base, LoRA-extension and LM-head GEMMs)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_tc,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
-                     "frac": (achieved / peak_tc) if achieved else None, "traffic": None,
-                     "launches_per_step": lm_launch / K,
-                     "algorithmic_flops_per_launch": lm_alg / max(1.0, lm_launch / K),
-                     "executed_tflops": executed,
-                     "gemm_family_tflops": family},
+                     "frac": (achieved / peak_tc) if achieved else None, "traffic": traffic,
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+                     "launches_per_step": tc_launch / K,
+                     "algorithmic_flops_per_launch": fl["tc256"] / max(1.0, tc_launch / K),
+                     "executed_tflops": executed},
         "kernels": kernels,
         "clocks": clk,
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
     return out, (cfg, base, ad, b)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / (ms_max * 1e-3)
 
 
 def make_oracle(cfg, base, ad):

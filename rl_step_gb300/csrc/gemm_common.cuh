@@ -28,7 +28,7 @@ enum EpiKind : int {
     EPI_STORE2 = 2,   // f32 = acc ; out0 = T(acc)                              (dh of the LM head)
     EPI_DSILU = 3,    // out0 = T(acc * silu'(aux))                             (du)
     EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
-    EPI_LMFWD = 5,    // per row: online max / sum-exp over cols < V, target z  (LM head)
+    EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z (LM head)
     EPI_LMDZ = 6,     // out0 = T(g (onehot(y) - exp(acc - lse)))               (LM head backward)
     EPI_GRAD = 7      // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
 };
@@ -44,10 +44,10 @@ struct EpiParams {
     int64_t ld_aux = 0;
     const float* gamma = nullptr;   // per adapter
     // LM head
-    float2* part = nullptr;         // [rows][part_ld] (running max, sum exp) per n-tile
+    float* part = nullptr;          // [rows][part_ld] log-sum-exp of each n-tile's columns
     float* zt = nullptr;            // target logit per row
     const int* tgt = nullptr;       // target id per padded row (-1: none)
-    int part_ld = 0;                // pitch of a row of partials (even)
+    int part_ld = 0;                // pitch of a row of partials (multiple of 4)
     int V = 0, Vpad = 0;
     const float* g = nullptr;       // dL/dl per padded row
     const float* lse = nullptr;     // logsumexp per padded row
@@ -256,7 +256,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
 __device__ __forceinline__ void epi_row_end(const EpiParams& ep, int64_t row, int ntile,
                                             const EpiRowState& st) {
     if (ep.kind == EPI_LMFWD) {
-        ep.part[row * ep.part_ld + ntile] = make_float2(st.m, st.s);
+        ep.part[row * ep.part_ld + ntile] = st.s > 0.f ? st.m + __logf(st.s) : -INFINITY;
         if (st.found) ep.zt[row] = st.zt;
     }
 }

@@ -43,8 +43,6 @@ void launch_embed(const int* perm_pad, const int* meta, int max_rows, const int*
                   const int* targets, const T* E, int V, int d, T* hb, float* h32, int* tgt_pad,
                   int* status, cudaStream_t s);
 
-constexpr int COMBINE_SPLIT = 4;    // CTAs per 128-row tile in the LM-head combine
-
 struct LossArgs {
     int kind;                 // -1 forward only, 0 CE, 1 IS, 2 PPO, 3 custom
     const float* w;
@@ -53,11 +51,12 @@ struct LossArgs {
     float clip;
     const float* dl;
 };
-void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, int part_ld, const float* zt,
+// LM-head partial combine + loss epilogue; per-row loss values to val_row.
+void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int part_ld, const float* zt,
                          const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
-                         float* logprobs_out, float* lse, float* g, double* loss_tile,
+                         float* logprobs_out, float* lse, float* g, double* val_row, int num_sms,
                          cudaStream_t s);
-void launch_loss_reduce(const double* loss_tile, const int* pad_off, int n_ad, double* loss_out,
+void launch_loss_reduce(const double* val_row, const int* pad_off, int n_ad, double* loss_out,
                         cudaStream_t s);
 
 struct AdamTab {

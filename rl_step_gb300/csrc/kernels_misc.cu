@@ -76,14 +76,13 @@ template void launch_embed<bf16>(const int*, const int*, int, const int*, const 
 
 // ----------------------------------------------------------------------------
 // LM-head combine + loss epilogue.
-// For padded row p: lse = M + log sum_j s_j exp(m_j - M) over the per-tile
-// partials (m_j, s_j); l = z[y] - lse (Tinker API Implementation on TPUs,
-// section 10.3: the target logprob is a gather minus a logsumexp).  Then the
-// per-token loss value and g = dL/dl (Deep Dive - Tinker, "The RL datum
-// shape"; custom: g is the caller's dC/dl), with non-finite inputs contained
-// (Tinker API Implementation on TPUs, section 12).  One CTA per 128-row tile;
-// the tile's loss sum (fp64) goes to loss_tile for a deterministic
-// per-adapter reduction.
+// For padded row p: lse = logsumexp_j(lse_j) over the log-sum-exp lse_j of
+// each 256-column vocabulary tile; l = z[y] - lse (Tinker API Implementation
+// on TPUs, section 10.3: the target logprob is a gather minus a logsumexp).
+// Then the per-token loss value and g = dL/dl (Deep Dive - Tinker, "The RL
+// datum shape"; custom: g is the caller's dC/dl), with non-finite inputs
+// contained (Tinker API Implementation on TPUs, section 12).  Per-row loss
+// values (fp64) are summed per adapter in row order: deterministic.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void token_loss_dev(int kind, float ell, int t, const LossArgs& la,
                                                double& val, float& g) {
@@ -123,7 +122,18 @@ __device__ __forceinline__ void token_loss_dev(int kind, float ell, int t, const
     if (!ok) { val = 0.0; g = 0.f; }
 }
 
-// (m, s) <- combination of two (max, sum exp(z - max)) partials
+// (m, s) <- (m, s) merged with one more log-sum-exp term x: afterwards
+// m + log(s) is the log-sum-exp of all terms folded so far.
+__device__ __forceinline__ void lse_fold(float& m, float& s, float x) {
+    if (x == -INFINITY) return;
+    if (x > m) {
+        s = s * __expf(m - x) + 1.f;
+        m = x;
+    } else {
+        s += __expf(x - m);
+    }
+}
+
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
     const float M = fmaxf(m, m2);
     if (M == -INFINITY) return;
@@ -131,108 +141,126 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     m = M;
 }
 
-// COMBINE_SPLIT CTAs (8 warps each) per 128-row tile; each warp combines
-// 128 / (8 * COMBINE_SPLIT) rows, one at a time: every lane issues up to
-// eight 16-byte loads of the row's partials before folding them into a
-// running (max, sum) pair, then the warp merges its lanes.  part_ld (even)
-// is the pitch of a row of partials, n_nt the number in use.  Each CTA's
-// loss sum goes to loss_part[tile * COMBINE_SPLIT + sub] for a deterministic
-// per-adapter reduction.
-constexpr int COMBINE_ROWS_PER_WARP = TILE_M / (8 * COMBINE_SPLIT);
+// Persistent combine: each warp walks padded rows (row = global warp id,
+// then + total warps).  The 16-byte loads of the next row's partials (one
+// log-sum-exp per 256-column vocabulary tile) and its metadata are issued
+// before the current row is folded, so HBM sees a steady stream; the warp
+// merges its lanes and lane 0 finishes the row (logprob, loss value, dL/dl).
+// part_ld (a multiple of 4) is the pitch of a row of partials, n_nt the
+// number in use.  Per-row loss values go to val_row for a deterministic
+// per-adapter reduction in row order.
+constexpr int COMBINE_VEC = 5;      // float4 per lane per row prefetched: 640 partials
+
+struct CombineRow {
+    float4 v[COMBINE_VEC];
+    int t, y;
+    float z;
+};
+
+__device__ __forceinline__ void combine_load(CombineRow& r, const float* __restrict__ part, int64_t p,
+                                             int n_nt, int part_ld, int lane, const float* __restrict__ zt,
+                                             const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad) {
+    const float4* row = reinterpret_cast<const float4*>(part + p * part_ld);
+    const int nvec = n_nt >> 2;
+#pragma unroll
+    for (int u = 0; u < COMBINE_VEC; ++u) {
+        const int j = lane + 32 * u;
+        r.v[u] = j < nvec ? row[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    r.t = -1; r.y = -1; r.z = 0.f;
+    if (lane == 0) {
+        r.t = perm_pad[p];
+        r.y = tgt_pad[p];
+        r.z = zt[p];
+    }
+}
 
 __global__ void __launch_bounds__(256) combine_loss_kernel(
-    LossArgs la, const float2* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
+    LossArgs la, const float* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
     const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
-    float* logprobs_out, float* lse_out, float* g_out, double* loss_part) {
-    const int mt = blockIdx.x / COMBINE_SPLIT;
-    const int sub = blockIdx.x % COMBINE_SPLIT;
-    if (mt >= meta[0]) return;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __shared__ double s_red[8];
-    double wsum = 0.0;
-    const int npair = n_nt >> 1;
-    for (int i = 0; i < COMBINE_ROWS_PER_WARP; ++i) {
-        const int64_t p = (int64_t)mt * TILE_M + (sub * 8 + warp) * COMBINE_ROWS_PER_WARP + i;
-        const float4* pr = reinterpret_cast<const float4*>(part + p * part_ld);
-        float m = -INFINITY, sum = 0.f;
-        for (int j0 = lane; j0 < npair; j0 += 32 * 8) {
-            float4 q[8];
+    float* logprobs_out, float* lse_out, float* g_out, double* val_row) {
+    const int rows = meta[0] * TILE_M;
+    const int lane = threadIdx.x & 31;
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    CombineRow cur, nxt;
+    int p = wid;
+    if (p < rows) combine_load(cur, part, p, n_nt, part_ld, lane, zt, perm_pad, tgt_pad);
+    for (; p < rows; p += nwarps) {
+        const int pn = p + nwarps;
+        if (pn < rows) combine_load(nxt, part, pn, n_nt, part_ld, lane, zt, perm_pad, tgt_pad);
+        float m = -INFINITY, sm = 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = j0 + 32 * u;
-                q[u] = j < npair ? pr[j] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                lse_merge(m, sum, q[u].x, q[u].y);
-                lse_merge(m, sum, q[u].z, q[u].w);
-            }
+        for (int u = 0; u < COMBINE_VEC; ++u) {
+            lse_fold(m, sm, cur.v[u].x);
+            lse_fold(m, sm, cur.v[u].y);
+            lse_fold(m, sm, cur.v[u].z);
+            lse_fold(m, sm, cur.v[u].w);
         }
-        if ((n_nt & 1) && lane == 0) {
-            const float2 q = part[p * part_ld + n_nt - 1];
-            lse_merge(m, sum, q.x, q.y);
-        }
+        // partials beyond the prefetched float4 groups (the n_nt % 4 tail, and
+        // vocabularies wider than 32 * COMBINE_VEC float4 groups)
+        const int done = 4 * min(n_nt >> 2, 32 * COMBINE_VEC);
+        for (int j = done + lane; j < n_nt; j += 32) lse_fold(m, sm, part[(int64_t)p * part_ld + j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-            lse_merge(m, sum, m2, s2);
+            const float mm = __shfl_xor_sync(0xffffffffu, m, o);
+            const float ss = __shfl_xor_sync(0xffffffffu, sm, o);
+            lse_merge(m, sm, mm, ss);
         }
         if (lane == 0) {
-            const int t = perm_pad[p];
+            double val = 0.0;
             float g = 0.f, lse = 0.f;
-            if (t >= 0) {
-                const int y = tgt_pad[p];
+            if (cur.t >= 0) {
                 float ell;
-                if (y >= 0) {
-                    lse = m + __logf(sum);
-                    ell = zt[p] - lse;
+                if (cur.y >= 0) {
+                    lse = m + __logf(sm);
+                    ell = cur.z - lse;
                 } else {
                     ell = __int_as_float(0x7fc00000);   // NaN: invalid token or target
                 }
-                double val;
-                token_loss_dev(la.kind, ell, t, la, val, g);
-                if (y < 0) g = 0.f, val = 0.0;
-                wsum += val;
-                if (logprobs_out) logprobs_out[t] = ell;
+                token_loss_dev(la.kind, ell, cur.t, la, val, g);
+                if (cur.y < 0) g = 0.f, val = 0.0;
+                if (logprobs_out) logprobs_out[cur.t] = ell;
             }
             lse_out[p] = lse;
             g_out[p] = g;
+            val_row[p] = val;
         }
-    }
-    if (lane == 0) s_red[warp] = wsum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < 8; ++w) t += s_red[w];
-        loss_part[blockIdx.x] = t;
+        cur = nxt;
     }
 }
 
-void launch_combine_loss(const LossArgs& la, const float2* part, int n_nt, int part_ld, const float* zt,
+void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int part_ld, const float* zt,
                          const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
-                         float* logprobs_out, float* lse, float* g, double* loss_part,
+                         float* logprobs_out, float* lse, float* g, double* val_row, int num_sms,
                          cudaStream_t s) {
     if (max_tiles <= 0) return;
-    combine_loss_kernel<<<max_tiles * COMBINE_SPLIT, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad,
-                                                                  tgt_pad, meta, logprobs_out, lse, g,
-                                                                  loss_part);
+    int blocks = num_sms * 4;
+    const int need = (max_tiles * TILE_M + 7) / 8;     // one row per warp at most
+    if (blocks > need) blocks = need;
+    combine_loss_kernel<<<blocks, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad, tgt_pad, meta,
+                                               logprobs_out, lse, g, val_row);
 }
 
-// Per-adapter loss: sum of its tiles' partial sums, in a fixed order.
-__global__ void loss_reduce_kernel(const double* loss_part, const int* pad_off, int n_ad,
-                                   double* loss_out) {
-    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n_ad; a += gridDim.x * blockDim.x) {
-        double s = 0.0;
-        for (int j = pad_off[a] / TILE_M * COMBINE_SPLIT; j < pad_off[a + 1] / TILE_M * COMBINE_SPLIT; ++j)
-            s += loss_part[j];
-        loss_out[a] = s;
+// Per-adapter loss: sum of its rows' loss values, in row order.
+__global__ void loss_reduce_kernel(const double* val_row, const int* pad_off, int n_ad, double* loss_out) {
+    const int a = blockIdx.x;
+    if (a >= n_ad) return;
+    __shared__ double sh[256];
+    double s = 0.0;
+    for (int j = pad_off[a] + threadIdx.x; j < pad_off[a + 1]; j += blockDim.x) s += val_row[j];
+    sh[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) loss_out[a] = sh[0];
 }
 
-void launch_loss_reduce(const double* loss_tile, const int* pad_off, int n_ad, double* loss_out,
+void launch_loss_reduce(const double* val_row, const int* pad_off, int n_ad, double* loss_out,
                         cudaStream_t s) {
-    loss_reduce_kernel<<<(n_ad + 127) / 128, 128, 0, s>>>(loss_tile, pad_off, n_ad, loss_out);
+    loss_reduce_kernel<<<n_ad, 256, 0, s>>>(val_row, pad_off, n_ad, loss_out);
 }
 
 // ----------------------------------------------------------------------------

@@ -80,11 +80,11 @@ struct mlora {
     void *dhb = nullptr, *dub = nullptr, *w1s = nullptr, *w2s = nullptr;
     // LM head
     int lm_bn = 32, n_nt = 0, part_ld = 0, nc_tiles = 0;
-    float2* part = nullptr;
+    float* part = nullptr;
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
     void* dz = nullptr;
-    double* loss_tile = nullptr;
+    double* val_row = nullptr;          // per padded row loss value
     int* status = nullptr;
     int* tile_counter = nullptr;        // GEMM tile scheduler (reset before each launch)
     // measurement: events around launches
@@ -236,7 +236,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
     h->Vpad = (h->V + 63) / 64 * 64;
     h->lm_bn = h->use_tc ? 256 : 32;
     h->n_nt = (h->V + h->lm_bn - 1) / h->lm_bn;
-    h->part_ld = (h->n_nt + 1) & ~1;   // even pitch: 16-byte aligned rows of partials
+    h->part_ld = (h->n_nt + 3) & ~3;   // 16-byte aligned rows of partials
 
     const int n_ad = h->n_ad, L = h->L, d = h->d, f = h->f, V = h->V;
     const size_t es = h->esize;
@@ -319,7 +319,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
             rc = fail(MLORA_E_CUDA, "cudaMemset of the dz chunk buffer failed");
             goto fail_out;
         }
-        ALLOC(h->loss_tile, (size_t)h->max_tiles * COMBINE_SPLIT);   // per (tile, combine CTA)
+        ALLOC(h->val_row, (size_t)MP);
         ALLOC(h->status, 1);
         ALLOC(h->tile_counter, 1);
     }
@@ -377,7 +377,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         CUDA_TRY(cudaMemset(h->touched, 0, sizeof(int) * n_ad));
         CUDA_TRY(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
         CUDA_TRY(cudaMemset(h->status, 0, sizeof(int)));
-        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float2) * (size_t)MP * h->part_ld));
+        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
         if (h->dtype == MLORA_BF16)
             launch_shadow_sync<bf16>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
         else
@@ -432,11 +432,26 @@ static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s, int cls) {
     return MLORA_OK;
 }
 
+// Raster band height (row tiles) for an A operand with K columns: tiles in
+// flight share B through L2 while a band of A (about 48 MB) stays resident.
+// For very long K every tile streams its whole operands, and a band of 16
+// row tiles keeps the set of tiles in flight close to square.
+static int band_for_k(int K) {
+    if (K >= 65536) return 16;
+    int rows = (int)((48ll << 20) / (2ll * K));
+    int tiles = rows / TILE_M;
+    tiles &= ~1;
+    if (tiles < 8) tiles = 8;
+    if (tiles > 64) tiles = 64;
+    return tiles;
+}
+
 // dense GEMM over the padded token rows of the current batch
 static GemmParams dense_params(mlora_t* h, int mt_upper, int N, int K) {
     GemmParams p;
     p.M = mt_upper * TILE_M;
     p.N = N; p.K = K; p.Kx = 0;
+    p.group_m = band_for_k(K);
     p.mtiles_dev = h->rb.meta;
     p.mt_base = 0; p.mt_count = mt_upper;
     p.tile_ad = h->rb.tile_ad;
@@ -540,7 +555,6 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         GemmParams p = dense_params(h, mt_upper, V, d);
         p.A = op_kmajor(h->hb[L], MP, d);
         p.B = op_kmajor(h->Wout, V, d);
-        p.group_m = 32;
         p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
         p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
         if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
@@ -549,12 +563,12 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     {
         ProfScope ps(h, s, MLORA_PROF_LOSS);
         launch_combine_loss(la, h->part, h->n_nt, h->part_ld, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
-                            logprobs_out, h->lse, h->gvec, h->loss_tile, s);
+                            logprobs_out, h->lse, h->gvec, h->val_row, h->num_sms, s);
         ++h->launches;
     }
     if (loss_out) {
         ProfScope ps(h, s, MLORA_PROF_OTHER);
-        launch_loss_reduce(h->loss_tile, h->rb.pad_off, n_ad, loss_out, s);
+        launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
         ++h->launches;
     }
     if (!backward) return MLORA_OK;
@@ -567,8 +581,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.mt_base = c0; p.mt_count = cnt;
             p.A = op_kmajor(h->hb[L], MP, d);
             p.B = op_kmajor(h->Wout, V, d);
-            p.group_m = 32;
-            p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
+                p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
             p.ep.tgt = h->tgt_pad; p.ep.V = V; p.ep.Vpad = h->Vpad;
             p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
