@@ -54,6 +54,8 @@ def parse_args():
                     help="tokens of the oracle's bounded CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="batch-invariant mode: one gradient chunk per adapter")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: override the block count (not a bench value)")
     return ap.parse_args()
@@ -226,6 +228,8 @@ def run_ours(args, rank, world):
     dad = [[[T(x) for x in row] for row in ad[k]] for k in ("A1", "B1", "A2", "B2")]
     h = m.mlora_create(cfg.vocab, cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.dtype, cfg.ranks,
                        cfg.alphas, N, dbase["E"], dbase["W1"], dbase["W2"], dbase["Wout"], *dad)
+    if args.deterministic:
+        m.mlora_set_deterministic(h, True)
     torch.cuda.synchronize()
     del dbase, dad                      # the library holds its own copies
     torch.cuda.empty_cache()
@@ -385,7 +389,8 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (frozen base %.1f GB)" %
                          ((2 * cfg.vocab * cfg.d_model + 2 * cfg.n_layers * cfg.d_model * cfg.d_ffn)
                           * (2 if cfg.dtype == "bf16" else 4) / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "deterministic": bool(args.deterministic)},
         "tflops_algorithmic": fl["total"] * K * world / (ms_max * 1e-3) / 1e12,
         "frac_of_bf16_peak": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
         "roofline": {"kernel": "tc_gemm_pair_kernel<256,6,2> (base, LoRA-extension and LM-head GEMMs)",

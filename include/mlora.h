@@ -197,6 +197,39 @@ int mlora_optim_step(mlora_t* h, const mlora_adam* p, const int32_t* adapters,
  * creates a recovery point".)  Errors: E_IO, E_CUDA. */
 int mlora_save_state(mlora_t* h, const char* path, void* stream);
 
+/* Restore every adapter from a checkpoint written by mlora_save_state
+ * (Deep Dive - Tinker, "optim_step advances adapter state" and "save_state
+ * creates a recovery point": loading weights alone resets the optimizer
+ * history; loading with the optimizer restores the saved moments).
+ * with_optimizer = 0 (load_state): weights from the file; first and second
+ * moments and step counts set to zero, so the next Adam step of each adapter
+ * is its first.  with_optimizer = 1 (load_state_with_optimizer): weights,
+ * moments and step counts from the file.  In both cases any gradient
+ * accumulated before the call is discarded (with its touched and non-finite
+ * flags), and the padded-rank copies the GEMMs read are refreshed.
+ * The file must match the handle: adapter count, n_layers, d_model, d_ffn,
+ * and per adapter rank and alpha (else E_ARG).  E_IO: cannot open, wrong
+ * magic or version, truncated, or trailing bytes.  The file is read and
+ * checked in full before the handle changes: on any error the adapter state
+ * is untouched.  Synchronises `stream` before and after the upload. */
+int mlora_load_state(mlora_t* h, const char* path, int32_t with_optimizer, void* stream);
+
+/* Export one adapted projection as a standalone base matrix (Deep Dive -
+ * Tinker, "Checkpoints and export paths": merging W' = W + gamma B A turns
+ * an adapter into a standalone model; gamma = alpha / r).
+ * which = 0: out = W1[layer] + gamma B1 A1, [d_ffn x d_model];
+ * which = 1: out = W2[layer] + gamma B2 A2, [d_model x d_ffn];
+ * row-major in the base dtype, out a DEVICE buffer (16-byte aligned) owned
+ * by the caller.  B A is taken from the adapter's fp32 master weights: on a
+ * bf16 base each factor is split into two bf16 parts so that the tensor-core
+ * product carries about 16 significant bits before the single rounding of
+ * W + gamma B A to bf16.  A model whose every W1, W2 is replaced by its
+ * export and that runs without the adapter gives the adapter's logprobs.
+ * Queued on `stream`.  Errors: E_ARG (NULL, unaligned out, adapter, layer
+ * or which out of range), E_CUDA. */
+int mlora_export_merged(mlora_t* h, int32_t adapter, int32_t layer, int32_t which, void* out,
+                        void* stream);
+
 /* Copy one fp32 adapter tensor (see mlora_tensor) of adapter `adapter`,
  * layer `layer` into dst (DEVICE, caller-owned, shape as documented there).
  * Test and inspection hook. */
@@ -245,6 +278,26 @@ int mlora_get_routing(mlora_t* h, const int32_t* adapter_ids, int64_t n, int32_t
 int mlora_routing_noalloc(const int32_t* adapter_ids, int64_t n, int32_t n_adapters,
                           int32_t* perm, int32_t* seg_off, int32_t* pad_off, int32_t* tile_ad,
                           void* stream);
+
+/* Deterministic (batch-invariant) mode (tinker-ticks, "Why RL needs
+ * batch-invariant kernels": a token's result must not depend on how many
+ * other tokens share the batch, and must repeat bit for bit).
+ *
+ * Logprobs and losses are batch-invariant in both modes: every GEMM's tile
+ * shape and instruction depend only on the layer widths, each output element
+ * sums its contraction in one fixed order inside one tile, the LM-head
+ * log-sum-exp merges its column-tile partials in a fixed order, and each
+ * adapter's loss sum runs over its own padded segment.  What on = 1 adds is
+ * the gradients: each adapter's token rows form ONE gradient work chunk
+ * (instead of chunks of 1024 padded rows met by fp32 atomics in arrival
+ * order), so every gradient element has one writer and one summation order.
+ * An adapter's gradients, and the weights after mlora_optim_step, are then
+ * bitwise the same on every run and whichever other adapters share the
+ * batch (given its own tokens in the same order).  Cost: an adapter with
+ * many tokens reduces over them in fewer, longer tiles.
+ * The mode is a host-side flag read at each forward/backward launch; the
+ * default is 0.  Errors: E_ARG (NULL handle, on not 0 or 1). */
+int mlora_set_deterministic(mlora_t* h, int32_t on);
 
 /* Synchronise `stream`, then return and clear the device status word:
  * MLORA_OK, MLORA_E_RANGE or MLORA_E_TIMEOUT. */

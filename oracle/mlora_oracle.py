@@ -257,6 +257,13 @@ class Oracle:
         h, _, _ = self.forward_hidden(tokens, adapter_ids)
         return self.logprobs_from_hidden(h, targets)[0]
 
+    def merged_weight(self, a: int, l: int, which: str) -> np.ndarray:
+        """W' = W + gamma B A for W1 or W2 of layer l with adapter a's factors
+        (Deep Dive - Tinker, "Checkpoints and export paths"), in fp64."""
+        if which == "W1":
+            return self.W1[l] + self.gamma[a] * (self.P["B1"][a][l] @ self.P["A1"][a][l])
+        return self.W2[l] + self.gamma[a] * (self.P["B2"][a][l] @ self.P["A2"][a][l])
+
     # -- backward -----------------------------------------------------------
     def dlogits(self, h_block, y_block, lse_block, g_block) -> np.ndarray:
         """dL/dz = g (onehot(y) - softmax(z)) for a block of tokens."""
@@ -401,3 +408,37 @@ def read_state_file(path: str) -> dict:
     if off != len(buf):
         raise ValueError("trailing bytes in checkpoint")
     return out
+
+
+def load_state_file(path: str, o: "Oracle", with_optimizer: bool) -> None:
+    """Restore the oracle's adapters from a checkpoint file.
+
+    Deep Dive - Tinker, "optim_step advances adapter state": loading the
+    weights alone resets the optimizer history, loading with the optimizer
+    restores the saved moments; "save_state creates a recovery point" names
+    the two calls load_state and load_state_with_optimizer.  Reading taken
+    where the page is silent: a reset history means zero moments and a step
+    count of zero (the next Adam step is the first, with its bias
+    correction), and any gradient accumulated before the load is dropped.
+    The file must describe the same adapters (count, layers, widths, ranks,
+    alphas); otherwise ValueError and the oracle is unchanged.
+    """
+    st = read_state_file(path)
+    if (st["n_adapters"], st["n_layers"], st["d_model"], st["d_ffn"]) != (o.n_adapters, o.L, o.d, o.f):
+        raise ValueError("checkpoint shape does not match")
+    for a, rec in enumerate(st["adapters"]):
+        if rec["rank"] != o.ranks[a] or np.float32(rec["alpha"]) != np.float32(o.alphas[a]):
+            raise ValueError(f"adapter {a}: rank or alpha does not match")
+    for a, rec in enumerate(st["adapters"]):
+        for k in TENSORS:
+            for l in range(o.L):
+                o.P[k][a][l] = rec["P"][k][l].astype(np.float64)
+                if with_optimizer:
+                    o.M[k][a][l] = rec["M"][k][l].astype(np.float64)
+                    o.Vm[k][a][l] = rec["V"][k][l].astype(np.float64)
+                else:
+                    o.M[k][a][l] = np.zeros_like(o.P[k][a][l])
+                    o.Vm[k][a][l] = np.zeros_like(o.P[k][a][l])
+                o.G[k][a][l] = np.zeros_like(o.P[k][a][l])
+        o.step[a] = int(rec["step"]) if with_optimizer else 0
+    o.touched = set()

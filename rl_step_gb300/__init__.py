@@ -27,9 +27,9 @@ from typing import Optional, Sequence
 __all__ = [
     "LIB_PATH", "load_library", "MLoRAError", "Handle",
     "mlora_create", "mlora_destroy", "mlora_forward", "mlora_forward_backward",
-    "mlora_forward_backward_custom", "mlora_optim_step", "mlora_save_state",
+    "mlora_forward_backward_custom", "mlora_optim_step", "mlora_save_state", "mlora_load_state", "mlora_export_merged",
     "mlora_read_adapter", "mlora_write_adapter", "mlora_get_steps", "mlora_get_routing",
-    "mlora_check_status", "mlora_routing_noalloc", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
+    "mlora_check_status", "mlora_routing_noalloc", "mlora_set_deterministic", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
     "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
 ]
 
@@ -91,6 +91,8 @@ _SIGNATURES = {
     "mlora_optim_step": (c_int32, [c_void_p, POINTER(_Adam), POINTER(c_int32), c_int32, c_void_p,
                                    c_void_p]),
     "mlora_save_state": (c_int32, [c_void_p, c_char_p, c_void_p]),
+    "mlora_load_state": (c_int32, [c_void_p, c_char_p, c_int32, c_void_p]),
+    "mlora_export_merged": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "mlora_read_adapter": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "mlora_write_adapter": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "mlora_get_steps": (c_int32, [c_void_p, POINTER(c_int64), c_void_p]),
@@ -99,6 +101,7 @@ _SIGNATURES = {
     "mlora_check_status": (c_int32, [c_void_p, c_void_p]),
     "mlora_routing_noalloc": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_void_p]),
+    "mlora_set_deterministic": (c_int32, [c_void_p, c_int32]),
     "mlora_profile_enable": (c_int32, [c_void_p, c_int32]),
     "mlora_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_kernel_launches": (c_int64, [c_void_p]),
@@ -146,8 +149,10 @@ def _stream(stream):
 class Handle:
     """Owns one mlora_t*; keeps the config it was created with."""
 
-    def __init__(self, ptr: int, n_adapters: int, ranks, d: int, f: int, n_layers: int):
+    def __init__(self, ptr: int, n_adapters: int, ranks, d: int, f: int, n_layers: int,
+                 dtype: str = "bf16"):
         self.ptr = c_void_p(ptr)
+        self.dtype = dtype
         self.n_adapters = n_adapters
         self.ranks = list(ranks)
         self.d, self.f, self.n_layers = d, f, n_layers
@@ -197,7 +202,7 @@ def mlora_create(vocab: int, d_model: int, d_ffn: int, n_layers: int, dtype: str
                  *[ctypes.cast(t, POINTER(c_void_p)) if t is not None else None for t in tabs])
     out = c_void_p()
     _check(_lib.mlora_create(ctypes.byref(cfg), ctypes.byref(init), ctypes.byref(out)))
-    return Handle(out.value, n_ad, ranks, d_model, d_ffn, n_layers)
+    return Handle(out.value, n_ad, ranks, d_model, d_ffn, n_layers, dtype)
 
 
 def mlora_destroy(h: Handle):
@@ -274,6 +279,25 @@ def mlora_save_state(h: Handle, path: str, stream=None):
     _check(_lib.mlora_save_state(h.ptr, os.fsencode(path), _stream(stream)))
 
 
+def mlora_load_state(h: Handle, path: str, with_optimizer: bool = False, stream=None):
+    """load_state (weights; optimizer reset) or load_state_with_optimizer."""
+    _check(_lib.mlora_load_state(h.ptr, os.fsencode(path), 1 if with_optimizer else 0,
+                                 _stream(stream)))
+
+
+def mlora_export_merged(h: Handle, adapter: int, layer: int, which: str, out=None, stream=None):
+    """W' = W + gamma B A of W1 (which="W1", [f, d]) or W2 ("W2", [d, f]) in the base dtype."""
+    import torch
+    idx = {"W1": 0, "W2": 1}[which]
+    shape = (h.f, h.d) if idx == 0 else (h.d, h.f)
+    if out is None:
+        dt = torch.bfloat16 if h.dtype == "bf16" else torch.float32
+        out = torch.empty(shape, dtype=dt, device="cuda")
+    assert tuple(out.shape) == shape and out.is_contiguous()
+    _check(_lib.mlora_export_merged(h.ptr, adapter, layer, idx, _ptr(out), _stream(stream)))
+    return out
+
+
 def mlora_read_adapter(h: Handle, adapter: int, layer: int, which: str, stream=None):
     import torch
     out = torch.empty(h.shape_of(which, adapter), dtype=torch.float32, device="cuda")
@@ -332,6 +356,11 @@ def mlora_routing_noalloc(adapter_ids, n_adapters: int, stream=None):
 def mlora_check_status(h: Handle, stream=None) -> int:
     """Synchronise and return the device status code (0, -2 E_RANGE, -5 E_TIMEOUT)."""
     return int(_lib.mlora_check_status(h.ptr, _stream(stream)))
+
+
+def mlora_set_deterministic(h: Handle, on: bool = True):
+    """One gradient chunk per adapter: bitwise-reproducible gradients."""
+    _check(_lib.mlora_set_deterministic(h.ptr, 1 if on else 0))
 
 
 def mlora_profile_enable(h: Handle, on: bool = True):

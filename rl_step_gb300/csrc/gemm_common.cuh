@@ -30,7 +30,8 @@ enum EpiKind : int {
     EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
     EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z (LM head)
     EPI_LMDZ = 6,     // out0 = T(g (onehot(y) - exp(acc - lse)))               (LM head backward)
-    EPI_GRAD = 7      // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
+    EPI_GRAD = 7,     // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
+    EPI_MERGE = 8     // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
 };
 
 struct EpiParams {
@@ -232,6 +233,14 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
             }
         }
         store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, d);
+    } break;
+    case EPI_MERGE: {
+        float w[32];
+        load32<T>(reinterpret_cast<const T*>(ep.aux) + row * ep.ld_aux + col0, w);
+        const float gm = ep.gamma[adapter];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = fmaf(gm, acc[j], w[j]);
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, w);
     } break;
     case EPI_GRAD: {
         int r = ep.ranks[adapter];

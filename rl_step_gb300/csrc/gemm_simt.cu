@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(128) simt_gemm_kernel(GemmParams p) {
     if (p.Kx > 0) simt_k_loop<T>(p.Ax, p.Bx, adapter, m0, n0, 0, p.Kx, acc, As, Bs);
 
     const int64_t row = m0 + threadIdx.x;
-    if (p.grouped && row >= p.M) return;
+    if (row >= p.M) return;
     EpiRowState st;
     epi_row_begin(st);
     epi_chunk<T>(p.ep, row, (int)n0, adapter, acc, st);

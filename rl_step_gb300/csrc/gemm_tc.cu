@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const int64_t row = (int64_t)c.mt * BM + 32 * q + lane;
-            const bool row_ok = !p.grouped || row < p.M;
+            const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
             epilogue_row<BN>(p, tbase, row, row_ok, c.nt * BN, c.adapter, c.nt);
             tc_fence_before();
@@ -934,8 +934,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const int my_mt = c.mt + (int)rank;
-            const bool tile_ok = (my_mt - p.mt_base) < cnt;
             const int64_t row = (int64_t)my_mt * BM + 32 * q + lane;
+            const bool tile_ok = (my_mt - p.mt_base) < cnt && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
             epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
             tc_fence_before();

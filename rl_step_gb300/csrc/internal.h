@@ -32,8 +32,10 @@ struct RouteBufs {
 constexpr int ROUTE_BLOCK = 1024;   // tokens per routing block
 constexpr int GRAD_CHUNK = 1024;    // padded token rows per gradient work chunk
 
+// chunk_rows: padded rows per gradient chunk; 0 = one chunk per adapter segment
 void launch_routing(const int* adapter_ids, int64_t n, int n_ad, const RouteBufs& rb,
-                    int* touched, int* status, cudaStream_t s, int64_t* launches);
+                    int* touched, int* status, cudaStream_t s, int64_t* launches,
+                    int chunk_rows = GRAD_CHUNK);
 void launch_compact_perm(const RouteBufs& rb, int n_ad, int* perm_out, cudaStream_t s,
                          int64_t* launches);
 
@@ -80,6 +82,11 @@ void launch_adam(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d
 template <typename T>
 void launch_shadow_sync(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d, int f,
                         int64_t total, const float* P, const ShadowMap& sh, cudaStream_t s);
+
+// GEMM operands of W' = W + gamma B A (bf16: hi/lo split, K = 3*RP; fp32: K = RP)
+template <typename T>
+void launch_merge_operands(const float* Bf, const float* Af, int M, int N, int r, T* Aop, T* Bop,
+                           cudaStream_t s);
 
 template <typename T>
 void launch_transpose(const T* in, T* out, int rows, int cols, cudaStream_t s);

@@ -472,4 +472,57 @@ void launch_transpose(const T* in, T* out, int rows, int cols, cudaStream_t s) {
 template void launch_transpose<float>(const float*, float*, int, int, cudaStream_t);
 template void launch_transpose<bf16>(const bf16*, bf16*, int, int, cudaStream_t);
 
+// ----------------------------------------------------------------------------
+// Operands of the merge W' = W + gamma B A (B: [M x r], A: [r x N], fp32
+// masters) for one tensor-core GEMM with K = 3 * RP.  Each factor is split
+// into bf16 parts, x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), and
+//   Aop [M x 3RP]  = [ B_hi | B_hi | B_lo ]      (K-major)
+//   Bop [3RP x N]  = [ A_hi ; A_lo ; A_hi ]      (rows = K, MN-major)
+// so that Aop Bop = B_hi A_hi + B_hi A_lo + B_lo A_hi, which differs from
+// B A only by B_lo A_lo (relative size 2^-16).  Columns / rows j >= r are 0.
+// For an fp32 base the factors are copied as they are into the first RP
+// columns / rows (K = RP).
+// ----------------------------------------------------------------------------
+template <typename T>
+__global__ void merge_operands_kernel(const float* __restrict__ Bf, const float* __restrict__ Af,
+                                      int M, int N, int r, T* __restrict__ Aop, T* __restrict__ Bop) {
+    constexpr bool SPLIT = sizeof(T) == 2;
+    constexpr int KP = SPLIT ? 3 * RP : RP;
+    const int64_t na = (int64_t)M * KP, nb = (int64_t)KP * N;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < na + nb;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        if (i < na) {
+            const int64_t m = i / KP;
+            const int c = (int)(i - m * KP), part = c / RP, j = c % RP;
+            float x = j < r ? Bf[m * r + j] : 0.f;
+            if (SPLIT) {
+                float hi = __bfloat162float(__float2bfloat16_rn(x));
+                x = part < 2 ? hi : x - hi;
+            }
+            Aop[i] = from_f<T>(x);
+        } else {
+            const int64_t q = i - na;
+            const int c = (int)(q / N);
+            const int64_t n = q - (int64_t)c * N;
+            const int part = c / RP, j = c % RP;
+            float x = j < r ? Af[(int64_t)j * N + n] : 0.f;
+            if (SPLIT) {
+                float hi = __bfloat162float(__float2bfloat16_rn(x));
+                x = part == 1 ? x - hi : hi;
+            }
+            Bop[q] = from_f<T>(x);
+        }
+    }
+}
+
+template <typename T>
+void launch_merge_operands(const float* Bf, const float* Af, int M, int N, int r, T* Aop, T* Bop,
+                           cudaStream_t s) {
+    merge_operands_kernel<T><<<152 * 8, 256, 0, s>>>(Bf, Af, M, N, r, Aop, Bop);
+}
+template void launch_merge_operands<float>(const float*, const float*, int, int, int, float*, float*,
+                                           cudaStream_t);
+template void launch_merge_operands<bf16>(const float*, const float*, int, int, int, bf16*, bf16*,
+                                          cudaStream_t);
+
 }  // namespace mlk

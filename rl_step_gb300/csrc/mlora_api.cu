@@ -53,6 +53,7 @@ struct mlora {
     std::vector<void*> allocs;
     int64_t bytes = 0;
     int64_t launches = 0;
+    int deterministic = 0;   // 1: one gradient chunk per adapter (fixed-order reductions)
 
     // frozen base
     void* E = nullptr;
@@ -87,6 +88,7 @@ struct mlora {
     double* val_row = nullptr;          // per padded row loss value
     int* status = nullptr;
     int* tile_counter = nullptr;        // GEMM tile scheduler (reset before each launch)
+    void *mg_a = nullptr, *mg_b = nullptr;  // merge operands, max(d, f) x 3*RP each
     // measurement: events around launches
     bool prof = false;
     std::vector<cudaEvent_t> ev;      // pairs (start, stop)
@@ -322,6 +324,8 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOC(h->val_row, (size_t)MP);
         ALLOC(h->status, 1);
         ALLOC(h->tile_counter, 1);
+        ALLOCB(h->mg_a, (size_t)(d > f ? d : f) * 3 * RP * es);
+        ALLOCB(h->mg_b, (size_t)(d > f ? d : f) * 3 * RP * es);
     }
 #undef ALLOC
 #undef ALLOCB
@@ -502,7 +506,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     {
         ProfScope ps(h, s, MLORA_PROF_ROUTING);
         launch_routing(b->adapter_ids, N, n_ad, h->rb, backward ? h->touched : nullptr, h->status, s,
-                       &h->launches);
+                       &h->launches, h->deterministic ? 0 : GRAD_CHUNK);
     }
     // a2 embedding
     {
@@ -864,6 +868,133 @@ extern "C" int mlora_save_state(mlora_t* h, const char* path, void* stream) {
     }
     ok = (fclose(fh) == 0) && ok;
     if (!ok) return fail(MLORA_E_IO, "write to %s failed", path);
+    return MLORA_OK;
+}
+
+template <typename T>
+static int export_impl(mlora_t* h, int a, int l, int which, void* out, cudaStream_t s) {
+    const int r = h->ranks[a];
+    // W1 [f x d] = W1 + g B1 [f x r] A1 [r x d];  W2 [d x f] = W2 + g B2 [d x r] A2 [r x f]
+    const int M = which == 0 ? h->f : h->d;
+    const int N = which == 0 ? h->d : h->f;
+    const float* Bf = h->P + tensor_off(h, a, l, which == 0 ? 1 : 3);
+    const float* Af = h->P + tensor_off(h, a, l, which == 0 ? 0 : 2);
+    const int KP = sizeof(T) == 2 ? 3 * RP : RP;
+    launch_merge_operands<T>(Bf, Af, M, N, r, reinterpret_cast<T*>(h->mg_a), reinterpret_cast<T*>(h->mg_b), s);
+    ++h->launches;
+    GemmParams p;
+    p.M = M; p.N = N; p.K = KP; p.Kx = 0;
+    p.group_m = band_for_k(KP);
+    p.mtiles_dev = nullptr;
+    p.mt_base = 0; p.mt_count = (M + TILE_M - 1) / TILE_M;
+    p.tile_ad = nullptr;
+    p.A = op_kmajor(h->mg_a, M, KP);
+    p.B = op_mnmajor(h->mg_b, KP, N);
+    p.ep.kind = EPI_MERGE;
+    p.ep.aux = which == 0 ? h->W1[l] : h->W2[l];
+    p.ep.ld_aux = N;
+    p.ep.out0 = out;
+    p.ep.ld0 = N;
+    p.ep.gamma = h->gamma_d + a;
+    return run_gemm<T>(h, p, s, MLORA_PROF_OTHER);
+}
+
+extern "C" int mlora_export_merged(mlora_t* h, int32_t adapter, int32_t layer, int32_t which, void* out,
+                                   void* stream) {
+    if (!h || !out) return fail(MLORA_E_ARG, "NULL argument");
+    if (adapter < 0 || adapter >= h->n_ad) return fail(MLORA_E_ARG, "adapter %d out of range", adapter);
+    if (layer < 0 || layer >= h->L) return fail(MLORA_E_ARG, "layer %d out of range", layer);
+    if (which != 0 && which != 1) return fail(MLORA_E_ARG, "which must be 0 (W1) or 1 (W2)");
+    if ((reinterpret_cast<uintptr_t>(out) & 15) != 0) return fail(MLORA_E_ARG, "out must be 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc = h->dtype == MLORA_BF16 ? export_impl<bf16>(h, adapter, layer, which, out, s)
+                                    : export_impl<float>(h, adapter, layer, which, out, s);
+    if (rc) return rc;
+    CUDA_TRY(cudaGetLastError());
+    return MLORA_OK;
+}
+
+// Reads the whole file into host memory and checks it before touching the
+// handle, so a rejected file leaves the adapter state as it was.
+extern "C" int mlora_load_state(mlora_t* h, const char* path, int32_t with_optimizer, void* stream) {
+    if (!h || !path) return fail(MLORA_E_ARG, "NULL argument");
+    if (with_optimizer != 0 && with_optimizer != 1) return fail(MLORA_E_ARG, "with_optimizer must be 0 or 1");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    FILE* fh = fopen(path, "rb");
+    if (!fh) return fail(MLORA_E_IO, "cannot open %s for reading", path);
+    std::vector<float> P(h->n_params), M(h->n_params), Vv(h->n_params);
+    std::vector<int64_t> steps(h->n_ad);
+    bool ok = true;
+    auto get = [&](void* p, size_t n) { ok = ok && fread(p, 1, n, fh) == n; return ok; };
+    char magic[8];
+    uint32_t hdr[6];
+    int rc = MLORA_OK;
+    if (!get(magic, 8) || memcmp(magic, "MLORASTA", 8) != 0) {
+        rc = fail(MLORA_E_IO, "%s is not an adapter checkpoint", path);
+    } else if (!get(hdr, sizeof(hdr))) {
+        rc = fail(MLORA_E_IO, "%s: truncated header", path);
+    } else if (hdr[0] != 1u) {
+        rc = fail(MLORA_E_IO, "%s: unsupported checkpoint version %u", path, hdr[0]);
+    } else if (hdr[1] != (uint32_t)h->n_ad || hdr[2] != (uint32_t)h->L || hdr[3] != (uint32_t)h->d ||
+               hdr[4] != (uint32_t)h->f) {
+        rc = fail(MLORA_E_ARG, "%s holds %u adapters, L=%u d=%u f=%u; the handle has %d, L=%d d=%d f=%d",
+                  path, hdr[1], hdr[2], hdr[3], hdr[4], h->n_ad, h->L, h->d, h->f);
+    }
+    for (int a = 0; a < h->n_ad && rc == MLORA_OK; ++a) {
+        uint32_t r;
+        float al;
+        uint64_t st;
+        if (!get(&r, 4) || !get(&al, 4) || !get(&st, 8)) {
+            rc = fail(MLORA_E_IO, "%s: truncated at adapter %d", path, a);
+            break;
+        }
+        if ((int)r != h->ranks[a] || al != h->alphas[a]) {
+            rc = fail(MLORA_E_ARG, "%s: adapter %d has rank %u alpha %g; the handle has rank %d alpha %g",
+                      path, a, r, (double)al, h->ranks[a], (double)h->alphas[a]);
+            break;
+        }
+        steps[a] = (int64_t)st;
+        std::vector<float>* grp[3] = {&P, &M, &Vv};
+        for (int g = 0; g < 3; ++g)
+            for (int l = 0; l < h->L; ++l)
+                for (int k = 0; k < 4; ++k)
+                    get(grp[g]->data() + tensor_off(h, a, l, k),
+                        sizeof(float) * tensor_size(k, h->ranks[a], h->d, h->f));
+        if (!ok) rc = fail(MLORA_E_IO, "%s: truncated in adapter %d", path, a);
+    }
+    if (rc == MLORA_OK && fgetc(fh) != EOF) rc = fail(MLORA_E_IO, "%s: trailing bytes", path);
+    fclose(fh);
+    if (rc != MLORA_OK) return rc;
+
+    const size_t nb = sizeof(float) * h->n_params;
+    CUDA_TRY(cudaStreamSynchronize(s));
+    CUDA_TRY(cudaMemcpyAsync(h->P, P.data(), nb, cudaMemcpyHostToDevice, s));
+    if (with_optimizer) {
+        CUDA_TRY(cudaMemcpyAsync(h->M, M.data(), nb, cudaMemcpyHostToDevice, s));
+        CUDA_TRY(cudaMemcpyAsync(h->Vm, Vv.data(), nb, cudaMemcpyHostToDevice, s));
+        CUDA_TRY(cudaMemcpyAsync(h->step, steps.data(), sizeof(int64_t) * h->n_ad, cudaMemcpyHostToDevice, s));
+    } else {
+        CUDA_TRY(cudaMemsetAsync(h->M, 0, nb, s));
+        CUDA_TRY(cudaMemsetAsync(h->Vm, 0, nb, s));
+        CUDA_TRY(cudaMemsetAsync(h->step, 0, sizeof(int64_t) * h->n_ad, s));
+    }
+    CUDA_TRY(cudaMemsetAsync(h->G, 0, nb, s));
+    CUDA_TRY(cudaMemsetAsync(h->touched, 0, sizeof(int) * h->n_ad, s));
+    CUDA_TRY(cudaMemsetAsync(h->nonfinite, 0, sizeof(int) * h->n_ad, s));
+    if (h->dtype == MLORA_BF16)
+        launch_shadow_sync<bf16>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->P, h->shadow, s);
+    else
+        launch_shadow_sync<float>(h->n_ad, h->ad_off, h->ranks_d, h->L, h->d, h->f, h->n_params, h->P, h->shadow, s);
+    ++h->launches;
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return MLORA_OK;
+}
+
+extern "C" int mlora_set_deterministic(mlora_t* h, int32_t on) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    if (on != 0 && on != 1) return fail(MLORA_E_ARG, "on must be 0 or 1");
+    h->deterministic = on;
     return MLORA_OK;
 }
 

@@ -6,7 +6,10 @@
 // rows ("padded order"), so each 128-row GEMM tile belongs to exactly one
 // adapter.  perm_pad[p] is the batch position of padded row p, or -1 for a
 // padding row.  The same pass emits the per-tile adapter map and the list of
-// gradient work chunks (at most GRAD_CHUNK padded rows of one adapter each).
+// gradient work chunks (at most chunk_rows padded rows of one adapter each;
+// chunk_rows == 0 makes each adapter's whole padded segment one chunk, so
+// its gradient reduction runs in one fixed order with one writer per
+// element: the deterministic mode).
 //
 // Three launches, all on the caller's stream, no host synchronisation:
 //   route_count    per 1024-token block, per-adapter counts
@@ -36,7 +39,7 @@ __global__ void route_count(const int* __restrict__ ids, int64_t n, int n_ad, in
 
 __global__ void route_scan(int nblk, int n_ad, int* blk_cnt, int* seg_off, int* pad_off,
                            int* tile_ad, int max_tiles, int* meta, int4* chunks, int max_chunks,
-                           int* touched) {
+                           int chunk_rows, int* touched) {
     extern __shared__ int sh[];
     int* s_cnt = sh;             // [n_ad]
     int* s_pad = sh + n_ad;      // [n_ad + 1] padded offsets
@@ -64,7 +67,7 @@ __global__ void route_scan(int nblk, int n_ad, int* blk_cnt, int* seg_off, int* 
             int padded = (c + TILE_M - 1) / TILE_M * TILE_M;
             seg += c;
             pad += padded;
-            nch += (padded + GRAD_CHUNK - 1) / GRAD_CHUNK;
+            nch += chunk_rows > 0 ? (padded + chunk_rows - 1) / chunk_rows : (padded > 0);
         }
         seg_off[n_ad] = seg;
         pad_off[n_ad] = pad;
@@ -78,12 +81,12 @@ __global__ void route_scan(int nblk, int n_ad, int* blk_cnt, int* seg_off, int* 
         int t0 = s_pad[a] / TILE_M, t1 = s_pad[a + 1] / TILE_M;
         for (int j = t0; j < t1 && j < max_tiles; ++j) tile_ad[j] = a;
         int padded = s_pad[a + 1] - s_pad[a];
-        int nc = (padded + GRAD_CHUNK - 1) / GRAD_CHUNK;
+        const int step = chunk_rows > 0 ? chunk_rows : padded;
+        const int nc = padded > 0 ? (padded + step - 1) / step : 0;
         for (int c = 0; c < nc; ++c) {
             int ci = s_ch[a] + c;
             if (ci < max_chunks)
-                chunks[ci] = make_int4(a, s_pad[a] + c * GRAD_CHUNK,
-                                       min(GRAD_CHUNK, padded - c * GRAD_CHUNK), 0);
+                chunks[ci] = make_int4(a, s_pad[a] + c * step, min(step, padded - c * step), 0);
         }
     }
     for (int j = s_pad[n_ad] / TILE_M + threadIdx.x; j < max_tiles; j += blockDim.x) tile_ad[j] = -1;
@@ -121,7 +124,7 @@ __global__ void route_scatter(const int* __restrict__ ids, int64_t n, int n_ad,
 }
 
 void launch_routing(const int* adapter_ids, int64_t n, int n_ad, const RouteBufs& rb, int* touched,
-                    int* status, cudaStream_t s, int64_t* launches) {
+                    int* status, cudaStream_t s, int64_t* launches, int chunk_rows) {
     int nblk = (int)((n + ROUTE_BLOCK - 1) / ROUTE_BLOCK);
     cudaMemsetAsync(rb.perm_pad, 0xff, sizeof(int) * (size_t)rb.max_pad, s);
     if (nblk > 0) {
@@ -131,7 +134,7 @@ void launch_routing(const int* adapter_ids, int64_t n, int n_ad, const RouteBufs
     }
     route_scan<<<1, 1024, sizeof(int) * (3 * n_ad + 2), s>>>(
         nblk, n_ad, rb.blk_cnt, rb.seg_off, rb.pad_off, rb.tile_ad, rb.max_tiles, rb.meta, rb.chunks,
-        rb.max_chunks, touched);
+        rb.max_chunks, chunk_rows, touched);
     ++*launches;
     if (nblk > 0) {
         route_scatter<<<nblk, ROUTE_BLOCK, sizeof(int) * n_ad, s>>>(adapter_ids, n, n_ad, rb.blk_cnt,

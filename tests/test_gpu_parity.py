@@ -238,3 +238,90 @@ def test_save_state_round_trip(tmp_path):
                 assert np.array_equal(rec["P"][k][l], m.mlora_read_adapter(h, a, l, k).cpu().numpy())
                 assert np.array_equal(rec["M"][k][l], m.mlora_read_adapter(h, a, l, "m" + k).cpu().numpy())
                 assert np.array_equal(rec["V"][k][l], m.mlora_read_adapter(h, a, l, "v" + k).cpu().numpy())
+
+
+def _state(h, cfg, prefixes=("", "m", "v")):
+    import rl_step_gb300 as m
+    return {(p, a, l, k): m.mlora_read_adapter(h, a, l, p + k).cpu().numpy()
+            for p in prefixes for a in range(cfg.n_adapters) for l in range(cfg.n_layers)
+            for k in oracle.TENSORS}
+
+
+def test_load_state_with_and_without_optimizer(tmp_path):
+    """load_state_with_optimizer restores weights, moments and step counts
+    bitwise and the resumed run takes the uninterrupted run's next step;
+    load_state restores the weights only, and the next step matches the
+    oracle restarted from the same file."""
+    import rl_step_gb300 as m
+    cfg, base, ad, b, o, _ = _setup("tiny_fp32", None)
+    N = len(b["tokens"])
+    ha = create_handle(cfg, base, ad, N)
+    for _ in range(2):
+        run_gpu_step(ha, b, "cross_entropy")
+        m.mlora_optim_step(ha, lr=1e-3)
+    path = str(tmp_path / "state.bin")
+    m.mlora_save_state(ha, path)
+    saved = _state(ha, cfg)
+    # resume with the optimizer in a handle that holds a pending gradient
+    hb = create_handle(cfg, base, ad, N)
+    run_gpu_step(hb, b, "cross_entropy")
+    m.mlora_load_state(hb, path, with_optimizer=True)
+    assert m.mlora_get_steps(hb) == [2, 2, 2]
+    got = _state(hb, cfg, ("", "m", "v", "g"))
+    for key, x in saved.items():
+        assert np.array_equal(got[key], x), key
+    assert not any(got[("g",) + key[1:]].any() for key in saved if key[0] == "")
+    for h in (ha, hb):
+        run_gpu_step(h, b, "cross_entropy")
+        m.mlora_optim_step(h, lr=1e-3)
+    sa, sb = _state(ha, cfg), _state(hb, cfg)
+    for key in sa:
+        assert np.array_equal(sa[key], sb[key]), key
+    # weights only: moments and steps reset; next step as the oracle's
+    hc = create_handle(cfg, base, ad, N)
+    m.mlora_load_state(hc, path, with_optimizer=False)
+    assert m.mlora_get_steps(hc) == [0, 0, 0]
+    got = _state(hc, cfg)
+    for key, x in saved.items():
+        if key[0] == "":
+            assert np.array_equal(got[key], x), key
+        else:
+            assert not got[key].any(), key
+    oracle.load_state_file(path, o, with_optimizer=False)
+    run_gpu_step(hc, b, "cross_entropy")
+    run_oracle_step(o, b, "cross_entropy")
+    m.mlora_optim_step(hc, lr=1e-3)
+    o.optim_step(lr=1e-3)
+    assert m.mlora_get_steps(hc) == o.step == [1, 1, 1]
+    p_err, _ = grad_errors(hc, o, range(3), which_prefix="p")
+    assert p_err <= 1e-4
+
+
+def test_load_state_rejects_bad_files(tmp_path):
+    """A file of other shapes is E_ARG, a missing, foreign or truncated file
+    E_IO; none of them changes the handle."""
+    import rl_step_gb300 as m
+    cfg, base, ad, b, o, _ = _setup("tiny_fp32", None)
+    h = create_handle(cfg, base, ad, len(b["tokens"]))
+    before = _state(h, cfg)
+    good = str(tmp_path / "good.bin")
+    m.mlora_save_state(h, good)
+    other = oracle.Oracle(base, ad, cfg.ranks, [2.0 * x for x in cfg.alphas])
+    bad_alpha = str(tmp_path / "alpha.bin")
+    oracle.write_state_file(bad_alpha, other)
+    raw = open(good, "rb").read()
+    trunc = str(tmp_path / "trunc.bin")
+    open(trunc, "wb").write(raw[:-4])
+    extra = str(tmp_path / "extra.bin")
+    open(extra, "wb").write(raw + b"\0")
+    foreign = str(tmp_path / "foreign.bin")
+    open(foreign, "wb").write(b"NOTMLORA" + raw[8:])
+    cases = [(bad_alpha, "E_ARG"), (str(tmp_path / "missing.bin"), "E_IO"), (trunc, "E_IO"),
+             (extra, "E_IO"), (foreign, "E_IO")]
+    for path, code in cases:
+        with pytest.raises(m.MLoRAError) as ei:
+            m.mlora_load_state(h, path, with_optimizer=True)
+        assert code in str(ei.value), (path, str(ei.value))
+        now = _state(h, cfg)
+        for key in before:
+            assert np.array_equal(now[key], before[key])

@@ -378,6 +378,101 @@ def test_state_file_round_trip(tmp_path):
                 np.testing.assert_array_equal(rec["V"][k][l], o.Vm[k][a][l].astype(np.float32))
 
 
+def _ce_step(o, b, lr=1e-3):
+    o.forward_backward(b["tokens"], b["targets"], b["adapter_ids"], "cross_entropy", weights=b["weights"])
+    return o.optim_step(lr=lr)
+
+
+def test_load_weights_only_restarts_adam(tmp_path):
+    """load_state resets the history: the next step of every adapter is a
+    first Adam step, whose update is the closed form -lr g / (|g| + eps)."""
+    o, params, b = _make(14)
+    _ce_step(o, b)
+    _ce_step(o, b)
+    p = str(tmp_path / "s.bin")
+    oracle.write_state_file(p, o)
+    q, _, _ = _make(15)                              # other base and adapters, same shapes
+    q.forward_backward(b["tokens"], b["targets"], b["adapter_ids"], "cross_entropy",
+                       weights=b["weights"])                    # a pending gradient ...
+    oracle.load_state_file(p, q, with_optimizer=False)
+    assert q.step == [0, 0, 0] and not q.touched                # ... is dropped
+    assert not any(g.any() for row in q.G["B1"] for g in row)
+    for a in range(3):
+        np.testing.assert_array_equal(q.P["A2"][a][1], o.P["A2"][a][1].astype(np.float32))
+        assert not q.M["A2"][a][1].any() and not q.Vm["B2"][a][0].any()
+    P0 = {k: [[x.copy() for x in row] for row in q.P[k]] for k in oracle.TENSORS}
+    q.forward_backward(b["tokens"], b["targets"], b["adapter_ids"], "cross_entropy", weights=b["weights"])
+    G = {k: [[x.copy() for x in row] for row in q.G[k]] for k in oracle.TENSORS}
+    q.optim_step(lr=1e-3)
+    assert q.step == [1, 1, 1]
+    for k in oracle.TENSORS:
+        for a in range(3):
+            for l in range(q.L):
+                g = G[k][a][l]
+                np.testing.assert_allclose(q.P[k][a][l] - P0[k][a][l], -1e-3 * g / (np.abs(g) + 1e-8),
+                                           rtol=1e-9, atol=1e-15)
+
+
+def test_load_with_optimizer_resumes_the_run(tmp_path):
+    """load_state_with_optimizer: a run saved after two steps and resumed in a
+    fresh oracle takes the same third step as the uninterrupted run (up to
+    the fp32 rounding of the file), and differs from a weights-only resume."""
+    o, params, b = _make(16)
+    _ce_step(o, b)
+    _ce_step(o, b)
+    p = str(tmp_path / "s.bin")
+    oracle.write_state_file(p, o)
+    before = {k: [[x.copy() for x in row] for row in o.P[k]] for k in oracle.TENSORS}
+    _ce_step(o, b)
+    for with_opt in (True, False):
+        q, _, _ = _make(16)                          # same base; adapters overwritten
+        oracle.load_state_file(p, q, with_optimizer=with_opt)
+        assert q.step == ([2, 2, 2] if with_opt else [0, 0, 0])
+        start = {k: [[x.copy() for x in row] for row in q.P[k]] for k in oracle.TENSORS}
+        _ce_step(q, b)
+        worst = 0.0
+        for k in oracle.TENSORS:
+            for a in range(3):
+                for l in range(q.L):
+                    du_o = o.P[k][a][l] - before[k][a][l]
+                    du_q = q.P[k][a][l] - start[k][a][l]
+                    worst = max(worst, float(np.linalg.norm(du_q - du_o) / np.linalg.norm(du_o)))
+        if with_opt:
+            assert q.step == [3, 3, 3] and worst <= 1e-4
+        else:
+            assert q.step == [1, 1, 1] and worst > 1e-2
+
+
+def test_load_rejects_a_mismatched_checkpoint(tmp_path):
+    o, params, b = _make(18)
+    p = str(tmp_path / "s.bin")
+    oracle.write_state_file(p, o)
+    q, _, _ = _make(18, ranks=(4, 8, 4))
+    before = q.P["A1"][1][0].copy()
+    with pytest.raises(ValueError):
+        oracle.load_state_file(p, q, with_optimizer=True)
+    np.testing.assert_array_equal(q.P["A1"][1][0], before)
+
+
+def test_merged_weights_reproduce_the_adapter():
+    """Export: a base whose W1, W2 are W + gamma B A of adapter a, run with
+    zero adapters, gives adapter a's logprobs (and differs from the bare base)."""
+    o, params, b = _make(19)
+    base, ad, ranks, alphas = params
+    tok, tgt = b["tokens"], b["targets"]
+    for a in range(3):
+        merged = {"E": base["E"], "Wout": base["Wout"],
+                  "W1": [o.merged_weight(a, l, "W1") for l in range(o.L)],
+                  "W2": [o.merged_weight(a, l, "W2") for l in range(o.L)]}
+        zero = {k: [[np.zeros_like(x) for x in row] for row in ad[k]] for k in ad}
+        q = oracle.Oracle(merged, zero, ranks, alphas)
+        ids = np.full(len(tok), a)
+        ref = o.forward(tok, tgt, ids)
+        np.testing.assert_allclose(q.forward(tok, tgt, ids), ref, rtol=0, atol=1e-12)
+        bare = oracle.Oracle(base, zero, ranks, alphas).forward(tok, tgt, ids)
+        assert np.max(np.abs(bare - ref)) > 1e-3
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_planted_silu_grad_error_is_caught(monkeypatch):
