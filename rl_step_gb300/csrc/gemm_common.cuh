@@ -28,10 +28,9 @@ enum EpiKind : int {
     EPI_STORE2 = 2,   // f32 = acc ; out0 = T(acc)                              (dh of the LM head)
     EPI_DSILU = 3,    // out0 = T(acc * silu'(aux))                             (du)
     EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
-    EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z (LM head)
-    EPI_LMDZ = 6,     // out0 = T(g (onehot(y) - exp(acc - lse)))               (LM head backward)
-    EPI_GRAD = 7,     // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
-    EPI_MERGE = 8     // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
+    EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z; z kept if out0 (LM head)
+    EPI_GRAD = 6,     // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
+    EPI_MERGE = 7     // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
 };
 
 struct EpiParams {
@@ -50,8 +49,6 @@ struct EpiParams {
     const int* tgt = nullptr;       // target id per padded row (-1: none)
     int part_ld = 0;                // pitch of a row of partials (multiple of 4)
     int V = 0, Vpad = 0;
-    const float* g = nullptr;       // dL/dl per padded row
-    const float* lse = nullptr;     // logsumexp per padded row
     int64_t out_row_shift = 0;      // output row = row + out_row_shift (chunk buffers)
     // adapter gradients
     float* grad = nullptr;
@@ -194,6 +191,8 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
     } break;
     case EPI_LMFWD: {
+        if (ep.out0 && col0 < ep.Vpad)     // keep the logits (fp32) for the backward
+            store32<float>(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
         int t = ep.tgt[row];
         float cm = -INFINITY;
 #pragma unroll
@@ -213,26 +212,6 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
             st.s = st.s * sc + sum;
             st.m = mn;
         }
-    } break;
-    case EPI_LMDZ: {
-        if (col0 >= ep.Vpad) break;
-        float gr = ep.g[row];
-        float d[32];
-        if (gr == 0.f) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = 0.f;
-        } else {
-            int t = ep.tgt[row];
-            float lb = ep.lse[row] * LOG2E;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                int c = col0 + j;
-                float p = exp2f(fmaf(acc[j], LOG2E, -lb));
-                float v = gr * ((c == t ? 1.f : 0.f) - p);
-                d[j] = c < ep.V ? v : 0.f;
-            }
-        }
-        store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, d);
     } break;
     case EPI_MERGE: {
         float w[32];

@@ -54,10 +54,15 @@ struct LossArgs {
     const float* dl;
 };
 // LM-head partial combine + loss epilogue; per-row loss values to val_row.
+// rows of the m-tiles [tile0, tile0 + ntiles) (and below the batch's valid m-tiles)
 void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int part_ld, const float* zt,
-                         const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
+                         const int* perm_pad, const int* tgt_pad, const int* meta, int tile0, int ntiles,
                          float* logprobs_out, float* lse, float* g, double* val_row, int num_sms,
                          cudaStream_t s);
+// dz of the LM head from stored fp32 logits, one chunk of padded rows
+template <typename T>
+void launch_lm_dz(const float* z, T* dz, int64_t ld, int V, int Vpad, const float* g, const float* lse,
+                  const int* tgt, const int* meta, int row0, int nrows, cudaStream_t s);
 void launch_loss_reduce(const double* val_row, const int* pad_off, int n_ad, double* loss_out,
                         cudaStream_t s);
 

@@ -178,13 +178,13 @@ __device__ __forceinline__ void combine_load(CombineRow& r, const float* __restr
 __global__ void __launch_bounds__(256) combine_loss_kernel(
     LossArgs la, const float* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
     const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
-    float* logprobs_out, float* lse_out, float* g_out, double* val_row) {
-    const int rows = meta[0] * TILE_M;
+    int row0, int row1, float* logprobs_out, float* lse_out, float* g_out, double* val_row) {
+    const int rows = min(meta[0] * TILE_M, row1);
     const int lane = threadIdx.x & 31;
     const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     CombineRow cur, nxt;
-    int p = wid;
+    int p = row0 + wid;
     if (p < rows) combine_load(cur, part, p, n_nt, part_ld, lane, zt, perm_pad, tgt_pad);
     for (; p < rows; p += nwarps) {
         const int pn = p + nwarps;
@@ -231,16 +231,93 @@ __global__ void __launch_bounds__(256) combine_loss_kernel(
 }
 
 void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int part_ld, const float* zt,
-                         const int* perm_pad, const int* tgt_pad, const int* meta, int max_tiles,
+                         const int* perm_pad, const int* tgt_pad, const int* meta, int tile0, int ntiles,
                          float* logprobs_out, float* lse, float* g, double* val_row, int num_sms,
                          cudaStream_t s) {
-    if (max_tiles <= 0) return;
+    if (ntiles <= 0) return;
     int blocks = num_sms * 4;
-    const int need = (max_tiles * TILE_M + 7) / 8;     // one row per warp at most
+    const int need = (ntiles * TILE_M + 7) / 8;        // one row per warp at most
     if (blocks > need) blocks = need;
     combine_loss_kernel<<<blocks, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad, tgt_pad, meta,
+                                               tile0 * TILE_M, (tile0 + ntiles) * TILE_M,
                                                logprobs_out, lse, g, val_row);
 }
+
+// ----------------------------------------------------------------------------
+// LM-head backward from stored logits, for the padded rows [row0, row0 + nrows)
+// of one chunk (z and dz hold the chunk's rows, pitch ld):
+//   dz[r][v] = g (onehot(v == y) - exp(z[r][v] - lse))   for v < V
+//   dz[r][v] = 0                                          for V <= v < Vpad
+// with g = dL/dl, lse and y of padded row row0 + r.  Rows with g = 0 (padding,
+// masked or invalid tokens) are written as zeros without reading z.  Each
+// thread covers 16 consecutive columns: four 16-byte loads in flight, one
+// (bf16) or four (fp32) 16-byte stores.  Rows at or past the batch's valid
+// m-tiles are skipped (the dh GEMM does not read them).
+// ----------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void store16(T* dst, const float* v);
+template <> __device__ __forceinline__ void store16<bf16>(bf16* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+template <> __device__ __forceinline__ void store16<float>(float* dst, const float* v) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) lm_dz_kernel(const float* __restrict__ z, T* __restrict__ dz,
+                                                    int64_t ld, int V, int Vpad, const float* __restrict__ g,
+                                                    const float* __restrict__ lse,
+                                                    const int* __restrict__ tgt, const int* __restrict__ meta,
+                                                    int row0, int nrows) {
+    const float LOG2E = 1.4426950408889634f;
+    const int r = blockIdx.y;
+    const int p = row0 + r;
+    if (r >= nrows || p >= meta[0] * TILE_M) return;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 16;
+    if (c >= Vpad) return;
+    const float gr = g[p];
+    float d[16];
+    if (gr == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) d[j] = 0.f;
+    } else {
+        const float4* zp = reinterpret_cast<const float4*>(z + (int64_t)r * ld + c);
+        float4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = __ldcs(zp + u);
+        const float lb = lse[p] * LOG2E;
+        const int y = tgt[p];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float zz[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int v = c + 4 * u + e;
+                const float pr = exp2f(fmaf(zz[e], LOG2E, -lb));
+                d[4 * u + e] = v < V ? gr * ((v == y ? 1.f : 0.f) - pr) : 0.f;
+            }
+        }
+    }
+    store16<T>(dz + (int64_t)r * ld + c, d);
+}
+
+template <typename T>
+void launch_lm_dz(const float* z, T* dz, int64_t ld, int V, int Vpad, const float* g, const float* lse,
+                  const int* tgt, const int* meta, int row0, int nrows, cudaStream_t s) {
+    if (nrows <= 0) return;
+    dim3 grid((unsigned)((Vpad / 16 + 255) / 256), (unsigned)nrows);
+    lm_dz_kernel<T><<<grid, 256, 0, s>>>(z, dz, ld, V, Vpad, g, lse, tgt, meta, row0, nrows);
+}
+template void launch_lm_dz<float>(const float*, float*, int64_t, int, int, const float*, const float*,
+                                  const int*, const int*, int, int, cudaStream_t);
+template void launch_lm_dz<bf16>(const float*, bf16*, int64_t, int, int, const float*, const float*,
+                                 const int*, const int*, int, int, cudaStream_t);
 
 // Per-adapter loss: sum of its rows' loss values, in row order.
 __global__ void loss_reduce_kernel(const double* val_row, const int* pad_off, int n_ad, double* loss_out) {

@@ -85,6 +85,7 @@ struct mlora {
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
     void* dz = nullptr;
+    float* zbuf = nullptr;              // fp32 logits of one chunk of rows (backward)
     double* val_row = nullptr;          // per padded row loss value
     int* status = nullptr;
     int* tile_counter = nullptr;        // GEMM tile scheduler (reset before each launch)
@@ -317,6 +318,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOC(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 64 ? h->max_tiles : 64;   // 8192-row chunks
         ALLOCB(h->dz, (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
+        ALLOC(h->zbuf, (size_t)h->nc_tiles * TILE_M * h->Vpad);
         if (cudaMemset(h->dz, 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
             rc = fail(MLORA_E_CUDA, "cudaMemset of the dz chunk buffer failed");
             goto fail_out;
@@ -554,41 +556,57 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W2_FWD))) return rc;
         }
     }
-    // a6 LM head: per-tile (max, sum exp) and the target logit
-    {
-        GemmParams p = dense_params(h, mt_upper, V, d);
-        p.A = op_kmajor(h->hb[L], MP, d);
-        p.B = op_kmajor(h->Wout, V, d);
-        p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
-        p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
-        if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
-    }
-    // a7 combine + loss epilogue
-    {
-        ProfScope ps(h, s, MLORA_PROF_LOSS);
-        launch_combine_loss(la, h->part, h->n_nt, h->part_ld, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta, mt_upper,
-                            logprobs_out, h->lse, h->gvec, h->val_row, h->num_sms, s);
-        ++h->launches;
-    }
-    if (loss_out) {
-        ProfScope ps(h, s, MLORA_PROF_OTHER);
-        launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
-        ++h->launches;
-    }
-    if (!backward) return MLORA_OK;
-
-    // a8 LM head backward, chunk by chunk: recompute z, dz = g (onehot - softmax), dh = dz Wout
-    for (int c0 = 0; c0 < mt_upper; c0 += h->nc_tiles) {
-        int cnt = mt_upper - c0 < h->nc_tiles ? mt_upper - c0 : h->nc_tiles;
+    // a6-a8 LM head.  Forward only: per-tile log-sum-exp partials and the
+    // target logit over all rows, then the combine + loss epilogue.  With the
+    // backward, chunk by chunk of rows: the same GEMM also keeps the chunk's
+    // fp32 logits, the combine finishes the chunk's rows, dz = g (onehot -
+    // softmax) is computed from the kept logits, and dh = dz Wout.
+    if (!backward) {
         {
-            GemmParams p = dense_params(h, mt_upper, h->Vpad, d);
-            p.mt_base = c0; p.mt_count = cnt;
+            GemmParams p = dense_params(h, mt_upper, V, d);
             p.A = op_kmajor(h->hb[L], MP, d);
             p.B = op_kmajor(h->Wout, V, d);
-                p.ep.kind = EPI_LMDZ; p.ep.out0 = h->dz; p.ep.ld0 = h->Vpad; p.ep.g = h->gvec; p.ep.lse = h->lse;
-            p.ep.tgt = h->tgt_pad; p.ep.V = V; p.ep.Vpad = h->Vpad;
-            p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
+            p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
+            p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
+        }
+        {
+            ProfScope ps(h, s, MLORA_PROF_LOSS);
+            launch_combine_loss(la, h->part, h->n_nt, h->part_ld, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta,
+                                0, mt_upper, logprobs_out, h->lse, h->gvec, h->val_row, h->num_sms, s);
+            ++h->launches;
+        }
+        if (loss_out) {
+            ProfScope ps(h, s, MLORA_PROF_OTHER);
+            launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
+            ++h->launches;
+        }
+        return MLORA_OK;
+    }
+    for (int c0 = 0; c0 < mt_upper; c0 += h->nc_tiles) {
+        const int cnt = mt_upper - c0 < h->nc_tiles ? mt_upper - c0 : h->nc_tiles;
+        {
+            GemmParams p = dense_params(h, mt_upper, V, d);
+            p.mt_base = c0; p.mt_count = cnt;
+            p.group_m = (cnt + 1) & ~1;            // the chunk is one raster band
+            p.A = op_kmajor(h->hb[L], MP, d);
+            p.B = op_kmajor(h->Wout, V, d);
+            p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
+            p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
+            p.ep.out0 = h->zbuf; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
+        }
+        {
+            ProfScope ps(h, s, MLORA_PROF_LOSS);
+            launch_combine_loss(la, h->part, h->n_nt, h->part_ld, h->zt, h->rb.perm_pad, h->tgt_pad, h->rb.meta,
+                                c0, cnt, logprobs_out, h->lse, h->gvec, h->val_row, h->num_sms, s);
+            ++h->launches;
+        }
+        {
+            ProfScope ps(h, s, MLORA_PROF_LM_DZ);
+            launch_lm_dz<T>(h->zbuf, reinterpret_cast<T*>(h->dz), h->Vpad, V, h->Vpad, h->gvec, h->lse, h->tgt_pad,
+                            h->rb.meta, c0 * TILE_M, cnt * TILE_M, s);
+            ++h->launches;
         }
         {
             GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
@@ -599,6 +617,12 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH))) return rc;
         }
     }
+    if (loss_out) {
+        ProfScope ps(h, s, MLORA_PROF_OTHER);
+        launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
+        ++h->launches;
+    }
+
     // a9-a11 layers in reverse
     for (int l = L - 1; l >= 0; --l) {
         {   // w2s = gamma * B2_a^T dh
