@@ -353,7 +353,7 @@ def run_ours(args, rank, world):
     fl = flop_model(cfg, b)
     K = args.steps
     # dominant kernel: the CTA-pair tcgen05 GEMM, which carries every base and
-    # LM-head GEMM (34 launches per step at L=4: 16 block GEMMs and 9 + 9
+    # LM-head GEMM (22 launches per step at L=4: 16 block GEMMs and 3 + 3
     # LM-head chunks).  Algorithmic FLOPs credit the base and LoRA-extension
     # GEMMs, the LM-head forward and dh; padding rows are executed work only.
     tc_ms = sum(prof[c][0] for c in TC_CLASSES)

@@ -316,7 +316,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOC(h->part, (size_t)MP * h->part_ld);
         ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
         ALLOC(h->tgt_pad, MP);
-        h->nc_tiles = h->max_tiles < 64 ? h->max_tiles : 64;   // 8192-row chunks
+        h->nc_tiles = h->max_tiles < 256 ? h->max_tiles : 256;   // chunks of up to 32,768 rows
         ALLOCB(h->dz, (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
         ALLOC(h->zbuf, (size_t)h->nc_tiles * TILE_M * h->Vpad);
         if (cudaMemset(h->dz, 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
@@ -583,12 +583,17 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         }
         return MLORA_OK;
     }
-    for (int c0 = 0; c0 < mt_upper; c0 += h->nc_tiles) {
-        const int cnt = mt_upper - c0 < h->nc_tiles ? mt_upper - c0 : h->nc_tiles;
+    // equal chunks (an even number of row tiles, for the CTA-pair GEMMs) of at
+    // most nc_tiles tiles: no small last chunk whose GEMMs fill a wave poorly
+    const int n_chunks = (mt_upper + h->nc_tiles - 1) / h->nc_tiles;
+    int chunk = (mt_upper + n_chunks - 1) / n_chunks;
+    chunk = (chunk + 1) & ~1;
+    if (chunk > h->nc_tiles) chunk = h->nc_tiles;
+    for (int c0 = 0; c0 < mt_upper; c0 += chunk) {
+        const int cnt = mt_upper - c0 < chunk ? mt_upper - c0 : chunk;
         {
             GemmParams p = dense_params(h, mt_upper, V, d);
             p.mt_base = c0; p.mt_count = cnt;
-            p.group_m = (cnt + 1) & ~1;            // the chunk is one raster band
             p.A = op_kmajor(h->hb[L], MP, d);
             p.B = op_kmajor(h->Wout, V, d);
             p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
