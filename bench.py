@@ -54,6 +54,8 @@ def parse_args():
                     help="tokens of the oracle's bounded CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the sampler-decode and export-merge measurements")
     ap.add_argument("--deterministic", action="store_true",
                     help="batch-invariant mode: one gradient chunk per adapter")
     ap.add_argument("--layers", type=int, default=None,
@@ -348,8 +350,14 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
+    # ---- rows beyond the step (outside the timed region) ---------------------
+    extras = None if args.no_extras else measure_next_rows(m, h, cfg, b, dev, stream)
+
     # ---- derived numbers -----------------------------------------------------
     peaks, peak_src = load_peaks()
+    if extras:
+        for k in ("sampler_decode", "export_merge"):
+            extras[k]["frac_of_hbm"] = extras[k]["achieved_gbs"] / peaks["hbm_gbs"]
     fl = flop_model(cfg, b)
     K = args.steps
     # dominant kernel: the CTA-pair tcgen05 GEMM, which carries every base and
@@ -417,7 +425,63 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
+    if extras:
+        out["next_rows"] = extras
     return out, (cfg, base, ad, b)
+
+
+def measure_next_rows(m, h, cfg, b, dev, stream, reps=20):
+    """Time the sampler's decode step and the export merge on the benchmark's
+    handle (CUDA events on the launch stream, after a warm-up call).
+
+    decode: one mlora_sampler_sample over `rows` rows spread over every
+    adapter (one slot each); algorithmic bytes = the frozen base it streams
+    (W1, W2 of every layer and Wout, base dtype) + every slot's factors + the
+    rows' fp32 logits written and read.  export: one W1' = W1 + gamma B A;
+    algorithmic bytes = W1 read + W1' written."""
+    import torch
+    es = 2 if cfg.dtype == "bf16" else 4
+    d, f, L, V = cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.vocab
+    out = {}
+    n_slots = min(cfg.n_adapters, 64)
+    rows = 256
+    smp = m.mlora_sampler_create(h, n_slots, rows)
+    for a in range(n_slots):
+        m.mlora_sampler_publish(smp, a, a)
+    rng = np.random.Generator(np.random.PCG64([cfg.seed, 31]))
+    tok = torch.from_numpy(rng.integers(0, V, rows).astype(np.int32)).to(dev)
+    sl = torch.from_numpy(rng.integers(0, n_slots, rows).astype(np.int32)).to(dev)
+    u = torch.from_numpy(rng.random(rows).astype(np.float32)).to(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    launches0 = smp.kernel_launches
+    ms = timed(lambda: m.mlora_sampler_sample(smp, tok, sl, u, stream=stream))
+    if m.mlora_sampler_check_status(smp) != 0:
+        raise RuntimeError("sampler status after the decode timing")
+    vpad = (V + 63) // 64 * 64
+    byt = (2 * L * d * f + V * d) * es + n_slots * 64 * 2 * (d + f) * L * es + rows * vpad * 8
+    out["sampler_decode"] = {"rows": rows, "slots": n_slots, "ms_per_step": ms,
+                             "tokens_per_s": rows / (ms * 1e-3),
+                             "bytes_per_step": byt, "achieved_gbs": byt / (ms * 1e-3) / 1e9,
+                             "gpu_launches_per_step": (smp.kernel_launches - launches0) / (reps + 1)}
+    del smp
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    buf = torch.empty((f, d), dtype=dt, device=dev)
+    ms = timed(lambda: m.mlora_export_merged(h, 0, 0, "W1", out=buf, stream=stream))
+    byt = 2 * f * d * es
+    out["export_merge"] = {"matrix": f"W1' [{f} x {d}]", "ms": ms, "bytes": byt,
+                           "achieved_gbs": byt / (ms * 1e-3) / 1e9}
+    return out
 
 
 def max_over_ranks(x: float, device=None) -> float:

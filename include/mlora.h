@@ -230,6 +230,68 @@ int mlora_load_state(mlora_t* h, const char* path, int32_t with_optimizer, void*
 int mlora_export_merged(mlora_t* h, int32_t adapter, int32_t layer, int32_t which, void* out,
                         void* stream);
 
+/* ------------------------------------------------------------------------
+ * Sampler side: scoring and one-token decode with pinned adapter snapshots
+ * (OpenTinker, "Multi-LoRA rollout": rows are batched by pinned adapter
+ * version over the shared base projection; tinker-ticks, "Why RL needs
+ * batch-invariant kernels": rollout and training logprobs must agree).
+ *
+ * A sampler shares the frozen base of a training handle (which must outlive
+ * it) and holds n_slots adapter snapshots.  Rows stay in batch order, each
+ * naming a slot; there is no per-adapter padding.  Every layer runs the
+ * training forward's kernels on the same operand values, with each row's
+ * adapter applied as its slot's block of a K extension whose other blocks
+ * are zero for that row, so a row's logprob is bitwise the one
+ * mlora_forward returns for the same token, target and adapter weights.
+ * ------------------------------------------------------------------------ */
+typedef struct mlora_sampler mlora_sampler_t;
+#define MLORA_SAMPLER_MAX_SLOTS 64
+#define MLORA_SAMPLER_MAX_ROWS 32768
+
+/* Create a sampler over `trainer`'s frozen base with n_slots (1..64) empty
+ * slots and room for max_rows (1..32768) rows per call.  Device memory:
+ * per layer 2 * n_slots * 64 * (d + f) base-dtype elements of snapshots,
+ * plus per row about 4 * Vpad bytes of kept logits and the activations of
+ * one forward.  Errors: E_ARG, E_NOMEM, E_CUDA. */
+int mlora_sampler_create(mlora_t* trainer, int32_t n_slots, int64_t max_rows,
+                         mlora_sampler_t** out);
+int mlora_sampler_destroy(mlora_sampler_t* s);
+
+/* Publish: copy `adapter`'s current weights (every layer's padded-rank
+ * base-dtype copies the GEMMs read, and its gamma) from the trainer into
+ * `slot`.  The slot keeps them until it is published again, whatever the
+ * trainer does meanwhile.  version_out (HOST, may be NULL) receives the
+ * adapter's optimizer step count at publication.  Synchronises `stream`.
+ * Errors: E_ARG (slot or adapter out of range), E_CUDA. */
+int mlora_sampler_publish(mlora_sampler_t* s, int32_t slot, int32_t adapter,
+                          int64_t* version_out, void* stream);
+
+/* Score: logprobs_out[t] = log softmax(z_t)[targets[t]] for row t computed
+ * with slot slots[t] (compute_logprobs / prefill).  tokens, targets, slots:
+ * DEVICE int32 [n]; logprobs_out: DEVICE fp32 [n].  A row whose token,
+ * target or slot is out of range or whose slot is unpublished gets NaN and
+ * raises the sampler's status bit (mlora_sampler_check_status -> E_RANGE).
+ * 0 <= n <= max_rows (else E_ARG).  Queued on `stream`. */
+int mlora_sampler_logprobs(mlora_sampler_t* s, const int32_t* tokens, const int32_t* targets,
+                           const int32_t* slots, int64_t n, float* logprobs_out, void* stream);
+
+/* One decode step: for row t, the next token is the smallest vocabulary id
+ * v with CDF(v) > uniforms[t], CDF the cumulative softmax of the row's
+ * logits in vocabulary order (inverse-CDF sampling at temperature 1; the
+ * caller draws the uniforms in [0, 1)); logprob_out[t] is that token's
+ * logprob, bitwise what mlora_sampler_logprobs returns for it as target.
+ * When rounding leaves the cumulative sum at or below u the last token with
+ * a non-zero probability is taken.  tokens, slots: DEVICE int32 [n];
+ * uniforms: DEVICE fp32 [n]; next_out: DEVICE int32 [n] (-1 for a bad row);
+ * logprob_out: DEVICE fp32 [n] (NaN for a bad row).  Queued on `stream`. */
+int mlora_sampler_sample(mlora_sampler_t* s, const int32_t* tokens, const int32_t* slots,
+                         const float* uniforms, int64_t n, int32_t* next_out, float* logprob_out,
+                         void* stream);
+
+/* Synchronise `stream`, return and clear the sampler's status word. */
+int mlora_sampler_check_status(mlora_sampler_t* s, void* stream);
+int64_t mlora_sampler_kernel_launches(const mlora_sampler_t* s);
+
 /* Copy one fp32 adapter tensor (see mlora_tensor) of adapter `adapter`,
  * layer `layer` into dst (DEVICE, caller-owned, shape as documented there).
  * Test and inspection hook. */

@@ -257,6 +257,35 @@ class Oracle:
         h, _, _ = self.forward_hidden(tokens, adapter_ids)
         return self.logprobs_from_hidden(h, targets)[0]
 
+    def next_token_cdf(self, tokens, adapter_ids) -> np.ndarray:
+        """Cumulative next-token distribution per row, [n x V] fp64: the
+        running sum of softmax(z) in vocabulary order (Deep Dive - Tinker,
+        "sample returns evidence for learning": the sampler returns generated
+        token ids and one logprob per generated token)."""
+        h, _, _ = self.forward_hidden(tokens, adapter_ids)
+        z = self.logits(h)
+        p = np.exp(z - logsumexp_rows(z)[:, None])
+        return np.cumsum(p, axis=1)
+
+    def sample(self, tokens, adapter_ids, uniforms):
+        """Inverse-CDF sampling at temperature 1: for row t the smallest id v
+        with CDF(v) > u_t (the last id when rounding leaves CDF(V-1) <= u_t).
+        Returns (next ids, their logprobs, CDF(v-1), CDF(v))."""
+        cdf = self.next_token_cdf(tokens, adapter_ids)
+        u = np.asarray(uniforms, dtype=np.float64)
+        n, V = cdf.shape
+        nxt = np.empty(n, dtype=np.int64)
+        lo = np.empty(n)
+        hi = np.empty(n)
+        for t in range(n):
+            v = int(np.searchsorted(cdf[t], u[t], side="right"))
+            v = min(v, V - 1)
+            nxt[t] = v
+            lo[t] = cdf[t, v - 1] if v > 0 else 0.0
+            hi[t] = cdf[t, v]
+        lp = np.log(hi - lo)
+        return nxt, lp, lo, hi
+
     def merged_weight(self, a: int, l: int, which: str) -> np.ndarray:
         """W' = W + gamma B A for W1 or W2 of layer l with adapter a's factors
         (Deep Dive - Tinker, "Checkpoints and export paths"), in fp64."""

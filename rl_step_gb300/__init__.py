@@ -29,7 +29,9 @@ __all__ = [
     "mlora_create", "mlora_destroy", "mlora_forward", "mlora_forward_backward",
     "mlora_forward_backward_custom", "mlora_optim_step", "mlora_save_state", "mlora_load_state", "mlora_export_merged",
     "mlora_read_adapter", "mlora_write_adapter", "mlora_get_steps", "mlora_get_routing",
-    "mlora_check_status", "mlora_routing_noalloc", "mlora_set_deterministic", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
+    "mlora_check_status", "mlora_routing_noalloc", "Sampler", "mlora_sampler_create",
+    "mlora_sampler_publish", "mlora_sampler_logprobs", "mlora_sampler_sample",
+    "mlora_sampler_check_status", "mlora_set_deterministic", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
     "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
 ]
 
@@ -93,6 +95,15 @@ _SIGNATURES = {
     "mlora_save_state": (c_int32, [c_void_p, c_char_p, c_void_p]),
     "mlora_load_state": (c_int32, [c_void_p, c_char_p, c_int32, c_void_p]),
     "mlora_export_merged": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
+    "mlora_sampler_create": (c_int32, [c_void_p, c_int32, c_int64, POINTER(c_void_p)]),
+    "mlora_sampler_destroy": (c_int32, [c_void_p]),
+    "mlora_sampler_publish": (c_int32, [c_void_p, c_int32, c_int32, POINTER(c_int64), c_void_p]),
+    "mlora_sampler_logprobs": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p,
+                                         c_void_p]),
+    "mlora_sampler_sample": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p,
+                                       c_void_p, c_void_p]),
+    "mlora_sampler_check_status": (c_int32, [c_void_p, c_void_p]),
+    "mlora_sampler_kernel_launches": (c_int64, [c_void_p]),
     "mlora_read_adapter": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "mlora_write_adapter": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "mlora_get_steps": (c_int32, [c_void_p, POINTER(c_int64), c_void_p]),
@@ -296,6 +307,65 @@ def mlora_export_merged(h: Handle, adapter: int, layer: int, which: str, out=Non
     assert tuple(out.shape) == shape and out.is_contiguous()
     _check(_lib.mlora_export_merged(h.ptr, adapter, layer, idx, _ptr(out), _stream(stream)))
     return out
+
+
+class Sampler:
+    """Owns one mlora_sampler_t*; keeps its training handle alive."""
+
+    def __init__(self, ptr: int, trainer: Handle, n_slots: int, max_rows: int):
+        self.ptr = c_void_p(ptr)
+        self.trainer = trainer
+        self.n_slots, self.max_rows = n_slots, max_rows
+
+    @property
+    def kernel_launches(self) -> int:
+        return int(_lib.mlora_sampler_kernel_launches(self.ptr))
+
+    def __del__(self):
+        try:
+            if self.ptr and _lib is not None:
+                _lib.mlora_sampler_destroy(self.ptr)
+                self.ptr = c_void_p(0)
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
+
+
+def mlora_sampler_create(h: Handle, n_slots: int, max_rows: int) -> Sampler:
+    out = c_void_p()
+    _check(_lib.mlora_sampler_create(h.ptr, n_slots, max_rows, ctypes.byref(out)))
+    return Sampler(out.value, h, n_slots, max_rows)
+
+
+def mlora_sampler_publish(s: Sampler, slot: int, adapter: int, stream=None) -> int:
+    """Snapshot adapter's current weights into slot; returns its optimizer step count."""
+    ver = c_int64(0)
+    _check(_lib.mlora_sampler_publish(s.ptr, slot, adapter, ctypes.byref(ver), _stream(stream)))
+    return int(ver.value)
+
+
+def mlora_sampler_logprobs(s: Sampler, tokens, targets, slots, stream=None):
+    import torch
+    n = int(tokens.numel())
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    _check(_lib.mlora_sampler_logprobs(s.ptr, _ptr(tokens), _ptr(targets), _ptr(slots), n, _ptr(out),
+                                       _stream(stream)))
+    return out
+
+
+def mlora_sampler_sample(s: Sampler, tokens, slots, uniforms, stream=None):
+    """One decode step: (next tokens int32, their logprobs fp32)."""
+    import torch
+    n = int(tokens.numel())
+    nxt = torch.empty(n, dtype=torch.int32, device="cuda")
+    lp = torch.empty(n, dtype=torch.float32, device="cuda")
+    _check(_lib.mlora_sampler_sample(s.ptr, _ptr(tokens), _ptr(slots), _ptr(uniforms), n, _ptr(nxt),
+                                     _ptr(lp), _stream(stream)))
+    return nxt, lp
+
+
+def mlora_sampler_check_status(s: Sampler, stream=None) -> int:
+    """0, or the negative MLORA_E_* code of the sampler's status word (cleared)."""
+    return int(_lib.mlora_sampler_check_status(s.ptr, _stream(stream)))
 
 
 def mlora_read_adapter(h: Handle, adapter: int, layer: int, which: str, stream=None):

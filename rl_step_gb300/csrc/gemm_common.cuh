@@ -30,7 +30,9 @@ enum EpiKind : int {
     EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
     EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z; z kept if out0 (LM head)
     EPI_GRAD = 6,     // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
-    EPI_MERGE = 7     // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
+    EPI_MERGE = 7,    // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
+    EPI_SHRINK_SEL = 8  // column block s = col / RP: out0 = T(gamma[s] * acc) on rows whose
+                        // slot is s, 0 elsewhere                                   (sampler shrink)
 };
 
 struct EpiParams {
@@ -57,6 +59,7 @@ struct EpiParams {
     int grad_trans = 0;             // 0: grad[m*r + n]; 1: grad[n*M + m]
     int grad_M = 0;
     int* nonfinite = nullptr;       // per adapter flag
+    const int* row_slot = nullptr;  // sampler: adapter slot per row (-1: none)
 };
 
 struct GemmParams {
@@ -73,6 +76,7 @@ struct GemmParams {
     int max_chunks = 0;
     int group_m = 8;                  // raster band height (m-tiles) for L2 reuse
     int* tile_counter = nullptr;      // device int, tile scheduler of the CTA-pair kernel
+    int force_bn64 = 0;               // run on the 128 x 64 single-CTA kernel whatever N is
     EpiParams ep;
 };
 
@@ -212,6 +216,14 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
             st.s = st.s * sc + sum;
             st.m = mn;
         }
+    } break;
+    case EPI_SHRINK_SEL: {
+        const int sl = col0 / RP;
+        const bool mine = ep.row_slot[row] == sl;
+        const float gm = ep.gamma[sl];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = mine ? acc[j] * gm : 0.f;
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
     } break;
     case EPI_MERGE: {
         float w[32];

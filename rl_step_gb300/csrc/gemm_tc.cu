@@ -1085,7 +1085,7 @@ bool tc_engine_available() { return get_encode(); }
 
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
     if (!get_encode()) return cudaErrorNotSupported;
-    if (p.N <= 64) return launch_bn<64, 8>(p, s, num_sms, status);
+    if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8>(p, s, num_sms, status);
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
     if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)

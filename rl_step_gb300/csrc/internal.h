@@ -79,6 +79,22 @@ struct ShadowMap {
     void* A2[64];
     void* B2[64];
 };
+
+// What the sampler (sampler.cu) reads from a training handle: the frozen base
+// it shares and the adapters' current padded-rank copies it snapshots.
+struct TrainerView {
+    int V, d, f, L, dtype, n_ad, Vpad, n_nt, part_ld, lm_bn, num_sms, use_tc;
+    size_t esize;
+    const void* E;
+    const void* Wout;
+    const void* const* W1;
+    const void* const* W2;
+    const ShadowMap* shadow;
+    const float* gamma_d;          // device, per adapter
+    const int64_t* step_d;         // device, optimizer steps per adapter
+    const int* ranks;              // host
+    const float* alphas;           // host
+};
 template <typename T>
 void launch_adam(int n_ad, const int64_t* ad_off, const int* ranks, int L, int d, int f,
                  int64_t total, const AdamTab* tab, float* P, float* G, float* M, float* Vm,

@@ -185,6 +185,18 @@ int mlk_report_error(int code, const char* msg) {
     return code;
 }
 
+// Read-only view of a handle for the sampler (sampler.cu).
+void mlk_trainer_view(const mlora_t* h, TrainerView* v) {
+    v->V = h->V; v->d = h->d; v->f = h->f; v->L = h->L; v->dtype = h->dtype; v->n_ad = h->n_ad;
+    v->Vpad = h->Vpad; v->n_nt = h->n_nt; v->part_ld = h->part_ld; v->lm_bn = h->lm_bn;
+    v->num_sms = h->num_sms; v->use_tc = h->use_tc; v->esize = h->esize;
+    v->E = h->E; v->Wout = h->Wout;
+    v->W1 = h->W1.data(); v->W2 = h->W2.data();
+    v->shadow = &h->shadow;
+    v->gamma_d = h->gamma_d; v->step_d = h->step;
+    v->ranks = h->ranks.data(); v->alphas = h->alphas.data();
+}
+
 extern "C" int64_t mlora_kernel_launches(const mlora_t* h) { return h ? h->launches : 0; }
 
 extern "C" int64_t mlora_device_bytes(const mlora_t* h) { return h ? h->bytes : 0; }

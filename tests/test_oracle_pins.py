@@ -473,6 +473,42 @@ def test_merged_weights_reproduce_the_adapter():
         assert np.max(np.abs(bare - ref)) > 1e-3
 
 
+def test_sampling_uniform_closed_form():
+    """Wout = 0 makes every next-token distribution uniform: the inverse CDF
+    at u is floor(u V) and its logprob -log V."""
+    o, params, b = _make(20)
+    o.Wout[...] = 0.0
+    u = np.array([0.0, 1e-9, 0.25, 0.5 - 1e-9, 0.731, 0.999999])
+    tok, ids = b["tokens"][:6], b["adapter_ids"][:6]
+    nxt, lp, lo, hi = o.sample(tok, ids, u)
+    assert nxt.tolist() == np.floor(u * o.V).astype(int).tolist()
+    np.testing.assert_allclose(lp, -np.log(o.V), rtol=0, atol=1e-12)
+    assert (lo <= u + 1e-15).all() and (u < hi).all()
+
+
+def test_sampling_matches_pure_python_walk():
+    """The inverse CDF equals a pure-Python walk over the softmax of the
+    brute-force logits, token by token."""
+    o, params, b = _make(21)
+    rng = np.random.Generator(np.random.PCG64([21, 1]))
+    u = rng.random(5)
+    tok, ids = b["tokens"][:5], b["adapter_ids"][:5]
+    nxt, lp, lo, hi = o.sample(tok, ids, u)
+    base, ad, ranks, alphas = params
+    for t in range(5):
+        # logprobs of every target via the brute-force forward
+        lps = [_brute_logprob(params, int(tok[t]), v, int(ids[t])) for v in range(o.V)]
+        ps = [math.exp(x) for x in lps]
+        run, pick = 0.0, o.V - 1
+        for v, pv in enumerate(ps):
+            run += pv
+            if run > u[t]:
+                pick = v
+                break
+        assert nxt[t] == pick
+        assert abs(lp[t] - lps[pick]) < 1e-9
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_planted_silu_grad_error_is_caught(monkeypatch):
