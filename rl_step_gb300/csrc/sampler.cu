@@ -416,6 +416,11 @@ static int s_forward(mlora_sampler_t* s, const int32_t* tokens, const int32_t* t
         p.tile_ad = nullptr;
         return p;
     };
+    // Few rows (decode): when the 256 x 256 pair tiles of a block GEMM would
+    // occupy under a quarter of the SMs while the weights stream, it runs on
+    // the 128 x 64 single-CTA kernel instead (four times the tiles; the same
+    // per-element K order and MMA K step, so the same bits).
+    auto small = [&](int N) { return ((mt + 1) / 2) * ((N + 255) / 256) * 2 < t.num_sms / 4; };
     for (int l = 0; l < t.L; ++l) {
         {   // v1[:, s-block] = gamma_s A1_s h on rows of slot s
             GemmParams p = dense(SK, t.d);
@@ -428,6 +433,7 @@ static int s_forward(mlora_sampler_t* s, const int32_t* tokens, const int32_t* t
         }
         {   // u = W1 h + sum_s B1_s v1[:, s-block] ; act = silu(u)
             GemmParams p = dense(t.f, t.d);
+            p.force_bn64 = small(t.f);
             p.A = s_op(s->hb, R, t.d);
             p.B = s_op(t.W1[l], t.f, t.d);
             p.Kx = SK;
@@ -447,6 +453,7 @@ static int s_forward(mlora_sampler_t* s, const int32_t* tokens, const int32_t* t
         }
         {   // h += W2 act + sum_s B2_s v2[:, s-block]
             GemmParams p = dense(t.d, t.f);
+            p.force_bn64 = small(t.d);
             p.A = s_op(s->actb, R, t.f);
             p.B = s_op(t.W2[l], t.d, t.f);
             p.Kx = SK;

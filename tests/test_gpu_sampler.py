@@ -50,17 +50,18 @@ def _rows(cfg, n, key):
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_scoring_is_bitwise_the_training_forward(dtype):
     """Slot a = snapshot of adapter a: the sampler's logprobs of mixed-slot
-    rows equal mlora_forward's bitwise, at 1, 77 and 700 rows."""
+    rows equal mlora_forward's bitwise, at 1, 77 and 700 rows (block GEMMs on
+    the single-CTA kernel) and 2048 rows (on the CTA-pair kernel)."""
     import rl_step_gb300 as m
     cfg = _cfg(dtype, seed=4001 if dtype == "bf16" else 4002)
     base = wl.make_base_weights(cfg)
     ad = wl.make_adapters(cfg, std_a=0.05, std_b=0.05)
-    h = create_handle(cfg, base, ad, 1024)
-    smp = m.mlora_sampler_create(h, 6, 1024)
+    h = create_handle(cfg, base, ad, 2048)
+    smp = m.mlora_sampler_create(h, 6, 2048)
     for a in range(cfg.n_adapters):
         assert m.mlora_sampler_publish(smp, a, a) == 0
     o = oracle.Oracle(base, ad, cfg.ranks, cfg.alphas)
-    for n in (1, 77, 700):
+    for n in (1, 77, 700, 2048):
         b = _rows(cfg, n, n)
         tok, tgt, ids = dev(b["tokens"]), dev(b["targets"]), dev(b["adapter_ids"])
         lp_s = m.mlora_sampler_logprobs(smp, tok, tgt, ids).cpu().numpy()
