@@ -60,6 +60,8 @@ def parse_args():
                     help="batch-invariant mode: one gradient chunk per adapter")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: override the block count (not a bench value)")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="profiling only: override the vocabulary size (not a bench value)")
     return ap.parse_args()
 
 
@@ -217,8 +219,9 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = wl.get_config(args.config)
-    if args.layers:
-        cfg = wl.get_config(args.config, n_layers=args.layers)
+    over = {k: v for k, v in (("n_layers", args.layers), ("vocab", args.vocab)) if v}
+    if over:
+        cfg = wl.get_config(args.config, **over)
     N_req = args.tokens or cfg.n_tokens
     b = wl.make_batch(cfg, N_req)
     N = len(b["tokens"])
@@ -350,6 +353,26 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
+    # ---- tokens whose dL/dl is non-zero (from this run's logprobs) ----------
+    nz_g = count_nonzero_g(cfg, b, lp_out.cpu().numpy(),
+                           s_dev.cpu().numpy() if s_dev is not None else None)
+
+    # ---- custom-loss protocol: the client's forward, then the custom step ----
+    protocol = None
+    if kind == "custom" and not args.no_extras:
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(args.steps):
+            m.mlora_forward(h, tok, tgt, ids, logprobs_out=lp_out)
+            step()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        pms = p0.elapsed_time(p1) / args.steps
+        protocol = {"what": "mlora_forward + mlora_forward_backward_custom + mlora_optim_step",
+                    "ms_per_step": pms, "tokens_per_s": N / (pms * 1e-3),
+                    "cost_vs_step": pms / (ms / args.steps)}
+
     # ---- rows beyond the step (outside the timed region) ---------------------
     extras = None if args.no_extras else measure_next_rows(m, h, cfg, b, dev, stream)
 
@@ -425,9 +448,31 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches),
         "e2e": e2e,
     }
+    out["config"]["tokens_nonzero_g"] = nz_g
+    if over:
+        out["config"]["profiling_override"] = over      # not a bench value
+    if protocol:
+        out["custom_protocol"] = protocol
     if extras:
         out["next_rows"] = extras
     return out, (cfg, base, ad, b)
+
+
+def count_nonzero_g(cfg, b, lp, s):
+    """Tokens whose dL/dl is non-zero for this batch (reported beside the
+    trained-token count): CE w != 0, IS A != 0, custom g != 0; PPO A != 0 and
+    the unclipped branch active at the run's logprobs."""
+    if cfg.loss == "cross_entropy":
+        return int(np.count_nonzero(b["weights"]))
+    if cfg.loss == "custom":
+        return int(np.count_nonzero(b["dloss"]))
+    A = b["advantages"].astype(np.float64)
+    if cfg.loss == "importance_sampling":
+        return int(np.count_nonzero(A))
+    r = np.exp(lp.astype(np.float64) - s.astype(np.float64))
+    un = r * A
+    cl = np.clip(r, 1 - cfg.clip_eps, 1 + cfg.clip_eps) * A
+    return int(np.count_nonzero((A != 0) & (un <= cl)))
 
 
 def measure_next_rows(m, h, cfg, b, dev, stream, reps=20):
