@@ -84,8 +84,11 @@ struct mlora {
     float* part = nullptr;
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
-    void* dz = nullptr;
-    float* zbuf = nullptr;              // fp32 logits of one chunk of rows (backward)
+    void* dz[2] = {nullptr, nullptr};   // bf16 dz of a chunk of rows, double-buffered
+    float* zbuf[2] = {nullptr, nullptr};  // fp32 logits of a chunk of rows (backward)
+    // the dz pass of chunk i runs on `side` beside the next chunk's GEMMs
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_comb[2] = {}, ev_dz[2] = {}, ev_dh[2] = {};
     double* val_row = nullptr;          // per padded row loss value
     int* status = nullptr;
     int* tile_counter = nullptr;        // GEMM tile scheduler (reset before each launch)
@@ -151,6 +154,14 @@ static void free_all(mlora_t* h) {
     h->allocs.clear();
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
     h->ev.clear();
+    for (int b = 0; b < 2; ++b) {
+        if (h->ev_comb[b]) cudaEventDestroy(h->ev_comb[b]);
+        if (h->ev_dz[b]) cudaEventDestroy(h->ev_dz[b]);
+        if (h->ev_dh[b]) cudaEventDestroy(h->ev_dh[b]);
+        h->ev_comb[b] = h->ev_dz[b] = h->ev_dh[b] = nullptr;
+    }
+    if (h->side) cudaStreamDestroy(h->side);
+    h->side = nullptr;
 }
 
 static inline int64_t tensor_size(int k, int r, int d, int f) {
@@ -328,12 +339,27 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOC(h->part, (size_t)MP * h->part_ld);
         ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
         ALLOC(h->tgt_pad, MP);
-        h->nc_tiles = h->max_tiles < 256 ? h->max_tiles : 256;   // chunks of up to 32,768 rows
-        ALLOCB(h->dz, (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
-        ALLOC(h->zbuf, (size_t)h->nc_tiles * TILE_M * h->Vpad);
-        if (cudaMemset(h->dz, 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
-            rc = fail(MLORA_E_CUDA, "cudaMemset of the dz chunk buffer failed");
+        h->nc_tiles = h->max_tiles < 128 ? h->max_tiles : 128;   // chunks of up to 16,384 rows
+        for (int b = 0; b < 2; ++b) {
+            ALLOCB(h->dz[b], (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
+            ALLOC(h->zbuf[b], (size_t)h->nc_tiles * TILE_M * h->Vpad);
+            if (cudaMemset(h->dz[b], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
+                rc = fail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
+                goto fail_out;
+            }
+        }
+        if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess) {
+            h->side = nullptr;
+            rc = fail(MLORA_E_CUDA, "cudaStreamCreate failed");
             goto fail_out;
+        }
+        for (int b = 0; b < 2; ++b) {
+            if (cudaEventCreateWithFlags(&h->ev_comb[b], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h->ev_dz[b], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h->ev_dh[b], cudaEventDisableTiming) != cudaSuccess) {
+                rc = fail(MLORA_E_CUDA, "cudaEventCreate failed");
+                goto fail_out;
+            }
         }
         ALLOC(h->val_row, (size_t)MP);
         ALLOC(h->status, 1);
@@ -601,8 +627,36 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     int chunk = (mt_upper + n_chunks - 1) / n_chunks;
     chunk = (chunk + 1) & ~1;
     if (chunk > h->nc_tiles) chunk = h->nc_tiles;
-    for (int c0 = 0; c0 < mt_upper; c0 += chunk) {
-        const int cnt = mt_upper - c0 < chunk ? mt_upper - c0 : chunk;
+    const int nch = (mt_upper + chunk - 1) / chunk;
+    // Chunk i uses logit / dz buffers i % 2.  The caller's stream runs
+    //   LMfwd(0) comb(0) | LMfwd(1) comb(1) dh(0) | LMfwd(2) comb(2) dh(1) | ... dh(n-1)
+    // and the side stream runs dz(i) after comb(i) (and after dh(i-2) has read
+    // buffer i % 2), so each HBM-bound dz pass overlaps the next chunk's
+    // compute-bound GEMMs on the SMs' spare warps.  dh(i) waits for dz(i); the
+    // caller's stream has waited for every dz pass when the last dh is queued.
+    auto chunk_rows = [&](int i, int& c0, int& cnt) {
+        c0 = i * chunk;
+        cnt = mt_upper - c0 < chunk ? mt_upper - c0 : chunk;
+    };
+    auto queue_dh = [&](int i) -> int {
+        int c0, cnt;
+        chunk_rows(i, c0, cnt);
+        const int buf = i & 1;
+        CUDA_TRY(cudaStreamWaitEvent(s, h->ev_dz[buf], 0));
+        GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
+        p.mt_base = c0; p.mt_count = cnt;
+        p.A = op_kmajor(h->dz[buf], (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
+        p.B = op_mnmajor(h->Wout, V, d);
+        p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
+        int r = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH);
+        if (r) return r;
+        CUDA_TRY(cudaEventRecord(h->ev_dh[buf], s));
+        return MLORA_OK;
+    };
+    for (int i = 0; i < nch; ++i) {
+        int c0, cnt;
+        chunk_rows(i, c0, cnt);
+        const int buf = i & 1;
         {
             GemmParams p = dense_params(h, mt_upper, V, d);
             p.mt_base = c0; p.mt_count = cnt;
@@ -610,7 +664,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.B = op_kmajor(h->Wout, V, d);
             p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
             p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
-            p.ep.out0 = h->zbuf; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+            p.ep.out0 = h->zbuf[buf]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
         }
         {
@@ -619,21 +673,19 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
                                 c0, cnt, logprobs_out, h->lse, h->gvec, h->val_row, h->num_sms, s);
             ++h->launches;
         }
+        CUDA_TRY(cudaEventRecord(h->ev_comb[buf], s));
+        CUDA_TRY(cudaStreamWaitEvent(h->side, h->ev_comb[buf], 0));
+        if (i >= 2) CUDA_TRY(cudaStreamWaitEvent(h->side, h->ev_dh[buf], 0));
         {
-            ProfScope ps(h, s, MLORA_PROF_LM_DZ);
-            launch_lm_dz<T>(h->zbuf, reinterpret_cast<T*>(h->dz), h->Vpad, V, h->Vpad, h->gvec, h->lse, h->tgt_pad,
-                            h->rb.meta, c0 * TILE_M, cnt * TILE_M, s);
+            ProfScope ps(h, h->side, MLORA_PROF_LM_DZ);
+            launch_lm_dz<T>(h->zbuf[buf], reinterpret_cast<T*>(h->dz[buf]), h->Vpad, V, h->Vpad, h->gvec, h->lse,
+                            h->tgt_pad, h->rb.meta, c0 * TILE_M, cnt * TILE_M, h->side);
             ++h->launches;
         }
-        {
-            GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
-            p.mt_base = c0; p.mt_count = cnt;
-            p.A = op_kmajor(h->dz, (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
-            p.B = op_mnmajor(h->Wout, V, d);
-            p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
-            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH))) return rc;
-        }
+        CUDA_TRY(cudaEventRecord(h->ev_dz[buf], h->side));
+        if (i >= 1 && (rc = queue_dh(i - 1))) return rc;
     }
+    if ((rc = queue_dh(nch - 1))) return rc;
     if (loss_out) {
         ProfScope ps(h, s, MLORA_PROF_OTHER);
         launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
