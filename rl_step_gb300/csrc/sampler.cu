@@ -242,6 +242,9 @@ static int s_alloc(mlora_sampler_t* s, void** p, size_t bytes) {
     return MLORA_OK;
 }
 
+template <typename P>
+static void assign_ptr(P*& dst, void* src) { dst = static_cast<P*>(src); }
+
 static void s_free(mlora_sampler_t* s) {
     for (void* p : s->allocs) cudaFree(p);
     s->allocs.clear();
@@ -269,7 +272,7 @@ extern "C" int mlora_sampler_create(mlora_t* trainer, int32_t n_slots, int64_t m
     const size_t es = t.esize, R = (size_t)s->rows_alloc, SK = (size_t)n_slots * RP;
     int rc = MLORA_OK;
 #define SALLOC(ptr, bytes) do { void* q_ = nullptr; if ((rc = s_alloc(s, &q_, (bytes))) != MLORA_OK) goto fail_out; \
-                                (ptr) = reinterpret_cast<decltype(ptr)>(q_); } while (0)
+                                assign_ptr(ptr, q_); } while (0)
     s->A1.assign(t.L, nullptr); s->B1.assign(t.L, nullptr); s->A2.assign(t.L, nullptr); s->B2.assign(t.L, nullptr);
     for (int l = 0; l < t.L; ++l) {
         SALLOC(s->A1[l], SK * t.d * es);
