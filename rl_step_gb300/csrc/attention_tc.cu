@@ -1,0 +1,832 @@
+// Causal grouped-head attention on tcgen05 for sm_103a: forward, and the
+// backward split into a key-side kernel (dK, dV) and a query-side kernel (dQ).
+//
+// Layout (padded token order, see routing.cu): the fused projection buffer
+// qkv [P x W] holds for each row the query heads (n_heads x 128), then the
+// key heads, then the value heads (n_kv x 128 each), bf16, after the rotary
+// embedding.  seq_start[p] is the padded row where row p's sequence starts;
+// rows of one sequence are consecutive, so row p attends to the keys
+// [seq_start[p], p].  Query head j reads key/value head j / (n_heads / n_kv).
+//
+// Softmax statistics travel "transposed", one contiguous run per head:
+// lseT [n_heads x ld_t] (natural-log log-sum-exp of a row's scaled scores)
+// and DT [n_heads x ld_t] (rowsum(dO * O)), so that 128 consecutive rows of
+// one head are one 512-byte bulk copy.
+//
+// Every kernel: warp 0 issues TMA loads (one elected thread), warp 1 owns
+// TMEM and issues tcgen05.mma (one elected thread), warps 2-5 (128 threads,
+// one tile row each, TMEM lane quarter = warp % 4) run the softmax arithmetic
+// from tcgen05.ld and write bf16 operands back to shared memory in the
+// 128-byte-swizzled K-major layout the next MMA reads.  Every mbarrier wait
+// is bounded; on expiry the CTA raises the timeout status bit, every role
+// stops, outstanding copies and MMAs are drained (bounded) and TMEM is freed.
+#include <cuda.h>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace mlk {
+
+namespace {
+
+using namespace tcx;
+
+constexpr int AT_THREADS = 192;
+constexpr int HD = 128;                 // head width
+constexpr int TB = 128;                 // rows per query / key tile
+constexpr int BLK = TB * 128;           // one 128-row x 64-element bf16 block (16 KB)
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct AttnMaps {
+    CUtensorMap rows128;   // qkv, boxes of 64 columns x 128 rows
+    CUtensorMap do128;     // dO [P x n_heads*128], boxes of 64 x 128 (backward only)
+};
+
+struct AttnParams {
+    const bf16* qkv;
+    int ld_qkv;            // elements per row of qkv
+    int n_heads, n_kv;
+    const int* seq_start;  // [P] padded row where the row's sequence starts
+    const int* meta;       // meta[0] = valid 128-row tiles
+    int max_tiles;
+    float scale;           // 1 / sqrt(head width)
+    // forward outputs
+    bf16* o;               // [P x n_heads*128]
+    float* lseT;           // [n_heads x ld_t]
+    int ld_t;
+    // backward inputs / outputs
+    const float* DT;       // [n_heads x ld_t]
+    bf16* dqkv;            // [P x ld_qkv]: dQ, dK, dV in the columns of q, k, v
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Wait of one warp: lane 0 polls the barrier, the warp learns the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Store 32 consecutive bf16 values (a 64-byte piece of a K-major row) into a
+// 128-byte-swizzled operand block: `blk` is the block's smem address, row r,
+// 16-byte chunks c0..c0+3 of the row.
+__device__ __forceinline__ void st_swizzled32(uint32_t blk, int r, int c0, const uint32_t (&w)[16]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t addr = blk + r * 128 + (((c0 + u) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]),
+                     "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                     : "memory");
+    }
+}
+
+// K-major 128-row operand block of 64 elements per row: K step kk (16 elements).
+__device__ __forceinline__ uint64_t kdesc(uint32_t blk, int kk) { return sdesc(blk + kk * 32, 16, 1024); }
+// The same bytes read as an MN-major operand whose K index is the row: a
+// 16-row K step at row 16*kk of K block kb (64 rows), MN halves 16 KB apart.
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kb, int kk) {
+    return sdesc(base + kb * 8192 + kk * 2048, 2 * 8192, 1024);
+}
+
+// 128 x 128 x 128 products: D (+)= A B^T with A, B both K-major (two 64-wide
+// K blocks each), or A K-major and B the MN-major view of a row-major tile.
+__device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 0, 128);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, kdesc(a + kb * BLK, kk), kdesc(b + kb * BLK, kk), id, (acc || kb || kk) ? 1u : 0u);
+}
+__device__ __forceinline__ void mma_kmn(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, kdesc(a + kb * BLK, kk), mndesc(b, kb, kk), id, (acc || kb || kk) ? 1u : 0u);
+}
+
+// Load a 128-row x 128-column bf16 tile of a row-major matrix as two
+// K-major blocks (columns 0-63, 64-127).
+__device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int row) {
+    tma_load_2d(dst, map, bar, col, row);
+    tma_load_2d(dst + BLK, map, bar, col + 64, row);
+}
+
+__device__ __forceinline__ void unpack32(const uint32_t (&r)[32], float (&v)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// Forward.  CTA = (128-row query tile, query head); key tiles of 128 rows run
+// from the first row of the tile's first sequence up to the tile's last row.
+// Per key tile j:  S = Q K_j^T (TMEM, double-buffered); the softmax warps
+// take the running row max, write P = exp(S - m) as bf16 to shared memory and
+// fold the previous tile's O_{j-1} = P_{j-1} V_{j-1} (TMEM, double-buffered)
+// into a register accumulator rescaled by exp(m_old - m_new).
+// ----------------------------------------------------------------------------
+namespace {
+
+struct FwdSmem {
+    static constexpr int Q = 0;
+    static constexpr int K0 = 2 * BLK;          // two stages of 32 KB
+    static constexpr int V0 = K0 + 4 * BLK;     // two stages of 32 KB
+    static constexpr int P = V0 + 4 * BLK;      // 32 KB
+    static constexpr int BAR = P + 2 * BLK;
+    enum { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_FREE = 9, P_FULL = 11,
+           O_FULL = 12, O_FREE = 14, DRAIN = 16, NBARS = 17 };
+    static constexpr int MISC = BAR + NBARS * 8;
+    static constexpr int TOTAL = MISC + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
+    using SL = FwdSmem;
+    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
+    const int tile = blockIdx.x / p.n_heads, h = blockIdx.x % p.n_heads;
+    if (tile >= mt_valid) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + SL::BAR + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int m0 = tile * TB;
+    const int kstart = p.seq_start[m0];
+    const int nt = (m0 + TB - kstart + TB - 1) / TB;
+    const int grp = p.n_heads / p.n_kv, g = h / grp;
+    const int qcol = h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+
+    if (threadIdx.x == 0) {
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 1, 4, 4, 1};
+        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+        tma_prefetch_desc(&maps.rows128);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;   // S[s] at columns 128 s, O[s] at 256 + 128 s
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued[2] = {-1, -1};
+            mbar_expect_tx(bar(SL::Q_FULL), 2 * BLK);
+            load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, m0);
+            for (int j = 0; j < nt; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                if (!mbar_wait(bar(SL::KV_EMPTY + s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                const int key0 = kstart + j * TB;
+                mbar_expect_tx(bar(SL::K_FULL + s), 2 * BLK);
+                load_tile128(sb + SL::K0 + s * 2 * BLK, &maps.rows128, bar(SL::K_FULL + s), kcol, key0);
+                mbar_expect_tx(bar(SL::V_FULL + s), 2 * BLK);
+                load_tile128(sb + SL::V0 + s * 2 * BLK, &maps.rows128, bar(SL::V_FULL + s), vcol, key0);
+                issued[s] = (int)ph;
+            }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            int dummy = 0;
+            bool dr = mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] >= 0) {
+                    dr &= mbar_wait(bar(SL::K_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
+                    dr &= mbar_wait(bar(SL::V_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
+                }
+            if (!dr) atomicOr(status, ST_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag);
+            auto pv = [&](int i) -> bool {
+                const int s = i & 1;
+                const uint32_t ph = (i >> 1) & 1;
+                if (!mbar_wait(bar(SL::V_FULL + s), ph, abort_flag)) return false;
+                if (!mbar_wait(bar(SL::P_FULL), (uint32_t)(i & 1), abort_flag)) return false;
+                if (!mbar_wait(bar(SL::O_FREE + s), ph ^ 1u, abort_flag)) return false;
+                tc_fence_after();
+                mma_kmn(tmem + 256 + 128 * s, sb + SL::P, sb + SL::V0 + s * 2 * BLK, false);
+                umma_commit(bar(SL::KV_EMPTY + s));
+                umma_commit(bar(SL::O_FULL + s));
+                return true;
+            };
+            for (int j = 0; j < nt && ok; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                if (!mbar_wait(bar(SL::K_FULL + s), ph, abort_flag) ||
+                    !mbar_wait(bar(SL::S_FREE + s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                mma_kk(tmem + 128 * s, sb + SL::Q, sb + SL::K0 + s * 2 * BLK, false);
+                umma_commit(bar(SL::S_FULL + s));
+                if (j >= 1 && !pv(j - 1)) ok = false;
+            }
+            if (ok && !pv(nt - 1)) ok = false;
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            umma_commit(bar(SL::DRAIN));
+            int dummy = 0;
+            if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const int i = m0 + r;
+        const int ss = p.seq_start[i];
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const float sc = p.scale * LOG2E;
+        float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
+        float O[HD];
+#pragma unroll
+        for (int e = 0; e < HD; ++e) O[e] = 0.f;
+        bool ok = true;
+        uint32_t rr[32];
+        float v[32];
+        // O <- O * alpha + (the finished P V tile in O[s])
+        auto fold = [&](int i_tile, float alpha) -> bool {
+            const int s = i_tile & 1;
+            if (!warp_wait(bar(SL::O_FULL + s), (uint32_t)((i_tile >> 1) & 1), abort_flag, lane)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 256 + 128 * s + 32 * c, rr);
+                tmem_ld_wait();
+                unpack32(rr, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) O[32 * c + e] = fmaf(O[32 * c + e], alpha, v[e]);
+            }
+            return true;
+        };
+        for (int j = 0; j < nt; ++j) {
+            const int s = j & 1;
+            if (!warp_wait(bar(SL::S_FULL + s), (uint32_t)((j >> 1) & 1), abort_flag, lane)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = kstart + j * TB;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 128 * s + 32 * c, rr);
+                tmem_ld_wait();
+                unpack32(rr, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int key = key0 + 32 * c + e;
+                    if (key >= ss && key <= i) mx = fmaxf(mx, v[e] * sc);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            if (j >= 1) {   // fold O_{j-1}; its MMA has then also finished reading P
+                if (!fold(j - 1, alpha_prev)) { ok = false; break; }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::O_FREE + ((j - 1) & 1)));
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 128 * s + 32 * c, rr);
+                tmem_ld_wait();
+                unpack32(rr, v);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int key = key0 + 32 * c + e;
+                    const float p0 = (key >= ss && key <= i) ? exp2f(fmaf(v[e], sc, -m_new)) : 0.f;
+                    const float p1 = (key + 1 >= ss && key + 1 <= i) ? exp2f(fmaf(v[e + 1], sc, -m_new)) : 0.f;
+                    rs += p0 + p1;
+                    w[e >> 1] = pack_bf16x2(p0, p1);
+                }
+                st_swizzled32(sb + SL::P + (c >> 1) * BLK, r, (c & 1) * 4, w);
+            }
+            tc_fence_before();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(SL::S_FREE + s));
+                mbar_arrive(bar(SL::P_FULL));
+            }
+            l_run = l_run * alpha + rs;
+            alpha_prev = alpha;
+            m_run = m_new;
+        }
+        if (ok) ok = fold(nt - 1, alpha_prev);
+        if (ok) {
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            bf16* dst = p.o + (int64_t)i * p.n_heads * HD + h * HD;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float t[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) t[e] = O[32 * c + e] * inv;
+                store32<bf16>(dst + 32 * c, t);
+            }
+            p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        } else if (lane == 0) {
+            atomicOr(status, ST_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// Backward, key side.  CTA = (128-row key tile, key/value head g).  For every
+// query head of the group and every query tile that can see these keys:
+//   S^T = K Q^T, dP^T = V dO^T                     (TMEM)
+//   P^T = exp(scale S^T - lse_q), dS^T = P^T (dP^T - D_q)   (softmax warps,
+//                                   one key row per thread, bf16 to smem)
+//   dV += P^T dO,  dK += dS^T Q                     (TMEM accumulators)
+// and finally dK *= scale.  Each dK / dV element has a single writer.
+// ----------------------------------------------------------------------------
+namespace {
+
+struct KvSmem {
+    static constexpr int K = 0;
+    static constexpr int V = 2 * BLK;
+    static constexpr int Q = 4 * BLK;
+    static constexpr int DO = 6 * BLK;
+    static constexpr int PT = 8 * BLK;
+    static constexpr int DST = 10 * BLK;
+    static constexpr int VEC = 12 * BLK;        // lse[128], D[128] (fp32), seq_start[128] of the query tile
+    static constexpr int BAR = VEC + 3 * 512;
+    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 2, ST_FULL = 3, ST_FREE = 4, P_FULL = 5, P_EMPTY = 6,
+           ACC_FULL = 7, DRAIN = 8, NBARS = 9 };
+    static constexpr int MISC = BAR + NBARS * 8;
+    static constexpr int TOTAL = MISC + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_bwd_kv_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
+    using SL = KvSmem;
+    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
+    const int kt = blockIdx.x / p.n_kv, g = blockIdx.x % p.n_kv;
+    if (kt >= mt_valid) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + SL::BAR + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int k0 = kt * TB;
+    const int grp = p.n_heads / p.n_kv;
+    const int kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+    // query tiles kt .. kt + nqt - 1: the first row of each starts its
+    // sequence at or before this tile's last key
+    int nqt = 0;
+    while (kt + nqt < mt_valid && p.seq_start[(kt + nqt) * TB] <= k0 + TB - 1) ++nqt;
+    const int niter = grp * nqt;
+
+    if (threadIdx.x == 0) {
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 4, 4, 1, 1, 1};
+        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+        tma_prefetch_desc(&maps.rows128);
+        tma_prefetch_desc(&maps.do128);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;   // S^T 0, dP^T 128, dV 256, dK 384
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int last = -1;
+            mbar_expect_tx(bar(SL::KV_FULL), 4 * BLK);
+            load_tile128(sb + SL::K, &maps.rows128, bar(SL::KV_FULL), kcol, k0);
+            load_tile128(sb + SL::V, &maps.rows128, bar(SL::KV_FULL), vcol, k0);
+            for (int n = 0; n < niter; ++n) {
+                const int h = g * grp + n / nqt, q0 = (kt + n % nqt) * TB;
+                if (!mbar_wait(bar(SL::QD_EMPTY), (uint32_t)(n & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                const uint32_t fb = bar(SL::QD_FULL);
+                mbar_expect_tx(fb, 4 * BLK + 3 * 512);
+                load_tile128(sb + SL::Q, &maps.rows128, fb, h * HD, q0);
+                load_tile128(sb + SL::DO, &maps.do128, fb, h * HD, q0);
+                bulk_load(sb + SL::VEC, p.lseT + (int64_t)h * p.ld_t + q0, 512, fb);
+                bulk_load(sb + SL::VEC + 512, p.DT + (int64_t)h * p.ld_t + q0, 512, fb);
+                bulk_load(sb + SL::VEC + 1024, p.seq_start + q0, 512, fb);
+                last = n;
+            }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            int dummy = 0;
+            bool dr = mbar_wait(bar(SL::KV_FULL), 0, (volatile int*)&dummy);
+            if (last >= 0) dr &= mbar_wait(bar(SL::QD_FULL), (uint32_t)(last & 1), (volatile int*)&dummy);
+            if (!dr) atomicOr(status, ST_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(SL::KV_FULL), 0, abort_flag);
+            for (int n = 0; n < niter && ok; ++n) {
+                const uint32_t ph = (uint32_t)(n & 1);
+                if (!mbar_wait(bar(SL::QD_FULL), ph, abort_flag) ||
+                    !mbar_wait(bar(SL::ST_FREE), ph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                mma_kk(tmem, sb + SL::K, sb + SL::Q, false);
+                mma_kk(tmem + 128, sb + SL::V, sb + SL::DO, false);
+                umma_commit(bar(SL::ST_FULL));
+                if (!mbar_wait(bar(SL::P_FULL), ph, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                mma_kmn(tmem + 256, sb + SL::PT, sb + SL::DO, n > 0);
+                mma_kmn(tmem + 384, sb + SL::DST, sb + SL::Q, n > 0);
+                umma_commit(bar(SL::QD_EMPTY));
+                umma_commit(bar(SL::P_EMPTY));
+            }
+            if (ok) umma_commit(bar(SL::ACC_FULL));
+            else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            umma_commit(bar(SL::DRAIN));
+            int dummy = 0;
+            if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const int j = k0 + r;                          // this thread's key row
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const float sc = p.scale * LOG2E;
+        const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC);
+        const float* D_s = reinterpret_cast<const float*>(smem + SL::VEC + 512);
+        const int* ss_s = reinterpret_cast<const int*>(smem + SL::VEC + 1024);
+        bool ok = true;
+        uint32_t ra[32], rb[32];
+        float s_[32], dp[32];
+        for (int n = 0; n < niter; ++n) {
+            const uint32_t ph = (uint32_t)(n & 1);
+            const int q0 = (kt + n % nqt) * TB;
+            if (!warp_wait(bar(SL::QD_FULL), ph, abort_flag, lane) ||
+                !warp_wait(bar(SL::ST_FULL), ph, abort_flag, lane) ||
+                !warp_wait(bar(SL::P_EMPTY), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 32 * c, ra);
+                tmem_ld32(tl + 128 + 32 * c, rb);
+                tmem_ld_wait();
+                unpack32(ra, s_);
+                unpack32(rb, dp);
+                uint32_t wp[16], wd[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = 32 * c + e + u;
+                        const bool valid = (q0 + q >= j) && (ss_s[q] <= j);
+                        pr[u] = valid ? exp2f(fmaf(s_[e + u], sc, -lse_s[q] * LOG2E)) : 0.f;
+                        ds[u] = pr[u] * (dp[e + u] - D_s[q]);
+                    }
+                    wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
+                    wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                }
+                st_swizzled32(sb + SL::PT + (c >> 1) * BLK, r, (c & 1) * 4, wp);
+                st_swizzled32(sb + SL::DST + (c >> 1) * BLK, r, (c & 1) * 4, wd);
+            }
+            tc_fence_before();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(SL::ST_FREE));
+                mbar_arrive(bar(SL::P_FULL));
+            }
+        }
+        if (ok && niter > 0) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
+        if (ok && niter > 0) {
+            tc_fence_after();
+            bf16* row = p.dqkv + (int64_t)j * p.ld_qkv;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 256 + 32 * c, ra);
+                tmem_ld32(tl + 384 + 32 * c, rb);
+                tmem_ld_wait();
+                unpack32(ra, s_);
+                unpack32(rb, dp);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dp[e] *= p.scale;
+                store32<bf16>(row + vcol + 32 * c, s_);
+                store32<bf16>(row + kcol + 32 * c, dp);
+            }
+        } else if (!ok && lane == 0) {
+            atomicOr(status, ST_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// Backward, query side.  CTA = (128-row query tile, query head).  Over the
+// forward's key tiles:  S = Q K_j^T, dP = dO V_j^T (TMEM);  P = exp(scale S -
+// lse), dS = P (dP - D) (softmax warps, one query row per thread, bf16 to
+// smem);  dQ += dS K_j (TMEM);  finally dQ *= scale.
+// ----------------------------------------------------------------------------
+namespace {
+
+struct QSmem {
+    static constexpr int Q = 0;
+    static constexpr int DO = 2 * BLK;
+    static constexpr int K0 = 4 * BLK;          // two stages of 32 KB
+    static constexpr int V0 = 8 * BLK;          // two stages of 32 KB
+    static constexpr int DS = 12 * BLK;
+    static constexpr int BAR = 14 * BLK;
+    enum { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_FREE = 8, DS_FULL = 9,
+           DS_EMPTY = 10, ACC_FULL = 11, DRAIN = 12, NBARS = 13 };
+    static constexpr int MISC = BAR + NBARS * 8;
+    static constexpr int TOTAL = MISC + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_bwd_q_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
+    using SL = QSmem;
+    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
+    const int tile = blockIdx.x / p.n_heads, h = blockIdx.x % p.n_heads;
+    if (tile >= mt_valid) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + SL::BAR + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int m0 = tile * TB;
+    const int kstart = p.seq_start[m0];
+    const int nt = (m0 + TB - kstart + TB - 1) / TB;
+    const int grp = p.n_heads / p.n_kv, g = h / grp;
+    const int qcol = h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+
+    if (threadIdx.x == 0) {
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1};
+        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+        tma_prefetch_desc(&maps.rows128);
+        tma_prefetch_desc(&maps.do128);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;   // S 0, dP 128, dQ 256
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued[2] = {-1, -1};
+            mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
+            load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, m0);
+            load_tile128(sb + SL::DO, &maps.do128, bar(SL::Q_FULL), qcol, m0);
+            for (int j = 0; j < nt; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                if (!mbar_wait(bar(SL::KV_EMPTY + s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                const int key0 = kstart + j * TB;
+                mbar_expect_tx(bar(SL::K_FULL + s), 2 * BLK);
+                load_tile128(sb + SL::K0 + s * 2 * BLK, &maps.rows128, bar(SL::K_FULL + s), kcol, key0);
+                mbar_expect_tx(bar(SL::V_FULL + s), 2 * BLK);
+                load_tile128(sb + SL::V0 + s * 2 * BLK, &maps.rows128, bar(SL::V_FULL + s), vcol, key0);
+                issued[s] = (int)ph;
+            }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            int dummy = 0;
+            bool dr = mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] >= 0) {
+                    dr &= mbar_wait(bar(SL::K_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
+                    dr &= mbar_wait(bar(SL::V_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
+                }
+            if (!dr) atomicOr(status, ST_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag);
+            for (int j = 0; j < nt && ok; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1, pj = (uint32_t)(j & 1);
+                if (!mbar_wait(bar(SL::K_FULL + s), ph, abort_flag) ||
+                    !mbar_wait(bar(SL::V_FULL + s), ph, abort_flag) ||
+                    !mbar_wait(bar(SL::S_FREE), pj ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                mma_kk(tmem, sb + SL::Q, sb + SL::K0 + s * 2 * BLK, false);
+                mma_kk(tmem + 128, sb + SL::DO, sb + SL::V0 + s * 2 * BLK, false);
+                umma_commit(bar(SL::S_FULL));
+                if (!mbar_wait(bar(SL::DS_FULL), pj, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                mma_kmn(tmem + 256, sb + SL::DS, sb + SL::K0 + s * 2 * BLK, j > 0);
+                umma_commit(bar(SL::KV_EMPTY + s));
+                umma_commit(bar(SL::DS_EMPTY));
+            }
+            if (ok) umma_commit(bar(SL::ACC_FULL));
+            else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            umma_commit(bar(SL::DRAIN));
+            int dummy = 0;
+            if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const int i = m0 + r;
+        const int ss = p.seq_start[i];
+        const float lse2 = p.lseT[(int64_t)h * p.ld_t + i] * LOG2E;
+        const float Di = p.DT[(int64_t)h * p.ld_t + i];
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const float sc = p.scale * LOG2E;
+        bool ok = true;
+        uint32_t ra[32], rb[32];
+        float s_[32], dp[32];
+        for (int j = 0; j < nt; ++j) {
+            const uint32_t pj = (uint32_t)(j & 1);
+            if (!warp_wait(bar(SL::S_FULL), pj, abort_flag, lane) ||
+                !warp_wait(bar(SL::DS_EMPTY), pj ^ 1u, abort_flag, lane)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = kstart + j * TB;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 32 * c, ra);
+                tmem_ld32(tl + 128 + 32 * c, rb);
+                tmem_ld_wait();
+                unpack32(ra, s_);
+                unpack32(rb, dp);
+                uint32_t wd[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int key = key0 + 32 * c + e + u;
+                        const float pr = (key >= ss && key <= i) ? exp2f(fmaf(s_[e + u], sc, -lse2)) : 0.f;
+                        ds[u] = pr * (dp[e + u] - Di);
+                    }
+                    wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                }
+                st_swizzled32(sb + SL::DS + (c >> 1) * BLK, r, (c & 1) * 4, wd);
+            }
+            tc_fence_before();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(SL::S_FREE));
+                mbar_arrive(bar(SL::DS_FULL));
+            }
+        }
+        if (ok) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
+        if (ok) {
+            tc_fence_after();
+            bf16* row = p.dqkv + (int64_t)i * p.ld_qkv + qcol;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 256 + 32 * c, ra);
+                tmem_ld_wait();
+                unpack32(ra, s_);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s_[e] *= p.scale;
+                store32<bf16>(row + 32 * c, s_);
+            }
+        } else if (lane == 0) {
+            atomicOr(status, ST_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// D[h][p] = sum_c dO[p][h*128 + c] O[p][h*128 + c]: 16 threads per (row, head),
+// 8 elements each.
+__global__ void attn_rowdot_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, int n_heads,
+                                   const int* __restrict__ meta, int max_tiles, float* __restrict__ DT, int ld_t) {
+    const int mt = *meta < max_tiles ? *meta : max_tiles;
+    const int64_t rows = (int64_t)mt * TB;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t unit = gid >> 4;                 // (row, head)
+    const int part = (int)(gid & 15);
+    const int64_t row = unit / n_heads;
+    const int h = (int)(unit % n_heads);
+    float acc = 0.f;
+    if (row < rows) {
+        const int64_t off = row * (int64_t)n_heads * HD + h * HD + part * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(dO + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(O + off);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (row < rows && part == 0) DT[(int64_t)h * ld_t + row] = acc;
+}
+
+template <typename K>
+cudaError_t launch_attn(K kernel, int smem_bytes, const AttnMaps& maps, const AttnParams& p, int grid, int* status,
+                        cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (grid <= 0) return cudaSuccess;
+    kernel<<<grid, AT_THREADS, smem_bytes, s>>>(maps, p, status);
+    return cudaGetLastError();
+}
+
+bool make_maps(AttnMaps& m, const AttnArgs& a) {
+    const int64_t W = (int64_t)(a.n_heads + 2 * a.n_kv) * HD;
+    if (!tc_encode_bf16(&m.rows128, a.qkv, a.max_rows, W, W, 64, TB)) return false;
+    if (a.dO) {
+        if (!tc_encode_bf16(&m.do128, a.dO, a.max_rows, (int64_t)a.n_heads * HD, (int64_t)a.n_heads * HD, 64, TB))
+            return false;
+    } else {
+        m.do128 = m.rows128;
+    }
+    return true;
+}
+
+AttnParams make_params(const AttnArgs& a) {
+    AttnParams p;
+    p.qkv = a.qkv;
+    p.ld_qkv = (a.n_heads + 2 * a.n_kv) * HD;
+    p.n_heads = a.n_heads;
+    p.n_kv = a.n_kv;
+    p.seq_start = a.seq_start;
+    p.meta = a.meta;
+    p.max_tiles = a.max_rows / TB;
+    p.scale = 1.0f / sqrtf((float)HD);
+    p.o = a.o;
+    p.lseT = a.lseT;
+    p.ld_t = a.ld_t;
+    p.DT = a.DT;
+    p.dqkv = a.dqkv;
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s) {
+    AttnMaps maps;
+    if (!make_maps(maps, a) || a.max_rows % TB || a.ld_t % 4) return cudaErrorInvalidValue;
+    const AttnParams p = make_params(a);
+    return launch_attn(attn_fwd_kernel, FwdSmem::TOTAL, maps, p, p.max_tiles * a.n_heads, status, s);
+}
+
+cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s) {
+    AttnMaps maps;
+    if (!a.dO || !make_maps(maps, a) || a.max_rows % TB || a.ld_t % 4) return cudaErrorInvalidValue;
+    const AttnParams p = make_params(a);
+    const int threads = 256;
+    const int64_t units = (int64_t)a.max_rows * a.n_heads * 16;
+    attn_rowdot_kernel<<<(unsigned)((units + threads - 1) / threads), threads, 0, s>>>(
+        a.dO, a.o, a.n_heads, a.meta, p.max_tiles, a.DT, a.ld_t);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_attn(attn_bwd_kv_kernel, KvSmem::TOTAL, maps, p, p.max_tiles * a.n_kv, status, s);
+    if (e != cudaSuccess) return e;
+    return launch_attn(attn_bwd_q_kernel, QSmem::TOTAL, maps, p, p.max_tiles * a.n_heads, status, s);
+}
+
+}  // namespace mlk

@@ -31,9 +31,20 @@ enum EpiKind : int {
     EPI_LMFWD = 5,    // per row: log-sum-exp over the tile's cols < V, target z; z kept if out0 (LM head)
     EPI_GRAD = 6,     // grad[a] += acc (fp32 atomics), non-finite flag         (dA / dB)
     EPI_MERGE = 7,    // out0 = T(aux + gamma[a] * acc)                         (W' = W + gamma B A)
-    EPI_SHRINK_SEL = 8  // column block s = col / RP: out0 = T(gamma[s] * acc) on rows whose
+    EPI_SHRINK_SEL = 8, // column block s = col / RP: out0 = T(gamma[s] * acc) on rows whose
                         // slot is s, 0 elsewhere                                   (sampler shrink)
+    EPI_STORE = 9,      // out0 = T(acc)                                            (q, k, v / dO)
+    EPI_F32 = 10,       // f32 = acc                                                (norm input grads)
+    EPI_SWIGLU = 11,    // columns interleave 16 gate / 16 up: out0 = T(acc) (kept for the
+                        // backward), out1[col/2 ..] = T(silu(gate) * up)             (gated MLP)
+    EPI_DSWIGLU = 12    // acc = d act; aux = the kept gate/up rows (interleaved as above):
+                        // out0 = T(d gate | d up) in the same interleaved columns
 };
+
+// Gate/up interleave of the fused gated-MLP projection: output column n of
+// the fused weight is gate row (n / 32) * 16 + n % 16 when (n / 16) is even,
+// up row of the same index otherwise.
+constexpr int GU_ILV = 16;
 
 struct EpiParams {
     int kind = 0;
@@ -58,6 +69,9 @@ struct EpiParams {
     const int* ranks = nullptr;
     int grad_trans = 0;             // 0: grad[m*r + n]; 1: grad[n*M + m]
     int grad_M = 0;
+    int grad_ilv = 0;               // > 0: rows interleave two tensors in blocks of grad_ilv;
+    int grad_sub = 0;               //      only rows of block parity grad_sub are accumulated,
+                                    //      at row (row / (2 ilv)) ilv + row % ilv
     int* nonfinite = nullptr;       // per adapter flag
     const int* row_slot = nullptr;  // sampler: adapter slot per row (-1: none)
 };
@@ -107,6 +121,21 @@ template <> __device__ __forceinline__ void store32<float>(float* dst, const flo
     float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+// first 16 of the values, 16 consecutive elements (32 bytes bf16, 64 bytes fp32)
+template <typename T> __device__ __forceinline__ void store16v(T* dst, const float* v);
+template <> __device__ __forceinline__ void store16v<bf16>(bf16* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+template <> __device__ __forceinline__ void store16v<float>(float* dst, const float* v) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 template <typename T> __device__ __forceinline__ void load32(const T* src, float* v);
@@ -172,11 +201,43 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
 #pragma unroll
         for (int j = 0; j < 32; ++j) h[j] += acc[j];
         store32<float>(hp, h);
-        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, h);
+        if (ep.out0) store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, h);
     } break;
     case EPI_STORE2: {
         store32<float>(ep.f32 + row * ep.ldf + col0, acc);
+        if (ep.out0) store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+    } break;
+    case EPI_STORE: {
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+    } break;
+    case EPI_F32: {
+        store32<float>(ep.f32 + row * ep.ldf + col0, acc);
+    } break;
+    case EPI_SWIGLU: {
+        store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a[j] = acc[j] * sigmoidf_(acc[j]) * acc[16 + j];
+#pragma unroll
+        for (int j = 16; j < 32; ++j) a[j] = 0.f;
+        store16v<T>(reinterpret_cast<T*>(ep.out1) + row * ep.ld1 + col0 / 2, a);
+    } break;
+    case EPI_DSWIGLU: {
+        const T* gu = reinterpret_cast<const T*>(ep.aux) + row * ep.ld_aux + 2 * col0;
+        T* dgu = reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + 2 * col0;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            float g[32], o[32];
+            load32<T>(gu + 32 * hb, g);     // g[0..15] gate, g[16..31] up
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float da = acc[16 * hb + j];
+                const float sg = sigmoidf_(g[j]);
+                o[j] = da * g[16 + j] * (sg * (1.f + g[j] * (1.f - sg)));
+                o[16 + j] = da * g[j] * sg;
+            }
+            store32<T>(dgu + 32 * hb, o);
+        }
     } break;
     case EPI_DSILU: {
         float u[32];
@@ -236,6 +297,10 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     case EPI_GRAD: {
         int r = ep.ranks[adapter];
         float* base = ep.grad + ep.grad_off[adapter];
+        if (ep.grad_ilv) {
+            if ((int)((row / ep.grad_ilv) & 1) != ep.grad_sub) break;
+            row = (row / (2 * ep.grad_ilv)) * ep.grad_ilv + row % ep.grad_ilv;
+        }
         bool bad = false;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {

@@ -13,9 +13,60 @@ template <typename T> void launch_simt_gemm(const GemmParams& p, cudaStream_t s)
 // tcgen05 engine (bf16 only).  Returns cudaSuccess or the first error.
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status);
 bool tc_engine_available();
+// TMA descriptor (CUtensorMap, 128-byte swizzle) of a row-major bf16 matrix
+// [rows x cols] with row pitch ld elements, boxes of box_cols x box_rows.
+bool tc_encode_bf16(void* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+                    uint32_t box_rows);
 // CTA-pair (cta_group::2) variant for GEMMs whose B is shared by all rows.
 cudaError_t launch_tc_gemm_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status,
                                 int acc_buffers, int* dbg);
+
+// ---- attention (attention_tc.cu) ---------------------------------------------
+// Causal grouped-head attention over padded token rows; head width 128.
+struct AttnArgs {
+    const bf16* qkv = nullptr;     // [max_rows x (n_heads + 2 n_kv) * 128]: q heads, k heads, v heads
+    int n_heads = 0, n_kv = 0;
+    int max_rows = 0;              // rows of every buffer below (multiple of 128)
+    const int* seq_start = nullptr;  // [max_rows] first padded row of the row's sequence
+    const int* meta = nullptr;     // meta[0] = valid 128-row tiles
+    bf16* o = nullptr;             // [max_rows x n_heads*128]
+    float* lseT = nullptr;         // [n_heads x ld_t] log-sum-exp of the scaled scores
+    float* DT = nullptr;           // [n_heads x ld_t] rowsum(dO * O) (backward)
+    int ld_t = 0;                  // multiple of 4
+    const bf16* dO = nullptr;      // backward: dL/dO [max_rows x n_heads*128]
+    bf16* dqkv = nullptr;          // backward: dL/d(q, k, v), same layout as qkv
+};
+cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s);
+// rowsum kernel, key-side (dK, dV) kernel, query-side (dQ) kernel
+cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s);
+
+// ---- transformer block (tf_kernels.cu) ----------------------------------------
+constexpr int TF_NPROJ = 7;        // q, k, v, o, gate, up, down
+// Where the bf16 padded-rank copy of each projection's factors lives.  A
+// projection belongs to a fused group (q/k/v, o, gate/up, down) whose
+// shadows are A_g [n_ad * kx x in] (sub-projection s in rows 64 s ..) and
+// B_g [n_ad * n_rows x kx] (sub-projection s in columns 64 s ..; its output
+// rows at row_off + i, or interleaved in blocks of ilv for gate/up).
+struct TfMirrorProj {
+    bf16* A = nullptr;
+    bf16* B = nullptr;
+    int64_t a_layer = 0, b_layer = 0;  // elements between consecutive layers' shadows
+    int in = 0, out = 0;
+    int kx = 0, sub = 0, n_rows = 0, row_off = 0, ilv = 0;
+};
+struct TfMirror {
+    TfMirrorProj p[TF_NPROJ];
+    int64_t sum_in_out = 0;            // sum over projections of in + out
+};
+void launch_tf_rows(const int* perm_pad, const int* meta, const int* tile_ad, const int* pad_off,
+                    const int* positions, const int* adapter_ids, int max_pos, int max_rows, int* pos_pad,
+                    int* seq_start, int* status, cudaStream_t s);
+void launch_rmsnorm_fwd(const float* x, const bf16* g, int d, float eps, const int* meta, int max_rows, bf16* y,
+                        float* rstd, float* snap, cudaStream_t s);
+void launch_rmsnorm_bwd(const float* dy, const float* x, const bf16* g, const float* rstd, int d, const int* meta,
+                        int max_rows, int accumulate, float* dh, bf16* dhb, cudaStream_t s);
+void launch_rope(bf16* buf, int64_t ld, int col0, int n_heads, const int* pos_pad, const float2* cs,
+                 const int* meta, int max_rows, int inverse, cudaStream_t s);
 
 // ---- routing ----------------------------------------------------------------
 struct RouteBufs {
@@ -72,6 +123,10 @@ struct AdamTab {
 };
 void launch_adam_prep(int n_ad, const int* sel_mask, int* touched, int* nonfinite, int64_t* step,
                       float beta1, float beta2, AdamTab* tab, int* skipped_out, cudaStream_t s);
+
+void launch_tf_adam(int n_ad, const int64_t* ad_off, const int* ranks, int64_t total, const AdamTab* tab, float* P,
+                    float* G, float* M, float* Vm, float lr, float beta1, float beta2, float eps, float wd,
+                    const TfMirror& mr, int sync_only, int num_sms, cudaStream_t s);
 
 struct ShadowMap {
     void* A1[64];

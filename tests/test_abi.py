@@ -69,3 +69,22 @@ def test_argument_errors_need_no_gpu(lib):
 def test_build_is_for_sm103a():
     src = open(os.path.join(ROOT, "rl_step_gb300", "_build.py")).read()
     assert "arch=compute_103a,code=sm_103a" in src
+
+
+def test_transformer_entry_points_reject_bad_arguments_without_a_gpu(lib):
+    import ctypes
+    import rl_step_gb300.transformer as t
+    tl = t._lib()
+    out = ctypes.c_void_p()
+    assert tl.mlora_tf_create(None, None, ctypes.byref(out)) == -1
+    assert b"NULL" in tl.mlora_last_error()
+    ranks = (ctypes.c_int32 * 1)(8)
+    alphas = (ctypes.c_float * 1)(16.0)
+    cfg = t._TfConfig(100, 256, 4, 3, 128, 512, 2, 1, ranks, alphas, 1e6, 1e-6, 64)   # 3 does not divide 4
+    init = t._TfInit()
+    assert tl.mlora_tf_create(ctypes.byref(cfg), ctypes.byref(init), ctypes.byref(out)) == -1
+    cfg = t._TfConfig(100, 256, 4, 2, 64, 512, 2, 1, ranks, alphas, 1e6, 1e-6, 64)    # head_dim 64
+    assert tl.mlora_tf_create(ctypes.byref(cfg), ctypes.byref(init), ctypes.byref(out)) == -1
+    assert b"head_dim" in tl.mlora_last_error()
+    assert tl.mlora_tf_forward(None, None, None, None) == -1
+    assert tl.mlora_tf_kernel_launches(None) == 0

@@ -22,7 +22,10 @@ Draws follow the MLP workloads: numpy PCG64 streams keyed by (seed, tensor
 id, block); base weights N(0, w_std) rounded to bf16; norm gains 1 + N(0,
 0.1) rounded to bf16; adapters fp32 masters, A ~ N(0, 0.02), B ~ N(0, 0.01);
 token ids uniform; sequences laid out contiguously in generation order, each
-token's position its index inside its sequence.
+token's position its index inside its sequence.  qk_std > 0 draws the q and k
+weights at that scale instead (at d = 256, 0.08 makes the attention scores
+spread like those of the 8B widths at 0.02: query entries of standard
+deviation ~1.3).
 """
 from __future__ import annotations
 
@@ -57,6 +60,7 @@ class TfConfig:
     seq_hi: int
     adapter_dist: str = "uniform"     # uniform | zipf
     w_std: float = 0.02
+    qk_std: float = 0.0                # q / k weights (0: w_std)
     clip_eps: float = 0.2
     sampler_sigma: float = 0.1
     rope_theta: float = 1e6
@@ -78,7 +82,7 @@ _TF = {
     "tf_small": TfConfig(
         name="tf_small", vocab=1000, d_model=256, n_heads=4, n_kv_heads=2, head_dim=128,
         d_ffn=512, n_layers=2, n_adapters=3, ranks=(8, 16, 32), alphas=(16.0, 16.0, 32.0),
-        n_tokens=1024, loss="ppo", seed=2001, seq_lo=20, seq_hi=300, w_std=0.06,
+        n_tokens=1024, loss="ppo", seed=2001, seq_lo=20, seq_hi=300,
         description="small transformer bf16: V=1000 d=256 4q/2kv heads x 128 f=512 L=2, "
                     "3 adapters r=8/16/32, seqs of 20-300 tokens"),
     "qwen3_8b_tf_ppo": TfConfig(
@@ -106,7 +110,8 @@ def make_tf_base_weights(cfg: TfConfig) -> dict:
     with ThreadPoolExecutor(_n_threads()) as pool:
         E = _normal_matrix((cfg.seed, 0, 0), V, d, cfg.w_std, True, pool)
         Wout = _normal_matrix((cfg.seed, 0, 1), V, d, cfg.w_std, True, pool)
-        W = {p: [_normal_matrix((cfg.seed, 0, 10 + 10 * i, l), *shapes[p], cfg.w_std, True, pool)
+        std = {p: (cfg.qk_std if p in ("q", "k") and cfg.qk_std > 0 else cfg.w_std) for p in PROJ}
+        W = {p: [_normal_matrix((cfg.seed, 0, 10 + 10 * i, l), *shapes[p], std[p], True, pool)
                  for l in range(L)] for i, p in enumerate(PROJ)}
 
     def gain(key):
