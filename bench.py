@@ -56,6 +56,14 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the sampler-decode and export-merge measurements")
+    ap.add_argument("--no-tf", action="store_true",
+                    help="skip the transformer-block row (next_rows.transformer_step)")
+    ap.add_argument("--tf-only", action="store_true",
+                    help="run only the transformer-block row and print it (profiling)")
+    ap.add_argument("--tf-tokens", type=int, default=None,
+                    help="override the transformer row's batch size (profiling; not a bench value)")
+    ap.add_argument("--tf-layers", type=int, default=None,
+                    help="override the transformer row's layer count (profiling; not a bench value)")
     ap.add_argument("--deterministic", action="store_true",
                     help="batch-invariant mode: one gradient chunk per adapter")
     ap.add_argument("--layers", type=int, default=None,
@@ -378,6 +386,10 @@ def run_ours(args, rank, world):
 
     # ---- derived numbers -----------------------------------------------------
     peaks, peak_src = load_peaks()
+    if extras is not None and not args.no_tf:
+        del h
+        torch.cuda.empty_cache()
+        extras["transformer_step"] = measure_transformer_row(args, dev, stream, peaks)
     if extras:
         for k in ("sampler_decode", "export_merge"):
             extras[k]["frac_of_hbm"] = extras[k]["achieved_gbs"] / peaks["hbm_gbs"]
@@ -456,6 +468,128 @@ def run_ours(args, rank, world):
     if extras:
         out["next_rows"] = extras
     return out, (cfg, base, ad, b)
+
+
+TF_TC_CLASSES = ("qkv", "o", "gateup", "down", "lm_fwd", "lm_dh", "down_bwd", "gateup_bwd", "o_bwd",
+                 "qkv_bwd")
+
+
+def tf_flop_model(cfg, b):
+    """Algorithmic FLOPs of one transformer-block step (no recompute, no
+    padding rows, no masked attention pairs): the seven projections forward
+    and their dgrad backward, the LoRA shrink / expand and gradient GEMMs,
+    causal attention (QK^T and PV forward; dV, dP, dQ, dK backward) over the
+    (query, key) pairs of each sequence, and the LM head (forward + dh)."""
+    d, f, L, V = cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.vocab
+    q, kv, hd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.head_dim
+    N = len(b["tokens"])
+    io = [(q, d), (kv, d), (kv, d), (d, q), (f, d), (f, d), (d, f)]
+    macs = sum(o * i for o, i in io)
+    sr = float(np.array(cfg.ranks)[b["adapter_ids"]].sum())
+    proj = 4.0 * N * macs * L                                  # forward + dgrad
+    lora = 6.0 * sr * sum(o + i for o, i in io) * L            # 2 r(in+out) forward, twice that backward
+    pairs = float((b["positions"].astype(np.int64) + 1).sum())  # causal (query, key) pairs
+    attn_fwd = 4.0 * pairs * hd * cfg.n_heads * L
+    attn_bwd = 2.0 * attn_fwd
+    lm = 4.0 * N * V * d
+    return {"proj_lm": proj + lm, "lora": lora, "attn_fwd": attn_fwd, "attn_bwd": attn_bwd,
+            "total": proj + lora + attn_fwd + attn_bwd + lm}
+
+
+def measure_transformer_row(args, dev, stream, peaks):
+    """One forward_backward + optim_step of the transformer-block model at the
+    Qwen3-8B widths (qwen3_8b_tf_ppo: 32 / 8 heads of 128, L = 4, 32 adapters,
+    65,536 tokens in sequences of 512-2048, PPO), device-timed with CUDA
+    events on the launch stream after warm-up; per-class times from the
+    library's per-launch events."""
+    import torch
+
+    import rl_step_gb300.transformer as t
+    import workloads.transformer as wt
+    over = {k: v for k, v in (("n_layers", args.tf_layers),) if v}
+    cfg = wt.get_tf_config("qwen3_8b_tf_ppo", **over)
+    b = wt.make_tf_batch(cfg, args.tf_tokens)
+    N = len(b["tokens"])
+    base = wt.make_tf_base_weights(cfg)
+    ad = wt.make_tf_adapters(cfg)
+
+    def T(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(x).to(dev)
+
+    dbase = {"E": T(base["E"]), "Wout": T(base["Wout"]), "final_norm": T(base["final_norm"]),
+             "attn_norm": [T(g) for g in base["attn_norm"]], "mlp_norm": [T(g) for g in base["mlp_norm"]],
+             "W": {p: [T(w) for w in base["W"][p]] for p in t.PROJ}}
+    A = {p: [[T(x) for x in row] for row in ad["A"][p]] for p in t.PROJ}
+    B = {p: [[T(x) for x in row] for row in ad["B"][p]] for p in t.PROJ}
+    del base, ad
+    h = t.tf_create(cfg.vocab, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.n_layers, cfg.ranks,
+                    cfg.alphas, N, dbase, A, B, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
+    torch.cuda.synchronize()
+    del dbase, A, B
+    torch.cuda.empty_cache()
+    tok, tgt, pos, ids = T(b["tokens"]), T(b["targets"]), T(b["positions"]), T(b["adapter_ids"])
+    s_dev = (t.tf_forward(h, tok, tgt, pos, ids) + T(b["sampler_noise"])).contiguous()
+    a_dev = T(b["advantages"])
+    lp_out = torch.empty(N, dtype=torch.float32, device=dev)
+    loss_out = torch.empty(cfg.n_adapters, dtype=torch.float64, device=dev)
+    skipped = torch.empty(cfg.n_adapters, dtype=torch.int32, device=dev)
+
+    def step():
+        t.tf_forward_backward(h, tok, tgt, pos, ids, "ppo", advantages=a_dev, sampler_logprobs=s_dev,
+                              clip_eps=cfg.clip_eps, logprobs_out=lp_out, loss_out=loss_out)
+        t.tf_optim_step(h, lr=cfg.lr, skipped_out=skipped)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if t.tf_check_status(h) != 0:
+        raise RuntimeError("transformer row: device status after warm-up")
+    K = max(1, min(args.steps, 5))
+    t.tf_profile_read(h, reset=True)
+    t.tf_profile_enable(h, True)
+    launches0 = h.kernel_launches
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t.tf_profile_enable(h, False)
+    prof = t.tf_profile_read(h, reset=True)
+    launches = (h.kernel_launches - launches0) / K
+    if t.tf_check_status(h) != 0:
+        raise RuntimeError("transformer row: device status in the timed region")
+    ms = e0.elapsed_time(e1) / K
+    fl = tf_flop_model(cfg, b)
+    peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    kern = {c: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for c, v in prof.items() if v[1] > 0}
+
+    def rate(flops, classes):
+        tms = sum(prof[c][0] for c in classes) / K
+        return (flops / (tms * 1e-3) / 1e12) if tms > 0 else None
+    att_f, att_b = rate(fl["attn_fwd"], ("attn_fwd",)), rate(fl["attn_bwd"], ("attn_bwd",))
+    gemm = rate(fl["proj_lm"], TF_TC_CLASSES)
+    row = {
+        "workload": cfg.description + (f" (override {over})" if over else ""),
+        "tokens": N, "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
+        "tflops_algorithmic": fl["total"] / (ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": fl["total"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "flops_per_step": fl,
+        "attention": {"fwd_tflops": att_f, "bwd_tflops": att_b, "peak": peak_tc,
+                      "fwd_frac": att_f / peak_tc if att_f else None,
+                      "bwd_frac": att_b / peak_tc if att_b else None,
+                      "bound": "tensor", "unit": "TFLOP/s (algorithmic, causal pairs only; backward "
+                                                "includes its rowsum pass, the S recompute is not credited)"},
+        "projection_and_lm_gemms": {"tflops": gemm, "frac": gemm / peak_tc if gemm else None},
+        "kernels": kern, "gpu_launches_per_step": launches,
+        "device_bytes": h.device_bytes,
+    }
+    del h
+    torch.cuda.empty_cache()
+    return row
 
 
 def count_nonzero_g(cfg, b, lp, s):
@@ -616,6 +750,17 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.tf_only:
+        import torch
+
+        from rl_step_gb300 import _build
+        _build.build()
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        row = measure_transformer_row(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))),
+                                      torch.cuda.current_stream(), load_peaks()[0])
+        if rank == 0:
+            print(json.dumps({"transformer_step": row}), flush=True)
         return
     if world > 1:
         import torch
