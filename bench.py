@@ -386,10 +386,12 @@ def run_ours(args, rank, world):
 
     # ---- derived numbers -----------------------------------------------------
     peaks, peak_src = load_peaks()
-    if extras is not None and not args.no_tf:
+    if extras is not None:
         del h
         torch.cuda.empty_cache()
-        extras["transformer_step"] = measure_transformer_row(args, dev, stream, peaks)
+        extras["loss_epilogue_scaled"] = measure_loss_epilogue_scaled(dev, stream, peaks)
+        if not args.no_tf:
+            extras["transformer_step"] = measure_transformer_row(args, dev, stream, peaks)
     if extras:
         for k in ("sampler_decode", "export_merge"):
             extras[k]["frac_of_hbm"] = extras[k]["achieved_gbs"] / peaks["hbm_gbs"]
@@ -590,6 +592,62 @@ def measure_transformer_row(args, dev, stream, peaks):
     del h
     torch.cuda.empty_cache()
     return row
+
+
+def measure_loss_epilogue_scaled(dev, stream, peaks, n_tokens=1 << 24, reps=3):
+    """The LM-head partial combine + loss epilogue as one launch over many rows.
+
+    Inside the step the kernel runs per chunk of at most 16,384 rows (~39 MB
+    each), too little work per launch to reach HBM bandwidth.  Here the same
+    kernel runs once over n_tokens rows through mlora_forward (whose LM head
+    keeps no logits and combines all rows at once) on a handle of the same
+    vocabulary (V = 151,936, so 594 vocabulary-tile partials per row) whose
+    model is shrunk to d = f = 64, L = 1, so that the rows are cheap to
+    produce.  Bytes per padded row: 4 B per partial + 20 B of per-row scalars;
+    per token the 4-byte logprob written.  Timed by the library's per-launch
+    events (class "loss")."""
+    import torch
+
+    import rl_step_gb300 as m
+    cfg = wl.get_config("qwen3_8b_ppo", d_model=64, d_ffn=64, n_layers=1, n_adapters=1, ranks=(32,),
+                        alphas=(32.0,))
+    base = wl.make_base_weights(cfg)
+    ad = wl.make_adapters(cfg)
+
+    def T(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(x).to(dev)
+
+    h = m.mlora_create(cfg.vocab, cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.dtype, cfg.ranks, cfg.alphas,
+                       n_tokens, T(base["E"]), [T(w) for w in base["W1"]], [T(w) for w in base["W2"]],
+                       T(base["Wout"]), *[[[T(x) for x in row] for row in ad[k]] for k in ("A1", "B1", "A2", "B2")])
+    rng = np.random.Generator(np.random.PCG64([cfg.seed, 41]))
+    tok = T(rng.integers(0, cfg.vocab, n_tokens).astype(np.int32))
+    tgt = T(rng.integers(0, cfg.vocab, n_tokens).astype(np.int32))
+    ids = torch.zeros(n_tokens, dtype=torch.int32, device=dev)
+    lp = torch.empty(n_tokens, dtype=torch.float32, device=dev)
+    m.mlora_forward(h, tok, tgt, ids, logprobs_out=lp)
+    torch.cuda.synchronize()
+    m.mlora_profile_read(h, reset=True)
+    m.mlora_profile_enable(h, True)
+    for _ in range(reps):
+        m.mlora_forward(h, tok, tgt, ids, logprobs_out=lp)
+    torch.cuda.synchronize()
+    m.mlora_profile_enable(h, False)
+    prof = m.mlora_profile_read(h, reset=True)
+    if m.mlora_check_status(h) != 0 or not bool(torch.isfinite(lp).all()):
+        raise RuntimeError("scaled loss-epilogue run: bad status or logprobs")
+    ms, n = prof["loss"]
+    rows = (n_tokens + 127) // 128 * 128
+    byt = rows * (4.0 * ((cfg.vocab + 255) // 256) + 20.0) + 4.0 * n_tokens
+    del h
+    torch.cuda.empty_cache()
+    gbs = byt / (ms / n * 1e-3) / 1e9
+    return {"kernel": "combine_loss_kernel", "tokens": n_tokens, "launches": n / reps, "ms": ms / n,
+            "bytes": byt, "achieved_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "what": "one launch over all rows of a forward (V = 151,936; model shrunk to d = f = 64, L = 1)"}
 
 
 def count_nonzero_g(cfg, b, lp, s):

@@ -122,111 +122,102 @@ __device__ __forceinline__ void token_loss_dev(int kind, float ell, int t, const
     if (!ok) { val = 0.0; g = 0.f; }
 }
 
-// (m, s) <- (m, s) merged with one more log-sum-exp term x: afterwards
-// m + log(s) is the log-sum-exp of all terms folded so far.
-__device__ __forceinline__ void lse_fold(float& m, float& s, float x) {
-    if (x == -INFINITY) return;
-    if (x > m) {
-        s = s * __expf(m - x) + 1.f;
-        m = x;
-    } else {
-        s += __expf(x - m);
-    }
-}
-
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-    const float M = fmaxf(m, m2);
-    if (M == -INFINITY) return;
-    s = s * __expf(m - M) + s2 * __expf(m2 - M);
-    m = M;
-}
-
-// Persistent combine: each warp walks padded rows (row = global warp id,
-// then + total warps).  The 16-byte loads of the next row's partials (one
-// log-sum-exp per 256-column vocabulary tile) and its metadata are issued
-// before the current row is folded, so HBM sees a steady stream; the warp
-// merges its lanes and lane 0 finishes the row (logprob, loss value, dL/dl).
+// Combine: each warp takes groups of G consecutive padded rows (G <= 32,
+// chosen at launch so that the groups cover the GPU's warps).  For every row
+// of the group the warp reads the row's partials (one log-sum-exp per
+// 256-column vocabulary tile) with lane-strided 16-byte loads -- the next
+// row's loads are issued before the current row is reduced -- and reduces
+// them in a fixed order: the maximum over each lane's values and a butterfly
+// maximum, then the sum of exp(x - m) over each lane's values and a butterfly
+// sum.  Lane i keeps row i's (m, s); then every lane finishes its own row
+// (target logprob, loss value, dL/dl) and the per-row stores are coalesced.
 // part_ld (a multiple of 4) is the pitch of a row of partials, n_nt the
 // number in use.  Per-row loss values go to val_row for a deterministic
-// per-adapter reduction in row order.
+// per-adapter reduction in row order.  The result of a row depends on that
+// row alone (batch-invariant) and repeats bit for bit.
 constexpr int COMBINE_VEC = 5;      // float4 per lane per row prefetched: 640 partials
+constexpr int COMBINE_CTAS_PER_SM = 3;   // resident at 256 threads and <= 85 registers
 
 struct CombineRow {
     float4 v[COMBINE_VEC];
-    int t, y;
-    float z;
+    float tail;                     // partial 4 * 32 * COMBINE_VEC + lane, if any
 };
 
 __device__ __forceinline__ void combine_load(CombineRow& r, const float* __restrict__ part, int64_t p,
-                                             int n_nt, int part_ld, int lane, const float* __restrict__ zt,
-                                             const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad) {
-    const float4* row = reinterpret_cast<const float4*>(part + p * part_ld);
+                                             int n_nt, int part_ld, int lane) {
+    const float* rowp = part + p * part_ld;
+    const float4* row4 = reinterpret_cast<const float4*>(rowp);
     const int nvec = n_nt >> 2;
 #pragma unroll
     for (int u = 0; u < COMBINE_VEC; ++u) {
         const int j = lane + 32 * u;
-        r.v[u] = j < nvec ? row[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        r.v[u] = j < nvec ? row4[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
-    r.t = -1; r.y = -1; r.z = 0.f;
-    if (lane == 0) {
-        r.t = perm_pad[p];
-        r.y = tgt_pad[p];
-        r.z = zt[p];
-    }
+    const int done = 4 * min(nvec, 32 * COMBINE_VEC);
+    r.tail = done + lane < n_nt ? rowp[done + lane] : -INFINITY;
 }
 
-__global__ void __launch_bounds__(256) combine_loss_kernel(
+__global__ void __launch_bounds__(256, COMBINE_CTAS_PER_SM) combine_loss_kernel(
     LossArgs la, const float* __restrict__ part, int n_nt, int part_ld, const float* __restrict__ zt,
     const int* __restrict__ perm_pad, const int* __restrict__ tgt_pad, const int* __restrict__ meta,
-    int row0, int row1, float* logprobs_out, float* lse_out, float* g_out, double* val_row) {
+    int row0, int row1, int G, float* logprobs_out, float* lse_out, float* g_out, double* val_row) {
     const int rows = min(meta[0] * TILE_M, row1);
     const int lane = threadIdx.x & 31;
     const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    CombineRow cur, nxt;
-    int p = row0 + wid;
-    if (p < rows) combine_load(cur, part, p, n_nt, part_ld, lane, zt, perm_pad, tgt_pad);
-    for (; p < rows; p += nwarps) {
-        const int pn = p + nwarps;
-        if (pn < rows) combine_load(nxt, part, pn, n_nt, part_ld, lane, zt, perm_pad, tgt_pad);
-        float m = -INFINITY, sm = 0.f;
+    // partials past the prefetched float4 groups and the one tail value per lane
+    const int beyond = 4 * min(n_nt >> 2, 32 * COMBINE_VEC) + 32;
+    for (int g0 = row0 + G * wid; g0 < rows; g0 += G * nwarps) {
+        const int gn = min(G, rows - g0);
+        float my_m = -INFINITY, my_s = 0.f;
+        CombineRow cur, nxt;
+        combine_load(cur, part, g0, n_nt, part_ld, lane);
+        for (int i = 0; i < gn; ++i) {
+            const int64_t p = g0 + i;
+            if (i + 1 < gn) combine_load(nxt, part, p + 1, n_nt, part_ld, lane);
+            float m = cur.tail;
 #pragma unroll
-        for (int u = 0; u < COMBINE_VEC; ++u) {
-            lse_fold(m, sm, cur.v[u].x);
-            lse_fold(m, sm, cur.v[u].y);
-            lse_fold(m, sm, cur.v[u].z);
-            lse_fold(m, sm, cur.v[u].w);
-        }
-        // partials beyond the prefetched float4 groups (the n_nt % 4 tail, and
-        // vocabularies wider than 32 * COMBINE_VEC float4 groups)
-        const int done = 4 * min(n_nt >> 2, 32 * COMBINE_VEC);
-        for (int j = done + lane; j < n_nt; j += 32) lse_fold(m, sm, part[(int64_t)p * part_ld + j]);
+            for (int u = 0; u < COMBINE_VEC; ++u)
+                m = fmaxf(fmaxf(m, fmaxf(cur.v[u].x, cur.v[u].y)), fmaxf(cur.v[u].z, cur.v[u].w));
+            for (int j = beyond + lane; j < n_nt; j += 32) m = fmaxf(m, part[p * part_ld + j]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float mm = __shfl_xor_sync(0xffffffffu, m, o);
-            const float ss = __shfl_xor_sync(0xffffffffu, sm, o);
-            lse_merge(m, sm, mm, ss);
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float sm = 0.f;
+            if (m > -INFINITY) {
+                sm = __expf(cur.tail - m);
+#pragma unroll
+                for (int u = 0; u < COMBINE_VEC; ++u)
+                    sm += (__expf(cur.v[u].x - m) + __expf(cur.v[u].y - m)) +
+                          (__expf(cur.v[u].z - m) + __expf(cur.v[u].w - m));
+                for (int j = beyond + lane; j < n_nt; j += 32) sm += __expf(part[p * part_ld + j] - m);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+            if (lane == i) { my_m = m; my_s = sm; }
+            cur = nxt;
         }
-        if (lane == 0) {
+        if (lane < gn) {
+            const int p = g0 + lane;
+            const int t = perm_pad[p];
+            const int y = tgt_pad[p];
             double val = 0.0;
             float g = 0.f, lse = 0.f;
-            if (cur.t >= 0) {
+            if (t >= 0) {
                 float ell;
-                if (cur.y >= 0) {
-                    lse = m + __logf(sm);
-                    ell = cur.z - lse;
+                if (y >= 0) {
+                    lse = my_m + __logf(my_s);
+                    ell = zt[p] - lse;
                 } else {
                     ell = __int_as_float(0x7fc00000);   // NaN: invalid token or target
                 }
-                token_loss_dev(la.kind, ell, cur.t, la, val, g);
-                if (cur.y < 0) g = 0.f, val = 0.0;
-                if (logprobs_out) logprobs_out[cur.t] = ell;
+                token_loss_dev(la.kind, ell, t, la, val, g);
+                if (y < 0) g = 0.f, val = 0.0;
+                if (logprobs_out) logprobs_out[t] = ell;
             }
             lse_out[p] = lse;
             g_out[p] = g;
             val_row[p] = val;
         }
-        cur = nxt;
     }
 }
 
@@ -235,11 +226,16 @@ void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int pa
                          float* logprobs_out, float* lse, float* g, double* val_row, int num_sms,
                          cudaStream_t s) {
     if (ntiles <= 0) return;
-    int blocks = num_sms * 4;
-    const int need = (ntiles * TILE_M + 7) / 8;        // one row per warp at most
+    const int rows = ntiles * TILE_M;
+    const int warps = num_sms * COMBINE_CTAS_PER_SM * 8;
+    int G = rows / warps;                 // rows per group: 1 .. 32
+    if (G < 1) G = 1;
+    if (G > 32) G = 32;
+    int blocks = num_sms * COMBINE_CTAS_PER_SM;
+    const int need = ((rows + G - 1) / G + 7) / 8;   // one group per warp at most
     if (blocks > need) blocks = need;
     combine_loss_kernel<<<blocks, 256, 0, s>>>(la, part, n_nt, part_ld, zt, perm_pad, tgt_pad, meta,
-                                               tile0 * TILE_M, (tile0 + ntiles) * TILE_M,
+                                               tile0 * TILE_M, (tile0 + ntiles) * TILE_M, G,
                                                logprobs_out, lse, g, val_row);
 }
 
