@@ -22,6 +22,8 @@
 // stops, outstanding copies and MMAs are drained (bounded) and TMEM is freed.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -133,32 +135,48 @@ __device__ __forceinline__ void unpack32(const uint32_t (&r)[32], float (&v)[32]
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// Forward.  CTA = (128-row query tile, query head); key tiles of 128 rows run
-// from the first row of the tile's first sequence up to the tile's last row.
-// Per key tile j:  S = Q K_j^T (TMEM, double-buffered); the softmax warps
-// take the running row max, write P = exp(S - m) as bf16 to shared memory and
-// fold the previous tile's O_{j-1} = P_{j-1} V_{j-1} (TMEM, double-buffered)
-// into a register accumulator rescaled by exp(m_old - m_new).
+// Forward.  CTA = (128-row query tile, two query heads of one key/value
+// group); key tiles of 128 rows run from the first row of the tile's first
+// sequence up to the tile's last row and are loaded once for both heads.
+// Warps: 0 loads K, 1 loads Q and V, 2 issues the MMAs, 4-7 and 8-11 are the
+// softmax warpgroups of the two heads (one query row per thread).  Per key
+// tile j and head h:  S_h = Q_h K_j^T (TMEM); the warpgroup takes the row max,
+// writes P_h = exp(S_h - m) in bf16 to shared memory; O_h += P_h V_j in TMEM.
+// The MMA warp issues head h's P V and then its next S as soon as that head's
+// P is ready, so the two warpgroups' softmax work alternates around the
+// tensor core.  The running max m of a row is raised (and O_h, l rescaled in
+// place) only when the tile's max exceeds it by more than 2^8 in exp2 units;
+// otherwise P is formed against the stale m (entries up to 2^8), which the
+// final O / l and log-sum-exp m + log2(l) account for exactly.
 // ----------------------------------------------------------------------------
 namespace {
 
+constexpr int FWD_THREADS = 384;
+constexpr float RESCALE_LOG2 = 8.f;
+
 struct FwdSmem {
-    static constexpr int Q = 0;
-    static constexpr int K0 = 2 * BLK;          // two stages of 32 KB
-    static constexpr int V0 = K0 + 4 * BLK;     // two stages of 32 KB
-    static constexpr int P = V0 + 4 * BLK;      // 32 KB
-    static constexpr int BAR = P + 2 * BLK;
-    enum { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_FREE = 9, P_FULL = 11,
-           O_FULL = 12, O_FREE = 14, DRAIN = 16, NBARS = 17 };
+    static constexpr int Q0 = 0;                // Q of head 0, then head 1 (32 KB each)
+    static constexpr int K = 4 * BLK;
+    static constexpr int V = 6 * BLK;
+    static constexpr int P0 = 8 * BLK;          // P of head 0, then head 1 (32 KB each)
+    static constexpr int BAR = 12 * BLK;
+    enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 2, V_FULL = 3, V_EMPTY = 4, S_FULL = 5, S_FREE = 7,
+           P_FULL = 9, O_DONE = 11, DRAIN = 13, NBARS = 14 };
     static constexpr int MISC = BAR + NBARS * 8;
     static constexpr int TOTAL = MISC + 16 + 1024;
 };
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
     using SL = FwdSmem;
     const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
-    const int tile = blockIdx.x / p.n_heads, h = blockIdx.x % p.n_heads;
+    const int grp = p.n_heads / p.n_kv;
+    const int pairs = (grp + 1) / 2;                    // head pairs per key/value group
+    const int tile = blockIdx.x / (p.n_kv * pairs);
+    const int rest = blockIdx.x % (p.n_kv * pairs);
+    const int g = rest / pairs;
+    const int h0 = g * grp + 2 * (rest % pairs);
+    const int h1 = h0 + 1 < (g + 1) * grp ? h0 + 1 : h0;  // an odd group's last pair repeats its head
     if (tile >= mt_valid) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,178 +189,194 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int m0 = tile * TB;
     const int kstart = p.seq_start[m0];
     const int nt = (m0 + TB - kstart + TB - 1) / TB;
-    const int grp = p.n_heads / p.n_kv, g = h / grp;
-    const int qcol = h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+    const int kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 1, 4, 4, 1};
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 1};
         for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
         tma_prefetch_desc(&maps.rows128);
     }
-    if (warp == 1) {
+    if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;   // S[s] at columns 128 s, O[s] at 256 + 128 s
+    const uint32_t tmem = *tmem_slot;   // S_h at columns 128 h, O_h at 256 + 128 h
+    int dummy = 0;
 
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
-            int issued[2] = {-1, -1};
-            mbar_expect_tx(bar(SL::Q_FULL), 2 * BLK);
-            load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, m0);
             for (int j = 0; j < nt; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(bar(SL::KV_EMPTY + s), ph ^ 1u, abort_flag)) { ok = false; break; }
-                const int key0 = kstart + j * TB;
-                mbar_expect_tx(bar(SL::K_FULL + s), 2 * BLK);
-                load_tile128(sb + SL::K0 + s * 2 * BLK, &maps.rows128, bar(SL::K_FULL + s), kcol, key0);
-                mbar_expect_tx(bar(SL::V_FULL + s), 2 * BLK);
-                load_tile128(sb + SL::V0 + s * 2 * BLK, &maps.rows128, bar(SL::V_FULL + s), vcol, key0);
-                issued[s] = (int)ph;
+                if (j > 0 && !mbar_wait(bar(SL::K_EMPTY), (uint32_t)((j - 1) & 1), abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::K_FULL), 2 * BLK);
+                load_tile128(sb + SL::K, &maps.rows128, bar(SL::K_FULL), kcol, kstart + j * TB);
+                if (j == nt - 1 && !mbar_wait(bar(SL::K_FULL), (uint32_t)(j & 1), (volatile int*)&dummy))
+                    ok = false;       // our last copy has landed
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
-            int dummy = 0;
-            bool dr = mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy);
-            for (int s = 0; s < 2; ++s)
-                if (issued[s] >= 0) {
-                    dr &= mbar_wait(bar(SL::K_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
-                    dr &= mbar_wait(bar(SL::V_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
-                }
-            if (!dr) atomicOr(status, ST_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag);
-            auto pv = [&](int i) -> bool {
-                const int s = i & 1;
-                const uint32_t ph = (i >> 1) & 1;
-                if (!mbar_wait(bar(SL::V_FULL + s), ph, abort_flag)) return false;
-                if (!mbar_wait(bar(SL::P_FULL), (uint32_t)(i & 1), abort_flag)) return false;
-                if (!mbar_wait(bar(SL::O_FREE + s), ph ^ 1u, abort_flag)) return false;
-                tc_fence_after();
-                mma_kmn(tmem + 256 + 128 * s, sb + SL::P, sb + SL::V0 + s * 2 * BLK, false);
-                umma_commit(bar(SL::KV_EMPTY + s));
-                umma_commit(bar(SL::O_FULL + s));
-                return true;
-            };
-            for (int j = 0; j < nt && ok; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(bar(SL::K_FULL + s), ph, abort_flag) ||
-                    !mbar_wait(bar(SL::S_FREE + s), ph ^ 1u, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                mma_kk(tmem + 128 * s, sb + SL::Q, sb + SL::K0 + s * 2 * BLK, false);
-                umma_commit(bar(SL::S_FULL + s));
-                if (j >= 1 && !pv(j - 1)) ok = false;
+            bool ok = true;
+            mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
+            load_tile128(sb + SL::Q0, &maps.rows128, bar(SL::Q_FULL), h0 * HD, m0);
+            load_tile128(sb + SL::Q0 + 2 * BLK, &maps.rows128, bar(SL::Q_FULL), h1 * HD, m0);
+            for (int j = 0; j < nt; ++j) {
+                if (j > 0 && !mbar_wait(bar(SL::V_EMPTY), (uint32_t)((j - 1) & 1), abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::V_FULL), 2 * BLK);
+                load_tile128(sb + SL::V, &maps.rows128, bar(SL::V_FULL), vcol, kstart + j * TB);
+                if (j == nt - 1 && !mbar_wait(bar(SL::V_FULL), (uint32_t)(j & 1), (volatile int*)&dummy))
+                    ok = false;
             }
-            if (ok && !pv(nt - 1)) ok = false;
+            if (!mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy)) ok = false;
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag) && mbar_wait(bar(SL::K_FULL), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                for (int hh = 0; hh < 2; ++hh) {
+                    mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K, false);
+                    umma_commit(bar(SL::S_FULL + hh));
+                }
+                umma_commit(bar(SL::K_EMPTY));
+            }
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t ph = (uint32_t)(j & 1);
+                if (!mbar_wait(bar(SL::V_FULL), ph, abort_flag)) { ok = false; break; }
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (!mbar_wait(bar(SL::P_FULL + hh), ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V, j > 0);
+                    umma_commit(bar(SL::O_DONE + hh));
+                    if (j + 1 < nt) {
+                        if ((hh == 0 && !mbar_wait(bar(SL::K_FULL), ph ^ 1u, abort_flag)) ||
+                            !mbar_wait(bar(SL::S_FREE + hh), ph, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K, false);
+                        umma_commit(bar(SL::S_FULL + hh));
+                        if (hh == 1) umma_commit(bar(SL::K_EMPTY));
+                    }
+                }
+                if (ok) umma_commit(bar(SL::V_EMPTY));
+            }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
-            int dummy = 0;
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
-    } else {
+    } else if (warp >= 4) {
+        const int hh = (warp - 4) >> 2;                 // head slot of this warpgroup
+        const int h = hh ? h1 : h0;
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
         const int i = m0 + r;
         const int ss = p.seq_start[i];
-        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const uint32_t tS = tmem + ((uint32_t)(32 * q4) << 16) + 128 * hh;
+        const uint32_t tO = tS + 256;
+        const uint32_t sP = sb + SL::P0 + hh * 2 * BLK;
         const float sc = p.scale * LOG2E;
-        float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
-        float O[HD];
-#pragma unroll
-        for (int e = 0; e < HD; ++e) O[e] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         uint32_t rr[32];
-        float v[32];
-        // O <- O * alpha + (the finished P V tile in O[s])
-        auto fold = [&](int i_tile, float alpha) -> bool {
-            const int s = i_tile & 1;
-            if (!warp_wait(bar(SL::O_FULL + s), (uint32_t)((i_tile >> 1) & 1), abort_flag, lane)) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(tl + 256 + 128 * s + 32 * c, rr);
-                tmem_ld_wait();
-                unpack32(rr, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) O[32 * c + e] = fmaf(O[32 * c + e], alpha, v[e]);
-            }
-            return true;
-        };
         for (int j = 0; j < nt; ++j) {
-            const int s = j & 1;
-            if (!warp_wait(bar(SL::S_FULL + s), (uint32_t)((j >> 1) & 1), abort_flag, lane)) { ok = false; break; }
+            const uint32_t ph = (uint32_t)(j & 1);
+            if (!warp_wait(bar(SL::S_FULL + hh), ph, abort_flag, lane)) { ok = false; break; }
             tc_fence_after();
             const int key0 = kstart + j * TB;
+            // valid key columns of this row: [lo, hi]; a warp whose rows all see
+            // the whole tile takes the unmasked copy of the loops
+            const int lo = ss - key0, hi = i - key0;
+            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
             float mx = -INFINITY;
+            auto row_max = [&](auto masked) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(tl + 128 * s + 32 * c, rr);
-                tmem_ld_wait();
-                unpack32(rr, v);
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + 32 * c, rr);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int key = key0 + 32 * c + e;
-                    if (key >= ss && key <= i) mx = fmaxf(mx, v[e] * sc);
+                    for (int e = 0; e < 32; ++e) {
+                        const int idx = 32 * c + e;
+                        const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                        mx = fmaxf(mx, v ? __uint_as_float(rr[e]) * sc : -INFINITY);
+                    }
                 }
+            };
+            if (whole) row_max(std::false_type{});
+            else row_max(std::true_type{});
+            if (j > 0) {   // head h's previous P V is done: O_h is stable and P_h free
+                if (!warp_wait(bar(SL::O_DONE + hh), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
+                tc_fence_after();
             }
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-            if (j >= 1) {   // fold O_{j-1}; its MMA has then also finished reading P
-                if (!fold(j - 1, alpha_prev)) { ok = false; break; }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(SL::O_FREE + ((j - 1) & 1)));
+            const bool raise = mx > m_run + RESCALE_LOG2;
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                const float alpha = raise ? exp2f(m_run - mx) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tO + 32 * c, rr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                    tmem_st32(tO + 32 * c, rr);
+                }
+                tmem_st_wait();
+                l_run *= alpha;
             }
+            if (raise) m_run = mx;
             float rs = 0.f;
+            auto write_p = [&](auto masked) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(tl + 128 * s + 32 * c, rr);
-                tmem_ld_wait();
-                unpack32(rr, v);
-                uint32_t w[16];
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + 32 * c, rr);
+                    tmem_ld_wait();
+                    uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int key = key0 + 32 * c + e;
-                    const float p0 = (key >= ss && key <= i) ? exp2f(fmaf(v[e], sc, -m_new)) : 0.f;
-                    const float p1 = (key + 1 >= ss && key + 1 <= i) ? exp2f(fmaf(v[e + 1], sc, -m_new)) : 0.f;
-                    rs += p0 + p1;
-                    w[e >> 1] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; e += 2) {
+                        const int idx = 32 * c + e;
+                        const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                        const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
+                        // masked entries give exp2(-inf) = 0: no branch around the exponential
+                        const float p0 = exp2f(v0 ? fmaf(__uint_as_float(rr[e]), sc, -m_run) : -INFINITY);
+                        const float p1 = exp2f(v1 ? fmaf(__uint_as_float(rr[e + 1]), sc, -m_run) : -INFINITY);
+                        rs += p0 + p1;
+                        w[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    st_swizzled32(sP + (c >> 1) * BLK, r, (c & 1) * 4, w);
                 }
-                st_swizzled32(sb + SL::P + (c >> 1) * BLK, r, (c & 1) * 4, w);
-            }
+            };
+            if (whole) write_p(std::false_type{});
+            else write_p(std::true_type{});
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(bar(SL::S_FREE + s));
-                mbar_arrive(bar(SL::P_FULL));
+                mbar_arrive(bar(SL::S_FREE + hh));
+                mbar_arrive(bar(SL::P_FULL + hh));
             }
-            l_run = l_run * alpha + rs;
-            alpha_prev = alpha;
-            m_run = m_new;
+            l_run += rs;
         }
-        if (ok) ok = fold(nt - 1, alpha_prev);
+        if (ok) ok = warp_wait(bar(SL::O_DONE + hh), (uint32_t)((nt - 1) & 1), abort_flag, lane);
         if (ok) {
+            tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             bf16* dst = p.o + (int64_t)i * p.n_heads * HD + h * HD;
+            const bool store = hh == 0 || h1 != h0;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tO + 32 * c, rr);
+                tmem_ld_wait();
                 float t[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) t[e] = O[32 * c + e] * inv;
-                store32<bf16>(dst + 32 * c, t);
+                for (int e = 0; e < 32; ++e) t[e] = __uint_as_float(rr[e]) * inv;
+                if (store) store32<bf16>(dst + 32 * c, t);
             }
-            p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            if (store) p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
         } else if (lane == 0) {
             atomicOr(status, ST_TIMEOUT);
             *abort_flag = 1;
@@ -351,7 +385,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -361,26 +395,37 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // query head of the group and every query tile that can see these keys:
 //   S^T = K Q^T, dP^T = V dO^T                     (TMEM)
 //   P^T = exp(scale S^T - lse_q), dS^T = P^T (dP^T - D_q)   (softmax warps,
-//                                   one key row per thread, bf16 to smem)
-//   dV += P^T dO,  dK += dS^T Q                     (TMEM accumulators)
-// and finally dK *= scale.  Each dK / dV element has a single writer.
+//        one key row per thread; bf16, written back into TMEM over the
+//        S^T / dP^T columns just read)
+//   dV += P^T dO,  dK += dS^T Q                     (A operand read from TMEM)
+// and finally dK *= scale.  Each dK / dV element has a single writer.  The
+// query-side tiles (Q, dO, their log-sum-exp, rowsum and sequence starts) are
+// double-buffered, so the next tile loads while this one is processed.
 // ----------------------------------------------------------------------------
 namespace {
 
 struct KvSmem {
     static constexpr int K = 0;
     static constexpr int V = 2 * BLK;
-    static constexpr int Q = 4 * BLK;
-    static constexpr int DO = 6 * BLK;
-    static constexpr int PT = 8 * BLK;
-    static constexpr int DST = 10 * BLK;
-    static constexpr int VEC = 12 * BLK;        // lse[128], D[128] (fp32), seq_start[128] of the query tile
-    static constexpr int BAR = VEC + 3 * 512;
-    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 2, ST_FULL = 3, ST_FREE = 4, P_FULL = 5, P_EMPTY = 6,
-           ACC_FULL = 7, DRAIN = 8, NBARS = 9 };
+    static constexpr int Q0 = 4 * BLK;           // stage s: Q at Q0 + 4 BLK s, dO 2 BLK after
+    static constexpr int VEC0 = 12 * BLK;        // stage s: lse[128], D[128], seq_start[128] at VEC0 + 1536 s
+    static constexpr int BAR = VEC0 + 2 * 3 * 512;
+    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 6, PT_DONE = 7, ACC_FULL = 8,
+           DRAIN = 9, NBARS = 10 };
     static constexpr int MISC = BAR + NBARS * 8;
     static constexpr int TOTAL = MISC + 16 + 1024;
 };
+
+// D (+)= A B^T for 128 x 128 x 128 with A (bf16 pairs) in TMEM columns
+// a_tmem .. a_tmem + 63 and B the MN-major view of a row-major smem tile.
+__device__ __forceinline__ void mma_tmn(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ts(d, a_tmem + 8 * (4 * kb + kk), mndesc(b, kb, kk), id, (acc || kb || kk) ? 1u : 0u);
+}
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_bwd_kv_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
@@ -406,7 +451,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int niter = grp * nqt;
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 4, 4, 1, 1, 1};
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 4, 1, 1, 1};
         for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -421,55 +466,60 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;   // S^T 0, dP^T 128, dV 256, dK 384
+    const uint32_t tmem = *tmem_slot;   // S^T / P^T 0, dP^T / dS^T 128, dV 256, dK 384
+    int dummy = 0;
 
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
-            int last = -1;
+            int last[2] = {-1, -1};
             mbar_expect_tx(bar(SL::KV_FULL), 4 * BLK);
             load_tile128(sb + SL::K, &maps.rows128, bar(SL::KV_FULL), kcol, k0);
             load_tile128(sb + SL::V, &maps.rows128, bar(SL::KV_FULL), vcol, k0);
             for (int n = 0; n < niter; ++n) {
+                const int s = n & 1;
+                const uint32_t sp = (uint32_t)((n >> 1) & 1);
                 const int h = g * grp + n / nqt, q0 = (kt + n % nqt) * TB;
-                if (!mbar_wait(bar(SL::QD_EMPTY), (uint32_t)(n & 1) ^ 1u, abort_flag)) { ok = false; break; }
-                const uint32_t fb = bar(SL::QD_FULL);
+                if (!mbar_wait(bar(SL::QD_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
+                const uint32_t fb = bar(SL::QD_FULL + s);
+                const uint32_t st = sb + SL::Q0 + s * 4 * BLK, vec = sb + SL::VEC0 + s * 1536;
                 mbar_expect_tx(fb, 4 * BLK + 3 * 512);
-                load_tile128(sb + SL::Q, &maps.rows128, fb, h * HD, q0);
-                load_tile128(sb + SL::DO, &maps.do128, fb, h * HD, q0);
-                bulk_load(sb + SL::VEC, p.lseT + (int64_t)h * p.ld_t + q0, 512, fb);
-                bulk_load(sb + SL::VEC + 512, p.DT + (int64_t)h * p.ld_t + q0, 512, fb);
-                bulk_load(sb + SL::VEC + 1024, p.seq_start + q0, 512, fb);
-                last = n;
+                load_tile128(st, &maps.rows128, fb, h * HD, q0);
+                load_tile128(st + 2 * BLK, &maps.do128, fb, h * HD, q0);
+                bulk_load(vec, p.lseT + (int64_t)h * p.ld_t + q0, 512, fb);
+                bulk_load(vec + 512, p.DT + (int64_t)h * p.ld_t + q0, 512, fb);
+                bulk_load(vec + 1024, p.seq_start + q0, 512, fb);
+                last[s] = (int)sp;
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
-            int dummy = 0;
             bool dr = mbar_wait(bar(SL::KV_FULL), 0, (volatile int*)&dummy);
-            if (last >= 0) dr &= mbar_wait(bar(SL::QD_FULL), (uint32_t)(last & 1), (volatile int*)&dummy);
+            for (int s = 0; s < 2; ++s)
+                if (last[s] >= 0) dr &= mbar_wait(bar(SL::QD_FULL + s), (uint32_t)last[s], (volatile int*)&dummy);
             if (!dr) atomicOr(status, ST_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = mbar_wait(bar(SL::KV_FULL), 0, abort_flag);
             for (int n = 0; n < niter && ok; ++n) {
-                const uint32_t ph = (uint32_t)(n & 1);
-                if (!mbar_wait(bar(SL::QD_FULL), ph, abort_flag) ||
-                    !mbar_wait(bar(SL::ST_FREE), ph ^ 1u, abort_flag)) { ok = false; break; }
+                const int s = n & 1;
+                const uint32_t sp = (uint32_t)((n >> 1) & 1), pn = (uint32_t)(n & 1);
+                const uint32_t st = sb + SL::Q0 + s * 4 * BLK;
+                if (!mbar_wait(bar(SL::QD_FULL + s), sp, abort_flag) ||
+                    (n > 0 && !mbar_wait(bar(SL::PT_DONE), pn ^ 1u, abort_flag))) { ok = false; break; }
                 tc_fence_after();
-                mma_kk(tmem, sb + SL::K, sb + SL::Q, false);
-                mma_kk(tmem + 128, sb + SL::V, sb + SL::DO, false);
+                mma_kk(tmem, sb + SL::K, st, false);
+                mma_kk(tmem + 128, sb + SL::V, st + 2 * BLK, false);
                 umma_commit(bar(SL::ST_FULL));
-                if (!mbar_wait(bar(SL::P_FULL), ph, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(bar(SL::P_FULL), pn, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                mma_kmn(tmem + 256, sb + SL::PT, sb + SL::DO, n > 0);
-                mma_kmn(tmem + 384, sb + SL::DST, sb + SL::Q, n > 0);
-                umma_commit(bar(SL::QD_EMPTY));
-                umma_commit(bar(SL::P_EMPTY));
+                mma_tmn(tmem + 256, tmem, st + 2 * BLK, n > 0);
+                mma_tmn(tmem + 384, tmem + 128, st, n > 0);
+                umma_commit(bar(SL::QD_EMPTY + s));
+                umma_commit(bar(SL::PT_DONE));
             }
             if (ok) umma_commit(bar(SL::ACC_FULL));
             else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
-            int dummy = 0;
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
     } else {
@@ -478,66 +528,79 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int j = k0 + r;                          // this thread's key row
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
-        const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC);
-        const float* D_s = reinterpret_cast<const float*>(smem + SL::VEC + 512);
-        const int* ss_s = reinterpret_cast<const int*>(smem + SL::VEC + 1024);
         bool ok = true;
         uint32_t ra[32], rb[32];
-        float s_[32], dp[32];
         for (int n = 0; n < niter; ++n) {
-            const uint32_t ph = (uint32_t)(n & 1);
+            const int s = n & 1;
+            const uint32_t sp = (uint32_t)((n >> 1) & 1), pn = (uint32_t)(n & 1);
             const int q0 = (kt + n % nqt) * TB;
-            if (!warp_wait(bar(SL::QD_FULL), ph, abort_flag, lane) ||
-                !warp_wait(bar(SL::ST_FULL), ph, abort_flag, lane) ||
-                !warp_wait(bar(SL::P_EMPTY), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
+            const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC0 + s * 1536);
+            const float* D_s = lse_s + 128;
+            const int* ss_s = reinterpret_cast<const int*>(lse_s + 256);
+            if (!warp_wait(bar(SL::QD_FULL + s), sp, abort_flag, lane) ||
+                !warp_wait(bar(SL::ST_FULL), pn, abort_flag, lane)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(tl + 32 * c, ra);
-                tmem_ld32(tl + 128 + 32 * c, rb);
-                tmem_ld_wait();
-                unpack32(ra, s_);
-                unpack32(rb, dp);
-                uint32_t wp[16], wd[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2], ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int q = 32 * c + e + u;
-                        const bool valid = (q0 + q >= j) && (ss_s[q] <= j);
-                        pr[u] = valid ? exp2f(fmaf(s_[e + u], sc, -lse_s[q] * LOG2E)) : 0.f;
-                        ds[u] = pr[u] * (dp[e + u] - D_s[q]);
-                    }
-                    wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
-                    wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+            // valid query columns of this key row: [qmin, qmax] -- queries at or after
+            // it whose sequence starts at or before it (sequence starts do not
+            // decrease along the tile, so the second condition holds on a prefix)
+            const int qmin = j - q0;
+            int qmax = -1;
+            if (ss_s[0] <= j) {
+                int a = 0, b = TB - 1;
+                while (a < b) {
+                    const int mid = (a + b + 1) >> 1;
+                    if (ss_s[mid] <= j) a = mid; else b = mid - 1;
                 }
-                st_swizzled32(sb + SL::PT + (c >> 1) * BLK, r, (c & 1) * 4, wp);
-                st_swizzled32(sb + SL::DST + (c >> 1) * BLK, r, (c & 1) * 4, wd);
+                qmax = a;
             }
+            const bool whole = __all_sync(0xffffffffu, qmin <= 0 && qmax >= TB - 1);
+            auto write_pd = [&](auto masked) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tl + 32 * c, ra);
+                    tmem_ld32(tl + 128 + 32 * c, rb);
+                    tmem_ld_wait();
+                    uint32_t wp[16], wd[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int q = 32 * c + e + u;
+                            const bool valid = !decltype(masked)::value || ((q >= qmin) & (q <= qmax));
+                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ra[e + u]), sc, -lse_s[q] * LOG2E) : -INFINITY);
+                            ds[u] = pr[u] * (__uint_as_float(rb[e + u]) - D_s[q]);
+                        }
+                        wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
+                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                    }
+                    tmem_st16(tl + 16 * c, wp);             // over columns already read
+                    tmem_st16(tl + 128 + 16 * c, wd);
+                }
+            };
+            if (whole) write_pd(std::false_type{});
+            else write_pd(std::true_type{});
+            tmem_st_wait();
             tc_fence_before();
-            fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(SL::ST_FREE));
-                mbar_arrive(bar(SL::P_FULL));
-            }
+            if (lane == 0) mbar_arrive(bar(SL::P_FULL));
         }
         if (ok && niter > 0) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
         if (ok && niter > 0) {
             tc_fence_after();
             bf16* row = p.dqkv + (int64_t)j * p.ld_qkv;
+            float v[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 tmem_ld32(tl + 256 + 32 * c, ra);
                 tmem_ld32(tl + 384 + 32 * c, rb);
                 tmem_ld_wait();
-                unpack32(ra, s_);
-                unpack32(rb, dp);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) dp[e] *= p.scale;
-                store32<bf16>(row + vcol + 32 * c, s_);
-                store32<bf16>(row + kcol + 32 * c, dp);
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]);
+                store32<bf16>(row + vcol + 32 * c, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rb[e]) * p.scale;
+                store32<bf16>(row + kcol + 32 * c, v);
             }
         } else if (!ok && lane == 0) {
             atomicOr(status, ST_TIMEOUT);
@@ -682,27 +745,34 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 !warp_wait(bar(SL::DS_EMPTY), pj ^ 1u, abort_flag, lane)) { ok = false; break; }
             tc_fence_after();
             const int key0 = kstart + j * TB;
+            const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
+            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
+            auto write_ds = [&](auto masked) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(tl + 32 * c, ra);
-                tmem_ld32(tl + 128 + 32 * c, rb);
-                tmem_ld_wait();
-                unpack32(ra, s_);
-                unpack32(rb, dp);
-                uint32_t wd[16];
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tl + 32 * c, ra);
+                    tmem_ld32(tl + 128 + 32 * c, rb);
+                    tmem_ld_wait();
+                    unpack32(ra, s_);
+                    unpack32(rb, dp);
+                    uint32_t wd[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float ds[2];
+                    for (int e = 0; e < 32; e += 2) {
+                        float ds[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int key = key0 + 32 * c + e + u;
-                        const float pr = (key >= ss && key <= i) ? exp2f(fmaf(s_[e + u], sc, -lse2)) : 0.f;
-                        ds[u] = pr * (dp[e + u] - Di);
+                        for (int u = 0; u < 2; ++u) {
+                            const int idx = 32 * c + e + u;
+                            const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                            const float pr = exp2f(v ? fmaf(s_[e + u], sc, -lse2) : -INFINITY);
+                            ds[u] = pr * (dp[e + u] - Di);
+                        }
+                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                    st_swizzled32(sb + SL::DS + (c >> 1) * BLK, r, (c & 1) * 4, wd);
                 }
-                st_swizzled32(sb + SL::DS + (c >> 1) * BLK, r, (c & 1) * 4, wd);
-            }
+            };
+            if (whole) write_ds(std::false_type{});
+            else write_ds(std::true_type{});
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
@@ -766,12 +836,12 @@ __global__ void attn_rowdot_kernel(const bf16* __restrict__ dO, const bf16* __re
 }
 
 template <typename K>
-cudaError_t launch_attn(K kernel, int smem_bytes, const AttnMaps& maps, const AttnParams& p, int grid, int* status,
-                        cudaStream_t s) {
+cudaError_t launch_attn(K kernel, int smem_bytes, int threads, const AttnMaps& maps, const AttnParams& p, int grid,
+                        int* status, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     if (grid <= 0) return cudaSuccess;
-    kernel<<<grid, AT_THREADS, smem_bytes, s>>>(maps, p, status);
+    kernel<<<grid, threads, smem_bytes, s>>>(maps, p, status);
     return cudaGetLastError();
 }
 
@@ -811,7 +881,9 @@ cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s)
     AttnMaps maps;
     if (!make_maps(maps, a) || a.max_rows % TB || a.ld_t % 4) return cudaErrorInvalidValue;
     const AttnParams p = make_params(a);
-    return launch_attn(attn_fwd_kernel, FwdSmem::TOTAL, maps, p, p.max_tiles * a.n_heads, status, s);
+    const int pairs = (a.n_heads / a.n_kv + 1) / 2;
+    return launch_attn(attn_fwd_kernel, FwdSmem::TOTAL, FWD_THREADS, maps, p, p.max_tiles * a.n_kv * pairs, status,
+                       s);
 }
 
 cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s) {
@@ -824,9 +896,9 @@ cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s)
         a.dO, a.o, a.n_heads, a.meta, p.max_tiles, a.DT, a.ld_t);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_attn(attn_bwd_kv_kernel, KvSmem::TOTAL, maps, p, p.max_tiles * a.n_kv, status, s);
+    e = launch_attn(attn_bwd_kv_kernel, KvSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_kv, status, s);
     if (e != cudaSuccess) return e;
-    return launch_attn(attn_bwd_q_kernel, QSmem::TOTAL, maps, p, p.max_tiles * a.n_heads, status, s);
+    return launch_attn(attn_bwd_q_kernel, QSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_heads, status, s);
 }
 
 }  // namespace mlk
