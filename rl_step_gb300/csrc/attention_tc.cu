@@ -9,7 +9,7 @@
 // [seq_start[p], p].  Query head j reads key/value head j / (n_heads / n_kv).
 //
 // Softmax statistics travel "transposed", one contiguous run per head:
-// lseT [n_heads x ld_t] (natural-log log-sum-exp of a row's scaled scores)
+// lseT [n_heads x ld_t] (log-sum-exp of a row's scaled scores, in log2 units)
 // and DT [n_heads x ld_t] (rowsum(dO * O)), so that 128 consecutive rows of
 // one head are one 512-byte bulk copy.
 //
@@ -38,7 +38,6 @@ constexpr int HD = 128;                 // head width
 constexpr int TB = 128;                 // rows per query / key tile
 constexpr int BLK = TB * 128;           // one 128-row x 64-element bf16 block (16 KB)
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float LN2 = 0.6931471805599453f;
 
 struct AttnMaps {
     CUtensorMap rows128;   // qkv, boxes of 64 columns x 128 rows
@@ -125,11 +124,6 @@ __device__ __forceinline__ void mma_kmn(uint32_t d, uint32_t a, uint32_t b, bool
 __device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int row) {
     tma_load_2d(dst, map, bar, col, row);
     tma_load_2d(dst + BLK, map, bar, col + 64, row);
-}
-
-__device__ __forceinline__ void unpack32(const uint32_t (&r)[32], float (&v)[32]) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
 }
 
 }  // namespace
@@ -376,7 +370,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 for (int e = 0; e < 32; ++e) t[e] = __uint_as_float(rr[e]) * inv;
                 if (store) store32<bf16>(dst + 32 * c, t);
             }
-            if (store) p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            if (store) p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
         } else if (lane == 0) {
             atomicOr(status, ST_TIMEOUT);
             *abort_flag = 1;
@@ -392,15 +386,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
 // ----------------------------------------------------------------------------
 // Backward, key side.  CTA = (128-row key tile, key/value head g).  For every
-// query head of the group and every query tile that can see these keys:
-//   S^T = K Q^T, dP^T = V dO^T                     (TMEM)
+// query head of the group and every query tile that can see these keys, in
+// two halves of 64 query rows:
+//   S^T = K Q^T, dP^T = V dO^T                   (TMEM, two buffers)
 //   P^T = exp(scale S^T - lse_q), dS^T = P^T (dP^T - D_q)   (softmax warps,
 //        one key row per thread; bf16, written back into TMEM over the
 //        S^T / dP^T columns just read)
-//   dV += P^T dO,  dK += dS^T Q                     (A operand read from TMEM)
-// and finally dK *= scale.  Each dK / dV element has a single writer.  The
-// query-side tiles (Q, dO, their log-sum-exp, rowsum and sequence starts) are
-// double-buffered, so the next tile loads while this one is processed.
+//   dV += P^T dO,  dK += dS^T Q                   (A operand read from TMEM)
+// and finally dK *= scale.  The MMA warp issues the next half's S^T and dP^T
+// before it waits for this half's P^T, so the tensor core works while the
+// softmax warps do.  Query-side tiles (Q, dO, their log-sum-exp, rowsum and
+// sequence starts) are double-buffered.  Each dK / dV element has one writer.
 // ----------------------------------------------------------------------------
 namespace {
 
@@ -408,23 +404,32 @@ struct KvSmem {
     static constexpr int K = 0;
     static constexpr int V = 2 * BLK;
     static constexpr int Q0 = 4 * BLK;           // stage s: Q at Q0 + 4 BLK s, dO 2 BLK after
-    static constexpr int VEC0 = 12 * BLK;        // stage s: lse[128], D[128], seq_start[128] at VEC0 + 1536 s
+    static constexpr int VEC0 = 12 * BLK;        // stage s: lse[128] (log2 units), D[128], seq_start[128]
     static constexpr int BAR = VEC0 + 2 * 3 * 512;
-    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 6, PT_DONE = 7, ACC_FULL = 8,
-           DRAIN = 9, NBARS = 10 };
+    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 7, PT_DONE = 9, ACC_FULL = 11,
+           DRAIN = 12, NBARS = 13 };
     static constexpr int MISC = BAR + NBARS * 8;
     static constexpr int TOTAL = MISC + 16 + 1024;
 };
 
-// D (+)= A B^T for 128 x 128 x 128 with A (bf16 pairs) in TMEM columns
-// a_tmem .. a_tmem + 63 and B the MN-major view of a row-major smem tile.
-__device__ __forceinline__ void mma_tmn(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
-    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+// D = A B^T, M = 128, N = 64, K = 128: A a K-major 128-row tile, B 64 rows
+// (half `s` of a K-major 128-row tile).
+__device__ __forceinline__ void mma_kk64(uint32_t d, uint32_t a, uint32_t b, int s) {
+    const uint32_t id = idesc_bf16(64, 0, 0, 128);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ts(d, a_tmem + 8 * (4 * kb + kk), mndesc(b, kb, kk), id, (acc || kb || kk) ? 1u : 0u);
+            umma_bf16(d, kdesc(a + kb * BLK, kk), kdesc(b + kb * BLK + 8192 * s, kk), id, (kb || kk) ? 1u : 0u);
+}
+// D (+)= A B^T, M = 128, N = 128, K = 64: A (bf16 pairs) in TMEM columns
+// a_tmem .. a_tmem + 31, B rows 64 s .. 64 s + 63 of a row-major smem tile
+// read MN-major.
+__device__ __forceinline__ void mma_t64mn(uint32_t d, uint32_t a_tmem, uint32_t b, int s, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        umma_bf16_ts(d, a_tmem + 8 * kk, mndesc(b, s, kk), id, (acc || kk) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -448,10 +453,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // sequence at or before this tile's last key
     int nqt = 0;
     while (kt + nqt < mt_valid && p.seq_start[(kt + nqt) * TB] <= k0 + TB - 1) ++nqt;
-    const int niter = grp * nqt;
+    const int niter = grp * nqt;          // query tiles (head, tile); two halves each
+    const int nhalf = 2 * niter;
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 4, 1, 1, 1};
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
         for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -466,7 +472,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;   // S^T / P^T 0, dP^T / dS^T 128, dV 256, dK 384
+    // buffer b: S^T / P^T at columns 64 b, dP^T / dS^T at 128 + 64 b; dV 256, dK 384
+    const uint32_t tmem = *tmem_slot;
     int dummy = 0;
 
     if (warp == 0) {
@@ -499,23 +506,29 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(bar(SL::KV_FULL), 0, abort_flag);
-            for (int n = 0; n < niter && ok; ++n) {
-                const int s = n & 1;
-                const uint32_t sp = (uint32_t)((n >> 1) & 1), pn = (uint32_t)(n & 1);
-                const uint32_t st = sb + SL::Q0 + s * 4 * BLK;
-                if (!mbar_wait(bar(SL::QD_FULL + s), sp, abort_flag) ||
-                    (n > 0 && !mbar_wait(bar(SL::PT_DONE), pn ^ 1u, abort_flag))) { ok = false; break; }
+            // half m: query tile n = m / 2 in stage n & 1, rows 64 (m & 1) .., TMEM buffer m & 1
+            auto issue_s = [&](int m) -> bool {
+                const int n = m >> 1, b = m & 1;
+                const uint32_t st = sb + SL::Q0 + (n & 1) * 4 * BLK;
+                if (b == 0 && !mbar_wait(bar(SL::QD_FULL + (n & 1)), (uint32_t)((n >> 1) & 1), abort_flag)) return false;
+                if (m >= 2 && !mbar_wait(bar(SL::PT_DONE + b), (uint32_t)(((m >> 1) - 1) & 1), abort_flag)) return false;
                 tc_fence_after();
-                mma_kk(tmem, sb + SL::K, st, false);
-                mma_kk(tmem + 128, sb + SL::V, st + 2 * BLK, false);
-                umma_commit(bar(SL::ST_FULL));
-                if (!mbar_wait(bar(SL::P_FULL), pn, abort_flag)) { ok = false; break; }
+                mma_kk64(tmem + 64 * b, sb + SL::K, st, b);
+                mma_kk64(tmem + 128 + 64 * b, sb + SL::V, st + 2 * BLK, b);
+                umma_commit(bar(SL::ST_FULL + b));
+                return true;
+            };
+            bool ok = mbar_wait(bar(SL::KV_FULL), 0, abort_flag) && (nhalf == 0 || issue_s(0));
+            for (int m = 0; m < nhalf && ok; ++m) {
+                const int n = m >> 1, b = m & 1;
+                const uint32_t st = sb + SL::Q0 + (n & 1) * 4 * BLK;
+                if (m + 1 < nhalf && !issue_s(m + 1)) { ok = false; break; }
+                if (!mbar_wait(bar(SL::P_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                mma_tmn(tmem + 256, tmem, st + 2 * BLK, n > 0);
-                mma_tmn(tmem + 384, tmem + 128, st, n > 0);
-                umma_commit(bar(SL::QD_EMPTY + s));
-                umma_commit(bar(SL::PT_DONE));
+                mma_t64mn(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
+                mma_t64mn(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
+                umma_commit(bar(SL::PT_DONE + b));
+                if (b == 1) umma_commit(bar(SL::QD_EMPTY + (n & 1)));
             }
             if (ok) umma_commit(bar(SL::ACC_FULL));
             else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
@@ -530,35 +543,38 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float sc = p.scale * LOG2E;
         bool ok = true;
         uint32_t ra[32], rb[32];
-        for (int n = 0; n < niter; ++n) {
-            const int s = n & 1;
-            const uint32_t sp = (uint32_t)((n >> 1) & 1), pn = (uint32_t)(n & 1);
+        int qmin = 0, qmax = -1;
+        for (int m = 0; m < nhalf; ++m) {
+            const int n = m >> 1, b = m & 1, s = n & 1;
             const int q0 = (kt + n % nqt) * TB;
             const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC0 + s * 1536);
             const float* D_s = lse_s + 128;
             const int* ss_s = reinterpret_cast<const int*>(lse_s + 256);
-            if (!warp_wait(bar(SL::QD_FULL + s), sp, abort_flag, lane) ||
-                !warp_wait(bar(SL::ST_FULL), pn, abort_flag, lane)) { ok = false; break; }
-            tc_fence_after();
-            // valid query columns of this key row: [qmin, qmax] -- queries at or after
-            // it whose sequence starts at or before it (sequence starts do not
-            // decrease along the tile, so the second condition holds on a prefix)
-            const int qmin = j - q0;
-            int qmax = -1;
-            if (ss_s[0] <= j) {
-                int a = 0, b = TB - 1;
-                while (a < b) {
-                    const int mid = (a + b + 1) >> 1;
-                    if (ss_s[mid] <= j) a = mid; else b = mid - 1;
+            if (b == 0) {
+                if (!warp_wait(bar(SL::QD_FULL + s), (uint32_t)((n >> 1) & 1), abort_flag, lane)) { ok = false; break; }
+                // valid query columns of this key row: [qmin, qmax] -- queries at or
+                // after it whose sequence starts at or before it (sequence starts do
+                // not decrease along the tile, so the second condition is a prefix)
+                qmin = j - q0;
+                qmax = -1;
+                if (ss_s[0] <= j) {
+                    int a = 0, c = TB - 1;
+                    while (a < c) {
+                        const int mid = (a + c + 1) >> 1;
+                        if (ss_s[mid] <= j) a = mid; else c = mid - 1;
+                    }
+                    qmax = a;
                 }
-                qmax = a;
             }
-            const bool whole = __all_sync(0xffffffffu, qmin <= 0 && qmax >= TB - 1);
+            if (!warp_wait(bar(SL::ST_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag, lane)) { ok = false; break; }
+            tc_fence_after();
+            const int lo = qmin - 64 * b, hi = qmax - 64 * b;      // in this half's columns
+            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
             auto write_pd = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tl + 32 * c, ra);
-                    tmem_ld32(tl + 128 + 32 * c, rb);
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tl + 64 * b + 32 * c, ra);
+                    tmem_ld32(tl + 128 + 64 * b + 32 * c, rb);
                     tmem_ld_wait();
                     uint32_t wp[16], wd[16];
 #pragma unroll
@@ -566,16 +582,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         float pr[2], ds[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int q = 32 * c + e + u;
-                            const bool valid = !decltype(masked)::value || ((q >= qmin) & (q <= qmax));
-                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ra[e + u]), sc, -lse_s[q] * LOG2E) : -INFINITY);
+                            const int qc = 32 * c + e + u, q = 64 * b + qc;
+                            const bool valid = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
+                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ra[e + u]), sc, -lse_s[q]) : -INFINITY);
                             ds[u] = pr[u] * (__uint_as_float(rb[e + u]) - D_s[q]);
                         }
                         wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
                         wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    tmem_st16(tl + 16 * c, wp);             // over columns already read
-                    tmem_st16(tl + 128 + 16 * c, wd);
+                    tmem_st16(tl + 64 * b + 16 * c, wp);           // over columns already read
+                    tmem_st16(tl + 128 + 64 * b + 16 * c, wd);
                 }
             };
             if (whole) write_pd(std::false_type{});
@@ -583,10 +599,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SL::P_FULL));
+            if (lane == 0) mbar_arrive(bar(SL::P_FULL + b));
         }
-        if (ok && niter > 0) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
-        if (ok && niter > 0) {
+        if (ok && nhalf > 0) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
+        if (ok && nhalf > 0) {
             tc_fence_after();
             bf16* row = p.dqkv + (int64_t)j * p.ld_qkv;
             float v[32];
@@ -617,21 +633,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
 // ----------------------------------------------------------------------------
 // Backward, query side.  CTA = (128-row query tile, query head).  Over the
-// forward's key tiles:  S = Q K_j^T, dP = dO V_j^T (TMEM);  P = exp(scale S -
-// lse), dS = P (dP - D) (softmax warps, one query row per thread, bf16 to
-// smem);  dQ += dS K_j (TMEM);  finally dQ *= scale.
+// forward's key tiles, in halves of 64 keys:  S = Q K^T, dP = dO V^T (TMEM,
+// two buffers);  P = exp(scale S - lse), dS = P (dP - D) (softmax warps, one
+// query row per thread, bf16 written back into TMEM over the S columns just
+// read);  dQ += dS K (A operand from TMEM);  finally dQ *= scale.  The MMA
+// warp issues the next half's S and dP before it waits for this half's dS.
 // ----------------------------------------------------------------------------
 namespace {
 
 struct QSmem {
     static constexpr int Q = 0;
     static constexpr int DO = 2 * BLK;
-    static constexpr int K0 = 4 * BLK;          // two stages of 32 KB
-    static constexpr int V0 = 8 * BLK;          // two stages of 32 KB
-    static constexpr int DS = 12 * BLK;
-    static constexpr int BAR = 14 * BLK;
-    enum { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_FREE = 8, DS_FULL = 9,
-           DS_EMPTY = 10, ACC_FULL = 11, DRAIN = 12, NBARS = 13 };
+    static constexpr int K0 = 4 * BLK;          // stage s: K at K0 + 4 BLK s, V 2 BLK after
+    static constexpr int BAR = 12 * BLK;
+    enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, DS_FULL = 7, DS_DONE = 9, ACC_FULL = 11,
+           DRAIN = 12, NBARS = 13 };
     static constexpr int MISC = BAR + NBARS * 8;
     static constexpr int TOTAL = MISC + 16 + 1024;
 };
@@ -653,11 +669,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int m0 = tile * TB;
     const int kstart = p.seq_start[m0];
     const int nt = (m0 + TB - kstart + TB - 1) / TB;
+    const int nhalf = 2 * nt;
     const int grp = p.n_heads / p.n_kv, g = h / grp;
     const int qcol = h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1};
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
         for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -672,59 +689,61 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;   // S 0, dP 128, dQ 256
+    const uint32_t tmem = *tmem_slot;   // buffer b: S / dS at 64 b, dP at 128 + 64 b; dQ at 256
+    int dummy = 0;
 
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
-            int issued[2] = {-1, -1};
+            int last[2] = {-1, -1};
             mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
             load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, m0);
             load_tile128(sb + SL::DO, &maps.do128, bar(SL::Q_FULL), qcol, m0);
             for (int j = 0; j < nt; ++j) {
                 const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(bar(SL::KV_EMPTY + s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                const uint32_t sp = (uint32_t)((j >> 1) & 1);
+                if (!mbar_wait(bar(SL::KV_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
                 const int key0 = kstart + j * TB;
-                mbar_expect_tx(bar(SL::K_FULL + s), 2 * BLK);
-                load_tile128(sb + SL::K0 + s * 2 * BLK, &maps.rows128, bar(SL::K_FULL + s), kcol, key0);
-                mbar_expect_tx(bar(SL::V_FULL + s), 2 * BLK);
-                load_tile128(sb + SL::V0 + s * 2 * BLK, &maps.rows128, bar(SL::V_FULL + s), vcol, key0);
-                issued[s] = (int)ph;
+                const uint32_t fb = bar(SL::KV_FULL + s), st = sb + SL::K0 + s * 4 * BLK;
+                mbar_expect_tx(fb, 4 * BLK);
+                load_tile128(st, &maps.rows128, fb, kcol, key0);
+                load_tile128(st + 2 * BLK, &maps.rows128, fb, vcol, key0);
+                last[s] = (int)sp;
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
-            int dummy = 0;
             bool dr = mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy);
             for (int s = 0; s < 2; ++s)
-                if (issued[s] >= 0) {
-                    dr &= mbar_wait(bar(SL::K_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
-                    dr &= mbar_wait(bar(SL::V_FULL + s), (uint32_t)issued[s], (volatile int*)&dummy);
-                }
+                if (last[s] >= 0) dr &= mbar_wait(bar(SL::KV_FULL + s), (uint32_t)last[s], (volatile int*)&dummy);
             if (!dr) atomicOr(status, ST_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag);
-            for (int j = 0; j < nt && ok; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1, pj = (uint32_t)(j & 1);
-                if (!mbar_wait(bar(SL::K_FULL + s), ph, abort_flag) ||
-                    !mbar_wait(bar(SL::V_FULL + s), ph, abort_flag) ||
-                    !mbar_wait(bar(SL::S_FREE), pj ^ 1u, abort_flag)) { ok = false; break; }
+            // half m: key tile j = m / 2 in stage j & 1, keys 64 (m & 1) .., TMEM buffer m & 1
+            auto issue_s = [&](int m) -> bool {
+                const int j = m >> 1, b = m & 1;
+                const uint32_t st = sb + SL::K0 + (j & 1) * 4 * BLK;
+                if (b == 0 && !mbar_wait(bar(SL::KV_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+                if (m >= 2 && !mbar_wait(bar(SL::DS_DONE + b), (uint32_t)(((m >> 1) - 1) & 1), abort_flag)) return false;
                 tc_fence_after();
-                mma_kk(tmem, sb + SL::Q, sb + SL::K0 + s * 2 * BLK, false);
-                mma_kk(tmem + 128, sb + SL::DO, sb + SL::V0 + s * 2 * BLK, false);
-                umma_commit(bar(SL::S_FULL));
-                if (!mbar_wait(bar(SL::DS_FULL), pj, abort_flag)) { ok = false; break; }
+                mma_kk64(tmem + 64 * b, sb + SL::Q, st, b);
+                mma_kk64(tmem + 128 + 64 * b, sb + SL::DO, st + 2 * BLK, b);
+                umma_commit(bar(SL::S_FULL + b));
+                return true;
+            };
+            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag) && issue_s(0);
+            for (int m = 0; m < nhalf && ok; ++m) {
+                const int j = m >> 1, b = m & 1;
+                const uint32_t st = sb + SL::K0 + (j & 1) * 4 * BLK;
+                if (m + 1 < nhalf && !issue_s(m + 1)) { ok = false; break; }
+                if (!mbar_wait(bar(SL::DS_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                mma_kmn(tmem + 256, sb + SL::DS, sb + SL::K0 + s * 2 * BLK, j > 0);
-                umma_commit(bar(SL::KV_EMPTY + s));
-                umma_commit(bar(SL::DS_EMPTY));
+                mma_t64mn(tmem + 256, tmem + 64 * b, st, b, m > 0);
+                umma_commit(bar(SL::DS_DONE + b));
+                if (b == 1) umma_commit(bar(SL::KV_EMPTY + (j & 1)));
             }
             if (ok) umma_commit(bar(SL::ACC_FULL));
             else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
-            int dummy = 0;
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
     } else {
@@ -732,29 +751,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int r = 32 * q4 + lane;
         const int i = m0 + r;
         const int ss = p.seq_start[i];
-        const float lse2 = p.lseT[(int64_t)h * p.ld_t + i] * LOG2E;
+        const float lse2 = p.lseT[(int64_t)h * p.ld_t + i];
         const float Di = p.DT[(int64_t)h * p.ld_t + i];
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
         uint32_t ra[32], rb[32];
-        float s_[32], dp[32];
-        for (int j = 0; j < nt; ++j) {
-            const uint32_t pj = (uint32_t)(j & 1);
-            if (!warp_wait(bar(SL::S_FULL), pj, abort_flag, lane) ||
-                !warp_wait(bar(SL::DS_EMPTY), pj ^ 1u, abort_flag, lane)) { ok = false; break; }
+        for (int m = 0; m < nhalf; ++m) {
+            const int b = m & 1;
+            if (!warp_wait(bar(SL::S_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag, lane)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = kstart + j * TB;
+            const int key0 = kstart + (m >> 1) * TB + 64 * b;
             const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
-            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
+            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
             auto write_ds = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tl + 32 * c, ra);
-                    tmem_ld32(tl + 128 + 32 * c, rb);
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tl + 64 * b + 32 * c, ra);
+                    tmem_ld32(tl + 128 + 64 * b + 32 * c, rb);
                     tmem_ld_wait();
-                    unpack32(ra, s_);
-                    unpack32(rb, dp);
                     uint32_t wd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -763,36 +778,33 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         for (int u = 0; u < 2; ++u) {
                             const int idx = 32 * c + e + u;
                             const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                            const float pr = exp2f(v ? fmaf(s_[e + u], sc, -lse2) : -INFINITY);
-                            ds[u] = pr * (dp[e + u] - Di);
+                            const float pr = exp2f(v ? fmaf(__uint_as_float(ra[e + u]), sc, -lse2) : -INFINITY);
+                            ds[u] = pr * (__uint_as_float(rb[e + u]) - Di);
                         }
                         wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    st_swizzled32(sb + SL::DS + (c >> 1) * BLK, r, (c & 1) * 4, wd);
+                    tmem_st16(tl + 64 * b + 16 * c, wd);           // over columns already read
                 }
             };
             if (whole) write_ds(std::false_type{});
             else write_ds(std::true_type{});
+            tmem_st_wait();
             tc_fence_before();
-            fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(SL::S_FREE));
-                mbar_arrive(bar(SL::DS_FULL));
-            }
+            if (lane == 0) mbar_arrive(bar(SL::DS_FULL + b));
         }
         if (ok) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
         if (ok) {
             tc_fence_after();
             bf16* row = p.dqkv + (int64_t)i * p.ld_qkv + qcol;
+            float v[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 tmem_ld32(tl + 256 + 32 * c, ra);
                 tmem_ld_wait();
-                unpack32(ra, s_);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s_[e] *= p.scale;
-                store32<bf16>(row + 32 * c, s_);
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]) * p.scale;
+                store32<bf16>(row + 32 * c, v);
             }
         } else if (lane == 0) {
             atomicOr(status, ST_TIMEOUT);

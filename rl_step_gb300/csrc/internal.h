@@ -30,7 +30,7 @@ struct AttnArgs {
     const int* seq_start = nullptr;  // [max_rows] first padded row of the row's sequence
     const int* meta = nullptr;     // meta[0] = valid 128-row tiles
     bf16* o = nullptr;             // [max_rows x n_heads*128]
-    float* lseT = nullptr;         // [n_heads x ld_t] log-sum-exp of the scaled scores
+    float* lseT = nullptr;         // [n_heads x ld_t] log2-sum-exp2 of the scaled scores (log2 units)
     float* DT = nullptr;           // [n_heads x ld_t] rowsum(dO * O) (backward)
     int ld_t = 0;                  // multiple of 4
     const bf16* dO = nullptr;      // backward: dL/dO [max_rows x n_heads*128]
