@@ -132,8 +132,9 @@ __device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* ma
 // Forward.  CTA = (128-row query tile, two query heads of one key/value
 // group); key tiles of 128 rows run from the first row of the tile's first
 // sequence up to the tile's last row and are loaded once for both heads.
-// Warps: 0 loads K, 1 loads Q and V, 2 issues the MMAs, 4-7 and 8-11 are the
-// softmax warpgroups of the two heads (one query row per thread).  Per key
+// Warps: 0 loads K, 1 loads Q and V, 2 issues the MMAs, 3-6 and 7-10 are the
+// softmax warpgroups of the two heads (one query row per thread; warp w reads
+// TMEM lanes 32 (w % 4) ..).  Per key
 // tile j and head h:  S_h = Q_h K_j^T (TMEM); the warpgroup takes the row max,
 // writes P_h = exp(S_h - m) in bf16 to shared memory; O_h += P_h V_j in TMEM.
 // The MMA warp issues head h's P V and then its next S as soon as that head's
@@ -145,17 +146,17 @@ __device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* ma
 // ----------------------------------------------------------------------------
 namespace {
 
-constexpr int FWD_THREADS = 384;
+constexpr int FWD_THREADS = 352;
 constexpr float RESCALE_LOG2 = 8.f;
 
 struct FwdSmem {
     static constexpr int Q0 = 0;                // Q of head 0, then head 1 (32 KB each)
     static constexpr int K = 4 * BLK;
-    static constexpr int V = 6 * BLK;
-    static constexpr int P0 = 8 * BLK;          // P of head 0, then head 1 (32 KB each)
-    static constexpr int BAR = 12 * BLK;
-    enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 2, V_FULL = 3, V_EMPTY = 4, S_FULL = 5, S_FREE = 7,
-           P_FULL = 9, O_DONE = 11, DRAIN = 13, NBARS = 14 };
+    static constexpr int V0 = 6 * BLK;          // V of key tile j in stage j % 2 (32 KB each)
+    static constexpr int P0 = 10 * BLK;         // P of head 0, then head 1 (32 KB each)
+    static constexpr int BAR = 14 * BLK;
+    enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 2, V_FULL = 3, V_EMPTY = 5, S_FULL = 7, S_FREE = 9,
+           P_FULL = 11, O_DONE = 13, DRAIN = 15, NBARS = 16 };
     static constexpr int MISC = BAR + NBARS * 8;
     static constexpr int TOTAL = MISC + 16 + 1024;
 };
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const int kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 1};
+        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 1};
         for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -221,13 +222,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
             load_tile128(sb + SL::Q0, &maps.rows128, bar(SL::Q_FULL), h0 * HD, m0);
             load_tile128(sb + SL::Q0 + 2 * BLK, &maps.rows128, bar(SL::Q_FULL), h1 * HD, m0);
+            int last[2] = {-1, -1};
             for (int j = 0; j < nt; ++j) {
-                if (j > 0 && !mbar_wait(bar(SL::V_EMPTY), (uint32_t)((j - 1) & 1), abort_flag)) { ok = false; break; }
-                mbar_expect_tx(bar(SL::V_FULL), 2 * BLK);
-                load_tile128(sb + SL::V, &maps.rows128, bar(SL::V_FULL), vcol, kstart + j * TB);
-                if (j == nt - 1 && !mbar_wait(bar(SL::V_FULL), (uint32_t)(j & 1), (volatile int*)&dummy))
-                    ok = false;
+                const int vs = j & 1;
+                const uint32_t vp = (uint32_t)((j >> 1) & 1);
+                if (!mbar_wait(bar(SL::V_EMPTY + vs), vp ^ 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::V_FULL + vs), 2 * BLK);
+                load_tile128(sb + SL::V0 + vs * 2 * BLK, &maps.rows128, bar(SL::V_FULL + vs), vcol, kstart + j * TB);
+                last[vs] = (int)vp;
             }
+            for (int vs = 0; vs < 2; ++vs)      // our copies have landed
+                if (last[vs] >= 0 && !mbar_wait(bar(SL::V_FULL + vs), (uint32_t)last[vs], (volatile int*)&dummy))
+                    ok = false;
             if (!mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy)) ok = false;
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
         }
@@ -244,11 +250,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
             for (int j = 0; j < nt && ok; ++j) {
                 const uint32_t ph = (uint32_t)(j & 1);
-                if (!mbar_wait(bar(SL::V_FULL), ph, abort_flag)) { ok = false; break; }
+                const int vs = j & 1;
+                if (!mbar_wait(bar(SL::V_FULL + vs), (uint32_t)((j >> 1) & 1), abort_flag)) { ok = false; break; }
                 for (int hh = 0; hh < 2 && ok; ++hh) {
                     if (!mbar_wait(bar(SL::P_FULL + hh), ph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V, j > 0);
+                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V0 + vs * 2 * BLK, j > 0);
                     umma_commit(bar(SL::O_DONE + hh));
                     if (j + 1 < nt) {
                         if ((hh == 0 && !mbar_wait(bar(SL::K_FULL), ph ^ 1u, abort_flag)) ||
@@ -259,14 +266,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         if (hh == 1) umma_commit(bar(SL::K_EMPTY));
                     }
                 }
-                if (ok) umma_commit(bar(SL::V_EMPTY));
+                if (ok) umma_commit(bar(SL::V_EMPTY + vs));
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
-    } else if (warp >= 4) {
-        const int hh = (warp - 4) >> 2;                 // head slot of this warpgroup
+    } else {
+        const int hh = (warp - 3) >> 2;                 // head slot of this warpgroup
         const int h = hh ? h1 : h0;
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const float sc = p.scale * LOG2E;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        uint32_t rr[32];
+        uint32_t rr[32], rq[32];
         for (int j = 0; j < nt; ++j) {
             const uint32_t ph = (uint32_t)(j & 1);
             if (!warp_wait(bar(SL::S_FULL + hh), ph, abort_flag, lane)) { ok = false; break; }
@@ -290,15 +297,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
             float mx = -INFINITY;
             auto row_max = [&](auto masked) {
+                tmem_ld32(tS, rr);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + 32 * c, rr);
-                    tmem_ld_wait();
+                for (int c = 0; c < 4; ++c) {       // chunk c + 1 loads while chunk c is processed
+                    uint32_t (&cur)[32] = (c & 1) ? rq : rr;
+                    tmem_ld_wait_regs(cur);
+                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), (c & 1) ? rr : rq);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int idx = 32 * c + e;
                         const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                        mx = fmaxf(mx, v ? __uint_as_float(rr[e]) * sc : -INFINITY);
+                        mx = fmaxf(mx, v ? __uint_as_float(cur[e]) * sc : -INFINITY);
                     }
                 }
             };
@@ -325,10 +334,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (raise) m_run = mx;
             float rs = 0.f;
             auto write_p = [&](auto masked) {
+                tmem_ld32(tS, rr);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + 32 * c, rr);
-                    tmem_ld_wait();
+                    uint32_t (&cur)[32] = (c & 1) ? rq : rr;
+                    tmem_ld_wait_regs(cur);
+                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), (c & 1) ? rr : rq);
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -336,8 +347,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
                         const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
                         // masked entries give exp2(-inf) = 0: no branch around the exponential
-                        const float p0 = exp2f(v0 ? fmaf(__uint_as_float(rr[e]), sc, -m_run) : -INFINITY);
-                        const float p1 = exp2f(v1 ? fmaf(__uint_as_float(rr[e + 1]), sc, -m_run) : -INFINITY);
+                        const float p0 = exp2f(v0 ? fmaf(__uint_as_float(cur[e]), sc, -m_run) : -INFINITY);
+                        const float p1 = exp2f(v1 ? fmaf(__uint_as_float(cur[e + 1]), sc, -m_run) : -INFINITY);
                         rs += p0 + p1;
                         w[e >> 1] = pack_bf16x2(p0, p1);
                     }
@@ -542,7 +553,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32], rb[32], ra2[32], rb2[32];
         int qmin = 0, qmax = -1;
         for (int m = 0; m < nhalf; ++m) {
             const int n = m >> 1, b = m & 1, s = n & 1;
@@ -571,11 +582,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const int lo = qmin - 64 * b, hi = qmax - 64 * b;      // in this half's columns
             const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
             auto write_pd = [&](auto masked) {
+                tmem_ld32(tl + 64 * b, ra);
+                tmem_ld32(tl + 128 + 64 * b, rb);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tl + 64 * b + 32 * c, ra);
-                    tmem_ld32(tl + 128 + 64 * b + 32 * c, rb);
-                    tmem_ld_wait();
+                for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
+                    uint32_t (&ca)[32] = c ? ra2 : ra;
+                    uint32_t (&cb)[32] = c ? rb2 : rb;
+                    tmem_ld_wait_regs(ca);
+                    tmem_ld_wait_regs(cb);
+                    if (c == 0) {
+                        tmem_ld32(tl + 64 * b + 32, ra2);
+                        tmem_ld32(tl + 128 + 64 * b + 32, rb2);
+                    }
                     uint32_t wp[16], wd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -584,8 +602,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         for (int u = 0; u < 2; ++u) {
                             const int qc = 32 * c + e + u, q = 64 * b + qc;
                             const bool valid = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
-                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ra[e + u]), sc, -lse_s[q]) : -INFINITY);
-                            ds[u] = pr[u] * (__uint_as_float(rb[e + u]) - D_s[q]);
+                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ca[e + u]), sc, -lse_s[q]) : -INFINITY);
+                            ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - D_s[q]);
                         }
                         wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
                         wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
@@ -756,7 +774,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32], rb[32], ra2[32], rb2[32];
         for (int m = 0; m < nhalf; ++m) {
             const int b = m & 1;
             if (!warp_wait(bar(SL::S_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag, lane)) { ok = false; break; }
@@ -765,11 +783,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
             const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
             auto write_ds = [&](auto masked) {
+                tmem_ld32(tl + 64 * b, ra);
+                tmem_ld32(tl + 128 + 64 * b, rb);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tl + 64 * b + 32 * c, ra);
-                    tmem_ld32(tl + 128 + 64 * b + 32 * c, rb);
-                    tmem_ld_wait();
+                for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
+                    uint32_t (&ca)[32] = c ? ra2 : ra;
+                    uint32_t (&cb)[32] = c ? rb2 : rb;
+                    tmem_ld_wait_regs(ca);
+                    tmem_ld_wait_regs(cb);
+                    if (c == 0) {
+                        tmem_ld32(tl + 64 * b + 32, ra2);
+                        tmem_ld32(tl + 128 + 64 * b + 32, rb2);
+                    }
                     uint32_t wd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -778,8 +803,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         for (int u = 0; u < 2; ++u) {
                             const int idx = 32 * c + e + u;
                             const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                            const float pr = exp2f(v ? fmaf(__uint_as_float(ra[e + u]), sc, -lse2) : -INFINITY);
-                            ds[u] = pr * (__uint_as_float(rb[e + u]) - Di);
+                            const float pr = exp2f(v ? fmaf(__uint_as_float(ca[e + u]), sc, -lse2) : -INFINITY);
+                            ds[u] = pr * (__uint_as_float(cb[e + u]) - Di);
                         }
                         wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
                     }
