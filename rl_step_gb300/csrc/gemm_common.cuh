@@ -232,7 +232,9 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float da = acc[16 * hb + j];
-                const float sg = sigmoidf_(g[j]);
+                // hardware reciprocal: this epilogue also waits on its gate/up
+                // loads, and the IEEE division measured 14 % slower here
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g[j]));
                 o[j] = da * g[16 + j] * (sg * (1.f + g[j] * (1.f - sg)));
                 o[16 + j] = da * g[j] * sg;
             }
