@@ -297,40 +297,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major);
             const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major);
+            // stage-0 descriptors, advanced by additions to the start-address field
+            // (see the CTA-pair kernel's MMA thread)
+            const uint32_t sb0 = sbase + SL::A_BYTES;
+            const uint64_t a0 = p.A.mn_major ? sdesc(sbase, 8192, 1024) : sdesc(sbase, 16, 1024);
+            const uint64_t b0 = p.B.mn_major ? sdesc(sb0, 8192, 1024) : sdesc(sb0, 16, 1024);
+            const uint64_t ax0 = p.Ax.mn_major ? sdesc(sbase, 8192, 1024) : sdesc(sbase, 16, 1024);
+            const uint64_t bx0 = p.Bx.mn_major ? sdesc(sb0, 8192, 1024) : sdesc(sb0, 16, 1024);
+            const uint32_t a_step = p.A.mn_major ? (2048 >> 4) : (32 >> 4);
+            const uint32_t b_step = p.B.mn_major ? (2048 >> 4) : (32 >> 4);
+            const uint32_t ax_step = p.Ax.mn_major ? (2048 >> 4) : (32 >> 4);
+            const uint32_t bx_step = p.Bx.mn_major ? (2048 >> 4) : (32 >> 4);
+            constexpr uint32_t STAGE_STEP = SL::STAGE_BYTES >> 4;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileCoord c = tile_coord<BN>(p, t);
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < c.nkb; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = p.A.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
-                                                         : sdesc(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = p.B.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
-                                                         : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, id_main, (kb > 0 || kk > 0) ? 1u : 0u);
+                    if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
+                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
+                    const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP);
+                    umma_bf16(d_tmem, ad, bd, id_main, kb > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, ad + kk * a_step, bd + kk * b_step, id_main, 1u);
                     umma_commit(bar_empty + 8 * stage);     // frees the stage when the MMAs finish
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 for (int kb = 0; kb < c.nkbx && ok; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = p.Ax.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
-                                                          : sdesc(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = p.Bx.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
-                                                          : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, id_ext, (c.nkb > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+                    if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
+                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint64_t ad = ax0 + (uint64_t)(stage * STAGE_STEP);
+                    const uint64_t bd = bx0 + (uint64_t)(stage * STAGE_STEP);
+                    umma_bf16(d_tmem, ad, bd, id_ext, (c.nkb > 0 || kb > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, ad + kk * ax_step, bd + kk * bx_step, id_ext, 1u);
                     umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -577,29 +589,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t sph = 0;
             const uint32_t sfull_peer = map_to_rank(bar_sfull, 1);
             const uint32_t slot_peer = map_to_rank(smem_u32(const_cast<int*>(slots)), 1);
-            for (;;) {
+            // scheduler (leader): the next pair tile is fetched from the global
+            // counter when the current one starts and published to both CTAs after
+            // the current tile's first stage is queued, so neither the atomic nor
+            // the peer's ring wait sits between two tiles' loads
+            auto publish = [&](int tp) -> bool {
+                if (!mbar_wait(bar_sempty + 8 * sslot, sph ^ 1u, abort_flag)) return false;
+                slots[sslot] = tp;
+                st_shared_cluster(slot_peer + 4 * sslot, tp);
+                mbar_arrive(bar_sfull + 8 * sslot);
+                mbar_arrive_cluster(sfull_peer + 8 * sslot);
+                if (++sslot == SL::SCHED) { sslot = 0; sph ^= 1u; }
+                return true;
+            };
+            auto fetch = [&]() -> int {
+                const int tf = atomicAdd(p.tile_counter, 1);
+                return tf >= ntiles ? -1 : tf;
+            };
+            int t_cur = -1;
+            if (leader) {
+                t_cur = fetch();
+                ok = publish(t_cur);
+            }
+            for (; ok;) {
                 int t;
                 if (leader) {
-                    // scheduler: next pair tile, published to both CTAs
-                    t = atomicAdd(p.tile_counter, 1);
-                    if (t >= ntiles) t = -1;
-                    if (!mbar_wait(bar_sempty + 8 * sslot, sph ^ 1u, abort_flag)) { ok = false; break; }
-                    slots[sslot] = t;
-                    st_shared_cluster(slot_peer + 4 * sslot, t);
-                    mbar_arrive(bar_sfull + 8 * sslot);
-                    mbar_arrive_cluster(sfull_peer + 8 * sslot);
-                    if (++sslot == SL::SCHED) { sslot = 0; sph ^= 1u; }
-                } else {
-                    if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, false, abort_flag, t)) {
-                        ok = false;
-                        break;
-                    }
+                    t = t_cur;
+                } else if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, false, abort_flag, t)) {
+                    ok = false;
+                    break;
                 }
                 if (t < 0) break;
+                const int t_next = leader ? fetch() : -1;
+                bool published = !leader;
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 const int m0 = (c.mt + (int)rank) * BM;
                 const int n0 = c.nt * BN + (int)rank * (BN / 2);
                 for (int kb = 0; kb < c.nkb && ok; ++kb) {
+                    if (kb == 1 && !published) {
+                        if (!publish(t_next)) { ok = false; break; }
+                        published = true;
+                    }
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
                     const uint32_t fb = full_leader + 8 * stage;
@@ -631,7 +661,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (ok && !published) ok = publish(t_next);
                 if (!ok) break;
+                t_cur = t_next;
             }
             if (!ok) {
                 atomicOr(status, ST_TIMEOUT);
@@ -659,6 +691,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t sph = 0;
             const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
             const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major, 2 * BM);
+            // Descriptors of stage 0; a stage / K step only moves the start-address
+            // field (bits 0-13, address >> 4), which stays below 2^14 for any
+            // shared-memory address, so they are advanced by plain additions.  A
+            // single thread issues every MMA: its work per K block is kept to a
+            // try-wait, a few adds, four MMAs and the commit.
+            const uint64_t a0 = sdesc(sbase, 16, 1024);   // A and Ax are K-major here
+            const uint64_t b0 = p.B.mn_major ? sdesc(sbase + SL::A_BYTES, 8192, 1024)
+                                             : sdesc(sbase + SL::A_BYTES, 16, 1024);
+            const uint64_t bx0 = p.Bx.mn_major ? sdesc(sbase + SL::A_BYTES, 8192, 1024)
+                                               : sdesc(sbase + SL::A_BYTES, 16, 1024);
+            const uint32_t b_step = p.B.mn_major ? (2048 >> 4) : (32 >> 4);
+            const uint32_t bx_step = p.Bx.mn_major ? (2048 >> 4) : (32 >> 4);
+            constexpr uint32_t STAGE_STEP = SL::STAGE_BYTES >> 4;
             for (;;) {
                 int t;
                 if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, true, abort_flag, t)) {
@@ -672,33 +717,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 const int nall = c.nkb + c.next;
                 for (int kb = 0; kb < c.nkb; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = p.A.mn_major ? sdesc(sa + kk * 2048, 8192, 1024)
-                                                         : sdesc(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = p.B.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
-                                                         : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16_pair(d_tmem, ad, bd, id_main, (kb > 0 || kk > 0) ? 1u : 0u);
+                    if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
+                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
+                    const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP);
+                    umma_bf16_pair(d_tmem, ad, bd, id_main, kb > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < BK / 16; ++kk)
+                        umma_bf16_pair(d_tmem, ad + kk * 2, bd + kk * b_step, id_main, 1u);
                     umma_commit_pair_mc(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 for (int kb = c.nkb; kb < nall && ok; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const uint32_t sb = sa + SL::A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);     // Ax is K-major
-                        const uint64_t bd = p.Bx.mn_major ? sdesc(sb + kk * 2048, 8192, 1024)
-                                                          : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16_pair(d_tmem, ad, bd, id_ext, 1u);
+                    if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
+                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
+                    const uint64_t bd = bx0 + (uint64_t)(stage * STAGE_STEP);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(d_tmem, ad + kk * 2, bd + kk * bx_step, id_ext, 1u);
                     umma_commit_pair_mc(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
