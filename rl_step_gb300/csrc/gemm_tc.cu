@@ -403,11 +403,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // the accumulator on the leader's "tmem empty" barrier.  Used for GEMMs whose
 // B operand is shared by all rows (the LM head); the per-adapter GEMMs keep
 // the single-CTA kernel.
-template <int BN, int STAGES, int NUM_ACC>
+template <int BN, int STAGES, int NUM_ACC, int SUB>
 struct SmemLayoutPair {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (BN / 2) * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SUB_BYTES = A_BYTES + B_BYTES;   // one 64-wide K block: A rows, then B rows
+    static constexpr int STAGE_BYTES = SUB * SUB_BYTES;   // a stage holds SUB consecutive K blocks
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr int SCHED = 4;                     // tile-index ring depth
     static constexpr int BAR_OFF = TILES_BYTES;
@@ -509,10 +510,10 @@ __device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_l
     return true;
 }
 
-template <int BN, int STAGES, int NUM_ACC>
+template <int BN, int STAGES, int NUM_ACC, int SUB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC>;
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
     static_assert(SL::SCHED == 4, "sched_take assumes a 4-slot ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -625,18 +626,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 const int m0 = (c.mt + (int)rank) * BM;
                 const int n0 = c.nt * BN + (int)rank * (BN / 2);
-                for (int kb = 0; kb < c.nkb && ok; ++kb) {
-                    if (kb == 1 && !published) {
+                const int nst = (c.nkb + SUB - 1) / SUB;
+                for (int ks = 0; ks < nst && ok; ++ks) {
+                    if (ks == 1 && !published) {
                         if (!publish(t_next)) { ok = false; break; }
                         published = true;
                     }
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
+                    const int nsub = c.nkb - ks * SUB < SUB ? c.nkb - ks * SUB : SUB;
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * nsub * SL::SUB_BYTES);
                     const uint32_t fb = full_leader + 8 * stage;
-                    const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    const int k = c.k0 + kb * BK;
-                    load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), true);
-                    load_tile_b<BN / 2>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, 0, true);
+                    for (int h = 0; h < nsub; ++h) {
+                        const uint32_t sa = sbase + stage * SL::STAGE_BYTES + h * SL::SUB_BYTES;
+                        const int k = c.k0 + (ks * SUB + h) * BK;
+                        load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), true);
+                        load_tile_b<BN / 2>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, 0, true);
+                    }
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // loads zeros, read out of bounds)
                 for (int e = 0; e < c.next && ok; ++e) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::STAGE_BYTES);
+                    if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * SL::SUB_BYTES);   // one K block
                     const uint32_t fb = full_leader + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
                     const int half = e / c.nkbx;
@@ -704,6 +709,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t b_step = p.B.mn_major ? (2048 >> 4) : (32 >> 4);
             const uint32_t bx_step = p.Bx.mn_major ? (2048 >> 4) : (32 >> 4);
             constexpr uint32_t STAGE_STEP = SL::STAGE_BYTES >> 4;
+            constexpr uint32_t SUB_STEP = SL::SUB_BYTES >> 4;
             for (;;) {
                 int t;
                 if (!sched_take(bar_sfull, sempty_leader, slots, sslot, sph, true, abort_flag, t)) {
@@ -715,8 +721,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const int nall = c.nkb + c.next;
-                for (int kb = 0; kb < c.nkb; ++kb) {
+                const int nst = (c.nkb + SUB - 1) / SUB;
+                for (int ks = 0; ks < nst; ++ks) {
                     if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
                         !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
                         ok = false;
@@ -725,14 +731,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
                     const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP);
-                    umma_bf16_pair(d_tmem, ad, bd, id_main, kb > 0 ? 1u : 0u);
+                    umma_bf16_pair(d_tmem, ad, bd, id_main, ks > 0 ? 1u : 0u);
 #pragma unroll
                     for (int kk = 1; kk < BK / 16; ++kk)
                         umma_bf16_pair(d_tmem, ad + kk * 2, bd + kk * b_step, id_main, 1u);
+#pragma unroll
+                    for (int h = 1; h < SUB; ++h) {
+                        if (ks * SUB + h >= c.nkb) break;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16_pair(d_tmem, ad + h * SUB_STEP + kk * 2, bd + h * SUB_STEP + kk * b_step,
+                                           id_main, 1u);
+                    }
                     umma_commit_pair_mc(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                for (int kb = c.nkb; kb < nall && ok; ++kb) {
+                for (int e = 0; e < c.next && ok; ++e) {
                     if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
                         !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
                         ok = false;
@@ -875,9 +889,9 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
     return cudaGetLastError();
 }
 
-template <int BN, int STAGES, int NUM_ACC>
+template <int BN, int STAGES, int NUM_ACC, int SUB>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC>;
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
     TcMaps maps;
     auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
         if (!operand_ok(op)) return false;
@@ -895,7 +909,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -919,20 +933,23 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     cfg.numAttrs = 1;
     cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);   // fresh tile counter
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC>, maps, p, status, dbg);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB>, maps, p, status, dbg);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// CTA-pair variants (exposed for the engine's own checks): acc_buffers = 1 or 2.
+// CTA-pair variants (exposed for the engine's own checks): acc_buffers = 1 or 2
+// with one 64-wide K block per stage; 3 = the engine's configuration (two
+// accumulators, two K blocks per stage).
 cudaError_t launch_tc_gemm_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status,
                                 int acc_buffers, int* dbg) {
     if (!get_encode()) return cudaErrorNotSupported;
     if (p.N < 256) return cudaErrorInvalidValue;
-    if (acc_buffers == 1) return launch_pair<256, 6, 1>(p, s, num_sms, status, dbg);
-    return launch_pair<256, 6, 2>(p, s, num_sms, status, dbg);
+    if (acc_buffers == 1) return launch_pair<256, 6, 1, 1>(p, s, num_sms, status, dbg);
+    if (acc_buffers == 2) return launch_pair<256, 6, 2, 1>(p, s, num_sms, status, dbg);
+    return launch_pair<256, 3, 2, 2>(p, s, num_sms, status, dbg);
 }
 
 bool tc_engine_available() { return get_encode(); }
@@ -952,7 +969,7 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
     if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
-        return launch_pair<256, 6, 2>(p, s, num_sms, status, nullptr);
+        return launch_pair<256, 3, 2, 2>(p, s, num_sms, status, nullptr);
     return launch_bn<256, 4>(p, s, num_sms, status);
 }
 
