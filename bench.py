@@ -449,7 +449,7 @@ def run_ours(args, rank, world):
                    "deterministic": bool(args.deterministic)},
         "tflops_algorithmic": fl["total"] * K * world / (ms_max * 1e-3) / 1e12,
         "frac_of_bf16_peak": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-        "roofline": {"kernel": "tc_gemm_pair_kernel<256,6,2> (base, LoRA-extension and LM-head GEMMs)",
+        "roofline": {"kernel": "tc_gemm_pair_kernel<256,3,2,2> (base, LoRA-extension and LM-head GEMMs)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_tc,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
                      "frac": (achieved / peak_tc) if achieved else None, "traffic": traffic,
