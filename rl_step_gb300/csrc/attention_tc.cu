@@ -72,8 +72,11 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Wait of one warp: lane 0 polls the barrier, the warp learns the outcome.
+// Wait of one warp.  Fast path: every lane tests the barrier (converged, no
+// shuffle); otherwise lane 0 polls it with the bounded wait and the warp
+// learns the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -92,31 +95,38 @@ __device__ __forceinline__ void st_swizzled32(uint32_t blk, int r, int c0, const
     }
 }
 
-// K-major 128-row operand block of 64 elements per row: K step kk (16 elements).
-__device__ __forceinline__ uint64_t kdesc(uint32_t blk, int kk) { return sdesc(blk + kk * 32, 16, 1024); }
-// The same bytes read as an MN-major operand whose K index is the row: a
-// 16-row K step at row 16*kk of K block kb (64 rows), MN halves 16 KB apart.
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kb, int kk) {
-    return sdesc(base + kb * 8192 + kk * 2048, 2 * 8192, 1024);
-}
+// Descriptors are built once per product and moved by additions to their
+// start-address field (bits 0-13, address >> 4): shared-memory addresses stay
+// below 2^18, so the field never carries.  The one issuing thread then spends
+// a few integer adds per MMA instead of rebuilding two descriptors.
+// K-major 128-row operand block of 64 elements per row, K step 0; +2 per K
+// step of 16 elements, +BLK_STEP per 64-element block.
+__device__ __forceinline__ uint64_t kdesc(uint32_t blk) { return sdesc(blk, 16, 1024); }
+constexpr uint32_t BLK_STEP = BLK >> 4;
+// The same bytes read as an MN-major operand whose K index is the row: K block
+// kb (64 rows) at +512 kb, 16-row K step at +128 kk, MN halves 16 KB apart.
+__device__ __forceinline__ uint64_t mndesc(uint32_t base) { return sdesc(base, 2 * 8192, 1024); }
 
 // 128 x 128 x 128 products: D (+)= A B^T with A, B both K-major (two 64-wide
 // K blocks each), or A K-major and B the MN-major view of a row-major tile.
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, bool acc) {
     const uint32_t id = idesc_bf16(128, 0, 0, 128);
+    const uint64_t ad = kdesc(a), bd = kdesc(b);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, kdesc(a + kb * BLK, kk), kdesc(b + kb * BLK, kk), id, (acc || kb || kk) ? 1u : 0u);
+            umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + kb * BLK_STEP + 2 * kk, id,
+                      (acc || kb || kk) ? 1u : 0u);
 }
 __device__ __forceinline__ void mma_kmn(uint32_t d, uint32_t a, uint32_t b, bool acc) {
     const uint32_t id = idesc_bf16(128, 0, 1, 128);
+    const uint64_t ad = kdesc(a), bd = mndesc(b);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, kdesc(a + kb * BLK, kk), mndesc(b, kb, kk), id, (acc || kb || kk) ? 1u : 0u);
+            umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + 512 * kb + 128 * kk, id, (acc || kb || kk) ? 1u : 0u);
 }
 
 // Load a 128-row x 128-column bf16 tile of a row-major matrix as two
@@ -255,8 +265,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 for (int hh = 0; hh < 2 && ok; ++hh) {
                     if (!mbar_wait(bar(SL::P_FULL + hh), ph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V0 + vs * 2 * BLK, j > 0);
-                    umma_commit(bar(SL::O_DONE + hh));
+                    // the next tile's scores before this P V: the softmax warps hold S_h
+                    // in registers already, and start on the next tile while P V runs
                     if (j + 1 < nt) {
                         if ((hh == 0 && !mbar_wait(bar(SL::K_FULL), ph ^ 1u, abort_flag)) ||
                             !mbar_wait(bar(SL::S_FREE + hh), ph, abort_flag)) { ok = false; break; }
@@ -265,6 +275,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         umma_commit(bar(SL::S_FULL + hh));
                         if (hh == 1) umma_commit(bar(SL::K_EMPTY));
                     }
+                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V0 + vs * 2 * BLK, j > 0);
+                    umma_commit(bar(SL::O_DONE + hh));
                 }
                 if (ok) umma_commit(bar(SL::V_EMPTY + vs));
             }
@@ -285,11 +297,25 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const float sc = p.scale * LOG2E;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        uint32_t rr[32], rq[32];
+        uint32_t rr[32];
         for (int j = 0; j < nt; ++j) {
             const uint32_t ph = (uint32_t)(j & 1);
             if (!warp_wait(bar(SL::S_FULL + hh), ph, abort_flag, lane)) { ok = false; break; }
             tc_fence_after();
+            // the whole score row in registers (one TMEM pass); S_h is free for the
+            // next tile's scores as soon as it has landed
+            uint32_t s0[32], s1[32], s2[32], s3[32];
+            tmem_ld32(tS, s0);
+            tmem_ld32(tS + 32, s1);
+            tmem_ld32(tS + 64, s2);
+            tmem_ld32(tS + 96, s3);
+            tmem_ld_wait_regs(s0);
+            tmem_ld_wait_regs(s1);
+            tmem_ld_wait_regs(s2);
+            tmem_ld_wait_regs(s3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SL::S_FREE + hh));
             const int key0 = kstart + j * TB;
             // valid key columns of this row: [lo, hi]; a warp whose rows all see
             // the whole tile takes the unmasked copy of the loops
@@ -297,19 +323,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
             float mx = -INFINITY;
             auto row_max = [&](auto masked) {
-                tmem_ld32(tS, rr);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {       // chunk c + 1 loads while chunk c is processed
-                    uint32_t (&cur)[32] = (c & 1) ? rq : rr;
-                    tmem_ld_wait_regs(cur);
-                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), (c & 1) ? rr : rq);
+                auto chunk = [&](const uint32_t (&cur)[32], int c) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int idx = 32 * c + e;
                         const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
                         mx = fmaxf(mx, v ? __uint_as_float(cur[e]) * sc : -INFINITY);
                     }
-                }
+                };
+                chunk(s0, 0);
+                chunk(s1, 1);
+                chunk(s2, 2);
+                chunk(s3, 3);
             };
             if (whole) row_max(std::false_type{});
             else row_max(std::true_type{});
@@ -318,28 +343,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 tc_fence_after();
             }
             const bool raise = mx > m_run + RESCALE_LOG2;
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                const float alpha = raise ? exp2f(m_run - mx) : 1.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tO + 32 * c, rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(tO + 32 * c, rr);
-                }
-                tmem_st_wait();
-                l_run *= alpha;
-            }
+            const float alpha = raise ? exp2f(m_run - mx) : 1.f;
             if (raise) m_run = mx;
             float rs = 0.f;
             auto write_p = [&](auto masked) {
-                tmem_ld32(tS, rr);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t (&cur)[32] = (c & 1) ? rq : rr;
-                    tmem_ld_wait_regs(cur);
-                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), (c & 1) ? rr : rq);
+                auto chunk = [&](const uint32_t (&cur)[32], int c) {
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -353,18 +361,31 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         w[e >> 1] = pack_bf16x2(p0, p1);
                     }
                     st_swizzled32(sP + (c >> 1) * BLK, r, (c & 1) * 4, w);
-                }
+                };
+                chunk(s0, 0);
+                chunk(s1, 1);
+                chunk(s2, 2);
+                chunk(s3, 3);
             };
             if (whole) write_p(std::false_type{});
             else write_p(std::true_type{});
+            // a raised max rescales O_h before this tile's P V accumulates into it
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tO + 32 * c, rr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                    tmem_st32(tO + 32 * c, rr);
+                }
+                tmem_st_wait();
+            }
+            l_run = l_run * alpha + rs;
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(SL::S_FREE + hh));
-                mbar_arrive(bar(SL::P_FULL + hh));
-            }
-            l_run += rs;
+            if (lane == 0) mbar_arrive(bar(SL::P_FULL + hh));
         }
         if (ok) ok = warp_wait(bar(SL::O_DONE + hh), (uint32_t)((nt - 1) & 1), abort_flag, lane);
         if (ok) {
@@ -427,20 +448,22 @@ struct KvSmem {
 // (half `s` of a K-major 128-row tile).
 __device__ __forceinline__ void mma_kk64(uint32_t d, uint32_t a, uint32_t b, int s) {
     const uint32_t id = idesc_bf16(64, 0, 0, 128);
+    const uint64_t ad = kdesc(a), bd = kdesc(b + 8192 * s);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, kdesc(a + kb * BLK, kk), kdesc(b + kb * BLK + 8192 * s, kk), id, (kb || kk) ? 1u : 0u);
+            umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + kb * BLK_STEP + 2 * kk, id, (kb || kk) ? 1u : 0u);
 }
 // D (+)= A B^T, M = 128, N = 128, K = 64: A (bf16 pairs) in TMEM columns
 // a_tmem .. a_tmem + 31, B rows 64 s .. 64 s + 63 of a row-major smem tile
 // read MN-major.
 __device__ __forceinline__ void mma_t64mn(uint32_t d, uint32_t a_tmem, uint32_t b, int s, bool acc) {
     const uint32_t id = idesc_bf16(128, 0, 1, 128);
+    const uint64_t bd = mndesc(b) + 512 * s;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_ts(d, a_tmem + 8 * kk, mndesc(b, s, kk), id, (acc || kk) ? 1u : 0u);
+        umma_bf16_ts(d, a_tmem + 8 * kk, bd + 128 * kk, id, (acc || kk) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -596,17 +619,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     }
                     uint32_t wp[16], wd[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2], ds[2];
+                    for (int e = 0; e < 32; e += 4) {
+                        // the query columns' lse and D, four at a time (same address in every lane)
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 64 * b + 32 * c + e);
+                        const float4 d4 = *reinterpret_cast<const float4*>(D_s + 64 * b + 32 * c + e);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pr[4], ds[4];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int qc = 32 * c + e + u, q = 64 * b + qc;
+                        for (int u = 0; u < 4; ++u) {
+                            const int qc = 32 * c + e + u;
                             const bool valid = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
-                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ca[e + u]), sc, -lse_s[q]) : -INFINITY);
-                            ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - D_s[q]);
+                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ca[e + u]), sc, -lv[u]) : -INFINITY);
+                            ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - dv[u]);
                         }
                         wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
+                        wp[(e >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
                         wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                        wd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
                     }
                     tmem_st16(tl + 64 * b + 16 * c, wp);           // over columns already read
                     tmem_st16(tl + 128 + 64 * b + 16 * c, wd);
