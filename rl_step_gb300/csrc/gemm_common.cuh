@@ -308,14 +308,23 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
         }
         bool bad = false;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            int c = col0 + j;
-            if (c < r) {
-                float v = acc[j];
-                bad |= !isfinite(v);
-                int64_t off = ep.grad_trans ? (int64_t)c * ep.grad_M + row : row * (int64_t)r + c;
-                atomicAdd(base + off, v);
-            }
+        for (int j = 0; j < 32; ++j) bad |= (col0 + j < r) && !isfinite(acc[j]);
+        if (ep.grad_trans) {
+            // [r x M] target: the warp's 32 rows are 32 consecutive floats per column
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < r) atomicAdd(base + (int64_t)(col0 + j) * ep.grad_M + row, acc[j]);
+        } else {
+            // [M x r] target: this row's columns are consecutive (r and col0 are
+            // multiples of 4, so every group of four is 16-byte aligned): one
+            // vector reduction per four values
+            float* dst = base + row * (int64_t)r + col0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                if (col0 + j < r)
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + j), "f"(acc[j]),
+                                 "f"(acc[j + 1]), "f"(acc[j + 2]), "f"(acc[j + 3])
+                                 : "memory");
         }
         if (bad) ep.nonfinite[adapter] = 1;
     } break;

@@ -69,12 +69,16 @@ def test_routing_flags_out_of_range_ids():
 
 # --------------------------------------------------------------- full steps
 
-CASES = [("tiny_fp32", None), ("qwen3_4b_is", 1024), ("qwen3_8b_ppo", 1024),
-         ("many_tenant_ce", 2048), ("long_custom", 512)]
+# Odd widths: d = 320 and f = 704 are 5 and 11 blocks of 64 along K, so the CTA-pair
+# GEMMs (two K blocks per pipeline stage) end every tile on a half-filled stage.
+ODD_K = {"d_model": 320, "d_ffn": 704, "vocab": 4000}
+
+CASES = [("tiny_fp32", None, None), ("qwen3_4b_is", 1024, None), ("qwen3_8b_ppo", 1024, None),
+         ("many_tenant_ce", 2048, None), ("long_custom", 512, None), ("qwen3_8b_ppo", 1024, ODD_K)]
 
 
-def _setup(name, n):
-    cfg = wl.get_config(name)
+def _setup(name, n, overrides=None):
+    cfg = wl.get_config(name, **(overrides or {}))
     base = wl.make_base_weights(cfg)
     ad = wl.make_adapters(cfg)
     b = wl.make_batch(cfg, n)
@@ -85,10 +89,11 @@ def _setup(name, n):
     return cfg, base, ad, b, o, s
 
 
-@pytest.mark.parametrize("name,n", CASES)
-def test_step_parity(name, n):
+@pytest.mark.parametrize("name,n,overrides", CASES,
+                         ids=[c[0] + ("_odd_k_blocks" if c[2] else "") for c in CASES])
+def test_step_parity(name, n, overrides):
     import rl_step_gb300 as m
-    cfg, base, ad, b, o, s = _setup(name, n)
+    cfg, base, ad, b, o, s = _setup(name, n, overrides)
     kind = cfg.loss
     N = len(b["tokens"])
     h = create_handle(cfg, base, ad, N)
