@@ -369,14 +369,23 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
     }
 #undef ALLOC
 #undef ALLOCB
+    // a failure while the handle is filled frees what it holds
+#define CUDA_TRY_OUT(expr)                                                                   \
+    do {                                                                                     \
+        cudaError_t _e = (expr);                                                             \
+        if (_e != cudaSuccess) {                                                             \
+            rc = fail(MLORA_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(_e));         \
+            goto fail_out;                                                                   \
+        }                                                                                    \
+    } while (0)
     {
         cudaStream_t s = 0;
         // copy the base
-        CUDA_TRY(cudaMemcpyAsync(h->E, init->E, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
-        CUDA_TRY(cudaMemcpyAsync(h->Wout, init->Wout, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
+        CUDA_TRY_OUT(cudaMemcpyAsync(h->E, init->E, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
+        CUDA_TRY_OUT(cudaMemcpyAsync(h->Wout, init->Wout, (size_t)V * d * es, cudaMemcpyDeviceToDevice, s));
         for (int l = 0; l < L; ++l) {
-            CUDA_TRY(cudaMemcpyAsync(h->W1[l], init->W1[l], (size_t)f * d * es, cudaMemcpyDeviceToDevice, s));
-            CUDA_TRY(cudaMemcpyAsync(h->W2[l], init->W2[l], (size_t)d * f * es, cudaMemcpyDeviceToDevice, s));
+            CUDA_TRY_OUT(cudaMemcpyAsync(h->W1[l], init->W1[l], (size_t)f * d * es, cudaMemcpyDeviceToDevice, s));
+            CUDA_TRY_OUT(cudaMemcpyAsync(h->W2[l], init->W2[l], (size_t)d * f * es, cudaMemcpyDeviceToDevice, s));
             if (h->dtype == MLORA_BF16) {
                 launch_transpose<bf16>(reinterpret_cast<const bf16*>(h->W1[l]), reinterpret_cast<bf16*>(h->W1T[l]), f, d, s);
                 launch_transpose<bf16>(reinterpret_cast<const bf16*>(h->W2[l]), reinterpret_cast<bf16*>(h->W2T[l]), d, f, s);
@@ -387,25 +396,25 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
             h->launches += 2;
         }
         // adapters
-        CUDA_TRY(cudaMemsetAsync(h->P, 0, sizeof(float) * h->n_params, s));
-        CUDA_TRY(cudaMemsetAsync(h->G, 0, sizeof(float) * h->n_params, s));
-        CUDA_TRY(cudaMemsetAsync(h->M, 0, sizeof(float) * h->n_params, s));
-        CUDA_TRY(cudaMemsetAsync(h->Vm, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY_OUT(cudaMemsetAsync(h->P, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY_OUT(cudaMemsetAsync(h->G, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY_OUT(cudaMemsetAsync(h->M, 0, sizeof(float) * h->n_params, s));
+        CUDA_TRY_OUT(cudaMemsetAsync(h->Vm, 0, sizeof(float) * h->n_params, s));
         const float* const* src[4] = {init->A1, init->B1, init->A2, init->B2};
         for (int a = 0; a < n_ad; ++a)
             for (int l = 0; l < L; ++l)
                 for (int k = 0; k < 4; ++k) {
                     const float* p = src[k] ? src[k][a * L + l] : nullptr;
                     if (p)
-                        CUDA_TRY(cudaMemcpyAsync(h->P + tensor_off(h, a, l, k), p,
+                        CUDA_TRY_OUT(cudaMemcpyAsync(h->P + tensor_off(h, a, l, k), p,
                                                  sizeof(float) * tensor_size(k, h->ranks[a], d, f),
                                                  cudaMemcpyDeviceToDevice, s));
                 }
         for (int l = 0; l < L; ++l) {
-            CUDA_TRY(cudaMemsetAsync(h->shadow.A1[l], 0, (size_t)n_ad * RP * d * es, s));
-            CUDA_TRY(cudaMemsetAsync(h->shadow.B1[l], 0, (size_t)n_ad * f * RP * es, s));
-            CUDA_TRY(cudaMemsetAsync(h->shadow.A2[l], 0, (size_t)n_ad * RP * f * es, s));
-            CUDA_TRY(cudaMemsetAsync(h->shadow.B2[l], 0, (size_t)n_ad * d * RP * es, s));
+            CUDA_TRY_OUT(cudaMemsetAsync(h->shadow.A1[l], 0, (size_t)n_ad * RP * d * es, s));
+            CUDA_TRY_OUT(cudaMemsetAsync(h->shadow.B1[l], 0, (size_t)n_ad * f * RP * es, s));
+            CUDA_TRY_OUT(cudaMemsetAsync(h->shadow.A2[l], 0, (size_t)n_ad * RP * f * es, s));
+            CUDA_TRY_OUT(cudaMemsetAsync(h->shadow.B2[l], 0, (size_t)n_ad * d * RP * es, s));
         }
         std::vector<float> gam(n_ad);
         for (int a = 0; a < n_ad; ++a) gam[a] = h->alphas[a] / (float)h->ranks[a];
@@ -413,23 +422,24 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         for (int l = 0; l < L; ++l)
             for (int k = 0; k < 4; ++k)
                 for (int a = 0; a < n_ad; ++a) goff[((size_t)l * 4 + k) * n_ad + a] = tensor_off(h, a, l, k);
-        CUDA_TRY(cudaMemcpy(h->ad_off, h->ad_off_h.data(), sizeof(int64_t) * (n_ad + 1), cudaMemcpyHostToDevice));
-        CUDA_TRY(cudaMemcpy(h->ranks_d, h->ranks.data(), sizeof(int) * n_ad, cudaMemcpyHostToDevice));
-        CUDA_TRY(cudaMemcpy(h->gamma_d, gam.data(), sizeof(float) * n_ad, cudaMemcpyHostToDevice));
-        CUDA_TRY(cudaMemcpy(h->grad_off, goff.data(), sizeof(int64_t) * goff.size(), cudaMemcpyHostToDevice));
-        CUDA_TRY(cudaMemset(h->step, 0, sizeof(int64_t) * n_ad));
-        CUDA_TRY(cudaMemset(h->touched, 0, sizeof(int) * n_ad));
-        CUDA_TRY(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
-        CUDA_TRY(cudaMemset(h->status, 0, sizeof(int)));
-        CUDA_TRY(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
+        CUDA_TRY_OUT(cudaMemcpy(h->ad_off, h->ad_off_h.data(), sizeof(int64_t) * (n_ad + 1), cudaMemcpyHostToDevice));
+        CUDA_TRY_OUT(cudaMemcpy(h->ranks_d, h->ranks.data(), sizeof(int) * n_ad, cudaMemcpyHostToDevice));
+        CUDA_TRY_OUT(cudaMemcpy(h->gamma_d, gam.data(), sizeof(float) * n_ad, cudaMemcpyHostToDevice));
+        CUDA_TRY_OUT(cudaMemcpy(h->grad_off, goff.data(), sizeof(int64_t) * goff.size(), cudaMemcpyHostToDevice));
+        CUDA_TRY_OUT(cudaMemset(h->step, 0, sizeof(int64_t) * n_ad));
+        CUDA_TRY_OUT(cudaMemset(h->touched, 0, sizeof(int) * n_ad));
+        CUDA_TRY_OUT(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
+        CUDA_TRY_OUT(cudaMemset(h->status, 0, sizeof(int)));
+        CUDA_TRY_OUT(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
         if (h->dtype == MLORA_BF16)
             launch_shadow_sync<bf16>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
         else
             launch_shadow_sync<float>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
         ++h->launches;
-        CUDA_TRY(cudaGetLastError());
-        CUDA_TRY(cudaDeviceSynchronize());
+        CUDA_TRY_OUT(cudaGetLastError());
+        CUDA_TRY_OUT(cudaDeviceSynchronize());
     }
+#undef CUDA_TRY_OUT
     *out = h;
     return MLORA_OK;
 fail_out:
