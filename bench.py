@@ -165,16 +165,31 @@ def adam_bytes(cfg, b):
     return 28.0 * n, n
 
 
-KERNEL_SOURCES = ("gemm_tc.cu", "gemm_common.cuh", "mlora_api.cu", "kernels_misc.cu")
+# Sources that determine the GEMM kernels and their launches: the kernel and
+# header files whole, and of the host code the span that builds the step's
+# launch descriptors (from the GEMM descriptor helpers to the first entry
+# point), so that a change elsewhere in the host code (create, checkpoints)
+# does not void the committed counters.
+KERNEL_SOURCES = ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh", "common.cuh", "internal.h",
+                  "kernels_misc.cu")
+LAUNCH_SPAN = ("mlora_api.cu", "// GEMM descriptor helpers", 'extern "C" int mlora_forward(')
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources that determine the GEMM kernels and their launches."""
+def kernel_source_hash(read=None) -> str:
+    """Hash of the sources that determine the GEMM kernels and their launches.
+    `read(name) -> bytes` reads a file of the kernel directory (default: the tree)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "rl_step_gb300", "csrc", name), "rb") as fh:
+                return fh.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "rl_step_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        h.update(read(name))
+    text = read(LAUNCH_SPAN[0])
+    a = text.index(LAUNCH_SPAN[1].encode())
+    b = text.index(LAUNCH_SPAN[2].encode(), a)
+    h.update(text[a:b])
     return h.hexdigest()
 
 
