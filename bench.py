@@ -202,7 +202,11 @@ def committed_traffic(workload: str, kernel: str, launches: int):
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_sha256") != kernel_source_hash():
+    try:
+        current = kernel_source_hash()
+    except (OSError, ValueError):          # a source or the launch span's markers are gone
+        return None
+    if rec.get("kernel_source_sha256") != current:
         return None
     k = rec.get("kernels", {}).get(kernel)
     if not k or k.get("launches_per_step") != launches:
