@@ -441,6 +441,9 @@ def run_ours(args, rank, world):
         kernels["lm_dz"]["achieved_gbs"] = zb * K / (prof["lm_dz"][0] * 1e-3) / 1e9
         kernels["lm_dz"]["frac_of_hbm"] = kernels["lm_dz"]["achieved_gbs"] / peaks["hbm_gbs"]
         kernels["lm_dz"]["bytes_per_step"] = zb
+        kernels["lm_dz"]["note"] = ("side stream, concurrent with the next chunk's LM-head GEMM: "
+                                    "ms_per_step is the span of its events under that overlap, "
+                                    "not its exclusive time (see the serialised ncu launch list)")
     if prof["loss"][0] > 0:
         lb = loss_epilogue_bytes(cfg, b)
         kernels["loss"]["achieved_gbs"] = lb * K / (prof["loss"][0] * 1e-3) / 1e9
