@@ -6,12 +6,14 @@ fails loudly if the compiled library is missing -- there is no fallback.
 
 The functions mirror the C entry points of include/mlora.h:
 
-    h = mlora_create(cfg, base, adapters, max_tokens)
+    h = mlora_create(V, d, f, L, "bf16"|"fp32", ranks, alphas, max_tokens,
+                     E, W1s, W2s, Wout, A1, B1, A2, B2)     # A1[a][l] ... fp32 factors
     mlora_forward(h, tokens, targets, adapter_ids)              -> logprobs
     mlora_forward_backward(h, tokens, targets, adapter_ids, kind, ...)
+                                                                -> (logprobs, loss per adapter)
     mlora_forward_backward_custom(h, tokens, targets, adapter_ids, dloss)
-    mlora_optim_step(h, lr=..., ...)                            -> skipped
-    mlora_save_state(h, path)
+    mlora_optim_step(h, lr=..., ...)                            -> skipped flags
+    mlora_save_state(h, path) / mlora_load_state(h, path, with_optimizer)
     mlora_destroy(h)
 
 Tensors passed in must be CUDA tensors of the documented dtype (int32 ids,
