@@ -301,21 +301,31 @@ extern "C" int mlora_sampler_create(mlora_t* trainer, int32_t n_slots, int64_t m
     SALLOC(s->status, sizeof(int));
     SALLOC(s->tile_counter, sizeof(int));
 #undef SALLOC
+    // a failure while the sampler is filled frees what it holds
+#define S_TRY_OUT(expr)                                                                  \
+    do {                                                                                 \
+        cudaError_t _e = (expr);                                                         \
+        if (_e != cudaSuccess) {                                                         \
+            rc = sfail(MLORA_E_CUDA, "%s failed: %s", #expr, cudaGetErrorString(_e));    \
+            goto fail_out;                                                               \
+        }                                                                                \
+    } while (0)
     {
         cudaStream_t st = 0;
         for (int l = 0; l < t.L; ++l) {
-            S_TRY(cudaMemsetAsync(s->A1[l], 0, SK * t.d * es, st));
-            S_TRY(cudaMemsetAsync(s->B1[l], 0, (size_t)t.f * SK * es, st));
-            S_TRY(cudaMemsetAsync(s->A2[l], 0, SK * t.f * es, st));
-            S_TRY(cudaMemsetAsync(s->B2[l], 0, (size_t)t.d * SK * es, st));
+            S_TRY_OUT(cudaMemsetAsync(s->A1[l], 0, SK * t.d * es, st));
+            S_TRY_OUT(cudaMemsetAsync(s->B1[l], 0, (size_t)t.f * SK * es, st));
+            S_TRY_OUT(cudaMemsetAsync(s->A2[l], 0, SK * t.f * es, st));
+            S_TRY_OUT(cudaMemsetAsync(s->B2[l], 0, (size_t)t.d * SK * es, st));
         }
-        S_TRY(cudaMemsetAsync(s->gamma, 0, sizeof(float) * n_slots, st));
-        S_TRY(cudaMemsetAsync(s->published_d, 0, sizeof(int) * n_slots, st));
-        S_TRY(cudaMemsetAsync(s->status, 0, sizeof(int), st));
-        S_TRY(cudaMemsetAsync(s->v1, 0, R * SK * es, st));
-        S_TRY(cudaMemsetAsync(s->v2, 0, R * SK * es, st));
-        S_TRY(cudaStreamSynchronize(st));
+        S_TRY_OUT(cudaMemsetAsync(s->gamma, 0, sizeof(float) * n_slots, st));
+        S_TRY_OUT(cudaMemsetAsync(s->published_d, 0, sizeof(int) * n_slots, st));
+        S_TRY_OUT(cudaMemsetAsync(s->status, 0, sizeof(int), st));
+        S_TRY_OUT(cudaMemsetAsync(s->v1, 0, R * SK * es, st));
+        S_TRY_OUT(cudaMemsetAsync(s->v2, 0, R * SK * es, st));
+        S_TRY_OUT(cudaStreamSynchronize(st));
     }
+#undef S_TRY_OUT
     *out = s;
     return MLORA_OK;
 fail_out:
