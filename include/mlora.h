@@ -12,7 +12,11 @@
  * boundary": W' = W + gamma B A); then an untied LM head Wout [V x d] and the
  * target-token logprob l_t = z[y_t] - logsumexp(z), z = Wout h (Tinker API
  * Implementation on TPUs, section 10.3-10.4: the [tokens x vocab] logits are
- * never stored; the backward recomputes them chunk by chunk).
+ * never stored whole).  The LM-head backward runs in chunks of at most 16,384
+ * rows and has two modes (mlora_set_lm_backward): by default it recomputes
+ * each chunk's logits with a second GEMM, as that section describes; on
+ * request it instead keeps each chunk's fp32 logits from the forward in a
+ * bounded buffer and reads them back.
  *
  * Conventions for every entry point:
  *  - Return value: MLORA_OK (0) or a negative MLORA_E_* code; the message of
@@ -360,6 +364,30 @@ int mlora_routing_noalloc(const int32_t* adapter_ids, int64_t n, int32_t n_adapt
  * The mode is a host-side flag read at each forward/backward launch; the
  * default is 0.  Errors: E_ARG (NULL handle, on not 0 or 1). */
 int mlora_set_deterministic(mlora_t* h, int32_t on);
+
+/* How the LM-head backward obtains each row chunk's logits (Tinker API
+ * Implementation on TPUs, section 10.4: fused linear cross-entropy, whose
+ * custom backward keeps only the hidden rows and recomputes one tile of
+ * logits at a time).  Both modes first run the LM-head forward and the loss
+ * epilogue, then walk the rows in chunks of at most 16,384:
+ *   MLORA_LM_RECOMPUTE (the default of a new handle): a second LM-head GEMM
+ *     over the chunk recomputes its logits and its epilogue writes
+ *     dz = g (onehot(y) - softmax(z)) into a bf16 chunk buffer, then
+ *     dh = dz Wout.  Extra device memory: one dz chunk buffer
+ *     (16,384 x Vpad base-dtype elements, 5 GB at V = 151,936 in bf16).
+ *   MLORA_LM_KEEP_LOGITS: the forward GEMM of each chunk also stores its fp32
+ *     logits; an elementwise pass turns them into dz on a side stream while
+ *     the next chunk's GEMMs run.  Saves the recompute GEMM (2 N V d FLOPs per
+ *     step) for two fp32 logit chunk buffers and a second dz buffer (25 GB
+ *     more at V = 151,936 in bf16).
+ * Both modes give bitwise the same logprobs, losses and gradients: the
+ * recomputed accumulator is the forward's, and dz is formed by the same
+ * arithmetic.  Selecting KEEP_LOGITS allocates its buffers (E_NOMEM if they do
+ * not fit; the handle then stays in RECOMPUTE); selecting RECOMPUTE frees
+ * them.  Synchronises the device.  Errors: E_ARG (NULL handle, unknown mode),
+ * E_NOMEM, E_CUDA. */
+enum { MLORA_LM_RECOMPUTE = 0, MLORA_LM_KEEP_LOGITS = 1 };
+int mlora_set_lm_backward(mlora_t* h, int32_t mode);
 
 /* Synchronise `stream`, then return and clear the device status word:
  * MLORA_OK, MLORA_E_RANGE or MLORA_E_TIMEOUT. */

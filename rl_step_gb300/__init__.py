@@ -33,14 +33,16 @@ __all__ = [
     "mlora_read_adapter", "mlora_write_adapter", "mlora_get_steps", "mlora_get_routing",
     "mlora_check_status", "mlora_routing_noalloc", "Sampler", "mlora_sampler_create",
     "mlora_sampler_publish", "mlora_sampler_logprobs", "mlora_sampler_sample",
-    "mlora_sampler_check_status", "mlora_set_deterministic", "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
-    "LOSS_KINDS", "TENSOR_IDS", "TILE_M", "MAX_RANK",
+    "mlora_sampler_check_status", "mlora_set_deterministic", "mlora_set_lm_backward",
+    "mlora_profile_enable", "mlora_profile_read", "PROF_CLASSES",
+    "LOSS_KINDS", "LM_BACKWARD_MODES", "TENSOR_IDS", "TILE_M", "MAX_RANK",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlora.so")
 TILE_M = 128
 MAX_RANK = 64
 LOSS_KINDS = {"cross_entropy": 0, "importance_sampling": 1, "ppo": 2}
+LM_BACKWARD_MODES = {"recompute": 0, "keep_logits": 1}
 TENSOR_IDS = {n: i for i, n in enumerate(
     ["A1", "B1", "A2", "B2", "gA1", "gB1", "gA2", "gB2",
      "mA1", "mB1", "mA2", "mB2", "vA1", "vB1", "vA2", "vB2"])}
@@ -115,6 +117,7 @@ _SIGNATURES = {
     "mlora_routing_noalloc": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_void_p]),
     "mlora_set_deterministic": (c_int32, [c_void_p, c_int32]),
+    "mlora_set_lm_backward": (c_int32, [c_void_p, c_int32]),
     "mlora_profile_enable": (c_int32, [c_void_p, c_int32]),
     "mlora_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_kernel_launches": (c_int64, [c_void_p]),
@@ -433,6 +436,11 @@ def mlora_check_status(h: Handle, stream=None) -> int:
 def mlora_set_deterministic(h: Handle, on: bool = True):
     """One gradient chunk per adapter: bitwise-reproducible gradients."""
     _check(_lib.mlora_set_deterministic(h.ptr, 1 if on else 0))
+
+
+def mlora_set_lm_backward(h: Handle, mode: str):
+    """LM-head backward mode: "recompute" (default) or "keep_logits"."""
+    _check(_lib.mlora_set_lm_backward(h.ptr, LM_BACKWARD_MODES[mode]))
 
 
 def mlora_profile_enable(h: Handle, on: bool = True):

@@ -37,8 +37,10 @@ enum EpiKind : int {
     EPI_F32 = 10,       // f32 = acc                                                (norm input grads)
     EPI_SWIGLU = 11,    // columns interleave 16 gate / 16 up: out0 = T(acc) (kept for the
                         // backward), out1[col/2 ..] = T(silu(gate) * up)             (gated MLP)
-    EPI_DSWIGLU = 12    // acc = d act; aux = the kept gate/up rows (interleaved as above):
+    EPI_DSWIGLU = 12,   // acc = d act; aux = the kept gate/up rows (interleaved as above):
                         // out0 = T(d gate | d up) in the same interleaved columns
+    EPI_LMDZ = 13       // acc = recomputed logits z: out0 = T(g (onehot(tgt) - exp(z - lse)))
+                        // for cols < V, 0 for V <= col < Vpad          (LM-head backward)
 };
 
 // Gate/up interleave of the fused gated-MLP projection: output column n of
@@ -63,6 +65,8 @@ struct EpiParams {
     int part_ld = 0;                // pitch of a row of partials (multiple of 4)
     int V = 0, Vpad = 0;
     int64_t out_row_shift = 0;      // output row = row + out_row_shift (chunk buffers)
+    const float* gv = nullptr;      // EPI_LMDZ: dL/dl per padded row
+    const float* lse = nullptr;     // EPI_LMDZ: log-sum-exp per padded row
     // adapter gradients
     float* grad = nullptr;
     const int64_t* grad_off = nullptr;  // per adapter element offset of this tensor
@@ -91,6 +95,12 @@ struct GemmParams {
     int group_m = 8;                  // raster band height (m-tiles) for L2 reuse
     int* tile_counter = nullptr;      // device int, tile scheduler of the CTA-pair kernel
     int force_bn64 = 0;               // run on the 128 x 64 single-CTA kernel whatever N is
+    // Test hook of the single-CTA kernel's bounded waits (mlk_test_gemm_withhold):
+    // CTA 0 skips the loads of K block test_withhold_kb of its first tile, so the
+    // MMA thread's wait for that stage gives up after test_wait_ns (0: the
+    // default bound).  -1: off.
+    int test_withhold_kb = -1;
+    unsigned long long test_wait_ns = 0;
     EpiParams ep;
 };
 
@@ -282,6 +292,27 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
             st.s = st.s * sc + sum;
             st.m = mn;
         }
+    } break;
+    case EPI_LMDZ: {
+        // The same arithmetic, in the same order, as the dz pass over kept fp32
+        // logits: the recomputed accumulator is bitwise the forward's, so both
+        // LM-head backward modes give the same dz.
+        const float gr = ep.gv[row];
+        float o[32];
+        if (gr == 0.f) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0.f;
+        } else {
+            const float lb = ep.lse[row] * LOG2E;
+            const int y = ep.tgt[row];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int v = col0 + j;
+                const float pr = exp2f(fmaf(acc[j], LOG2E, -lb));
+                o[j] = v < ep.V ? gr * ((v == y ? 1.f : 0.f) - pr) : 0.f;
+            }
+        }
+        store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, o);
     } break;
     case EPI_SHRINK_SEL: {
         const int sl = col0 / RP;

@@ -251,8 +251,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const TileCoord c = tile_coord<BN>(p, t);
                 const int m0 = c.mt * BM;
                 const int n0 = c.nt * BN;
+                const int withhold = (blockIdx.x == 0 && t == 0) ? p.test_withhold_kb : -1;
                 for (int kb = 0; kb < c.nkb && ok; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (kb == withhold) {   // test hook: this stage is never filled
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
                     mbar_expect_tx(fb, SL::STAGE_BYTES);
@@ -297,6 +302,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major);
             const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major);
+            const uint64_t full_limit = p.test_wait_ns ? p.test_wait_ns : TIMEOUT_NS;
             // stage-0 descriptors, advanced by additions to the start-address field
             // (see the CTA-pair kernel's MMA thread)
             const uint32_t sb0 = sbase + SL::A_BYTES;
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < c.nkb; ++kb) {
                     if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
-                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        !mbar_wait(bar_full + 8 * stage, phase, abort_flag, full_limit)) {
                         ok = false;
                         break;
                     }

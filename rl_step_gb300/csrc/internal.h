@@ -8,6 +8,10 @@
 
 namespace mlk {
 
+// Device allocation of every create call (cudaMalloc, with a test hook that
+// can make one chosen allocation fail).
+cudaError_t mlk_malloc(void** p, size_t bytes);
+
 // ---- GEMM engines ----------------------------------------------------------
 template <typename T> void launch_simt_gemm(const GemmParams& p, cudaStream_t s);
 // tcgen05 engine (bf16 only).  Returns cudaSuccess or the first error.

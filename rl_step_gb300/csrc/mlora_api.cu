@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <cmath>
 #include <string>
 #include <vector>
@@ -51,9 +52,12 @@ struct mlora {
     std::vector<int> ranks;
     std::vector<float> alphas;
     std::vector<void*> allocs;
+    std::vector<size_t> alloc_bytes;
     int64_t bytes = 0;
     int64_t launches = 0;
     int deterministic = 0;   // 1: one gradient chunk per adapter (fixed-order reductions)
+    int test_withhold_kb = -1;          // test hook, applied to the next single-CTA GEMM
+    unsigned long long test_wait_ns = 0;
 
     // frozen base
     void* E = nullptr;
@@ -84,9 +88,12 @@ struct mlora {
     float* part = nullptr;
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
-    void* dz[2] = {nullptr, nullptr};   // bf16 dz of a chunk of rows, double-buffered
-    float* zbuf[2] = {nullptr, nullptr};  // fp32 logits of a chunk of rows (backward)
-    // the dz pass of chunk i runs on `side` beside the next chunk's GEMMs
+    // LM-head backward (mlora_set_lm_backward).  Recompute: dz[0] only.  Kept
+    // logits: dz[0..1] and zbuf[0..1] double-buffered, the dz pass of chunk i
+    // on `side` beside the next chunk's GEMMs.
+    int lm_keep = 0;
+    void* dz[2] = {nullptr, nullptr};   // dz of a chunk of rows (base dtype)
+    float* zbuf[2] = {nullptr, nullptr};  // fp32 logits of a chunk of rows
     cudaStream_t side = nullptr;
     cudaEvent_t ev_comb[2] = {}, ev_dz[2] = {}, ev_dh[2] = {};
     double* val_row = nullptr;          // per padded row loss value
@@ -128,17 +135,52 @@ struct ProfScope {
     }
 };
 
+// Every device allocation of the library goes through here.  Test hook (not in
+// the public headers): mlk_test_fail_alloc_at(n) makes the allocation with
+// ordinal n (counted over the process, see mlk_test_alloc_calls) fail with
+// cudaErrorMemoryAllocation without calling the driver, so the create calls'
+// clean-up after a failed allocation can be exercised on any GPU.
+static std::atomic<int64_t> g_alloc_calls{0};
+static std::atomic<int64_t> g_fail_alloc_at{0};
+
+cudaError_t mlk::mlk_malloc(void** p, size_t bytes) {
+    const int64_t n = ++g_alloc_calls;
+    if (n == g_fail_alloc_at.load()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
+extern "C" int64_t mlk_test_alloc_calls(void) { return g_alloc_calls.load(); }
+extern "C" void mlk_test_fail_alloc_at(int64_t ordinal) { g_fail_alloc_at.store(ordinal); }
+
 static int dalloc(mlora_t* h, void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaError_t e = mlk_malloc(p, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *p = nullptr;
         return fail(MLORA_E_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
     }
     h->allocs.push_back(*p);
+    h->alloc_bytes.push_back(bytes);
     h->bytes += (int64_t)bytes;
     return MLORA_OK;
+}
+
+// Frees one allocation made by dalloc (the caller has synchronised the device).
+static void dfree(mlora_t* h, void** p) {
+    if (!*p) return;
+    for (size_t i = 0; i < h->allocs.size(); ++i)
+        if (h->allocs[i] == *p) {
+            cudaFree(*p);
+            h->bytes -= (int64_t)h->alloc_bytes[i];
+            h->allocs.erase(h->allocs.begin() + (ptrdiff_t)i);
+            h->alloc_bytes.erase(h->alloc_bytes.begin() + (ptrdiff_t)i);
+            break;
+        }
+    *p = nullptr;
 }
 
 template <typename P>
@@ -152,6 +194,7 @@ static int dalloc_t(mlora_t* h, P** p, size_t count) {
 static void free_all(mlora_t* h) {
     for (void* p : h->allocs) cudaFree(p);
     h->allocs.clear();
+    h->alloc_bytes.clear();
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
     h->ev.clear();
     for (int b = 0; b < 2; ++b) {
@@ -335,18 +378,17 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         ALLOCB(h->dub, (size_t)MP * f * es);
         ALLOCB(h->w1s, (size_t)MP * RP * es);
         ALLOCB(h->w2s, (size_t)MP * RP * es);
-        // LM head: partials, per-row scalars, and the bounded dz chunk buffer
+        // LM head: partials, per-row scalars, and the bounded dz chunk buffer of
+        // the recompute mode (the kept-logits mode adds its buffers on request)
         ALLOC(h->part, (size_t)MP * h->part_ld);
         ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
         ALLOC(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 128 ? h->max_tiles : 128;   // chunks of up to 16,384 rows
-        for (int b = 0; b < 2; ++b) {
-            ALLOCB(h->dz[b], (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
-            ALLOC(h->zbuf[b], (size_t)h->nc_tiles * TILE_M * h->Vpad);
-            if (cudaMemset(h->dz[b], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
-                rc = fail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
-                goto fail_out;
-            }
+        ALLOCB(h->dz[0], (size_t)h->nc_tiles * TILE_M * h->Vpad * es);
+        // columns V..Vpad of dz are never written by the GEMM epilogue: zero once
+        if (cudaMemset(h->dz[0], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * es) != cudaSuccess) {
+            rc = fail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
+            goto fail_out;
         }
         if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess) {
             h->side = nullptr;
@@ -476,6 +518,11 @@ template <typename T>
 static int run_gemm(mlora_t* h, GemmParams& p, cudaStream_t s, int cls) {
     ProfScope ps(h, s, cls);
     p.tile_counter = h->tile_counter;
+    if (h->use_tc && h->test_withhold_kb >= 0 && (p.N <= 64 || p.force_bn64)) {
+        p.test_withhold_kb = h->test_withhold_kb;
+        p.test_wait_ns = h->test_wait_ns;
+        h->test_withhold_kb = -1;
+    }
     if (h->use_tc) {
         cudaError_t e = launch_tc_gemm(p, s, h->num_sms, h->status);
         if (e != cudaSuccess) return fail(MLORA_E_CUDA, "tensor-core GEMM launch: %s", cudaGetErrorString(e));
@@ -604,12 +651,13 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_W2_FWD))) return rc;
         }
     }
-    // a6-a8 LM head.  Forward only: per-tile log-sum-exp partials and the
-    // target logit over all rows, then the combine + loss epilogue.  With the
-    // backward, chunk by chunk of rows: the same GEMM also keeps the chunk's
-    // fp32 logits, the combine finishes the chunk's rows, dz = g (onehot -
-    // softmax) is computed from the kept logits, and dh = dz Wout.
-    if (!backward) {
+    // a6-a8 LM head.  Forward: per-tile log-sum-exp partials and the target
+    // logit over all rows, then the combine + loss epilogue.  The backward
+    // walks the rows in chunks: by default each chunk's logits are recomputed
+    // by a second GEMM whose epilogue writes dz = g (onehot - softmax) into the
+    // chunk buffer, then dh = dz Wout; in the kept-logits mode the forward GEMM
+    // of each chunk also stores its fp32 logits and an elementwise pass forms dz.
+    if (!backward || !h->lm_keep) {
         {
             GemmParams p = dense_params(h, mt_upper, V, d);
             p.A = op_kmajor(h->hb[L], MP, d);
@@ -629,7 +677,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
             ++h->launches;
         }
-        return MLORA_OK;
+        if (!backward) return MLORA_OK;
     }
     // equal chunks (an even number of row tiles, for the CTA-pair GEMMs) of at
     // most nc_tiles tiles: no small last chunk whose GEMMs fill a wave poorly
@@ -638,6 +686,32 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     chunk = (chunk + 1) & ~1;
     if (chunk > h->nc_tiles) chunk = h->nc_tiles;
     const int nch = (mt_upper + chunk - 1) / chunk;
+    auto dh_params = [&](int c0, int cnt, const void* dzb) {
+        GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
+        p.mt_base = c0; p.mt_count = cnt;
+        p.A = op_kmajor(dzb, (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
+        p.B = op_mnmajor(h->Wout, V, d);
+        p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
+        return p;
+    };
+    if (!h->lm_keep) {
+        // recompute: chunk i's logits again, dz from them in the epilogue, dh
+        for (int c0 = 0; c0 < mt_upper; c0 += chunk) {
+            const int cnt = mt_upper - c0 < chunk ? mt_upper - c0 : chunk;
+            {
+                GemmParams p = dense_params(h, mt_upper, V, d);
+                p.mt_base = c0; p.mt_count = cnt;
+                p.A = op_kmajor(h->hb[L], MP, d);
+                p.B = op_kmajor(h->Wout, V, d);
+                p.ep.kind = EPI_LMDZ; p.ep.tgt = h->tgt_pad; p.ep.gv = h->gvec; p.ep.lse = h->lse;
+                p.ep.V = V; p.ep.Vpad = h->Vpad;
+                p.ep.out0 = h->dz[0]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+                if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
+            }
+            GemmParams p = dh_params(c0, cnt, h->dz[0]);
+            if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH))) return rc;
+        }
+    }
     // Chunk i uses logit / dz buffers i % 2.  The caller's stream runs
     //   LMfwd(0) comb(0) | LMfwd(1) comb(1) dh(0) | LMfwd(2) comb(2) dh(1) | ... dh(n-1)
     // and the side stream runs dz(i) after comb(i) (and after dh(i-2) has read
@@ -653,17 +727,13 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         chunk_rows(i, c0, cnt);
         const int buf = i & 1;
         CUDA_TRY(cudaStreamWaitEvent(s, h->ev_dz[buf], 0));
-        GemmParams p = dense_params(h, mt_upper, d, h->Vpad);
-        p.mt_base = c0; p.mt_count = cnt;
-        p.A = op_kmajor(h->dz[buf], (int64_t)h->nc_tiles * TILE_M, h->Vpad, 0, -(int64_t)c0 * TILE_M);
-        p.B = op_mnmajor(h->Wout, V, d);
-        p.ep.kind = EPI_STORE2; p.ep.f32 = h->dh32; p.ep.ldf = d; p.ep.out0 = h->dhb; p.ep.ld0 = d;
+        GemmParams p = dh_params(c0, cnt, h->dz[buf]);
         int r = run_gemm<T>(h, p, s, MLORA_PROF_LM_DH);
         if (r) return r;
         CUDA_TRY(cudaEventRecord(h->ev_dh[buf], s));
         return MLORA_OK;
     };
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < nch && h->lm_keep; ++i) {
         int c0, cnt;
         chunk_rows(i, c0, cnt);
         const int buf = i & 1;
@@ -695,11 +765,13 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         CUDA_TRY(cudaEventRecord(h->ev_dz[buf], h->side));
         if (i >= 1 && (rc = queue_dh(i - 1))) return rc;
     }
-    if ((rc = queue_dh(nch - 1))) return rc;
-    if (loss_out) {
-        ProfScope ps(h, s, MLORA_PROF_OTHER);
-        launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
-        ++h->launches;
+    if (h->lm_keep) {
+        if ((rc = queue_dh(nch - 1))) return rc;
+        if (loss_out) {
+            ProfScope ps(h, s, MLORA_PROF_OTHER);
+            launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
+            ++h->launches;
+        }
     }
 
     // a9-a11 layers in reverse
@@ -1098,6 +1170,46 @@ extern "C" int mlora_set_deterministic(mlora_t* h, int32_t on) {
     if (!h) return fail(MLORA_E_ARG, "NULL handle");
     if (on != 0 && on != 1) return fail(MLORA_E_ARG, "on must be 0 or 1");
     h->deterministic = on;
+    return MLORA_OK;
+}
+
+// Test hook (not in the public headers) of the bounded device waits: the next
+// single-CTA tensor-core GEMM this handle launches (the first LoRA shrink of a
+// step) leaves K block `kb` of CTA 0's first tile unloaded, and its MMA thread
+// gives up waiting for it after wait_ns nanoseconds.  No copy is in flight for
+// that stage, so the kernel raises the timeout status bit, drains what it did
+// issue, frees its tensor memory and returns; mlora_check_status then reports
+// MLORA_E_TIMEOUT.  kb must be below the GEMM's K blocks (d / 64) to fire.
+extern "C" int mlk_test_gemm_withhold(mlora_t* h, int32_t kb, int64_t wait_ns) {
+    if (!h || kb < 0 || wait_ns < 0) return fail(MLORA_E_ARG, "bad test-hook argument");
+    h->test_withhold_kb = kb;
+    h->test_wait_ns = (unsigned long long)wait_ns;
+    return MLORA_OK;
+}
+
+extern "C" int mlora_set_lm_backward(mlora_t* h, int32_t mode) {
+    if (!h) return fail(MLORA_E_ARG, "NULL handle");
+    if (mode != MLORA_LM_RECOMPUTE && mode != MLORA_LM_KEEP_LOGITS)
+        return fail(MLORA_E_ARG, "unknown LM-head backward mode %d", mode);
+    if (mode == h->lm_keep) return MLORA_OK;
+    CUDA_TRY(cudaDeviceSynchronize());   // no queued step may still use the buffers
+    const size_t rows = (size_t)h->nc_tiles * TILE_M;
+    if (mode == MLORA_LM_RECOMPUTE) {
+        dfree(h, &h->dz[1]);
+        for (int b = 0; b < 2; ++b) dfree(h, reinterpret_cast<void**>(&h->zbuf[b]));
+        h->lm_keep = 0;
+        return MLORA_OK;
+    }
+    int rc = dalloc(h, &h->dz[1], rows * h->Vpad * h->esize);
+    for (int b = 0; b < 2 && rc == MLORA_OK; ++b) rc = dalloc_t(h, &h->zbuf[b], rows * h->Vpad);
+    if (rc == MLORA_OK && cudaMemset(h->dz[1], 0, rows * h->Vpad * h->esize) != cudaSuccess)
+        rc = fail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
+    if (rc != MLORA_OK) {
+        dfree(h, &h->dz[1]);
+        for (int b = 0; b < 2; ++b) dfree(h, reinterpret_cast<void**>(&h->zbuf[b]));
+        return rc;
+    }
+    h->lm_keep = 1;
     return MLORA_OK;
 }
 

@@ -232,7 +232,7 @@ struct mlora_sampler {
 
 static int s_alloc(mlora_sampler_t* s, void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaError_t e = mlk_malloc(p, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *p = nullptr;

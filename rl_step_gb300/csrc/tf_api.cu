@@ -143,7 +143,7 @@ struct TfProf {
 
 int tf_alloc(mlora_tf_t* h, void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaError_t e = mlk_malloc(p, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *p = nullptr;

@@ -13,13 +13,18 @@ def dev(x, device="cuda"):
     return torch.from_numpy(x).to(device)
 
 
-def create_handle(cfg, base, ad, max_tokens):
+def create_handle(cfg, base, ad, max_tokens, lm_backward=None):
+    """A training handle; lm_backward ("recompute" / "keep_logits") selects the
+    LM-head backward mode (None keeps the library's default)."""
     import rl_step_gb300 as m
-    return m.mlora_create(cfg.vocab, cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.dtype, cfg.ranks,
-                          cfg.alphas, max_tokens, dev(base["E"]), [dev(w) for w in base["W1"]],
-                          [dev(w) for w in base["W2"]], dev(base["Wout"]),
-                          *[[[dev(x) for x in row] for row in ad[k]]
-                            for k in ("A1", "B1", "A2", "B2")])
+    h = m.mlora_create(cfg.vocab, cfg.d_model, cfg.d_ffn, cfg.n_layers, cfg.dtype, cfg.ranks,
+                       cfg.alphas, max_tokens, dev(base["E"]), [dev(w) for w in base["W1"]],
+                       [dev(w) for w in base["W2"]], dev(base["Wout"]),
+                       *[[[dev(x) for x in row] for row in ad[k]]
+                         for k in ("A1", "B1", "A2", "B2")])
+    if lm_backward is not None:
+        m.mlora_set_lm_backward(h, lm_backward)
+    return h
 
 
 def rel_fro(x, ref):

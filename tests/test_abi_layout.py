@@ -40,7 +40,8 @@ CONSTANTS = ["MLORA_TILE_M", "MLORA_MAX_RANK", "MLORA_CROSS_ENTROPY", "MLORA_IMP
              "MLORA_PPO", "MLORA_BF16", "MLORA_FP32", "MLORA_A1", "MLORA_B2", "MLORA_GRAD_A1",
              "MLORA_V_B2", "MLORA_TF_HEAD_DIM", "MLORA_TF_NPROJ", "MLORA_NOALLOC_MAX_TOKENS",
              "MLORA_NOALLOC_MAX_ADAPTERS", "MLORA_E_ARG", "MLORA_E_RANGE", "MLORA_E_CUDA",
-             "MLORA_E_NOMEM", "MLORA_E_TIMEOUT", "MLORA_E_IO", "MLORA_E_UNSUPPORTED"]
+             "MLORA_E_NOMEM", "MLORA_E_TIMEOUT", "MLORA_E_IO", "MLORA_E_UNSUPPORTED",
+             "MLORA_LM_RECOMPUTE", "MLORA_LM_KEEP_LOGITS"]
 
 
 def _resolve(path):
@@ -92,6 +93,8 @@ def test_binding_constants_match_the_header(c_layout):
     assert m.LOSS_KINDS == {"cross_entropy": c["MLORA_CROSS_ENTROPY"],
                             "importance_sampling": c["MLORA_IMPORTANCE_SAMPLING"],
                             "ppo": c["MLORA_PPO"]}
+    assert m.LM_BACKWARD_MODES == {"recompute": c["MLORA_LM_RECOMPUTE"],
+                                   "keep_logits": c["MLORA_LM_KEEP_LOGITS"]}
     assert m.TENSOR_IDS["A1"] == c["MLORA_A1"] and m.TENSOR_IDS["B2"] == c["MLORA_B2"]
     assert m.TENSOR_IDS["gA1"] == c["MLORA_GRAD_A1"] and m.TENSOR_IDS["vB2"] == c["MLORA_V_B2"]
     assert t.HEAD_DIM == c["MLORA_TF_HEAD_DIM"] and len(t.PROJ) == c["MLORA_TF_NPROJ"]

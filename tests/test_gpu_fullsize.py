@@ -20,6 +20,10 @@ from _gpu_util import create_handle, dev, rel_fro
 pytestmark = pytest.mark.gpu
 
 FULL = ["qwen3_4b_is", "qwen3_8b_ppo", "many_tenant_ce", "long_custom"]
+# the benchmark's LM-head mode on every workload, and the default (recompute)
+# mode on the 8B-width and the long-context workloads
+CASES = [(n, "keep_logits") for n in FULL] + [("qwen3_8b_ppo", "recompute"),
+                                               ("long_custom", "recompute")]
 N_SAMPLE = 384
 
 
@@ -55,8 +59,8 @@ def _sample(b, rng, n_sample):
     return np.array(sorted(set(pick) | set(int(x) for x in extra)), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_parity(name):
+@pytest.mark.parametrize("name,lm", CASES, ids=[f"{n}-{lm}" for n, lm in CASES])
+def test_full_size_sampled_parity(name, lm):
     import rl_step_gb300 as m
     cfg = wl.get_config(name)
     b = wl.make_batch(cfg)
@@ -80,23 +84,40 @@ def test_full_size_sampled_parity(name):
     s[S] = ell_S + b["sampler_noise"][S]
     s = s.astype(np.float32)
 
-    h = create_handle(cfg, base, ad, N)
+    h = create_handle(cfg, base, ad, N, lm_backward=lm)
     tok, tgt, ids = dev(b["tokens"]), dev(b["targets"]), dev(b["adapter_ids"])
     if cfg.loss == "custom":
-        lp, _ = m.mlora_forward_backward_custom(h, tok, tgt, ids, dev(g))
+        lp, loss = m.mlora_forward_backward_custom(h, tok, tgt, ids, dev(g))
         ref = o.forward_backward_custom(sub["tokens"], sub["targets"], sub["adapter_ids"], g[S])
+        kw = {"dloss": g[S]}
     elif cfg.loss == "cross_entropy":
-        lp, _ = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, weights=dev(w))
+        lp, loss = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, weights=dev(w))
         ref = o.forward_backward(sub["tokens"], sub["targets"], sub["adapter_ids"], cfg.loss,
                                  weights=w[S])
+        kw = {"weights": w[S]}
     else:
-        lp, _ = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, advantages=dev(A),
-                                         sampler_logprobs=dev(s), clip_eps=cfg.clip_eps)
+        lp, loss = m.mlora_forward_backward(h, tok, tgt, ids, cfg.loss, advantages=dev(A),
+                                            sampler_logprobs=dev(s), clip_eps=cfg.clip_eps)
         ref = o.forward_backward(sub["tokens"], sub["targets"], sub["adapter_ids"], cfg.loss,
                                  advantages=A[S], sampler_logprobs=s[S].astype(np.float64),
                                  clip_eps=cfg.clip_eps)
+        kw = {"advantages": A[S], "sampler_logprobs": s[S].astype(np.float64),
+              "clip_eps": cfg.clip_eps}
     assert m.mlora_check_status(h) == 0
     lp = lp.cpu().numpy()
+    # per-adapter loss sums: tokens outside S carry no loss, so the GPU's sums
+    # over the whole batch equal the oracle's over S (relative to sum |value|,
+    # since centred advantages make the sums cancel)
+    loss = loss.cpu().numpy()
+    val, _ = oracle.token_loss(cfg.loss, ref["logprobs"], **kw)
+    present_all = np.unique(b["adapter_ids"])
+    loss_err = 0.0
+    for a in present_all:
+        scale = np.abs(val[sub["adapter_ids"] == a]).sum()
+        if scale == 0:
+            assert loss[a] == 0.0
+        else:
+            loss_err = max(loss_err, abs(loss[a] - ref["loss_per_adapter"][a]) / scale)
     assert np.isfinite(lp).all()
     lp_err = float(np.max(np.abs(lp[S] - ref["logprobs"])))
     present = np.unique(sub["adapter_ids"])
@@ -118,8 +139,10 @@ def test_full_size_sampled_parity(name):
             for k in oracle.TENSORS:
                 x = m.mlora_read_adapter(h, int(a), l, k).cpu().numpy()
                 p_worst = max(p_worst, rel_fro(x, o.P[k][a][l]))
-    print(f"\n[{name} full N={N}, |S|={len(S)}, adapters in S={len(present)}] logprob max|err|="
-          f"{lp_err:.3e}; grad rel Fro max={worst:.3e}; post-Adam rel Fro max={p_worst:.3e}")
+    print(f"\n[{name} {lm} full N={N}, |S|={len(S)}, adapters in S={len(present)}] logprob "
+          f"max|err|={lp_err:.3e}; loss rel={loss_err:.3e}; grad rel Fro max={worst:.3e}; "
+          f"post-Adam rel Fro max={p_worst:.3e}")
     assert lp_err <= 2e-2
+    assert loss_err <= 1e-2
     assert worst <= 1e-2
     assert p_worst <= 1e-2

@@ -89,14 +89,15 @@ def _setup(name, n, overrides=None):
     return cfg, base, ad, b, o, s
 
 
+@pytest.mark.parametrize("lm", ["recompute", "keep_logits"])
 @pytest.mark.parametrize("name,n,overrides", CASES,
                          ids=[c[0] + ("_odd_k_blocks" if c[2] else "") for c in CASES])
-def test_step_parity(name, n, overrides):
+def test_step_parity(name, n, overrides, lm):
     import rl_step_gb300 as m
     cfg, base, ad, b, o, s = _setup(name, n, overrides)
     kind = cfg.loss
     N = len(b["tokens"])
-    h = create_handle(cfg, base, ad, N)
+    h = create_handle(cfg, base, ad, N, lm_backward=lm)
     lp, loss = run_gpu_step(h, b, kind, s)
     assert m.mlora_check_status(h) == 0
     ref = run_oracle_step(o, b, kind, s)
@@ -114,7 +115,7 @@ def test_step_parity(name, n, overrides):
     scale = np.array([np.abs(val[b["adapter_ids"] == a]).sum() for a in present])
     loss_err = float(np.max(np.abs(loss[present] - ref["loss_per_adapter"][present]) /
                             np.maximum(scale, 1e-30)))
-    print(f"\n[{name} N={N}] logprob max|err|={lp_err:.3e} (signal {np.max(np.abs(dev_ref)):.3e}, "
+    print(f"\n[{name} N={N} {lm}] logprob max|err|={lp_err:.3e} (signal {np.max(np.abs(dev_ref)):.3e}, "
           f"rel {rel_fro(dev_gpu, dev_ref):.3e}); loss rel={loss_err:.3e}; "
           f"grad rel Fro max={g_err:.3e} at {g_where}")
     assert lp_err <= LP_TOL[cfg.dtype]
@@ -143,6 +144,69 @@ def test_step_parity(name, n, overrides):
     assert p_err <= GRAD_TOL
     g_after, _ = grad_errors(h, o, present)
     assert g_after == 0.0                            # gradients consumed
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_lm_backward_modes_bitwise_equal(dtype):
+    """Recomputing each chunk's logits and keeping them from the forward give
+    bitwise the same logprobs, losses and gradients (the recompute GEMM's
+    accumulator is the forward's and dz is formed by the same arithmetic), over
+    a batch of three LM-head chunks.  Deterministic mode makes the gradient
+    reductions themselves repeatable (by default they meet in fp32 atomics in
+    arrival order).  The recompute handle holds less memory: no fp32 logit
+    chunks and one dz chunk buffer instead of two."""
+    import rl_step_gb300 as m
+    over = {"d_model": 256, "d_ffn": 512, "vocab": 1000} if dtype == "bf16" else \
+        {"d_model": 64, "d_ffn": 128, "vocab": 520, "dtype": "fp32"}
+    cfg = wl.get_config("qwen3_8b_ppo", **over)
+    base = wl.make_base_weights(cfg)
+    ad = wl.make_adapters(cfg)
+    b = wl.make_batch(cfg, 40000)
+    N = len(b["tokens"])
+    s = (np.full(N, -np.log(cfg.vocab)) + b["sampler_noise"]) if cfg.loss == "ppo" else None
+    res = {}
+    for lm in ("keep_logits", "recompute"):
+        h = create_handle(cfg, base, ad, N, lm_backward=lm)
+        m.mlora_set_deterministic(h, True)
+        lp, loss = run_gpu_step(h, b, cfg.loss, s)
+        assert m.mlora_check_status(h) == 0
+        grads = {(a, l, k): m.mlora_read_adapter(h, a, l, "g" + k).cpu().numpy()
+                 for a in range(cfg.n_adapters) for l in range(cfg.n_layers) for k in oracle.TENSORS}
+        res[lm] = (lp, loss, grads, h.device_bytes)
+        del h
+    lp_k, loss_k, g_k, bytes_k = res["keep_logits"]
+    lp_r, loss_r, g_r, bytes_r = res["recompute"]
+    assert np.array_equal(lp_k, lp_r)
+    assert np.array_equal(loss_k, loss_r)
+    assert any(x.any() for x in g_k.values())
+    for key in g_k:
+        assert np.array_equal(g_k[key], g_r[key]), key
+    es = 2 if cfg.dtype == "bf16" else 4
+    tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
+    assert tiles > 2 * 128                               # three LM-head chunks
+    rows, vpad = 128 * 128, (cfg.vocab + 63) // 64 * 64
+    assert bytes_k - bytes_r == rows * vpad * (es + 2 * 4)
+
+
+def test_lm_backward_mode_switch_frees_and_rejects():
+    """Switching modes allocates / frees the kept-logit buffers; an unknown mode
+    is E_ARG and leaves the handle as it was."""
+    import rl_step_gb300 as m
+    cfg, base, ad, b, o, _ = _setup("tiny_fp32", None)
+    h = create_handle(cfg, base, ad, len(b["tokens"]))
+    b0 = h.device_bytes
+    m.mlora_set_lm_backward(h, "keep_logits")
+    b1 = h.device_bytes
+    assert b1 > b0
+    m.mlora_set_lm_backward(h, "keep_logits")
+    assert h.device_bytes == b1
+    rc = m.load_library().mlora_set_lm_backward(h.ptr, 7)
+    assert rc == -1 and h.device_bytes == b1
+    m.mlora_set_lm_backward(h, "recompute")
+    assert h.device_bytes == b0
+    lp, _ = run_gpu_step(h, b, "cross_entropy")
+    ref = run_oracle_step(o, b, "cross_entropy")
+    assert np.max(np.abs(lp - ref["logprobs"])) <= 1e-4
 
 
 def test_tiny_two_steps_accumulate_and_custom_equals_ce():
