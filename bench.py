@@ -3,19 +3,27 @@
 
 A step is one pass of the whole hot path over one synthetic batch: routing,
 embedding, L LoRA-MLP blocks, LM head with the loss epilogue, the backward
-(LM head from the fp32 logits its forward keeps, the blocks in reverse,
-per-adapter gradient GEMMs) and the per-adapter Adam update.  Default workload: Qwen3-8B widths (V=151936,
-d=4096, f=12288, L=4), 32 rank-32 adapters with Zipf(1.1) traffic, 65,536
-tokens in sequences of 512-2048 tokens, PPO clip 0.2.
+(LM head chunk by chunk, the blocks in reverse, per-adapter gradient GEMMs)
+and the per-adapter Adam update.  Default workload: Qwen3-8B widths
+(V=151936, d=4096, f=12288, L=4), 32 rank-32 adapters with Zipf(1.1)
+traffic, 65,536 tokens in sequences of 512-2048 tokens, PPO clip 0.2.
+
+The LM-head backward has two modes (mlora_set_lm_backward): "keep_logits"
+(each chunk's fp32 logits kept from the forward; the headline by default,
+--lm-backward) and "recompute" (a second GEMM recomputes each chunk's
+logits; the library's default).  Both are timed; `lm_backward` reports the
+step time and device memory of each.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is device-timed throughput with the
 inputs resident in HBM (CUDA events on the launch stream, max over ranks);
 `e2e` is the same metric through the C-ABI with host buffers, the copies
-inside the timed region.  `roofline` reports the tcgen05 GEMM kernel family
-(algorithmic FLOPs only, timed live by per-launch CUDA events), `kernels` the
-per-class breakdown, `cpu_baseline` the CPU oracle on a bounded sample.
+inside the timed region.  The headline loop runs without instrumentation; a
+second loop of the same length records the library's per-launch CUDA events,
+from which `roofline` (the tcgen05 GEMM kernel family, algorithmic FLOPs
+only) and `kernels` (per-class breakdown) are taken.  `cpu_baseline` is the
+CPU oracle on a bounded sample.
 `--impl reference` times the CPU oracle itself (the reference arm).
 With N > 1 (torchrun) every rank runs an independent replica of the
 workload on its own GPU: the path has no cross-replica exchange in this
@@ -39,6 +47,11 @@ import numpy as np  # noqa: E402
 import workloads as wl  # noqa: E402
 
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 datasheet dense bf16 tensor-core peak (no sparsity), TFLOP/s, and the
+# dense bf16 rate of one SM's tensor cores per clock (FLOP), for the
+# clock-adjusted peak = SMs x rate x sampled median SM clock
+DATASHEET_BF16_TFLOPS = 2250.0
+BF16_FLOP_PER_CLK_SM = 8192
 TC_CLASSES = ("w1_fwd", "w2_fwd", "lm_fwd", "lm_dh", "w2_bwd", "w1_bwd")
 
 
@@ -66,6 +79,10 @@ def parse_args():
                     help="override the transformer row's layer count (profiling; not a bench value)")
     ap.add_argument("--deterministic", action="store_true",
                     help="batch-invariant mode: one gradient chunk per adapter")
+    ap.add_argument("--lm-backward", default="keep_logits", choices=["keep_logits", "recompute"],
+                    help="LM-head backward mode of the headline loop (the other mode is timed too)")
+    ap.add_argument("--no-other-lm-mode", action="store_true",
+                    help="skip timing the LM-head backward mode the headline does not use")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: override the block count (not a bench value)")
     ap.add_argument("--vocab", type=int, default=None,
@@ -268,6 +285,7 @@ def run_ours(args, rank, world):
                        cfg.alphas, N, dbase["E"], dbase["W1"], dbase["W2"], dbase["Wout"], *dad)
     if args.deterministic:
         m.mlora_set_deterministic(h, True)
+    m.mlora_set_lm_backward(h, args.lm_backward)
     torch.cuda.synchronize()
     del dbase, dad                      # the library holds its own copies
     torch.cuda.empty_cache()
@@ -311,32 +329,38 @@ def run_ours(args, rank, world):
         if dist is not None:
             dist.barrier()
 
-    # ---- device-timed region ------------------------------------------------
-    m.mlora_profile_read(h, reset=True)
-    m.mlora_profile_enable(h, True)
+    def timed_steps(n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # ---- device-timed region (no instrumentation) ----------------------------
     launches0 = h.kernel_launches
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
     barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms = timed_steps(args.steps)
     barrier()
     clk = clocks.stop()
-    m.mlora_profile_enable(h, False)
     launches = h.kernel_launches - launches0
-    prof = m.mlora_profile_read(h, reset=True)
-    ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, dev)
     status = m.mlora_check_status(h)
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
+
+    # ---- per-class timing: a second loop with the library's per-launch events
+    m.mlora_profile_read(h, reset=True)
+    m.mlora_profile_enable(h, True)
+    ms_prof = timed_steps(args.steps)
+    m.mlora_profile_enable(h, False)
+    prof = m.mlora_profile_read(h, reset=True)
 
     # ---- end-to-end through host buffers -------------------------------------
     e2e = None
@@ -400,6 +424,38 @@ def run_ours(args, rank, world):
                     "ms_per_step": pms, "tokens_per_s": N / (pms * 1e-3),
                     "cost_vs_step": pms / (ms / args.steps)}
 
+    # ---- the other LM-head backward mode --------------------------------------
+    fl = flop_model(cfg, b)
+    lm_modes = {args.lm_backward: {"ms_per_step": ms_max / args.steps,
+                                   "tokens_per_s": job_throughput(N, args.steps, world, ms_max),
+                                   "device_bytes": h.device_bytes, "headline": True}}
+    if not args.no_other_lm_mode:
+        other = "recompute" if args.lm_backward == "keep_logits" else "keep_logits"
+        m.mlora_set_lm_backward(h, other)
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        barrier()
+        oms = max_over_ranks(timed_steps(args.steps), dev)
+        if m.mlora_check_status(h) != 0:
+            raise RuntimeError(f"device status set in the {other} timing")
+        m.mlora_profile_read(h, reset=True)
+        m.mlora_profile_enable(h, True)
+        timed_steps(1)
+        m.mlora_profile_enable(h, False)
+        oprof = m.mlora_profile_read(h, reset=True)
+        lm_modes[other] = {"ms_per_step": oms / args.steps,
+                           "tokens_per_s": job_throughput(N, args.steps, world, oms),
+                           "device_bytes": h.device_bytes, "headline": False,
+                           "lm_ms_per_step": {c: oprof[c][0] for c in ("lm_fwd", "lm_dz", "lm_dh", "loss")}}
+        m.mlora_set_lm_backward(h, args.lm_backward)
+    for v in lm_modes.values():
+        v["frac_of_bf16_peak"] = fl["total"] / (v["ms_per_step"] * 1e-3) / 1e12 / \
+            load_peaks()[0]["bf16_tflops"]
+    lm_modes["note"] = ("recompute: a second LM-head GEMM per chunk (2 N V d executed FLOPs, not "
+                        "credited) and one dz chunk buffer; keep_logits: fp32 logits of each chunk "
+                        "kept from the forward, dz by an elementwise pass on a side stream")
+
     # ---- rows beyond the step (outside the timed region) ---------------------
     extras = None if args.no_extras else measure_next_rows(m, h, cfg, b, dev, stream)
 
@@ -414,14 +470,14 @@ def run_ours(args, rank, world):
     if extras:
         for k in ("sampler_decode", "export_merge"):
             extras[k]["frac_of_hbm"] = extras[k]["achieved_gbs"] / peaks["hbm_gbs"]
-    fl = flop_model(cfg, b)
     K = args.steps
     # dominant kernel: the CTA-pair tcgen05 GEMM, which carries every base and
     # LM-head GEMM (22 launches per step at L=4: 16 block GEMMs and 3 + 3
     # LM-head chunks).  Algorithmic FLOPs credit the base and LoRA-extension
     # GEMMs, the LM-head forward and dh; padding rows are executed work only.
-    tc_ms = sum(prof[c][0] for c in TC_CLASSES)
-    tc_launch = sum(prof[c][1] for c in TC_CLASSES)
+    tc_classes = TC_CLASSES + (("lm_dz",) if args.lm_backward == "recompute" else ())
+    tc_ms = sum(prof[c][0] for c in tc_classes)
+    tc_launch = sum(prof[c][1] for c in tc_classes)
     achieved = fl["tc256"] * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
     rows = padded_rows(cfg, b)
     exec_flops = fl["tc256"] * rows / max(1, N)
@@ -429,6 +485,7 @@ def run_ours(args, rank, world):
     peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     traffic = committed_traffic(cfg.name, "tc_gemm_pair_kernel", int(round(tc_launch / K)))
     step_ms = ms_max / K
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     adam_b, n_ad_params = adam_bytes(cfg, b)
     kernels = {c: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for c, v in prof.items()
                if v[1] > 0}
@@ -436,7 +493,7 @@ def run_ours(args, rank, world):
         kernels["adam"]["achieved_gbs"] = adam_b * K / (prof["adam"][0] * 1e-3) / 1e9
         kernels["adam"]["frac_of_hbm"] = kernels["adam"]["achieved_gbs"] / peaks["hbm_gbs"]
         kernels["adam"]["bytes_per_step"] = adam_b
-    if prof["lm_dz"][0] > 0:
+    if prof["lm_dz"][0] > 0 and args.lm_backward == "keep_logits":
         zb = lm_dz_bytes(cfg, b)
         kernels["lm_dz"]["achieved_gbs"] = zb * K / (prof["lm_dz"][0] * 1e-3) / 1e9
         kernels["lm_dz"]["frac_of_hbm"] = kernels["lm_dz"]["achieved_gbs"] / peaks["hbm_gbs"]
@@ -471,12 +528,25 @@ def run_ours(args, rank, world):
                    "deterministic": bool(args.deterministic)},
         "tflops_algorithmic": fl["total"] * K * world / (ms_max * 1e-3) / 1e12,
         "frac_of_bf16_peak": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "frac_of_bf16_peak_basis": {
+            "measured_burst": fl["total"] / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "measured_sustained": fl["total"] / (step_ms * 1e-3) / 1e12 /
+                                  peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+            "datasheet_dense_2250": fl["total"] / (step_ms * 1e-3) / 1e12 / DATASHEET_BF16_TFLOPS,
+            "clock_adjusted": (fl["total"] / (step_ms * 1e-3) / 1e12 /
+                               (BF16_FLOP_PER_CLK_SM * n_sms * clk["sm_mhz"] * 1e6 / 1e12))
+                              if clk.get("sm_mhz") else None,
+            "clock_adjusted_peak_tflops": (BF16_FLOP_PER_CLK_SM * n_sms * clk["sm_mhz"] * 1e6 / 1e12)
+                                          if clk.get("sm_mhz") else None},
+        "lm_backward": lm_modes,
         "roofline": {"kernel": "tc_gemm_pair_kernel<256,3,2,2> (base, LoRA-extension and LM-head GEMMs)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_tc,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
                      "frac": (achieved / peak_tc) if achieved else None, "traffic": traffic,
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                      "launches_per_step": tc_launch / K,
+                     "timed_in": "a second loop of the same steps with per-launch CUDA events "
+                                 f"({ms_prof / K:.2f} ms per step there, {step_ms:.2f} without)",
                      "algorithmic_flops_per_launch": fl["tc256"] / max(1.0, tc_launch / K),
                      "executed_tflops": executed},
         "kernels": kernels,
