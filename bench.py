@@ -75,6 +75,11 @@ def parse_args():
                     help="run only the transformer-block row and print it (profiling)")
     ap.add_argument("--tf-tokens", type=int, default=None,
                     help="override the transformer row's batch size (profiling; not a bench value)")
+    ap.add_argument("--tf-prefix", type=int, default=None,
+                    help="profiling: the first N tokens of the full-size batch (sequences keep "
+                         "their 512-2048 lengths; not a bench value)")
+    ap.add_argument("--tf-vocab", type=int, default=None,
+                    help="override the transformer row's vocabulary (profiling; not a bench value)")
     ap.add_argument("--tf-layers", type=int, default=None,
                     help="override the transformer row's layer count (profiling; not a bench value)")
     ap.add_argument("--deterministic", action="store_true",
@@ -600,9 +605,11 @@ def measure_transformer_row(args, dev, stream, peaks):
 
     import rl_step_gb300.transformer as t
     import workloads.transformer as wt
-    over = {k: v for k, v in (("n_layers", args.tf_layers),) if v}
+    over = {k: v for k, v in (("n_layers", args.tf_layers), ("vocab", args.tf_vocab)) if v}
     cfg = wt.get_tf_config("qwen3_8b_tf_ppo", **over)
     b = wt.make_tf_batch(cfg, args.tf_tokens)
+    if args.tf_prefix:
+        b = {k: (v[:args.tf_prefix] if isinstance(v, np.ndarray) else v) for k, v in b.items()}
     N = len(b["tokens"])
     base = wt.make_tf_base_weights(cfg)
     ad = wt.make_tf_adapters(cfg)

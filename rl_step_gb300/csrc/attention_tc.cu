@@ -59,6 +59,7 @@ struct AttnParams {
     // backward inputs / outputs
     const float* DT;       // [n_heads x ld_t]
     bf16* dqkv;            // [P x ld_qkv]: dQ, dK, dV in the columns of q, k, v
+    int* counter;          // item counter of the persistent kernels (zeroed before each launch)
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -80,6 +81,69 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     int ok = 1;
     if (lane == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// 2^x with subnormal results flushed to zero (ex2.approx.ftz): one MUFU
+// operation; softmax probabilities below 2^-126 do not matter.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Dynamic item scheduling of the persistent kernels.  The loading thread takes
+// item indices from a global counter (reset before each launch) and publishes
+// each through a RING-slot ring in shared memory (slot value, then an arrive
+// on the slot's "full" barrier, whose release orders the value before it);
+// every other role takes the items from the ring in the same order and frees
+// each slot on its "empty" barrier.  -1 ends the work.  Items are taken in
+// the order of the counter, so the CTAs that finish early take more work.
+constexpr int RING = 4;
+
+struct RingPos {
+    int slot = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void advance() {
+        if (++slot == RING) { slot = 0; ph ^= 1u; }
+    }
+};
+
+// Publish t (one thread).
+__device__ __forceinline__ bool ring_put(uint32_t full, uint32_t empty, volatile int* slots, RingPos& rp, int t,
+                                         volatile int* abort_flag) {
+    if (!mbar_wait(empty + 8 * rp.slot, rp.ph ^ 1u, abort_flag)) return false;
+    slots[rp.slot] = t;
+    mbar_arrive(full + 8 * rp.slot);
+    rp.advance();
+    return true;
+}
+
+// Take the next item (one thread).
+__device__ __forceinline__ bool ring_get(uint32_t full, uint32_t empty, const volatile int* slots, RingPos& rp, int& t,
+                                         volatile int* abort_flag) {
+    if (!mbar_wait(full + 8 * rp.slot, rp.ph, abort_flag)) return false;
+    t = slots[rp.slot];
+    mbar_arrive(empty + 8 * rp.slot);
+    rp.advance();
+    return true;
+}
+
+// Take the next item for a whole warp: lane 0 waits and frees the slot, the
+// warp learns the item.
+__device__ __forceinline__ bool ring_get_warp(uint32_t full, uint32_t empty, const volatile int* slots, RingPos& rp,
+                                              int& t, volatile int* abort_flag, int lane) {
+    int ok = 1, v = -1;
+    if (lane == 0) {
+        ok = mbar_wait(full + 8 * rp.slot, rp.ph, abort_flag) ? 1 : 0;
+        if (ok) {
+            v = slots[rp.slot];
+            mbar_arrive(empty + 8 * rp.slot);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    t = __shfl_sync(0xffffffffu, v, 0);
+    rp.advance();
+    return ok != 0;
 }
 
 // Store 32 consecutive bf16 values (a 64-byte piece of a K-major row) into a
@@ -139,17 +203,28 @@ __device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* ma
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// Forward.  CTA = (128-row query tile, two query heads of one key/value
+// Forward.  Work item = (128-row query tile, two query heads of one key/value
 // group); key tiles of 128 rows run from the first row of the tile's first
 // sequence up to the tile's last row and are loaded once for both heads.
-// Warps: 0 loads K, 1 loads Q and V, 2 issues the MMAs, 3-6 and 7-10 are the
-// softmax warpgroups of the two heads (one query row per thread; warp w reads
-// TMEM lanes 32 (w % 4) ..).  Per key
-// tile j and head h:  S_h = Q_h K_j^T (TMEM); the warpgroup takes the row max,
-// writes P_h = exp(S_h - m) in bf16 to shared memory; O_h += P_h V_j in TMEM.
-// The MMA warp issues head h's P V and then its next S as soon as that head's
-// P is ready, so the two warpgroups' softmax work alternates around the
-// tensor core.  The running max m of a row is raised (and O_h, l rescaled in
+// The kernel is persistent: one CTA per SM takes items from a global counter
+// in tile-major order (so the CTAs running together share K / V tiles in L2),
+// keeps its TMEM and barriers across items, and lets the next item's Q / K
+// loads and first scores overlap the current item's output store.  Barrier phases follow a running count of the key tiles this CTA
+// has processed.
+//
+// Warps: 0 loads K, 1 loads Q and V (K and V double-buffered), 2 issues the
+// MMAs, 3-6 and 7-10 are the softmax warpgroups of the two heads (one query
+// row per thread; warp w reads TMEM lanes 32 (w % 4) ..).  Per key tile j and
+// head h:  S_h = Q_h K_j^T into TMEM; the warpgroup reads the score row into
+// registers, takes its max, and writes P_h = exp(S_h - m) in bf16 back into
+// the first 64 columns of S_h; O_h += P_h V_j reads P_h from TMEM.  The MMA
+// thread issues head h's P V and right after it head h's next S (over the
+// same columns: the tensor core runs one thread's MMAs in issue order), so
+// while one warpgroup computes exponentials the tensor core works for the
+// other head, and the commit of the next S also tells the warpgroup that
+// O_h is stable.  For head width 128 a tile's exponentials (16 per clock per
+// SM) take as long as its MMAs, so the two alternate rather than wait on
+// each other.  The running max m of a row is raised (and O_h, l rescaled in
 // place) only when the tile's max exceeds it by more than 2^8 in exp2 units;
 // otherwise P is formed against the stale m (entries up to 2^8), which the
 // final O / l and log-sum-exp m + log2(l) account for exactly.
@@ -161,28 +236,54 @@ constexpr float RESCALE_LOG2 = 8.f;
 
 struct FwdSmem {
     static constexpr int Q0 = 0;                // Q of head 0, then head 1 (32 KB each)
-    static constexpr int K = 4 * BLK;
-    static constexpr int V0 = 6 * BLK;          // V of key tile j in stage j % 2 (32 KB each)
-    static constexpr int P0 = 10 * BLK;         // P of head 0, then head 1 (32 KB each)
-    static constexpr int BAR = 14 * BLK;
-    enum { Q_FULL = 0, K_FULL = 1, K_EMPTY = 2, V_FULL = 3, V_EMPTY = 5, S_FULL = 7, S_FREE = 9,
-           P_FULL = 11, O_DONE = 13, DRAIN = 15, NBARS = 16 };
-    static constexpr int MISC = BAR + NBARS * 8;
-    static constexpr int TOTAL = MISC + 16 + 1024;
+    static constexpr int K0 = 4 * BLK;          // K of key tile g in stage g % 2 (32 KB each)
+    static constexpr int V0 = 8 * BLK;          // V of key tile g in stage g % 2 (32 KB each)
+    static constexpr int BAR = 12 * BLK;
+    enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = 4, V_FULL = 6, V_EMPTY = 8, S_FULL = 10,
+           P_FULL = 12, O_DONE = 14, O_FREE = 16, DRAIN = 18, SCHED_FULL = 19, SCHED_EMPTY = 19 + RING,
+           NBARS = 19 + 2 * RING };
+    static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
+    static constexpr int TOTAL = MISC + 32 + 1024;
 };
 
-__global__ void __launch_bounds__(FWD_THREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
-    using SL = FwdSmem;
-    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
+// One forward work item: query tile, key/value group, the two heads, and the
+// key range [kstart, m0 + 128) in nt tiles.
+struct FwdItem {
+    int tile, g, h0, h1, m0, kstart, nt;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item) {
+    FwdItem it;
     const int grp = p.n_heads / p.n_kv;
     const int pairs = (grp + 1) / 2;                    // head pairs per key/value group
-    const int tile = blockIdx.x / (p.n_kv * pairs);
-    const int rest = blockIdx.x % (p.n_kv * pairs);
-    const int g = rest / pairs;
-    const int h0 = g * grp + 2 * (rest % pairs);
-    const int h1 = h0 + 1 < (g + 1) * grp ? h0 + 1 : h0;  // an odd group's last pair repeats its head
-    if (tile >= mt_valid) return;
+    it.tile = item / (p.n_kv * pairs);
+    const int rest = item % (p.n_kv * pairs);
+    it.g = rest / pairs;
+    it.h0 = it.g * grp + 2 * (rest % pairs);
+    it.h1 = it.h0 + 1 < (it.g + 1) * grp ? it.h0 + 1 : it.h0;  // an odd group's last pair repeats its head
+    it.m0 = it.tile * TB;
+    it.kstart = p.seq_start[it.m0];
+    it.nt = (it.m0 + TB - it.kstart + TB - 1) / TB;
+    return it;
+}
+
+// O (+)= P V: M = 128 query rows, N = 128 head columns, K = 128 keys; A = P
+// (bf16 pairs) in TMEM columns a_tmem .. a_tmem + 63, B = the row-major V tile
+// read MN-major.
+__device__ __forceinline__ void mma_pv_tmem(uint32_t d, uint32_t a_tmem, uint32_t v, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+    const uint64_t bd = mndesc(v);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ts(d, a_tmem + 32 * kb + 8 * kk, bd + 512 * kb + 128 * kk, id, (acc || kb || kk) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(FWD_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
+    using SL = FwdSmem;
+    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -190,15 +291,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int m0 = tile * TB;
-    const int kstart = p.seq_start[m0];
-    const int nt = (m0 + TB - kstart + TB - 1) / TB;
-    const int kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
+    // items in order; the valid tiles are a prefix of the tile-major order
+    const int pairs = (p.n_heads / p.n_kv + 1) / 2;
+    auto valid = [&](int item) -> bool { return item >= 0 && item < n_items && item / (p.n_kv * pairs) < mt_valid; };
+    if (blockIdx.x >= mt_valid * p.n_kv * pairs) return;   // more CTAs than items
 
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 1};
-        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        const int cnt[19] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
+        for (int i = 0; i < 19; ++i) mbar_init(bar(i), cnt[i]);
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(bar(SL::SCHED_FULL + i), 1);
+            mbar_init(bar(SL::SCHED_EMPTY + i), 10);   // Q/V loader, MMA thread, eight softmax warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -211,74 +316,136 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;   // S_h at columns 128 h, O_h at 256 + 128 h
+    const uint32_t tmem = *tmem_slot;   // S_h (and P_h over its first 64 columns) at 128 h, O_h at 256 + 128 h
     int dummy = 0;
 
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
-            for (int j = 0; j < nt; ++j) {
-                if (j > 0 && !mbar_wait(bar(SL::K_EMPTY), (uint32_t)((j - 1) & 1), abort_flag)) { ok = false; break; }
-                mbar_expect_tx(bar(SL::K_FULL), 2 * BLK);
-                load_tile128(sb + SL::K, &maps.rows128, bar(SL::K_FULL), kcol, kstart + j * TB);
-                if (j == nt - 1 && !mbar_wait(bar(SL::K_FULL), (uint32_t)(j & 1), (volatile int*)&dummy))
-                    ok = false;       // our last copy has landed
+            uint32_t gk = 0;                          // K tiles loaded by this CTA
+            int last[2] = {-1, -1};
+            RingPos rp;
+            while (ok) {
+                int item = atomicAdd(p.counter, 1);
+                if (!valid(item)) item = -1;
+                if (!ring_put(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const FwdItem it = fwd_item(p, item);
+                const int kcol = (p.n_heads + it.g) * HD;
+                for (int j = 0; j < it.nt; ++j, ++gk) {
+                    const int ks = gk & 1;
+                    const uint32_t kp = (gk >> 1) & 1u;
+                    if (!mbar_wait(bar(SL::K_EMPTY + ks), kp ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(bar(SL::K_FULL + ks), 2 * BLK);
+                    load_tile128(sb + SL::K0 + ks * 2 * BLK, &maps.rows128, bar(SL::K_FULL + ks), kcol,
+                                 it.kstart + j * TB);
+                    last[ks] = (int)kp;
+                }
             }
+            for (int ks = 0; ks < 2; ++ks)      // our copies have landed
+                if (last[ks] >= 0 && !mbar_wait(bar(SL::K_FULL + ks), (uint32_t)last[ks], (volatile int*)&dummy))
+                    ok = false;
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = true;
-            mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
-            load_tile128(sb + SL::Q0, &maps.rows128, bar(SL::Q_FULL), h0 * HD, m0);
-            load_tile128(sb + SL::Q0 + 2 * BLK, &maps.rows128, bar(SL::Q_FULL), h1 * HD, m0);
+            uint32_t gv = 0, nq = 0;                  // V tiles and Q tiles loaded
             int last[2] = {-1, -1};
-            for (int j = 0; j < nt; ++j) {
-                const int vs = j & 1;
-                const uint32_t vp = (uint32_t)((j >> 1) & 1);
-                if (!mbar_wait(bar(SL::V_EMPTY + vs), vp ^ 1u, abort_flag)) { ok = false; break; }
-                mbar_expect_tx(bar(SL::V_FULL + vs), 2 * BLK);
-                load_tile128(sb + SL::V0 + vs * 2 * BLK, &maps.rows128, bar(SL::V_FULL + vs), vcol, kstart + j * TB);
-                last[vs] = (int)vp;
+            RingPos rp;
+            while (ok) {
+                int item;
+                if (!ring_get(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const FwdItem it = fwd_item(p, item);
+                const int vcol = (p.n_heads + p.n_kv + it.g) * HD;
+                // the previous item's last scores have read Q
+                if (nq > 0 && !mbar_wait(bar(SL::Q_EMPTY), (nq - 1) & 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
+                load_tile128(sb + SL::Q0, &maps.rows128, bar(SL::Q_FULL), it.h0 * HD, it.m0);
+                load_tile128(sb + SL::Q0 + 2 * BLK, &maps.rows128, bar(SL::Q_FULL), it.h1 * HD, it.m0);
+                ++nq;
+                for (int j = 0; j < it.nt; ++j, ++gv) {
+                    const int vs = gv & 1;
+                    const uint32_t vp = (gv >> 1) & 1u;
+                    if (!mbar_wait(bar(SL::V_EMPTY + vs), vp ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(bar(SL::V_FULL + vs), 2 * BLK);
+                    load_tile128(sb + SL::V0 + vs * 2 * BLK, &maps.rows128, bar(SL::V_FULL + vs), vcol,
+                                 it.kstart + j * TB);
+                    last[vs] = (int)vp;
+                }
             }
             for (int vs = 0; vs < 2; ++vs)      // our copies have landed
                 if (last[vs] >= 0 && !mbar_wait(bar(SL::V_FULL + vs), (uint32_t)last[vs], (volatile int*)&dummy))
                     ok = false;
-            if (!mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy)) ok = false;
+            if (nq > 0 && !mbar_wait(bar(SL::Q_FULL), (nq - 1) & 1u, (volatile int*)&dummy)) ok = false;
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag) && mbar_wait(bar(SL::K_FULL), 0, abort_flag);
-            if (ok) {
+            bool ok = true;
+            uint32_t g0 = 0, nit = 0;                 // key tiles and items processed before this item
+            RingPos rp;
+            while (ok) {
+                int item;
+                if (!ring_get(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const int nt = fwd_item(p, item).nt;
+                // the item's first scores.  S_h last held the previous item's last P_h,
+                // whose P V was issued before (in order on the tensor core).
+                ok = mbar_wait(bar(SL::Q_FULL), nit & 1u, abort_flag) &&
+                     mbar_wait(bar(SL::K_FULL + (g0 & 1)), (g0 >> 1) & 1u, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
                 for (int hh = 0; hh < 2; ++hh) {
-                    mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K, false);
+                    mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K0 + (g0 & 1) * 2 * BLK, false);
                     umma_commit(bar(SL::S_FULL + hh));
                 }
-                umma_commit(bar(SL::K_EMPTY));
-            }
-            for (int j = 0; j < nt && ok; ++j) {
-                const uint32_t ph = (uint32_t)(j & 1);
-                const int vs = j & 1;
-                if (!mbar_wait(bar(SL::V_FULL + vs), (uint32_t)((j >> 1) & 1), abort_flag)) { ok = false; break; }
-                for (int hh = 0; hh < 2 && ok; ++hh) {
-                    if (!mbar_wait(bar(SL::P_FULL + hh), ph, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    // the next tile's scores before this P V: the softmax warps hold S_h
-                    // in registers already, and start on the next tile while P V runs
-                    if (j + 1 < nt) {
-                        if ((hh == 0 && !mbar_wait(bar(SL::K_FULL), ph ^ 1u, abort_flag)) ||
-                            !mbar_wait(bar(SL::S_FREE + hh), ph, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K, false);
-                        umma_commit(bar(SL::S_FULL + hh));
-                        if (hh == 1) umma_commit(bar(SL::K_EMPTY));
+                umma_commit(bar(SL::K_EMPTY + (g0 & 1)));
+                if (nt == 1) umma_commit(bar(SL::Q_EMPTY));
+                for (int j = 0; j < nt && ok; ++j) {
+                    const uint32_t g = g0 + j;
+                    const uint32_t ph = g & 1u;
+                    const int vs = g & 1, ks = (g + 1) & 1;
+                    if (!mbar_wait(bar(SL::V_FULL + vs), (g >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    if (j + 1 < nt && !mbar_wait(bar(SL::K_FULL + ks), ((g + 1) >> 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    mma_kmn(tmem + 256 + 128 * hh, sb + SL::P0 + hh * 2 * BLK, sb + SL::V0 + vs * 2 * BLK, j > 0);
-                    umma_commit(bar(SL::O_DONE + hh));
+                    for (int hh = 0; hh < 2 && ok; ++hh) {
+                        if (!mbar_wait(bar(SL::P_FULL + hh), ph, abort_flag)) { ok = false; break; }
+                        // O_h of the previous item has been read out
+                        if (j == 0 && nit > 0 && !mbar_wait(bar(SL::O_FREE + hh), (nit - 1) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_pv_tmem(tmem + 256 + 128 * hh, tmem + 128 * hh, sb + SL::V0 + vs * 2 * BLK, j > 0);
+                        if (j + 1 == nt) umma_commit(bar(SL::O_DONE + hh));
+                        if (j + 1 < nt) {
+                            // next scores over S_h / P_h: after this P V in issue order
+                            mma_kk(tmem + 128 * hh, sb + SL::Q0 + hh * 2 * BLK, sb + SL::K0 + ks * 2 * BLK, false);
+                            umma_commit(bar(SL::S_FULL + hh));
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(bar(SL::V_EMPTY + vs));
+                    if (j + 1 < nt) {
+                        umma_commit(bar(SL::K_EMPTY + ks));
+                        if (j + 2 == nt) umma_commit(bar(SL::Q_EMPTY));   // the item's last scores
+                    }
                 }
-                if (ok) umma_commit(bar(SL::V_EMPTY + vs));
+                g0 += nt;
+                ++nit;
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
@@ -286,113 +453,134 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
     } else {
         const int hh = (warp - 3) >> 2;                 // head slot of this warpgroup
-        const int h = hh ? h1 : h0;
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
-        const int i = m0 + r;
-        const int ss = p.seq_start[i];
         const uint32_t tS = tmem + ((uint32_t)(32 * q4) << 16) + 128 * hh;
         const uint32_t tO = tS + 256;
-        const uint32_t sP = sb + SL::P0 + hh * 2 * BLK;
         const float sc = p.scale * LOG2E;
-        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         uint32_t rr[32];
-        for (int j = 0; j < nt; ++j) {
-            const uint32_t ph = (uint32_t)(j & 1);
-            if (!warp_wait(bar(SL::S_FULL + hh), ph, abort_flag, lane)) { ok = false; break; }
-            tc_fence_after();
-            // the whole score row in registers (one TMEM pass); S_h is free for the
-            // next tile's scores as soon as it has landed
-            uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld32(tS, s0);
-            tmem_ld32(tS + 32, s1);
-            tmem_ld32(tS + 64, s2);
-            tmem_ld32(tS + 96, s3);
-            tmem_ld_wait_regs(s0);
-            tmem_ld_wait_regs(s1);
-            tmem_ld_wait_regs(s2);
-            tmem_ld_wait_regs(s3);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SL::S_FREE + hh));
-            const int key0 = kstart + j * TB;
-            // valid key columns of this row: [lo, hi]; a warp whose rows all see
-            // the whole tile takes the unmasked copy of the loops
-            const int lo = ss - key0, hi = i - key0;
-            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
-            float mx = -INFINITY;
-            auto row_max = [&](auto masked) {
-                auto chunk = [&](const uint32_t (&cur)[32], int c) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int idx = 32 * c + e;
-                        const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                        mx = fmaxf(mx, v ? __uint_as_float(cur[e]) * sc : -INFINITY);
-                    }
-                };
-                chunk(s0, 0);
-                chunk(s1, 1);
-                chunk(s2, 2);
-                chunk(s3, 3);
-            };
-            if (whole) row_max(std::false_type{});
-            else row_max(std::true_type{});
-            if (j > 0) {   // head h's previous P V is done: O_h is stable and P_h free
-                if (!warp_wait(bar(SL::O_DONE + hh), ph ^ 1u, abort_flag, lane)) { ok = false; break; }
-                tc_fence_after();
+        uint32_t g0 = 0, nit = 0;                       // key tiles and items processed before this item
+        RingPos rp;
+        while (ok) {
+            int item;
+            if (!ring_get_warp(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag, lane)) {
+                ok = false;
+                break;
             }
-            const bool raise = mx > m_run + RESCALE_LOG2;
-            const float alpha = raise ? exp2f(m_run - mx) : 1.f;
-            if (raise) m_run = mx;
-            float rs = 0.f;
-            auto write_p = [&](auto masked) {
-                auto chunk = [&](const uint32_t (&cur)[32], int c) {
-                    uint32_t w[16];
+            if (item < 0) break;
+            const FwdItem it = fwd_item(p, item);
+            const int h = hh ? it.h1 : it.h0;
+            const int i = it.m0 + r;
+            const int ss = p.seq_start[i];
+            const int nt = it.nt;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                const uint32_t ph = (g0 + j) & 1u;
+                // S_h of this tile; its commit also covers head h's previous P V, so
+                // O_h is stable and the P_h columns are free
+                if (!warp_wait(bar(SL::S_FULL + hh), ph, abort_flag, lane)) { ok = false; break; }
+                tc_fence_after();
+                const int key0 = it.kstart + j * TB;
+                // valid key columns of this row: [lo, hi]; a warp whose rows all see
+                // the whole tile takes the unmasked copy of the loops
+                const int lo = ss - key0, hi = i - key0;
+                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
+                // pass 1: the row max of the raw scores (the scale is positive, so
+                // scaling the max equals the max of the scaled scores), reading the
+                // row from TMEM 32 columns at a time, the next chunk in flight
+                float mx = -INFINITY;
+                {
+                    uint32_t ca[32], cb[32];
+                    auto chunk_max = [&](const uint32_t (&cur)[32], int c, auto masked) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int idx = 32 * c + e;
-                        const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                        const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
-                        // masked entries give exp2(-inf) = 0: no branch around the exponential
-                        const float p0 = exp2f(v0 ? fmaf(__uint_as_float(cur[e]), sc, -m_run) : -INFINITY);
-                        const float p1 = exp2f(v1 ? fmaf(__uint_as_float(cur[e + 1]), sc, -m_run) : -INFINITY);
-                        rs += p0 + p1;
-                        w[e >> 1] = pack_bf16x2(p0, p1);
+                        for (int e = 0; e < 32; ++e) {
+                            const int idx = 32 * c + e;
+                            const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                            mx = fmaxf(mx, v ? __uint_as_float(cur[e]) : -INFINITY);
+                        }
+                    };
+                    auto pass = [&](auto masked) {
+                        tmem_ld32(tS, ca);
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld32(tS + 32, cb);
+                        chunk_max(ca, 0, masked);
+                        tmem_ld_wait_regs(cb);
+                        tmem_ld32(tS + 64, ca);
+                        chunk_max(cb, 1, masked);
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld32(tS + 96, cb);
+                        chunk_max(ca, 2, masked);
+                        tmem_ld_wait_regs(cb);
+                        chunk_max(cb, 3, masked);
+                    };
+                    if (whole) pass(std::false_type{});
+                    else pass(std::true_type{});
+                }
+                mx *= sc;
+                const bool raise = mx > m_run + RESCALE_LOG2;
+                const float alpha = raise ? ex2_ftz(m_run - mx) : 1.f;
+                if (raise) m_run = mx;
+                // pass 2: P = exp2(scale s - m) in bf16, written over the first 64
+                // columns of S_h (bf16 pairs) after the chunk that held them is read
+                float rs = 0.f;
+                {
+                    uint32_t ca[32], cb[32];
+                    auto chunk_p = [&](const uint32_t (&cur)[32], int c, auto masked) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int idx = 32 * c + e;
+                            const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                            const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
+                            // masked entries give exp2(-inf) = 0: no branch around the exponential
+                            const float p0 = ex2_ftz(v0 ? fmaf(__uint_as_float(cur[e]), sc, -m_run) : -INFINITY);
+                            const float p1 = ex2_ftz(v1 ? fmaf(__uint_as_float(cur[e + 1]), sc, -m_run) : -INFINITY);
+                            rs += p0 + p1;
+                            w[e >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tS + 16 * c, w);     // keys 32 c .. 32 c + 31
+                    };
+                    auto pass = [&](auto masked) {
+                        tmem_ld32(tS, ca);
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld32(tS + 32, cb);
+                        chunk_p(ca, 0, masked);        // writes columns 0-15: chunk 0, already read
+                        tmem_ld_wait_regs(cb);
+                        tmem_ld32(tS + 64, ca);
+                        chunk_p(cb, 1, masked);        // columns 16-31: chunk 0
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld32(tS + 96, cb);
+                        chunk_p(ca, 2, masked);        // columns 32-47: chunk 1
+                        tmem_ld_wait_regs(cb);
+                        chunk_p(cb, 3, masked);        // columns 48-63: chunk 1
+                    };
+                    if (whole) pass(std::false_type{});
+                    else pass(std::true_type{});
+                }
+                // a raised max rescales O_h before this tile's P V accumulates into it
+                if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(tO + 32 * c, rr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                        tmem_st32(tO + 32 * c, rr);
                     }
-                    st_swizzled32(sP + (c >> 1) * BLK, r, (c & 1) * 4, w);
-                };
-                chunk(s0, 0);
-                chunk(s1, 1);
-                chunk(s2, 2);
-                chunk(s3, 3);
-            };
-            if (whole) write_p(std::false_type{});
-            else write_p(std::true_type{});
-            // a raised max rescales O_h before this tile's P V accumulates into it
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tO + 32 * c, rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(tO + 32 * c, rr);
                 }
                 tmem_st_wait();
+                l_run = l_run * alpha + rs;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::P_FULL + hh));
             }
-            l_run = l_run * alpha + rs;
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SL::P_FULL + hh));
-        }
-        if (ok) ok = warp_wait(bar(SL::O_DONE + hh), (uint32_t)((nt - 1) & 1), abort_flag, lane);
-        if (ok) {
+            if (ok) ok = warp_wait(bar(SL::O_DONE + hh), nit & 1u, abort_flag, lane);
+            if (!ok) break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             bf16* dst = p.o + (int64_t)i * p.n_heads * HD + h * HD;
-            const bool store = hh == 0 || h1 != h0;
+            const bool store = hh == 0 || it.h1 != it.h0;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 tmem_ld32(tO + 32 * c, rr);
@@ -403,7 +591,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 if (store) store32<bf16>(dst + 32 * c, t);
             }
             if (store) p.lseT[(int64_t)h * p.ld_t + i] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
-        } else if (lane == 0) {
+            // O_h has been read: the next item's first P V may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SL::O_FREE + hh));
+            g0 += nt;
+            ++nit;
+        }
+        if (!ok && lane == 0) {
             atomicOr(status, ST_TIMEOUT);
             *abort_flag = 1;
         }
@@ -417,7 +612,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// Backward, key side.  CTA = (128-row key tile, key/value head g).  For every
+// Backward, key side.  Work item = (128-row key tile, key/value head g).  For every
 // query head of the group and every query tile that can see these keys, in
 // two halves of 64 query rows:
 //   S^T = K Q^T, dP^T = V dO^T                   (TMEM, two buffers)
@@ -439,9 +634,10 @@ struct KvSmem {
     static constexpr int VEC0 = 12 * BLK;        // stage s: lse[128] (log2 units), D[128], seq_start[128]
     static constexpr int BAR = VEC0 + 2 * 3 * 512;
     enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 7, PT_DONE = 9, ACC_FULL = 11,
-           DRAIN = 12, NBARS = 13 };
-    static constexpr int MISC = BAR + NBARS * 8;
-    static constexpr int TOTAL = MISC + 16 + 1024;
+           DRAIN = 12, KV_EMPTY = 13, ACC_FREE = 14, SCHED_FULL = 15, SCHED_EMPTY = 15 + RING,
+           NBARS = 15 + 2 * RING };
+    static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
+    static constexpr int TOTAL = MISC + 32 + 1024;
 };
 
 // D = A B^T, M = 128, N = 64, K = 128: A a K-major 128-row tile, B 64 rows
@@ -466,12 +662,36 @@ __device__ __forceinline__ void mma_t64mn(uint32_t d, uint32_t a_tmem, uint32_t 
         umma_bf16_ts(d, a_tmem + 8 * kk, bd + 128 * kk, id, (acc || kk) ? 1u : 0u);
 }
 
+// Key-side work item: key tile kt of key/value head g; the query tiles
+// kt .. kt + nqt - 1 are those whose first row starts its sequence at or
+// before this tile's last key, taken for every query head of the group.
+struct KvItem {
+    int kt, g, k0, nqt, niter;
+};
+
+__device__ __forceinline__ KvItem kv_item(const AttnParams& p, int item, int mt_valid) {
+    KvItem it;
+    it.kt = item / p.n_kv;
+    it.g = item % p.n_kv;
+    it.k0 = it.kt * TB;
+    int nqt = 0;
+    while (it.kt + nqt < mt_valid && p.seq_start[(it.kt + nqt) * TB] <= it.k0 + TB - 1) ++nqt;
+    it.nqt = nqt;
+    it.niter = (p.n_heads / p.n_kv) * nqt;
+    return it;
+}
+
+// Persistent: one CTA per SM takes items (key tile * n_kv + head) from the
+// global counter, keeping TMEM and barriers; barrier
+// phases follow running counts of query tiles and halves.  The next item's
+// K / V load starts once the current item's last scores are issued, and its
+// first products overlap the read-out of the current dK / dV.
 __global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_bwd_kv_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
+    attn_bwd_kv_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
     using SL = KvSmem;
     const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
-    const int kt = blockIdx.x / p.n_kv, g = blockIdx.x % p.n_kv;
-    if (kt >= mt_valid) return;
+    auto valid = [&](int item) -> bool { return item >= 0 && item < n_items && item / p.n_kv < mt_valid; };
+    if (blockIdx.x >= mt_valid * p.n_kv) return;   // more CTAs than items
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -479,20 +699,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int k0 = kt * TB;
     const int grp = p.n_heads / p.n_kv;
-    const int kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
-    // query tiles kt .. kt + nqt - 1: the first row of each starts its
-    // sequence at or before this tile's last key
-    int nqt = 0;
-    while (kt + nqt < mt_valid && p.seq_start[(kt + nqt) * TB] <= k0 + TB - 1) ++nqt;
-    const int niter = grp * nqt;          // query tiles (head, tile); two halves each
-    const int nhalf = 2 * niter;
 
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
-        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 4};
+        for (int i = 0; i < 15; ++i) mbar_init(bar(i), cnt[i]);
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(bar(SL::SCHED_FULL + i), 1);
+            mbar_init(bar(SL::SCHED_EMPTY + i), 5);    // MMA thread, four softmax warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -514,142 +730,200 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (lane == 0) {
             bool ok = true;
             int last[2] = {-1, -1};
-            mbar_expect_tx(bar(SL::KV_FULL), 4 * BLK);
-            load_tile128(sb + SL::K, &maps.rows128, bar(SL::KV_FULL), kcol, k0);
-            load_tile128(sb + SL::V, &maps.rows128, bar(SL::KV_FULL), vcol, k0);
-            for (int n = 0; n < niter; ++n) {
-                const int s = n & 1;
-                const uint32_t sp = (uint32_t)((n >> 1) & 1);
-                const int h = g * grp + n / nqt, q0 = (kt + n % nqt) * TB;
-                if (!mbar_wait(bar(SL::QD_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
-                const uint32_t fb = bar(SL::QD_FULL + s);
-                const uint32_t st = sb + SL::Q0 + s * 4 * BLK, vec = sb + SL::VEC0 + s * 1536;
-                mbar_expect_tx(fb, 4 * BLK + 3 * 512);
-                load_tile128(st, &maps.rows128, fb, h * HD, q0);
-                load_tile128(st + 2 * BLK, &maps.do128, fb, h * HD, q0);
-                bulk_load(vec, p.lseT + (int64_t)h * p.ld_t + q0, 512, fb);
-                bulk_load(vec + 512, p.DT + (int64_t)h * p.ld_t + q0, 512, fb);
-                bulk_load(vec + 1024, p.seq_start + q0, 512, fb);
-                last[s] = (int)sp;
+            uint32_t nkv = 0, gn = 0;                  // K / V tiles and query tiles loaded
+            RingPos rp;
+            while (ok) {
+                int item = atomicAdd(p.counter, 1);
+                if (!valid(item)) item = -1;
+                if (!ring_put(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const KvItem it = kv_item(p, item, mt_valid);
+                const int kcol = (p.n_heads + it.g) * HD, vcol = (p.n_heads + p.n_kv + it.g) * HD;
+                // the previous item's last scores have read K and V
+                if (nkv > 0 && !mbar_wait(bar(SL::KV_EMPTY), (nkv - 1) & 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::KV_FULL), 4 * BLK);
+                load_tile128(sb + SL::K, &maps.rows128, bar(SL::KV_FULL), kcol, it.k0);
+                load_tile128(sb + SL::V, &maps.rows128, bar(SL::KV_FULL), vcol, it.k0);
+                ++nkv;
+                for (int n = 0; n < it.niter; ++n, ++gn) {
+                    const int s = gn & 1;
+                    const uint32_t sp = (gn >> 1) & 1u;
+                    const int h = it.g * grp + n / it.nqt, q0 = (it.kt + n % it.nqt) * TB;
+                    if (!mbar_wait(bar(SL::QD_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = bar(SL::QD_FULL + s);
+                    const uint32_t st = sb + SL::Q0 + s * 4 * BLK, vec = sb + SL::VEC0 + s * 1536;
+                    mbar_expect_tx(fb, 4 * BLK + 3 * 512);
+                    load_tile128(st, &maps.rows128, fb, h * HD, q0);
+                    load_tile128(st + 2 * BLK, &maps.do128, fb, h * HD, q0);
+                    bulk_load(vec, p.lseT + (int64_t)h * p.ld_t + q0, 512, fb);
+                    bulk_load(vec + 512, p.DT + (int64_t)h * p.ld_t + q0, 512, fb);
+                    bulk_load(vec + 1024, p.seq_start + q0, 512, fb);
+                    last[s] = (int)sp;
+                }
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
-            bool dr = mbar_wait(bar(SL::KV_FULL), 0, (volatile int*)&dummy);
+            bool dr = nkv == 0 || mbar_wait(bar(SL::KV_FULL), (nkv - 1) & 1u, (volatile int*)&dummy);
             for (int s = 0; s < 2; ++s)
                 if (last[s] >= 0) dr &= mbar_wait(bar(SL::QD_FULL + s), (uint32_t)last[s], (volatile int*)&dummy);
             if (!dr) atomicOr(status, ST_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // half m: query tile n = m / 2 in stage n & 1, rows 64 (m & 1) .., TMEM buffer m & 1
-            auto issue_s = [&](int m) -> bool {
-                const int n = m >> 1, b = m & 1;
-                const uint32_t st = sb + SL::Q0 + (n & 1) * 4 * BLK;
-                if (b == 0 && !mbar_wait(bar(SL::QD_FULL + (n & 1)), (uint32_t)((n >> 1) & 1), abort_flag)) return false;
-                if (m >= 2 && !mbar_wait(bar(SL::PT_DONE + b), (uint32_t)(((m >> 1) - 1) & 1), abort_flag)) return false;
-                tc_fence_after();
-                mma_kk64(tmem + 64 * b, sb + SL::K, st, b);
-                mma_kk64(tmem + 128 + 64 * b, sb + SL::V, st + 2 * BLK, b);
-                umma_commit(bar(SL::ST_FULL + b));
-                return true;
-            };
-            bool ok = mbar_wait(bar(SL::KV_FULL), 0, abort_flag) && (nhalf == 0 || issue_s(0));
-            for (int m = 0; m < nhalf && ok; ++m) {
-                const int n = m >> 1, b = m & 1;
-                const uint32_t st = sb + SL::Q0 + (n & 1) * 4 * BLK;
-                if (m + 1 < nhalf && !issue_s(m + 1)) { ok = false; break; }
-                if (!mbar_wait(bar(SL::P_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                mma_t64mn(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
-                mma_t64mn(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
-                umma_commit(bar(SL::PT_DONE + b));
-                if (b == 1) umma_commit(bar(SL::QD_EMPTY + (n & 1)));
+            bool ok = true;
+            uint32_t gm = 0, gn0 = 0, nit = 0;        // halves, query tiles and items before this item
+            RingPos rp;
+            while (ok) {
+                int item;
+                if (!ring_get(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const KvItem it = kv_item(p, item, mt_valid);
+                const int nhalf = 2 * it.niter;        // >= 2: the key tile's own query tile
+                // half m: query tile gn0 + m / 2 in stage (gn0 + m / 2) & 1, rows 64 (m & 1) ..,
+                // TMEM buffer m & 1 (gm is even)
+                auto issue_s = [&](int m) -> bool {
+                    const uint32_t M = gm + m, N = gn0 + (m >> 1);
+                    const int b = m & 1;
+                    const uint32_t st = sb + SL::Q0 + (N & 1) * 4 * BLK;
+                    if (b == 0 && !mbar_wait(bar(SL::QD_FULL + (N & 1)), (N >> 1) & 1u, abort_flag)) return false;
+                    if (M >= 2 && !mbar_wait(bar(SL::PT_DONE + b), ((M >> 1) - 1) & 1u, abort_flag)) return false;
+                    tc_fence_after();
+                    mma_kk64(tmem + 64 * b, sb + SL::K, st, b);
+                    mma_kk64(tmem + 128 + 64 * b, sb + SL::V, st + 2 * BLK, b);
+                    umma_commit(bar(SL::ST_FULL + b));
+                    return true;
+                };
+                ok = mbar_wait(bar(SL::KV_FULL), nit & 1u, abort_flag) && issue_s(0);
+                for (int m = 0; m < nhalf && ok; ++m) {
+                    const uint32_t M = gm + m, N = gn0 + (m >> 1);
+                    const int b = m & 1;
+                    const uint32_t st = sb + SL::Q0 + (N & 1) * 4 * BLK;
+                    if (m + 1 < nhalf) {
+                        if (!issue_s(m + 1)) { ok = false; break; }
+                        if (m + 2 == nhalf) umma_commit(bar(SL::KV_EMPTY));   // the item's last scores
+                    }
+                    if (!mbar_wait(bar(SL::P_FULL + b), (M >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    // dV / dK of the previous item have been read out
+                    if (m == 0 && nit > 0 && !mbar_wait(bar(SL::ACC_FREE), (nit - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_t64mn(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
+                    mma_t64mn(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
+                    umma_commit(bar(SL::PT_DONE + b));
+                    if (b == 1) umma_commit(bar(SL::QD_EMPTY + (N & 1)));
+                }
+                if (!ok) break;
+                umma_commit(bar(SL::ACC_FULL));
+                gm += nhalf;
+                gn0 += it.niter;
+                ++nit;
             }
-            if (ok) umma_commit(bar(SL::ACC_FULL));
-            else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
     } else {
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
-        const int j = k0 + r;                          // this thread's key row
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
         uint32_t ra[32], rb[32], ra2[32], rb2[32];
-        int qmin = 0, qmax = -1;
-        for (int m = 0; m < nhalf; ++m) {
-            const int n = m >> 1, b = m & 1, s = n & 1;
-            const int q0 = (kt + n % nqt) * TB;
-            const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC0 + s * 1536);
-            const float* D_s = lse_s + 128;
-            const int* ss_s = reinterpret_cast<const int*>(lse_s + 256);
-            if (b == 0) {
-                if (!warp_wait(bar(SL::QD_FULL + s), (uint32_t)((n >> 1) & 1), abort_flag, lane)) { ok = false; break; }
-                // valid query columns of this key row: [qmin, qmax] -- queries at or
-                // after it whose sequence starts at or before it (sequence starts do
-                // not decrease along the tile, so the second condition is a prefix)
-                qmin = j - q0;
-                qmax = -1;
-                if (ss_s[0] <= j) {
-                    int a = 0, c = TB - 1;
-                    while (a < c) {
-                        const int mid = (a + c + 1) >> 1;
-                        if (ss_s[mid] <= j) a = mid; else c = mid - 1;
-                    }
-                    qmax = a;
-                }
+        uint32_t gm = 0, gn0 = 0, nit = 0;
+        RingPos rp;
+        while (ok) {
+            int item;
+            if (!ring_get_warp(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag, lane)) {
+                ok = false;
+                break;
             }
-            if (!warp_wait(bar(SL::ST_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag, lane)) { ok = false; break; }
-            tc_fence_after();
-            const int lo = qmin - 64 * b, hi = qmax - 64 * b;      // in this half's columns
-            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
-            auto write_pd = [&](auto masked) {
-                tmem_ld32(tl + 64 * b, ra);
-                tmem_ld32(tl + 128 + 64 * b, rb);
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
-                    uint32_t (&ca)[32] = c ? ra2 : ra;
-                    uint32_t (&cb)[32] = c ? rb2 : rb;
-                    tmem_ld_wait_regs(ca);
-                    tmem_ld_wait_regs(cb);
-                    if (c == 0) {
-                        tmem_ld32(tl + 64 * b + 32, ra2);
-                        tmem_ld32(tl + 128 + 64 * b + 32, rb2);
-                    }
-                    uint32_t wp[16], wd[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        // the query columns' lse and D, four at a time (same address in every lane)
-                        const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 64 * b + 32 * c + e);
-                        const float4 d4 = *reinterpret_cast<const float4*>(D_s + 64 * b + 32 * c + e);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pr[4], ds[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int qc = 32 * c + e + u;
-                            const bool valid = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
-                            pr[u] = exp2f(valid ? fmaf(__uint_as_float(ca[e + u]), sc, -lv[u]) : -INFINITY);
-                            ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - dv[u]);
+            if (item < 0) break;
+            const KvItem it = kv_item(p, item, mt_valid);
+            const int j = it.k0 + r;                       // this thread's key row
+            const int kcol = (p.n_heads + it.g) * HD, vcol = (p.n_heads + p.n_kv + it.g) * HD;
+            const int nhalf = 2 * it.niter;
+            int qmin = 0, qmax = -1;
+            for (int m = 0; m < nhalf; ++m) {
+                const int n = m >> 1, b = m & 1;
+                const uint32_t M = gm + m, N = gn0 + n;
+                const int s = N & 1;
+                const int q0 = (it.kt + n % it.nqt) * TB;
+                const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC0 + s * 1536);
+                const float* D_s = lse_s + 128;
+                const int* ss_s = reinterpret_cast<const int*>(lse_s + 256);
+                if (b == 0) {
+                    if (!warp_wait(bar(SL::QD_FULL + s), (N >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
+                    // valid query columns of this key row: [qmin, qmax] -- queries at or
+                    // after it whose sequence starts at or before it (sequence starts do
+                    // not decrease along the tile, so the second condition is a prefix)
+                    qmin = j - q0;
+                    qmax = -1;
+                    if (ss_s[0] <= j) {
+                        int a = 0, c = TB - 1;
+                        while (a < c) {
+                            const int mid = (a + c + 1) >> 1;
+                            if (ss_s[mid] <= j) a = mid; else c = mid - 1;
                         }
-                        wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
-                        wp[(e >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-                        wd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
+                        qmax = a;
                     }
-                    tmem_st16(tl + 64 * b + 16 * c, wp);           // over columns already read
-                    tmem_st16(tl + 128 + 64 * b + 16 * c, wd);
                 }
-            };
-            if (whole) write_pd(std::false_type{});
-            else write_pd(std::true_type{});
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SL::P_FULL + b));
-        }
-        if (ok && nhalf > 0) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
-        if (ok && nhalf > 0) {
+                if (!warp_wait(bar(SL::ST_FULL + b), (M >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
+                tc_fence_after();
+                const int lo = qmin - 64 * b, hi = qmax - 64 * b;      // in this half's columns
+                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
+                auto write_pd = [&](auto masked) {
+                    tmem_ld32(tl + 64 * b, ra);
+                    tmem_ld32(tl + 128 + 64 * b, rb);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
+                        uint32_t (&ca)[32] = c ? ra2 : ra;
+                        uint32_t (&cb)[32] = c ? rb2 : rb;
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld_wait_regs(cb);
+                        if (c == 0) {
+                            tmem_ld32(tl + 64 * b + 32, ra2);
+                            tmem_ld32(tl + 128 + 64 * b + 32, rb2);
+                        }
+                        uint32_t wp[16], wd[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            // the query columns' lse and D, four at a time (same address in every lane)
+                            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 64 * b + 32 * c + e);
+                            const float4 d4 = *reinterpret_cast<const float4*>(D_s + 64 * b + 32 * c + e);
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                            float pr[4], ds[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int qc = 32 * c + e + u;
+                                const bool valid_q = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
+                                pr[u] = ex2_ftz(valid_q ? fmaf(__uint_as_float(ca[e + u]), sc, -lv[u]) : -INFINITY);
+                                ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - dv[u]);
+                            }
+                            wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
+                            wp[(e >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                            wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                            wd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
+                        }
+                        tmem_st16(tl + 64 * b + 16 * c, wp);           // over columns already read
+                        tmem_st16(tl + 128 + 64 * b + 16 * c, wd);
+                    }
+                };
+                if (whole) write_pd(std::false_type{});
+                else write_pd(std::true_type{});
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::P_FULL + b));
+            }
+            if (ok) ok = warp_wait(bar(SL::ACC_FULL), nit & 1u, abort_flag, lane);
+            if (!ok) break;
             tc_fence_after();
             bf16* row = p.dqkv + (int64_t)j * p.ld_qkv;
             float v[32];
@@ -665,7 +939,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rb[e]) * p.scale;
                 store32<bf16>(row + kcol + 32 * c, v);
             }
-        } else if (!ok && lane == 0) {
+            // dV / dK have been read: the next item's first products may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SL::ACC_FREE));
+            gm += nhalf;
+            gn0 += it.niter;
+            ++nit;
+        }
+        if (!ok && lane == 0) {
             atomicOr(status, ST_TIMEOUT);
             *abort_flag = 1;
         }
@@ -679,7 +961,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// Backward, query side.  CTA = (128-row query tile, query head).  Over the
+// Backward, query side.  Work item = (128-row query tile, query head).  Over the
 // forward's key tiles, in halves of 64 keys:  S = Q K^T, dP = dO V^T (TMEM,
 // two buffers);  P = exp(scale S - lse), dS = P (dP - D) (softmax warps, one
 // query row per thread, bf16 written back into TMEM over the S columns just
@@ -694,17 +976,36 @@ struct QSmem {
     static constexpr int K0 = 4 * BLK;          // stage s: K at K0 + 4 BLK s, V 2 BLK after
     static constexpr int BAR = 12 * BLK;
     enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, DS_FULL = 7, DS_DONE = 9, ACC_FULL = 11,
-           DRAIN = 12, NBARS = 13 };
-    static constexpr int MISC = BAR + NBARS * 8;
-    static constexpr int TOTAL = MISC + 16 + 1024;
+           DRAIN = 12, Q_EMPTY = 13, ACC_FREE = 14, SCHED_FULL = 15, SCHED_EMPTY = 15 + RING,
+           NBARS = 15 + 2 * RING };
+    static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
+    static constexpr int TOTAL = MISC + 32 + 1024;
 };
 
+// Query-side work item: query tile `tile` of query head h, over the
+// forward's key tiles [kstart, m0 + 128).
+struct QItem {
+    int tile, h, m0, kstart, nt;
+};
+
+__device__ __forceinline__ QItem q_item(const AttnParams& p, int item) {
+    QItem it;
+    it.tile = item / p.n_heads;
+    it.h = item % p.n_heads;
+    it.m0 = it.tile * TB;
+    it.kstart = p.seq_start[it.m0];
+    it.nt = (it.m0 + TB - it.kstart + TB - 1) / TB;
+    return it;
+}
+
+// Persistent like the key side: items query tile * n_heads + head; the next
+// item's Q / dO load starts once the current item's last scores are issued.
 __global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_bwd_q_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int* status) {
+    attn_bwd_q_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
     using SL = QSmem;
     const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
-    const int tile = blockIdx.x / p.n_heads, h = blockIdx.x % p.n_heads;
-    if (tile >= mt_valid) return;
+    auto valid = [&](int item) -> bool { return item >= 0 && item < n_items && item / p.n_heads < mt_valid; };
+    if (blockIdx.x >= mt_valid * p.n_heads) return;   // more CTAs than items
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -712,17 +1013,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = p.n_heads / p.n_kv;
 
-    const int m0 = tile * TB;
-    const int kstart = p.seq_start[m0];
-    const int nt = (m0 + TB - kstart + TB - 1) / TB;
-    const int nhalf = 2 * nt;
-    const int grp = p.n_heads / p.n_kv, g = h / grp;
-    const int qcol = h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
-
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
     if (threadIdx.x == 0) {
-        const int cnt[SL::NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1};
-        for (int i = 0; i < SL::NBARS; ++i) mbar_init(bar(i), cnt[i]);
+        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 4};
+        for (int i = 0; i < 15; ++i) mbar_init(bar(i), cnt[i]);
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(bar(SL::SCHED_FULL + i), 1);
+            mbar_init(bar(SL::SCHED_EMPTY + i), 5);    // MMA thread, four softmax warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -743,114 +1043,170 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (lane == 0) {
             bool ok = true;
             int last[2] = {-1, -1};
-            mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
-            load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, m0);
-            load_tile128(sb + SL::DO, &maps.do128, bar(SL::Q_FULL), qcol, m0);
-            for (int j = 0; j < nt; ++j) {
-                const int s = j & 1;
-                const uint32_t sp = (uint32_t)((j >> 1) & 1);
-                if (!mbar_wait(bar(SL::KV_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
-                const int key0 = kstart + j * TB;
-                const uint32_t fb = bar(SL::KV_FULL + s), st = sb + SL::K0 + s * 4 * BLK;
-                mbar_expect_tx(fb, 4 * BLK);
-                load_tile128(st, &maps.rows128, fb, kcol, key0);
-                load_tile128(st + 2 * BLK, &maps.rows128, fb, vcol, key0);
-                last[s] = (int)sp;
+            uint32_t nq = 0, gj = 0;                   // Q / dO tiles and key tiles loaded
+            RingPos rp;
+            while (ok) {
+                int item = atomicAdd(p.counter, 1);
+                if (!valid(item)) item = -1;
+                if (!ring_put(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const QItem it = q_item(p, item);
+                const int g = it.h / grp;
+                const int qcol = it.h * HD, kcol = (p.n_heads + g) * HD, vcol = (p.n_heads + p.n_kv + g) * HD;
+                // the previous item's last scores have read Q and dO
+                if (nq > 0 && !mbar_wait(bar(SL::Q_EMPTY), (nq - 1) & 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(bar(SL::Q_FULL), 4 * BLK);
+                load_tile128(sb + SL::Q, &maps.rows128, bar(SL::Q_FULL), qcol, it.m0);
+                load_tile128(sb + SL::DO, &maps.do128, bar(SL::Q_FULL), qcol, it.m0);
+                ++nq;
+                for (int j = 0; j < it.nt; ++j, ++gj) {
+                    const int s = gj & 1;
+                    const uint32_t sp = (gj >> 1) & 1u;
+                    if (!mbar_wait(bar(SL::KV_EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
+                    const int key0 = it.kstart + j * TB;
+                    const uint32_t fb = bar(SL::KV_FULL + s), st = sb + SL::K0 + s * 4 * BLK;
+                    mbar_expect_tx(fb, 4 * BLK);
+                    load_tile128(st, &maps.rows128, fb, kcol, key0);
+                    load_tile128(st + 2 * BLK, &maps.rows128, fb, vcol, key0);
+                    last[s] = (int)sp;
+                }
             }
             if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
-            bool dr = mbar_wait(bar(SL::Q_FULL), 0, (volatile int*)&dummy);
+            bool dr = nq == 0 || mbar_wait(bar(SL::Q_FULL), (nq - 1) & 1u, (volatile int*)&dummy);
             for (int s = 0; s < 2; ++s)
                 if (last[s] >= 0) dr &= mbar_wait(bar(SL::KV_FULL + s), (uint32_t)last[s], (volatile int*)&dummy);
             if (!dr) atomicOr(status, ST_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // half m: key tile j = m / 2 in stage j & 1, keys 64 (m & 1) .., TMEM buffer m & 1
-            auto issue_s = [&](int m) -> bool {
-                const int j = m >> 1, b = m & 1;
-                const uint32_t st = sb + SL::K0 + (j & 1) * 4 * BLK;
-                if (b == 0 && !mbar_wait(bar(SL::KV_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
-                if (m >= 2 && !mbar_wait(bar(SL::DS_DONE + b), (uint32_t)(((m >> 1) - 1) & 1), abort_flag)) return false;
-                tc_fence_after();
-                mma_kk64(tmem + 64 * b, sb + SL::Q, st, b);
-                mma_kk64(tmem + 128 + 64 * b, sb + SL::DO, st + 2 * BLK, b);
-                umma_commit(bar(SL::S_FULL + b));
-                return true;
-            };
-            bool ok = mbar_wait(bar(SL::Q_FULL), 0, abort_flag) && issue_s(0);
-            for (int m = 0; m < nhalf && ok; ++m) {
-                const int j = m >> 1, b = m & 1;
-                const uint32_t st = sb + SL::K0 + (j & 1) * 4 * BLK;
-                if (m + 1 < nhalf && !issue_s(m + 1)) { ok = false; break; }
-                if (!mbar_wait(bar(SL::DS_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                mma_t64mn(tmem + 256, tmem + 64 * b, st, b, m > 0);
-                umma_commit(bar(SL::DS_DONE + b));
-                if (b == 1) umma_commit(bar(SL::KV_EMPTY + (j & 1)));
+            bool ok = true;
+            uint32_t gm = 0, gj0 = 0, nit = 0;         // halves, key tiles and items before this item
+            RingPos rp;
+            while (ok) {
+                int item;
+                if (!ring_get(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const int nhalf = 2 * q_item(p, item).nt;   // >= 2
+                // half m: key tile gj0 + m / 2 in stage (gj0 + m / 2) & 1, keys 64 (m & 1) ..,
+                // TMEM buffer m & 1 (gm is even)
+                auto issue_s = [&](int m) -> bool {
+                    const uint32_t M = gm + m, J = gj0 + (m >> 1);
+                    const int b = m & 1;
+                    const uint32_t st = sb + SL::K0 + (J & 1) * 4 * BLK;
+                    if (b == 0 && !mbar_wait(bar(SL::KV_FULL + (J & 1)), (J >> 1) & 1u, abort_flag)) return false;
+                    if (M >= 2 && !mbar_wait(bar(SL::DS_DONE + b), ((M >> 1) - 1) & 1u, abort_flag)) return false;
+                    tc_fence_after();
+                    mma_kk64(tmem + 64 * b, sb + SL::Q, st, b);
+                    mma_kk64(tmem + 128 + 64 * b, sb + SL::DO, st + 2 * BLK, b);
+                    umma_commit(bar(SL::S_FULL + b));
+                    return true;
+                };
+                ok = mbar_wait(bar(SL::Q_FULL), nit & 1u, abort_flag) && issue_s(0);
+                for (int m = 0; m < nhalf && ok; ++m) {
+                    const uint32_t M = gm + m, J = gj0 + (m >> 1);
+                    const int b = m & 1;
+                    const uint32_t st = sb + SL::K0 + (J & 1) * 4 * BLK;
+                    if (m + 1 < nhalf) {
+                        if (!issue_s(m + 1)) { ok = false; break; }
+                        if (m + 2 == nhalf) umma_commit(bar(SL::Q_EMPTY));   // the item's last scores
+                    }
+                    if (!mbar_wait(bar(SL::DS_FULL + b), (M >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    // dQ of the previous item has been read out
+                    if (m == 0 && nit > 0 && !mbar_wait(bar(SL::ACC_FREE), (nit - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_t64mn(tmem + 256, tmem + 64 * b, st, b, m > 0);
+                    umma_commit(bar(SL::DS_DONE + b));
+                    if (b == 1) umma_commit(bar(SL::KV_EMPTY + (J & 1)));
+                }
+                if (!ok) break;
+                umma_commit(bar(SL::ACC_FULL));
+                gm += nhalf;
+                gj0 += nhalf >> 1;
+                ++nit;
             }
-            if (ok) umma_commit(bar(SL::ACC_FULL));
-            else { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
             umma_commit(bar(SL::DRAIN));
             if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
     } else {
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
-        const int i = m0 + r;
-        const int ss = p.seq_start[i];
-        const float lse2 = p.lseT[(int64_t)h * p.ld_t + i];
-        const float Di = p.DT[(int64_t)h * p.ld_t + i];
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
         uint32_t ra[32], rb[32], ra2[32], rb2[32];
-        for (int m = 0; m < nhalf; ++m) {
-            const int b = m & 1;
-            if (!warp_wait(bar(SL::S_FULL + b), (uint32_t)((m >> 1) & 1), abort_flag, lane)) { ok = false; break; }
-            tc_fence_after();
-            const int key0 = kstart + (m >> 1) * TB + 64 * b;
-            const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
-            const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
-            auto write_ds = [&](auto masked) {
-                tmem_ld32(tl + 64 * b, ra);
-                tmem_ld32(tl + 128 + 64 * b, rb);
+        uint32_t gm = 0, nit = 0;
+        RingPos rp;
+        while (ok) {
+            int item;
+            if (!ring_get_warp(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag, lane)) {
+                ok = false;
+                break;
+            }
+            if (item < 0) break;
+            const QItem it = q_item(p, item);
+            const int i = it.m0 + r;
+            const int ss = p.seq_start[i];
+            const float lse2 = p.lseT[(int64_t)it.h * p.ld_t + i];
+            const float Di = p.DT[(int64_t)it.h * p.ld_t + i];
+            const int nhalf = 2 * it.nt;
+            for (int m = 0; m < nhalf; ++m) {
+                const int b = m & 1;
+                const uint32_t M = gm + m;
+                if (!warp_wait(bar(SL::S_FULL + b), (M >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
+                tc_fence_after();
+                const int key0 = it.kstart + (m >> 1) * TB + 64 * b;
+                const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
+                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
+                auto write_ds = [&](auto masked) {
+                    tmem_ld32(tl + 64 * b, ra);
+                    tmem_ld32(tl + 128 + 64 * b, rb);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
-                    uint32_t (&ca)[32] = c ? ra2 : ra;
-                    uint32_t (&cb)[32] = c ? rb2 : rb;
-                    tmem_ld_wait_regs(ca);
-                    tmem_ld_wait_regs(cb);
-                    if (c == 0) {
-                        tmem_ld32(tl + 64 * b + 32, ra2);
-                        tmem_ld32(tl + 128 + 64 * b + 32, rb2);
-                    }
-                    uint32_t wd[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float ds[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int idx = 32 * c + e + u;
-                            const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                            const float pr = exp2f(v ? fmaf(__uint_as_float(ca[e + u]), sc, -lse2) : -INFINITY);
-                            ds[u] = pr * (__uint_as_float(cb[e + u]) - Di);
+                    for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
+                        uint32_t (&ca)[32] = c ? ra2 : ra;
+                        uint32_t (&cb)[32] = c ? rb2 : rb;
+                        tmem_ld_wait_regs(ca);
+                        tmem_ld_wait_regs(cb);
+                        if (c == 0) {
+                            tmem_ld32(tl + 64 * b + 32, ra2);
+                            tmem_ld32(tl + 128 + 64 * b + 32, rb2);
                         }
-                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                        uint32_t wd[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float ds[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int idx = 32 * c + e + u;
+                                const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                                const float pr = ex2_ftz(v ? fmaf(__uint_as_float(ca[e + u]), sc, -lse2) : -INFINITY);
+                                ds[u] = pr * (__uint_as_float(cb[e + u]) - Di);
+                            }
+                            wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                        }
+                        tmem_st16(tl + 64 * b + 16 * c, wd);           // over columns already read
                     }
-                    tmem_st16(tl + 64 * b + 16 * c, wd);           // over columns already read
-                }
-            };
-            if (whole) write_ds(std::false_type{});
-            else write_ds(std::true_type{});
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SL::DS_FULL + b));
-        }
-        if (ok) ok = warp_wait(bar(SL::ACC_FULL), 0, abort_flag, lane);
-        if (ok) {
+                };
+                if (whole) write_ds(std::false_type{});
+                else write_ds(std::true_type{});
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::DS_FULL + b));
+            }
+            if (ok) ok = warp_wait(bar(SL::ACC_FULL), nit & 1u, abort_flag, lane);
+            if (!ok) break;
             tc_fence_after();
-            bf16* row = p.dqkv + (int64_t)i * p.ld_qkv + qcol;
+            bf16* row = p.dqkv + (int64_t)i * p.ld_qkv + it.h * HD;
             float v[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -860,7 +1216,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]) * p.scale;
                 store32<bf16>(row + 32 * c, v);
             }
-        } else if (lane == 0) {
+            // dQ has been read: the next item's first products may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SL::ACC_FREE));
+            gm += nhalf;
+            ++nit;
+        }
+        if (!ok && lane == 0) {
             atomicOr(status, ST_TIMEOUT);
             *abort_flag = 1;
         }
@@ -901,13 +1264,18 @@ __global__ void attn_rowdot_kernel(const bf16* __restrict__ dO, const bf16* __re
     if (row < rows && part == 0) DT[(int64_t)h * ld_t + row] = acc;
 }
 
+// A persistent kernel: one CTA per SM (at most one per work item); the item
+// counter starts at zero.
 template <typename K>
-cudaError_t launch_attn(K kernel, int smem_bytes, int threads, const AttnMaps& maps, const AttnParams& p, int grid,
-                        int* status, cudaStream_t s) {
+cudaError_t launch_attn_persistent(K kernel, int smem_bytes, int threads, const AttnMaps& maps,
+                                   const AttnParams& p, int n_items, int num_sms, int* status, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    if (grid <= 0) return cudaSuccess;
-    kernel<<<grid, threads, smem_bytes, s>>>(maps, p, status);
+    if (n_items <= 0) return cudaSuccess;
+    const int grid = n_items < num_sms ? n_items : num_sms;
+    e = cudaMemsetAsync(p.counter, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, threads, smem_bytes, s>>>(maps, p, n_items, status);
     return cudaGetLastError();
 }
 
@@ -938,6 +1306,7 @@ AttnParams make_params(const AttnArgs& a) {
     p.ld_t = a.ld_t;
     p.DT = a.DT;
     p.dqkv = a.dqkv;
+    p.counter = a.counter;
     return p;
 }
 
@@ -948,8 +1317,9 @@ cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s)
     if (!make_maps(maps, a) || a.max_rows % TB || a.ld_t % 4) return cudaErrorInvalidValue;
     const AttnParams p = make_params(a);
     const int pairs = (a.n_heads / a.n_kv + 1) / 2;
-    return launch_attn(attn_fwd_kernel, FwdSmem::TOTAL, FWD_THREADS, maps, p, p.max_tiles * a.n_kv * pairs, status,
-                       s);
+    if (a.num_sms < 1 || !a.counter) return cudaErrorInvalidValue;
+    return launch_attn_persistent(attn_fwd_kernel, FwdSmem::TOTAL, FWD_THREADS, maps, p, p.max_tiles * a.n_kv * pairs,
+                                  a.num_sms, status, s);
 }
 
 cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s) {
@@ -962,9 +1332,12 @@ cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s)
         a.dO, a.o, a.n_heads, a.meta, p.max_tiles, a.DT, a.ld_t);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_attn(attn_bwd_kv_kernel, KvSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_kv, status, s);
+    if (a.num_sms < 1 || !a.counter) return cudaErrorInvalidValue;
+    e = launch_attn_persistent(attn_bwd_kv_kernel, KvSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_kv,
+                               a.num_sms, status, s);
     if (e != cudaSuccess) return e;
-    return launch_attn(attn_bwd_q_kernel, QSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_heads, status, s);
+    return launch_attn_persistent(attn_bwd_q_kernel, QSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_heads,
+                                  a.num_sms, status, s);
 }
 
 }  // namespace mlk

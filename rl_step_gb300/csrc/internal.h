@@ -39,6 +39,8 @@ struct AttnArgs {
     int ld_t = 0;                  // multiple of 4
     const bf16* dO = nullptr;      // backward: dL/dO [max_rows x n_heads*128]
     bf16* dqkv = nullptr;          // backward: dL/d(q, k, v), same layout as qkv
+    int num_sms = 0;               // persistent kernels: one CTA per SM
+    int* counter = nullptr;        // device int: their work-item counter
 };
 cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s);
 // rowsum kernel, key-side (dK, dV) kernel, query-side (dQ) kernel

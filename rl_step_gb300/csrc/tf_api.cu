@@ -663,6 +663,8 @@ AttnArgs attn_args(mlora_tf_t* h, int l, int mp) {
     a.ld_t = h->max_pad;
     a.dO = h->dO;
     a.dqkv = h->dqkv;
+    a.num_sms = h->num_sms;
+    a.counter = h->tile_counter;
     return a;
 }
 
