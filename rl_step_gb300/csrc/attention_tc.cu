@@ -33,7 +33,6 @@ namespace {
 
 using namespace tcx;
 
-constexpr int AT_THREADS = 192;
 constexpr int HD = 128;                 // head width
 constexpr int TB = 128;                 // rows per query / key tile
 constexpr int BLK = TB * 128;           // one 128-row x 64-element bf16 block (16 KB)
@@ -686,7 +685,23 @@ __device__ __forceinline__ KvItem kv_item(const AttnParams& p, int item, int mt_
 // phases follow running counts of query tiles and halves.  The next item's
 // K / V load starts once the current item's last scores are issued, and its
 // first products overlap the read-out of the current dK / dV.
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// The same with A in two 16-column pieces: K rows 0-31 (bf16 pairs) at
+// a_tmem .. a_tmem + 15 and K rows 32-63 at a_tmem + 32 .. a_tmem + 47, as the
+// two softmax warpgroups write them (each over the columns it has read).
+__device__ __forceinline__ void mma_t64mn_split(uint32_t d, uint32_t a_tmem, uint32_t b, int s, bool acc) {
+    const uint32_t id = idesc_bf16(128, 0, 1, 128);
+    const uint64_t bd = mndesc(b) + 512 * s;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        umma_bf16_ts(d, a_tmem + 8 * kk + (kk >= 2 ? 16 : 0), bd + 128 * kk, id, (acc || kk) ? 1u : 0u);
+}
+
+// Backward kernels: warp 0 loads, warp 1 issues the MMAs, warps 2-9 are two
+// softmax warpgroups over the same TMEM lanes (warp w reads lanes
+// 32 (w % 4) ..); warpgroup c takes columns 32 c .. 32 c + 31 of each half.
+constexpr int BWD_THREADS = 320;
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_kv_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
     using SL = KvSmem;
     const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
@@ -703,11 +718,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
     volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
     if (threadIdx.x == 0) {
-        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 4};
+        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 8, 8, 1, 1, 1, 1, 1, 8};
         for (int i = 0; i < 15; ++i) mbar_init(bar(i), cnt[i]);
         for (int i = 0; i < RING; ++i) {
             mbar_init(bar(SL::SCHED_FULL + i), 1);
-            mbar_init(bar(SL::SCHED_EMPTY + i), 5);    // MMA thread, four softmax warps
+            mbar_init(bar(SL::SCHED_EMPTY + i), 9);    // MMA thread, eight softmax warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -814,8 +829,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    mma_t64mn(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
-                    mma_t64mn(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
+                    mma_t64mn_split(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
+                    mma_t64mn_split(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
                     umma_commit(bar(SL::PT_DONE + b));
                     if (b == 1) umma_commit(bar(SL::QD_EMPTY + (N & 1)));
                 }
@@ -831,11 +846,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
     } else {
         const int q4 = warp & 3;
+        const int wg = (warp - 2) >> 2;                // column half of each 64-column half
         const int r = 32 * q4 + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
-        uint32_t ra[32], rb[32], ra2[32], rb2[32];
+        uint32_t ra[32], rb[32];
         uint32_t gm = 0, gn0 = 0, nit = 0;
         RingPos rp;
         while (ok) {
@@ -876,44 +892,37 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 }
                 if (!warp_wait(bar(SL::ST_FULL + b), (M >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
                 tc_fence_after();
-                const int lo = qmin - 64 * b, hi = qmax - 64 * b;      // in this half's columns
-                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
+                // this warpgroup's 32 query columns of the half
+                const int lo = qmin - 64 * b - 32 * wg, hi = qmax - 64 * b - 32 * wg;
+                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 31);
                 auto write_pd = [&](auto masked) {
-                    tmem_ld32(tl + 64 * b, ra);
-                    tmem_ld32(tl + 128 + 64 * b, rb);
+                    const uint32_t cs = tl + 64 * b + 32 * wg, cd = tl + 128 + 64 * b + 32 * wg;
+                    tmem_ld32(cs, ra);
+                    tmem_ld32(cd, rb);
+                    tmem_ld_wait_regs(ra);
+                    tmem_ld_wait_regs(rb);
+                    uint32_t wp[16], wd[16];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
-                        uint32_t (&ca)[32] = c ? ra2 : ra;
-                        uint32_t (&cb)[32] = c ? rb2 : rb;
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld_wait_regs(cb);
-                        if (c == 0) {
-                            tmem_ld32(tl + 64 * b + 32, ra2);
-                            tmem_ld32(tl + 128 + 64 * b + 32, rb2);
+                    for (int e = 0; e < 32; e += 4) {
+                        // the query columns' lse and D, four at a time (same address in every lane)
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 64 * b + 32 * wg + e);
+                        const float4 d4 = *reinterpret_cast<const float4*>(D_s + 64 * b + 32 * wg + e);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pr[4], ds[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int qc = e + u;
+                            const bool valid_q = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
+                            pr[u] = ex2_ftz(valid_q ? fmaf(__uint_as_float(ra[e + u]), sc, -lv[u]) : -INFINITY);
+                            ds[u] = pr[u] * (__uint_as_float(rb[e + u]) - dv[u]);
                         }
-                        uint32_t wp[16], wd[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            // the query columns' lse and D, four at a time (same address in every lane)
-                            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 64 * b + 32 * c + e);
-                            const float4 d4 = *reinterpret_cast<const float4*>(D_s + 64 * b + 32 * c + e);
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                            float pr[4], ds[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int qc = 32 * c + e + u;
-                                const bool valid_q = !decltype(masked)::value || ((qc >= lo) & (qc <= hi));
-                                pr[u] = ex2_ftz(valid_q ? fmaf(__uint_as_float(ca[e + u]), sc, -lv[u]) : -INFINITY);
-                                ds[u] = pr[u] * (__uint_as_float(cb[e + u]) - dv[u]);
-                            }
-                            wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
-                            wp[(e >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-                            wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-                            wd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
-                        }
-                        tmem_st16(tl + 64 * b + 16 * c, wp);           // over columns already read
-                        tmem_st16(tl + 128 + 64 * b + 16 * c, wd);
+                        wp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
+                        wp[(e >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+                        wd[(e >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
                     }
+                    tmem_st16(cs, wp);           // over this warpgroup's columns, already read
+                    tmem_st16(cd, wd);
                 };
                 if (whole) write_pd(std::false_type{});
                 else write_pd(std::true_type{});
@@ -928,7 +937,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             bf16* row = p.dqkv + (int64_t)j * p.ld_qkv;
             float v[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {           // this warpgroup's 64 of the 128 columns
+                const int c = 2 * wg + cc;
                 tmem_ld32(tl + 256 + 32 * c, ra);
                 tmem_ld32(tl + 384 + 32 * c, rb);
                 tmem_ld_wait();
@@ -1000,7 +1010,7 @@ __device__ __forceinline__ QItem q_item(const AttnParams& p, int item) {
 
 // Persistent like the key side: items query tile * n_heads + head; the next
 // item's Q / dO load starts once the current item's last scores are issued.
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_q_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
     using SL = QSmem;
     const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
@@ -1017,11 +1027,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
     volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
     if (threadIdx.x == 0) {
-        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 4};
+        const int cnt[15] = {1, 1, 1, 1, 1, 1, 1, 8, 8, 1, 1, 1, 1, 1, 8};
         for (int i = 0; i < 15; ++i) mbar_init(bar(i), cnt[i]);
         for (int i = 0; i < RING; ++i) {
             mbar_init(bar(SL::SCHED_FULL + i), 1);
-            mbar_init(bar(SL::SCHED_EMPTY + i), 5);    // MMA thread, four softmax warps
+            mbar_init(bar(SL::SCHED_EMPTY + i), 9);    // MMA thread, eight softmax warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1123,7 +1133,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    mma_t64mn(tmem + 256, tmem + 64 * b, st, b, m > 0);
+                    mma_t64mn_split(tmem + 256, tmem + 64 * b, st, b, m > 0);
                     umma_commit(bar(SL::DS_DONE + b));
                     if (b == 1) umma_commit(bar(SL::KV_EMPTY + (J & 1)));
                 }
@@ -1139,11 +1149,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
     } else {
         const int q4 = warp & 3;
+        const int wg = (warp - 2) >> 2;                // column half of each 64-column half
         const int r = 32 * q4 + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         const float sc = p.scale * LOG2E;
         bool ok = true;
-        uint32_t ra[32], rb[32], ra2[32], rb2[32];
+        uint32_t ra[32], rb[32];
         uint32_t gm = 0, nit = 0;
         RingPos rp;
         while (ok) {
@@ -1164,37 +1175,30 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 const uint32_t M = gm + m;
                 if (!warp_wait(bar(SL::S_FULL + b), (M >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
                 tc_fence_after();
-                const int key0 = it.kstart + (m >> 1) * TB + 64 * b;
-                const int lo = ss - key0, hi = i - key0;          // valid key columns [lo, hi]
-                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 63);
+                // this warpgroup's 32 key columns of the half: valid keys [lo, hi]
+                const int key0 = it.kstart + (m >> 1) * TB + 64 * b + 32 * wg;
+                const int lo = ss - key0, hi = i - key0;
+                const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 31);
                 auto write_ds = [&](auto masked) {
-                    tmem_ld32(tl + 64 * b, ra);
-                    tmem_ld32(tl + 128 + 64 * b, rb);
+                    const uint32_t cs = tl + 64 * b + 32 * wg;
+                    tmem_ld32(cs, ra);
+                    tmem_ld32(tl + 128 + 64 * b + 32 * wg, rb);
+                    tmem_ld_wait_regs(ra);
+                    tmem_ld_wait_regs(rb);
+                    uint32_t wd[16];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {   // chunk 1 loads while chunk 0 is processed
-                        uint32_t (&ca)[32] = c ? ra2 : ra;
-                        uint32_t (&cb)[32] = c ? rb2 : rb;
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld_wait_regs(cb);
-                        if (c == 0) {
-                            tmem_ld32(tl + 64 * b + 32, ra2);
-                            tmem_ld32(tl + 128 + 64 * b + 32, rb2);
+                    for (int e = 0; e < 32; e += 2) {
+                        float ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int idx = e + u;
+                            const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                            const float pr = ex2_ftz(v ? fmaf(__uint_as_float(ra[e + u]), sc, -lse2) : -INFINITY);
+                            ds[u] = pr * (__uint_as_float(rb[e + u]) - Di);
                         }
-                        uint32_t wd[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float ds[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int idx = 32 * c + e + u;
-                                const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                                const float pr = ex2_ftz(v ? fmaf(__uint_as_float(ca[e + u]), sc, -lse2) : -INFINITY);
-                                ds[u] = pr * (__uint_as_float(cb[e + u]) - Di);
-                            }
-                            wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-                        }
-                        tmem_st16(tl + 64 * b + 16 * c, wd);           // over columns already read
+                        wd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
                     }
+                    tmem_st16(cs, wd);           // over this warpgroup's columns, already read
                 };
                 if (whole) write_ds(std::false_type{});
                 else write_ds(std::true_type{});
@@ -1209,7 +1213,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             bf16* row = p.dqkv + (int64_t)i * p.ld_qkv + it.h * HD;
             float v[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {           // this warpgroup's 64 of the 128 columns
+                const int c = 2 * wg + cc;
                 tmem_ld32(tl + 256 + 32 * c, ra);
                 tmem_ld_wait();
 #pragma unroll
@@ -1333,10 +1338,10 @@ cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.num_sms < 1 || !a.counter) return cudaErrorInvalidValue;
-    e = launch_attn_persistent(attn_bwd_kv_kernel, KvSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_kv,
+    e = launch_attn_persistent(attn_bwd_kv_kernel, KvSmem::TOTAL, BWD_THREADS, maps, p, p.max_tiles * a.n_kv,
                                a.num_sms, status, s);
     if (e != cudaSuccess) return e;
-    return launch_attn_persistent(attn_bwd_q_kernel, QSmem::TOTAL, AT_THREADS, maps, p, p.max_tiles * a.n_heads,
+    return launch_attn_persistent(attn_bwd_q_kernel, QSmem::TOTAL, BWD_THREADS, maps, p, p.max_tiles * a.n_heads,
                                   a.num_sms, status, s);
 }
 
