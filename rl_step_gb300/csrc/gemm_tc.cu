@@ -109,6 +109,47 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, uint32_t tbase
     if (row_ok) epi_row_end(p.ep, row, nt, st);
 }
 
+// Epilogue of the export merge (EPI_MERGE: out = bf16(W + gamma acc)).  Its
+// GEMM has K = 192, so unlike the other epilogues this one is not hidden
+// behind a long mainloop: its time is the reads of W.  All of a row's W
+// pieces of the tile (BN / 32 chunks of 32 columns) are requested before the
+// first accumulator chunk is read, so each thread waits for memory once per
+// tile instead of once per chunk.  The arithmetic (fmaf(gamma, acc, w), one
+// rounding) is that of epi_chunk's EPI_MERGE.
+template <int BN>
+__device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t tbase, int64_t row, bool row_ok,
+                                                   int col_base, int adapter) {
+    constexpr int NCH = BN / 32;
+    constexpr int D = NCH;
+    const bf16* w = reinterpret_cast<const bf16*>(p.ep.aux) + row * p.ep.ld_aux + col_base;
+    bf16* out = reinterpret_cast<bf16*>(p.ep.out0) + row * p.ep.ld0 + col_base;
+    const float gm = p.ep.gamma[adapter];
+    uint4 wb[D][4];
+    auto load_w = [&](int ch, uint4 (&dst)[4]) {
+        if (row_ok && col_base + 32 * ch < p.N) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(w + 32 * ch);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = __ldcs(s4 + q);     // read once: evict first
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < D; ++c) load_w(c, wb[c]);
+    uint32_t ra[32];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        tmem_ld32(tbase + ch * 32, ra);
+        tmem_ld_wait();
+        if (row_ok && col_base + 32 * ch < p.N) {
+            float v[32];
+            load32<bf16>(reinterpret_cast<const bf16*>(wb[ch % D]), v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(gm, __uint_as_float(ra[j]), v[j]);
+            store32<bf16>(out + 32 * ch, v);
+        }
+        if (ch + D < NCH) load_w(ch + D, wb[ch % D]);
+    }
+}
+
 struct TcMaps {
     CUtensorMap A, B, Ax, Bx;
 };
@@ -189,7 +230,9 @@ struct SmemLayout {
     static constexpr int TOTAL = MISC_OFF + 16 + 1024;          // + alignment slack
 };
 
-template <int BN, int STAGES>
+// MERGE selects the export-merge epilogue (a separate instantiation, so the
+// other GEMMs keep their register allocation).
+template <int BN, int STAGES, bool MERGE = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status) {
     using SL = SmemLayout<BN, STAGES>;
@@ -383,7 +426,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = (int64_t)c.mt * BM + 32 * q + lane;
             const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-            epilogue_row<BN>(p, tbase, row, row_ok, c.nt * BN, c.adapter, c.nt);
+            if (MERGE) epilogue_row_merge<BN>(p, tbase, row, row_ok, c.nt * BN, c.adapter);
+            else epilogue_row<BN>(p, tbase, row, row_ok, c.nt * BN, c.adapter, c.nt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
@@ -516,7 +560,7 @@ __device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_l
     return true;
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB>
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
     using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
@@ -811,7 +855,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = (int64_t)my_mt * BM + 32 * q + lane;
             const bool tile_ok = (my_mt - p.mt_base) < cnt && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-            epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
+            if (MERGE) epilogue_row_merge<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0);
+            else epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -863,7 +908,7 @@ bool operand_ok(const GemmOperand& op) {
            op.cols > 0 && op.rows < (1LL << 31) && op.cols < (1LL << 31);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool MERGE = false>
 cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
     using SL = SmemLayout<BN, STAGES>;
     TcMaps maps;
@@ -881,7 +926,7 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, MERGE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -891,11 +936,11 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
                               : (int64_t)p.mt_count * n_nt;
     if (upper <= 0) return cudaSuccess;
     int grid = (int)(upper < num_sms ? upper : num_sms);
-    tc_gemm_kernel<BN, STAGES><<<grid, NUM_THREADS, SL::TOTAL, s>>>(maps, p, status);
+    tc_gemm_kernel<BN, STAGES, MERGE><<<grid, NUM_THREADS, SL::TOTAL, s>>>(maps, p, status);
     return cudaGetLastError();
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB>
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status, int* dbg) {
     using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
     TcMaps maps;
@@ -915,7 +960,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -939,7 +984,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     cfg.numAttrs = 1;
     cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);   // fresh tile counter
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB>, maps, p, status, dbg);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE>, maps, p, status, dbg);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -971,6 +1016,12 @@ bool tc_encode_bf16(void* map, const void* ptr, int64_t rows, int64_t cols, int6
 
 cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
     if (!get_encode()) return cudaErrorNotSupported;
+    if (p.ep.kind == EPI_MERGE) {
+        if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8, true>(p, s, num_sms, status);
+        if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
+            return launch_pair<256, 3, 2, 2, true>(p, s, num_sms, status, nullptr);
+        return launch_bn<256, 4, true>(p, s, num_sms, status);
+    }
     if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8>(p, s, num_sms, status);
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)

@@ -430,10 +430,10 @@ static int s_forward(mlora_sampler_t* s, const int32_t* tokens, const int32_t* t
         return p;
     };
     // Few rows (decode): when the 256 x 256 pair tiles of a block GEMM would
-    // occupy under a quarter of the SMs while the weights stream, it runs on
-    // the 128 x 64 single-CTA kernel instead (four times the tiles; the same
-    // per-element K order and MMA K step, so the same bits).
-    auto small = [&](int N) { return ((mt + 1) / 2) * ((N + 255) / 256) * 2 < t.num_sms / 4; };
+    // not fill the SMs once while the weights stream, it runs on the 128 x 64
+    // single-CTA kernel instead (four times the tiles; the same per-element K
+    // order and MMA K step, so the same bits).
+    auto small = [&](int N) { return ((mt + 1) / 2) * ((N + 255) / 256) * 2 < t.num_sms; };
     for (int l = 0; l < t.L; ++l) {
         {   // v1[:, s-block] = gamma_s A1_s h on rows of slot s
             GemmParams p = dense(SK, t.d);

@@ -84,28 +84,38 @@ def test_bounded_wait_runs_out_and_handle_recovers():
 
 def _sweep(lib, create, what):
     """Fail each allocation of create() in turn; every attempt returns E_NOMEM
-    and leaves the device's free memory where it was."""
+    and leaves the device's free memory where it was.  Garbage collection is
+    off meanwhile, so that no earlier test's handle is freed inside a
+    measurement."""
+    import gc
+
     import torch
     import rl_step_gb300 as m
+    gc.collect()
     torch.cuda.synchronize()
-    c0 = lib.mlk_test_alloc_calls()
-    obj = create()                               # a full create: counts its allocations
-    n_alloc = lib.mlk_test_alloc_calls() - c0
-    del obj
-    torch.cuda.synchronize()
-    assert n_alloc > 5, what
-    for k in range(1, n_alloc + 1):
+    torch.cuda.empty_cache()
+    gc.disable()
+    try:
+        c0 = lib.mlk_test_alloc_calls()
+        obj = create()                           # a full create: counts its allocations
+        n_alloc = lib.mlk_test_alloc_calls() - c0
+        del obj
         torch.cuda.synchronize()
-        free0 = torch.cuda.mem_get_info()[0]
-        lib.mlk_test_fail_alloc_at(lib.mlk_test_alloc_calls() + k)
-        try:
-            with pytest.raises(m.MLoRAError) as ei:
-                create()
-        finally:
-            lib.mlk_test_fail_alloc_at(0)
-        assert ei.value.code == E_NOMEM, (what, k, str(ei.value))
-        torch.cuda.synchronize()
-        assert torch.cuda.mem_get_info()[0] == free0, (what, k)
+        assert n_alloc > 5, what
+        for k in range(1, n_alloc + 1):
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
+            lib.mlk_test_fail_alloc_at(lib.mlk_test_alloc_calls() + k)
+            try:
+                with pytest.raises(m.MLoRAError) as ei:
+                    create()
+            finally:
+                lib.mlk_test_fail_alloc_at(0)
+            assert ei.value.code == E_NOMEM, (what, k, str(ei.value))
+            torch.cuda.synchronize()
+            assert torch.cuda.mem_get_info()[0] == free0, (what, k)
+    finally:
+        gc.enable()
     return n_alloc
 
 
