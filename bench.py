@@ -215,25 +215,34 @@ def kernel_source_hash(read=None) -> str:
     return h.hexdigest()
 
 
-def committed_traffic(workload: str, kernel: str, launches: int):
-    """Per-launch DRAM bytes of `kernel` from the committed full-size ncu
-    summary, or None when the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_tc_gemm_pair_kernel_small_case.json")
+BLOCK_KINDS = ("w1_fwd", "w2_fwd", "w2_bwd", "w1_bwd")
+
+
+def scaled_traffic(cfg, rows: int, launches_per_step: float, lm_mode: str, path: str = TRAFFIC_FILE):
+    """Per-launch DRAM bytes of the CTA-pair GEMM at this workload's size, from
+    the committed small-case capture: each launch kind's bytes scaled by the
+    padded rows (and, for the LM-head launches, by the vocabulary), summed
+    over the step's launches and divided by their number.  None when the
+    capture is missing, was taken at other widths or on other kernel sources."""
     try:
         with open(path) as fh:
             rec = json.load(fh)
-    except (OSError, ValueError):
-        return None
-    try:
         current = kernel_source_hash()
-    except (OSError, ValueError):          # a source or the launch span's markers are gone
+    except (OSError, ValueError):          # no capture, or a source / span marker is gone
         return None
     if rec.get("kernel_source_sha256") != current:
         return None
-    k = rec.get("kernels", {}).get(kernel)
-    if not k or k.get("launches_per_step") != launches:
+    if (rec.get("d_model"), rec.get("d_ffn")) != (cfg.d_model, cfg.d_ffn) or launches_per_step <= 0:
         return None
-    return k.get("dram_bytes_per_launch")
+    kinds = rec.get("bytes_per_launch", {}).get(lm_mode)
+    if not kinds:
+        return None
+    r = rows / rec["rows"]
+    v = cfg.vocab / rec["vocab"]
+    total = cfg.n_layers * sum(kinds[k] for k in BLOCK_KINDS) * r
+    total += sum(b for k, b in kinds.items() if k not in BLOCK_KINDS) * r * v
+    return total / launches_per_step
 
 
 def padded_rows(cfg, b):
@@ -249,6 +258,16 @@ def loss_epilogue_bytes(cfg, b, bn=256):
     rows = padded_rows(cfg, b)
     per_tok_in = {"cross_entropy": 4, "importance_sampling": 8, "ppo": 8, "custom": 4}[cfg.loss]
     return rows * (4.0 * n_nt + 20.0) + len(b["tokens"]) * (per_tok_in + 4.0)
+
+
+def lora_hbm_bytes(cfg, b):
+    """Bytes the LoRA shrinks (and, equally, the per-adapter gradient GEMMs)
+    must move per step: each reads one activation per launch once -- per
+    layer h and act forward, dh and du backward, [tokens x d or f] in the
+    base dtype -- and its [tokens x 64] factor operand."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    N = len(b["tokens"])
+    return cfg.n_layers * (2.0 * N * (cfg.d_model + cfg.d_ffn) * es + 4.0 * N * 64 * es)
 
 
 def lm_dz_bytes(cfg, b):
@@ -488,7 +507,7 @@ def run_ours(args, rank, world):
     exec_flops = fl["tc256"] * rows / max(1, N)
     executed = exec_flops * K / (tc_ms * 1e-3) / 1e12 if tc_ms > 0 else None
     peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    traffic = committed_traffic(cfg.name, "tc_gemm_pair_kernel", int(round(tc_launch / K)))
+    traffic = scaled_traffic(cfg, padded_rows(cfg, b), tc_launch / K, args.lm_backward)
     step_ms = ms_max / K
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     adam_b, n_ad_params = adam_bytes(cfg, b)
@@ -506,6 +525,12 @@ def run_ours(args, rank, world):
         kernels["lm_dz"]["note"] = ("side stream, concurrent with the next chunk's LM-head GEMM: "
                                     "ms_per_step is the span of its events under that overlap, "
                                     "not its exclusive time (see the serialised ncu launch list)")
+    lb_lora = lora_hbm_bytes(cfg, b)
+    for c in ("shrink", "grad"):
+        if prof[c][0] > 0:
+            kernels[c]["achieved_gbs"] = lb_lora * K / (prof[c][0] * 1e-3) / 1e9
+            kernels[c]["frac_of_hbm"] = kernels[c]["achieved_gbs"] / peaks["hbm_gbs"]
+            kernels[c]["bytes_per_step"] = lb_lora
     if prof["loss"][0] > 0:
         lb = loss_epilogue_bytes(cfg, b)
         kernels["loss"]["achieved_gbs"] = lb * K / (prof["loss"][0] * 1e-3) / 1e9
@@ -548,7 +573,8 @@ def run_ours(args, rank, world):
                      "bound": "tensor", "achieved": achieved, "peak": peak_tc,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
                      "frac": (achieved / peak_tc) if achieved else None, "traffic": traffic,
-                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu): small-case capture "
+                                     "scaled by padded rows (and vocabulary for the LM head)",
                      "launches_per_step": tc_launch / K,
                      "timed_in": "a second loop of the same steps with per-launch CUDA events "
                                  f"({ms_prof / K:.2f} ms per step there, {step_ms:.2f} without)",

@@ -133,6 +133,15 @@ template <> __device__ __forceinline__ void store32<float>(float* dst, const flo
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// 32 consecutive fp32 values with evict-first stores (st.global.cs): data
+// written once and read once much later (the kept LM-head logits), which should
+// not displace the GEMM operands in L2
+__device__ __forceinline__ void store32_stream(float* dst, const float* v) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) __stcs(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+}
+
 // first 16 of the values, 16 consecutive elements (32 bytes bf16, 64 bytes fp32)
 template <typename T> __device__ __forceinline__ void store16v(T* dst, const float* v);
 template <> __device__ __forceinline__ void store16v<bf16>(bf16* dst, const float* v) {
@@ -272,7 +281,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     } break;
     case EPI_LMFWD: {
         if (ep.out0 && col0 < ep.Vpad)     // keep the logits (fp32) for the backward
-            store32<float>(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
+            store32_stream(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
         int t = ep.tgt[row];
         float cm = -INFINITY;
 #pragma unroll

@@ -40,9 +40,21 @@ def test_hash_follows_the_kernel_sources_and_ignores_other_host_code():
     assert bench.kernel_source_hash(read) != h0
 
 
-def test_committed_traffic_is_void_when_launch_count_differs():
-    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic_qwen3_8b_ppo.json")) as fh:
-        rec = json.load(fh)
-    n = rec["kernels"]["tc_gemm_pair_kernel"]["launches_per_step"]
-    assert bench.committed_traffic("qwen3_8b_ppo", "tc_gemm_pair_kernel", n + 1) is None
-    assert bench.committed_traffic("no_such_workload", "tc_gemm_pair_kernel", n) is None
+def test_scaled_traffic_scales_rows_and_vocabulary(tmp_path):
+    import workloads as wl
+    cfg = wl.get_config("qwen3_8b_ppo")
+    rec = {"kernel_source_sha256": bench.kernel_source_hash(), "rows": 1000, "vocab": cfg.vocab // 2,
+           "d_model": cfg.d_model, "d_ffn": cfg.d_ffn,
+           "bytes_per_launch": {"keep_logits": {"w1_fwd": 1.0, "w2_fwd": 2.0, "w2_bwd": 3.0, "w1_bwd": 4.0,
+                                                "lm_fwd": 5.0, "lm_dh": 6.0}}}
+    path = tmp_path / "t.json"
+    path.write_text(json.dumps(rec))
+    got = bench.scaled_traffic(cfg, 3000, 10.0, "keep_logits", str(path))
+    want = (cfg.n_layers * 10.0 * 3 + 11.0 * 3 * 2) / 10.0
+    assert abs(got - want) < 1e-9
+    # other widths, another mode, or other kernel sources: no figure
+    assert bench.scaled_traffic(wl.get_config("qwen3_4b_is"), 3000, 10.0, "keep_logits", str(path)) is None
+    assert bench.scaled_traffic(cfg, 3000, 10.0, "recompute", str(path)) is None
+    rec["kernel_source_sha256"] = "0" * 64
+    path.write_text(json.dumps(rec))
+    assert bench.scaled_traffic(cfg, 3000, 10.0, "keep_logits", str(path)) is None

@@ -82,6 +82,17 @@ def test_full_size_sampled_parity(name, lm):
     g = np.where(mask, b["dloss"], 0).astype(np.float32)
     s = np.full(N, -np.log(cfg.vocab), np.float64) + b["sampler_noise"]
     s[S] = ell_S + b["sampler_noise"][S]
+    clipped_ad = None
+    if cfg.loss == "ppo":
+        # one adapter's sampled tokens sit far on the clipped side of the PPO
+        # objective (log-ratio +-1 against a clip of 0.2): their dL/dl is zero,
+        # so that adapter's gradient must be exactly zero on both sides while
+        # its loss value is not
+        present_S = np.unique(sub["adapter_ids"])
+        clipped_ad = int(present_S[len(present_S) // 2])
+        sel = S[(sub["adapter_ids"] == clipped_ad) & (A[S] != 0)]
+        assert len(sel) > 0
+        s[sel] = ell_S[np.searchsorted(S, sel)] - np.sign(A[sel])
     s = s.astype(np.float32)
 
     h = create_handle(cfg, base, ad, N, lm_backward=lm)
@@ -127,6 +138,11 @@ def test_full_size_sampled_parity(name, lm):
             for k in oracle.TENSORS:
                 x = m.mlora_read_adapter(h, int(a), l, "g" + k).cpu().numpy()
                 worst = max(worst, rel_fro(x, o.G[k][a][l]))
+    if clipped_ad is not None:
+        for l in range(cfg.n_layers):
+            for k in oracle.TENSORS:
+                assert not m.mlora_read_adapter(h, clipped_ad, l, "g" + k).cpu().numpy().any()
+                assert not o.G[k][clipped_ad][l].any()
     # adapters with no token in S received no gradient at all
     others = [a for a in np.unique(b["adapter_ids"]) if a not in set(present.tolist())]
     for a in others[:4]:
