@@ -654,6 +654,7 @@ def measure_transformer_row(args, dev, stream, peaks):
     del base, ad
     h = t.tf_create(cfg.vocab, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.n_layers, cfg.ranks,
                     cfg.alphas, N, dbase, A, B, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
+    t.tf_set_lm_backward(h, args.lm_backward)     # the MLP step's mode
     torch.cuda.synchronize()
     del dbase, A, B
     torch.cuda.empty_cache()
@@ -712,7 +713,7 @@ def measure_transformer_row(args, dev, stream, peaks):
                                                 "includes its rowsum pass, the S recompute is not credited)"},
         "projection_and_lm_gemms": {"tflops": gemm, "frac": gemm / peak_tc if gemm else None},
         "kernels": kern, "gpu_launches_per_step": launches,
-        "device_bytes": h.device_bytes,
+        "device_bytes": h.device_bytes, "lm_backward": args.lm_backward,
     }
     del h
     torch.cuda.empty_cache()

@@ -143,6 +143,16 @@ int mlora_tf_get_steps(mlora_tf_t* h, int64_t* steps_out, void* stream);
  * E_TIMEOUT). */
 int mlora_tf_check_status(mlora_tf_t* h, void* stream);
 
+/* LM-head backward mode, as mlora_set_lm_backward (MLORA_LM_RECOMPUTE, the
+ * default of a new handle, or MLORA_LM_KEEP_LOGITS; Tinker API Implementation
+ * on TPUs, section 10.4): recompute each row chunk's logits with a second
+ * GEMM whose epilogue forms dz, or keep the forward's fp32 logits of each
+ * chunk (two 16,384 x Vpad fp32 buffers and a second bf16 dz buffer, allocated
+ * when selected, freed when left).  Both give bitwise the same results.
+ * Synchronises the device.  Errors: E_ARG, E_NOMEM (the handle then stays in
+ * the recompute mode), E_CUDA. */
+int mlora_tf_set_lm_backward(mlora_tf_t* h, int32_t mode);
+
 /* Per-kernel-class timing, as mlora_profile_enable / mlora_profile_read, with
  * the classes below (arrays of MLORA_TF_PROF_CLASSES entries). */
 enum {

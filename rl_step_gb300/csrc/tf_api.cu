@@ -59,6 +59,7 @@ struct mlora_tf {
     std::vector<int> ranks;
     std::vector<float> alphas;
     std::vector<void*> allocs;
+    std::vector<size_t> alloc_bytes;
     int64_t bytes = 0;
     int64_t launches = 0;
 
@@ -98,6 +99,9 @@ struct mlora_tf {
     float* part = nullptr;
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
+    // LM-head backward mode (mlora_tf_set_lm_backward): recompute (dz[0] only) or
+    // kept logits (dz[0..1], zbuf[0..1], allocated when selected)
+    int lm_keep = 0;
     bf16* dz[2] = {nullptr, nullptr};
     float* zbuf[2] = {nullptr, nullptr};
     cudaStream_t side = nullptr;
@@ -150,8 +154,23 @@ int tf_alloc(mlora_tf_t* h, void** p, size_t bytes) {
         return tfail(MLORA_E_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
     }
     h->allocs.push_back(*p);
+    h->alloc_bytes.push_back(bytes);
     h->bytes += (int64_t)bytes;
     return MLORA_OK;
+}
+
+// Frees one allocation made by tf_alloc (the caller has synchronised the device).
+void tf_free(mlora_tf_t* h, void** p) {
+    if (!*p) return;
+    for (size_t i = 0; i < h->allocs.size(); ++i)
+        if (h->allocs[i] == *p) {
+            cudaFree(*p);
+            h->bytes -= (int64_t)h->alloc_bytes[i];
+            h->allocs.erase(h->allocs.begin() + (ptrdiff_t)i);
+            h->alloc_bytes.erase(h->alloc_bytes.begin() + (ptrdiff_t)i);
+            break;
+        }
+    *p = nullptr;
 }
 
 template <typename P>
@@ -165,6 +184,7 @@ int tf_alloc_t(mlora_tf_t* h, P** p, size_t count) {
 void tf_free_all(mlora_tf_t* h) {
     for (void* p : h->allocs) cudaFree(p);
     h->allocs.clear();
+    h->alloc_bytes.clear();
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
     h->ev.clear();
     for (int b = 0; b < 2; ++b) {
@@ -374,10 +394,7 @@ extern "C" int mlora_tf_create(const mlora_tf_config* cfg, const mlora_tf_init* 
         TA(h->part, (size_t)MP * h->part_ld);
         TA(h->zt, MP); TA(h->lse, MP); TA(h->gvec, MP); TA(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 128 ? h->max_tiles : 128;
-        for (int b = 0; b < 2; ++b) {
-            TA(h->dz[b], (size_t)h->nc_tiles * TILE_M * h->Vpad);
-            TA(h->zbuf[b], (size_t)h->nc_tiles * TILE_M * h->Vpad);
-        }
+        TA(h->dz[0], (size_t)h->nc_tiles * TILE_M * h->Vpad);   // the kept-logits mode adds its buffers
         TA(h->val_row, MP);
         TA(h->status, 1);
         TA(h->tile_counter, 1);
@@ -485,8 +502,7 @@ extern "C" int mlora_tf_create(const mlora_tf_config* cfg, const mlora_tf_init* 
              TF_CUDA(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
              TF_CUDA(cudaMemset(h->status, 0, sizeof(int)));
              TF_CUDA(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
-             for (int b = 0; b < 2; ++b)
-                 TF_CUDA(cudaMemset(h->dz[b], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * B2));
+             TF_CUDA(cudaMemset(h->dz[0], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * B2));
              launch_tf_adam(n_ad, h->ad_off, h->ranks_d, h->n_params, h->adam_tab, h->P, h->G, h->M, h->Vm, 0.f, 0.f,
                             0.f, 0.f, 0.f, h->mirror, 1, h->num_sms, s);
              ++h->launches;
@@ -740,9 +756,11 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
     if ((rc = tf_norm_fwd(h, h->gfinal, h->xf, h->rstdf, backward ? h->snapf : nullptr, mp, s))) return rc;
 
     // LM head (Tinker API Implementation on TPUs, section 10.3-10.4): per-tile
-    // log-sum-exp partials and the target logit; with the backward, chunk by
-    // chunk of rows with the chunk's fp32 logits kept for dz = g (onehot -
-    // softmax) and dxf = dz Wout.  The dz pass of chunk i runs on the side
+    // log-sum-exp partials and the target logit over all rows; the backward
+    // walks the rows in chunks and by default recomputes each chunk's logits
+    // with a second GEMM whose epilogue writes dz = g (onehot - softmax), then
+    // dxf = dz Wout.  In the kept-logits mode the forward GEMM of each chunk
+    // also stores its fp32 logits and the dz pass of chunk i runs on the side
     // stream beside chunk i+1's GEMMs (as in the MLP model's step).
     auto lm_fwd_params = [&](int c0, int cnt) {
         GemmParams p = tf_dense(h, mt_upper, V, d);
@@ -753,7 +771,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
         return p;
     };
-    if (!backward) {
+    if (!backward || !h->lm_keep) {
         GemmParams p = lm_fwd_params(0, mt_upper);
         if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_FWD))) return rc;
         {
@@ -767,7 +785,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
             launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
             ++h->launches;
         }
-        return MLORA_OK;
+        if (!backward) return MLORA_OK;
     }
     const int n_chunks = (mt_upper + h->nc_tiles - 1) / h->nc_tiles;
     int chunk = (mt_upper + n_chunks - 1) / n_chunks;
@@ -778,22 +796,41 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         c0 = i * chunk;
         cnt = mt_upper - c0 < chunk ? mt_upper - c0 : chunk;
     };
+    auto dh_params = [&](int c0, int cnt, const bf16* dzb) {
+        GemmParams p = tf_dense(h, mt_upper, d, h->Vpad);
+        p.mt_base = c0; p.mt_count = cnt;
+        p.A = opnd(dzb, (int64_t)h->nc_tiles * TILE_M, h->Vpad, h->Vpad, 0, 0, -(int64_t)c0 * TILE_M);
+        p.B = opnd(h->Wout, V, d, d, 1);
+        p.ep.kind = EPI_STORE2; p.ep.f32 = h->dxn32; p.ep.ldf = d; p.ep.out0 = nullptr;
+        return p;
+    };
+    if (!h->lm_keep) {
+        // recompute: chunk i's logits again, dz from them in the epilogue, then dxf
+        for (int i = 0; i < nch; ++i) {
+            int c0, cnt;
+            chunk_rows(i, c0, cnt);
+            {
+                GemmParams p = lm_fwd_params(c0, cnt);
+                p.ep.kind = EPI_LMDZ; p.ep.gv = h->gvec; p.ep.lse = h->lse;
+                p.ep.out0 = h->dz[0]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+                if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_DZ))) return rc;
+            }
+            GemmParams p = dh_params(c0, cnt, h->dz[0]);
+            if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_DH))) return rc;
+        }
+    }
     auto queue_dh = [&](int i) -> int {
         int c0, cnt;
         chunk_rows(i, c0, cnt);
         const int buf = i & 1;
         TF_CUDA(cudaStreamWaitEvent(s, h->ev_dz[buf], 0));
-        GemmParams p = tf_dense(h, mt_upper, d, h->Vpad);
-        p.mt_base = c0; p.mt_count = cnt;
-        p.A = opnd(h->dz[buf], (int64_t)h->nc_tiles * TILE_M, h->Vpad, h->Vpad, 0, 0, -(int64_t)c0 * TILE_M);
-        p.B = opnd(h->Wout, V, d, d, 1);
-        p.ep.kind = EPI_STORE2; p.ep.f32 = h->dxn32; p.ep.ldf = d; p.ep.out0 = nullptr;
+        GemmParams p = dh_params(c0, cnt, h->dz[buf]);
         const int r = tf_gemm(h, p, s, MLORA_TF_PROF_LM_DH);
         if (r) return r;
         TF_CUDA(cudaEventRecord(h->ev_dh[buf], s));
         return MLORA_OK;
     };
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < nch && h->lm_keep; ++i) {
         int c0, cnt;
         chunk_rows(i, c0, cnt);
         const int buf = i & 1;
@@ -820,11 +857,13 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         TF_CUDA(cudaEventRecord(h->ev_dz[buf], h->side));
         if (i >= 1 && (rc = queue_dh(i - 1))) return rc;
     }
-    if ((rc = queue_dh(nch - 1))) return rc;
-    if (loss_out) {
-        TfProf ps(h, s, MLORA_TF_PROF_OTHER);
-        launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
-        ++h->launches;
+    if (h->lm_keep) {
+        if ((rc = queue_dh(nch - 1))) return rc;
+        if (loss_out) {
+            TfProf ps(h, s, MLORA_TF_PROF_OTHER);
+            launch_loss_reduce(h->val_row, h->rb.pad_off, n_ad, loss_out, s);
+            ++h->launches;
+        }
     }
     // through the final norm: dh = RMSNorm_final'(dxf)
     if ((rc = tf_norm_bwd(h, h->snapf, h->gfinal, h->rstdf, 0, mp, s))) return rc;
@@ -1005,6 +1044,34 @@ extern "C" int mlora_tf_check_status(mlora_tf_t* h, void* stream) {
     TF_CUDA(cudaMemset(h->status, 0, sizeof(int)));
     if (st & ST_TIMEOUT) return tfail(MLORA_E_TIMEOUT, "a bounded device wait gave up");
     if (st & ST_RANGE) return tfail(MLORA_E_RANGE, "a token, target, adapter id or position was out of range");
+    return MLORA_OK;
+}
+
+extern "C" int mlora_tf_set_lm_backward(mlora_tf_t* h, int32_t mode) {
+    if (!h) return tfail(MLORA_E_ARG, "NULL handle");
+    if (mode != MLORA_LM_RECOMPUTE && mode != MLORA_LM_KEEP_LOGITS)
+        return tfail(MLORA_E_ARG, "unknown LM-head backward mode %d", mode);
+    if (mode == h->lm_keep) return MLORA_OK;
+    TF_CUDA(cudaDeviceSynchronize());   // no queued step may still use the buffers
+    const size_t n = (size_t)h->nc_tiles * TILE_M * h->Vpad;
+    auto drop = [&]() {
+        tf_free(h, reinterpret_cast<void**>(&h->dz[1]));
+        for (int b = 0; b < 2; ++b) tf_free(h, reinterpret_cast<void**>(&h->zbuf[b]));
+    };
+    if (mode == MLORA_LM_RECOMPUTE) {
+        drop();
+        h->lm_keep = 0;
+        return MLORA_OK;
+    }
+    int rc = tf_alloc_t(h, &h->dz[1], n);
+    for (int b = 0; b < 2 && rc == MLORA_OK; ++b) rc = tf_alloc_t(h, &h->zbuf[b], n);
+    if (rc == MLORA_OK && cudaMemset(h->dz[1], 0, n * sizeof(bf16)) != cudaSuccess)
+        rc = tfail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
+    if (rc != MLORA_OK) {
+        drop();
+        return rc;
+    }
+    h->lm_keep = 1;
     return MLORA_OK;
 }
 

@@ -18,7 +18,7 @@ from . import LOSS_KINDS, _Adam, _check, _LossInputs, _ptr, _stream, load_librar
 
 __all__ = ["PROJ", "TF_PROF_CLASSES", "TfHandle", "tf_create", "tf_destroy", "tf_forward",
            "tf_forward_backward", "tf_forward_backward_custom", "tf_optim_step", "tf_read_adapter",
-           "tf_get_steps", "tf_check_status", "tf_profile_enable", "tf_profile_read"]
+           "tf_get_steps", "tf_check_status", "tf_profile_enable", "tf_profile_read", "tf_set_lm_backward"]
 
 PROJ = ("q", "k", "v", "o", "gate", "up", "down")
 HEAD_DIM = 128
@@ -63,6 +63,7 @@ _SIGNATURES = {
     "mlora_tf_get_steps": (c_int32, [c_void_p, POINTER(c_int64), c_void_p]),
     "mlora_tf_check_status": (c_int32, [c_void_p, c_void_p]),
     "mlora_tf_profile_enable": (c_int32, [c_void_p, c_int32]),
+    "mlora_tf_set_lm_backward": (c_int32, [c_void_p, c_int32]),
     "mlora_tf_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_tf_kernel_launches": (c_int64, [c_void_p]),
     "mlora_tf_device_bytes": (c_int64, [c_void_p]),
@@ -245,6 +246,12 @@ def tf_get_steps(h: TfHandle, stream=None):
 
 def tf_check_status(h: TfHandle, stream=None) -> int:
     return int(_lib().mlora_tf_check_status(h.ptr, _stream(stream)))
+
+
+def tf_set_lm_backward(h: TfHandle, mode: str):
+    """LM-head backward mode: "recompute" (default) or "keep_logits"."""
+    from . import LM_BACKWARD_MODES
+    _check(_lib().mlora_tf_set_lm_backward(h.ptr, LM_BACKWARD_MODES[mode]))
 
 
 def tf_profile_enable(h: TfHandle, on: bool = True):

@@ -46,16 +46,19 @@ def _lib():
     __graft_entry__.build()
 
 
-def _make(cfg, base, ad, max_tokens):
+def _make(cfg, base, ad, max_tokens, lm=None):
     import rl_step_gb300.transformer as t
     dbase = {"E": dev(base["E"]), "Wout": dev(base["Wout"]), "final_norm": dev(base["final_norm"]),
              "attn_norm": [dev(g) for g in base["attn_norm"]], "mlp_norm": [dev(g) for g in base["mlp_norm"]],
              "W": {p: [dev(w) for w in base["W"][p]] for p in t.PROJ}}
     A = {p: [[dev(x) for x in row] for row in ad["A"][p]] for p in t.PROJ}
     B = {p: [[dev(x) for x in row] for row in ad["B"][p]] for p in t.PROJ}
-    return t.tf_create(cfg.vocab, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.n_layers,
-                       cfg.ranks, cfg.alphas, max_tokens, dbase, A, B, rope_theta=cfg.rope_theta,
-                       rms_eps=cfg.rms_eps)
+    h = t.tf_create(cfg.vocab, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.n_layers,
+                    cfg.ranks, cfg.alphas, max_tokens, dbase, A, B, rope_theta=cfg.rope_theta,
+                    rms_eps=cfg.rms_eps)
+    if lm is not None:
+        t.tf_set_lm_backward(h, lm)
+    return h
 
 
 def _oracle(cfg, base, ad):
@@ -146,11 +149,11 @@ def test_forward_matches_oracle(small):
     assert np.isfinite(lp).all() and err <= LP_TOL, err
 
 
-def _step_and_adam(prob, kind):
+def _step_and_adam(prob, kind, lm=None):
     import rl_step_gb300.transformer as t
     cfg, base, ad, b, lp0 = prob
     s = lp0 + b["sampler_noise"]
-    h = _make(cfg, base, ad, len(b["tokens"]))
+    h = _make(cfg, base, ad, len(b["tokens"]), lm)
     o = _oracle(cfg, base, ad)
     lp, loss = _gpu_step(h, b, kind, s)
     ref = _oracle_step(o, b, kind, s)
@@ -168,9 +171,38 @@ def _step_and_adam(prob, kind):
     assert t.tf_get_steps(h) == o.step
 
 
+@pytest.mark.parametrize("lm", ["recompute", "keep_logits"])
 @pytest.mark.parametrize("kind", ["ppo", "cross_entropy", "importance_sampling", "custom"])
-def test_step_and_adam_match_oracle(small, kind):
-    _step_and_adam(small, kind)
+def test_step_and_adam_match_oracle(small, kind, lm):
+    _step_and_adam(small, kind, lm)
+
+
+def test_lm_backward_modes_agree_over_three_chunks():
+    """Recomputing each LM-head chunk's logits and keeping them give bitwise
+    the same logprobs and losses, and the same gradients up to the arrival
+    order of the fp32 gradient atomics, on a batch of three LM-head chunks; the
+    kept-logits mode holds two fp32 logit chunks and a second dz chunk more."""
+    import rl_step_gb300.transformer as t
+    cfg = wt.get_tf_config("tf_small")
+    base, ad = wt.make_tf_base_weights(cfg), wt.make_tf_adapters(cfg)
+    b = wt.make_tf_batch(cfg, 40000)
+    N = len(b["tokens"])
+    res = {}
+    for lm in ("keep_logits", "recompute"):
+        h = _make(cfg, base, ad, N, lm)
+        lp, loss = t.tf_forward_backward(h, *_dargs(b), "cross_entropy", weights=dev(b["weights"]))
+        assert t.tf_check_status(h) == 0
+        g = {(a, l, p, fac): t.tf_read_adapter(h, a, l, p, fac, "grad").cpu().numpy()
+             for a in range(cfg.n_adapters) for l in range(cfg.n_layers) for p in t.PROJ for fac in ("A", "B")}
+        res[lm] = (lp.cpu().numpy(), loss.cpu().numpy(), g, h.device_bytes)
+        del h
+    (lp_k, loss_k, g_k, by_k), (lp_r, loss_r, g_r, by_r) = res["keep_logits"], res["recompute"]
+    assert np.array_equal(lp_k, lp_r) and np.array_equal(loss_k, loss_r)
+    assert max(rel_fro(g_r[k], g_k[k]) for k in g_k) <= 1e-4
+    tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
+    assert tiles > 256
+    vpad = (cfg.vocab + 63) // 64 * 64
+    assert by_k - by_r == 128 * 128 * vpad * (2 + 2 * 4)
 
 
 @pytest.mark.parametrize("kind", ["ppo", "custom"])

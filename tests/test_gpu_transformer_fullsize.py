@@ -48,7 +48,8 @@ def _lib():
     __graft_entry__.build()
 
 
-def test_full_size_prefix_parity_and_gradient_isolation():
+@pytest.mark.parametrize("lm", ["keep_logits", "recompute"])
+def test_full_size_prefix_parity_and_gradient_isolation(lm):
     import rl_step_gb300.transformer as t
     cfg = wt.get_tf_config("qwen3_8b_tf_ppo")
     base = wt.make_tf_base_weights(cfg)
@@ -62,7 +63,7 @@ def test_full_size_prefix_parity_and_gradient_isolation():
     w[rows] = 1.0
     assert (b["positions"][rows] == np.tile(np.arange(PREFIX), len(chosen))).all()
 
-    h = _make(cfg, base, ad, N)
+    h = _make(cfg, base, ad, N, lm)
     args = [dev(b[k]) for k in ("tokens", "targets", "positions", "adapter_ids")]
     lp, _ = t.tf_forward_backward(h, *args, "cross_entropy", weights=dev(w))
     assert t.tf_check_status(h) == 0
