@@ -580,6 +580,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC_OFF + 4);
     constexpr uint32_t TMEM_COLS = NUM_ACC * BN;
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    // WIDE: 256 x 512 tiles, each K step two N = 256 MMAs into TMEM columns
+    // 0-255 and 256-511; each CTA holds B columns [256 h + 128 rank, +128) of
+    // tile half h (the operand split of a cta_group::2 MMA), 16 KB apart
+    constexpr bool WIDE = BN > 256;
+    constexpr int BN_MMA = WIDE ? 256 : BN;
+    static_assert(!WIDE || (BN == 512 && NUM_ACC == 1), "wide tiles: 256 x 512, one accumulator");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -675,7 +681,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bool published = !leader;
                 const PairCoord c = pair_coord<BN>(p, t, cnt);
                 const int m0 = (c.mt + (int)rank) * BM;
-                const int n0 = c.nt * BN + (int)rank * (BN / 2);
+                const int n0 = c.nt * BN + (int)rank * (BN_MMA / 2);
                 const int nst = (c.nkb + SUB - 1) / SUB;
                 for (int ks = 0; ks < nst && ok; ++ks) {
                     if (ks == 1 && !published) {
@@ -690,7 +696,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t sa = sbase + stage * SL::STAGE_BYTES + h * SL::SUB_BYTES;
                         const int k = c.k0 + (ks * SUB + h) * BK;
                         load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), true);
-                        load_tile_b<BN / 2>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, 0, true);
+                        load_tile_b<BN_MMA / 2>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, 0, true);
+                        if (WIDE)
+                            load_tile_b<BN_MMA / 2>(sa + SL::A_BYTES + (BN_MMA / 2) * BK * 2, &maps.B, fb, p.B,
+                                                    n0 + BN_MMA, k, 0, true);
                     }
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -744,8 +753,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int sslot = 0;
             uint32_t sph = 0;
-            const uint32_t id_main = idesc_bf16(BN, p.A.mn_major, p.B.mn_major, 2 * BM);
-            const uint32_t id_ext = idesc_bf16(BN, p.Ax.mn_major, p.Bx.mn_major, 2 * BM);
+            const uint32_t id_main = idesc_bf16(BN_MMA, p.A.mn_major, p.B.mn_major, 2 * BM);
+            const uint32_t id_ext = idesc_bf16(BN_MMA, p.Ax.mn_major, p.Bx.mn_major, 2 * BM);
+            constexpr uint32_t B_HALF = ((BN_MMA / 2) * BK * 2) >> 4;   // second half's B, descriptor units
             // Descriptors of stage 0; a stage / K step only moves the start-address
             // field (bits 0-13, address >> 4), which stays below 2^14 for any
             // shared-memory address, so they are advanced by plain additions.  A
@@ -782,16 +792,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
                     const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP);
                     umma_bf16_pair(d_tmem, ad, bd, id_main, ks > 0 ? 1u : 0u);
+                    if (WIDE) umma_bf16_pair(d_tmem + BN_MMA, ad, bd + B_HALF, id_main, ks > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 1; kk < BK / 16; ++kk)
+                    for (int kk = 1; kk < BK / 16; ++kk) {
                         umma_bf16_pair(d_tmem, ad + kk * 2, bd + kk * b_step, id_main, 1u);
+                        if (WIDE) umma_bf16_pair(d_tmem + BN_MMA, ad + kk * 2, bd + B_HALF + kk * b_step, id_main, 1u);
+                    }
 #pragma unroll
                     for (int h = 1; h < SUB; ++h) {
                         if (ks * SUB + h >= c.nkb) break;
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
+                        for (int kk = 0; kk < BK / 16; ++kk) {
                             umma_bf16_pair(d_tmem, ad + h * SUB_STEP + kk * 2, bd + h * SUB_STEP + kk * b_step,
                                            id_main, 1u);
+                            if (WIDE)
+                                umma_bf16_pair(d_tmem + BN_MMA, ad + h * SUB_STEP + kk * 2,
+                                               bd + B_HALF + h * SUB_STEP + kk * b_step, id_main, 1u);
+                        }
                     }
                     umma_commit_pair_mc(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -949,8 +966,10 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         if (op.mn_major) return encode_2d(m, op, 64, 64);
         return encode_2d(m, op, 64, (uint32_t)rows_mn);
     };
+    constexpr int BN_MMA = BN > 256 ? 256 : BN;
     if (p.grouped || p.B.ad_rows != 0 || p.A.mn_major || !p.tile_counter) return cudaErrorInvalidValue;
-    if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN / 2)) return cudaErrorInvalidValue;
+    if (BN > 256 && p.Kx > 0) return cudaErrorInvalidValue;    // wide tiles carry no K extension
+    if (!enc(&maps.A, p.A, BM) || !enc(&maps.B, p.B, BN_MMA / 2)) return cudaErrorInvalidValue;
     if (p.Kx > 0) {
         if (p.Kx % BK || p.Ax.mn_major || !enc(&maps.Ax, p.Ax, BM) || !enc(&maps.Bx, p.Bx, BN / 2))
             return cudaErrorInvalidValue;
@@ -1023,6 +1042,18 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
         return launch_bn<256, 4, true>(p, s, num_sms, status);
     }
     if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8>(p, s, num_sms, status);
+    // a very long contraction (the LM head's dh, K = the vocabulary): 256 x 512
+    // tiles, so the 76 clusters' tiles in flight read the A band about half as
+    // often; one accumulator, whose unhidden epilogue is ~1 % of a tile here.
+    // Bands of 12 row pairs: 76 tiles in flight cover ~6 of a band's 8 column
+    // tiles, which balances the re-reads of A (per column tile not in flight)
+    // against those of B (per band).
+    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.K >= 65536 && p.Kx == 0 && p.N % 512 == 0 &&
+        p.tile_counter) {
+        GemmParams q = p;
+        q.group_m = 24;
+        return launch_pair<512, 4, 1, 1>(q, s, num_sms, status, nullptr);
+    }
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
     if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
