@@ -569,7 +569,8 @@ def run_ours(args, rank, world):
             "clock_adjusted_peak_tflops": (BF16_FLOP_PER_CLK_SM * n_sms * clk["sm_mhz"] * 1e6 / 1e12)
                                           if clk.get("sm_mhz") else None},
         "lm_backward": lm_modes,
-        "roofline": {"kernel": "tc_gemm_pair_kernel<256,3,2,2> (base, LoRA-extension and LM-head GEMMs)",
+        "roofline": {"kernel": "the CTA-pair tcgen05 GEMM: tc_gemm_pair_kernel<256,3,2,2> (base, LoRA-extension "
+                               "and LM-head forward GEMMs) and <512,4,1,1> (LM-head dh)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_tc,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
                      "frac": (achieved / peak_tc) if achieved else None, "traffic": traffic,
