@@ -7,6 +7,10 @@ definition evaluated with only the CUDA path's stored values rounded to bf16
 the GPU parity tests' bounds are derived from these figures.  At the 8B widths
 with four layers (not run here: minutes of fp64 at full widths) the same model
 gives logprob errors up to 0.057 and gradient errors up to 3.2 % (median 2.1 %).
+Left unrounded, the LM head's input changes that logprob figure to 0.059
+(BF16StorageModel.round_lm_input = False): the error comes from the layers'
+stored activations, so a split (hi + lo) bf16 LM-head input would not bring
+the block's logprobs under 2e-2.
 """
 import numpy as np
 
