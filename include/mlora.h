@@ -399,6 +399,8 @@ int mlora_check_status(mlora_t* h, void* stream);
  * mlora_profile_read synchronises those events and returns, per class, the
  * accumulated milliseconds and launch counts since the last reset
  * (ms_out / launches_out: HOST arrays of MLORA_PROF_CLASSES entries).
+ * MLORA_PROF_LM_DZ times how the LM-head backward forms dz: the elementwise
+ * pass over kept logits, or the recompute GEMM in the default mode.
  * Enabling costs two event records per launch. */
 enum {
     MLORA_PROF_ROUTING = 0, MLORA_PROF_EMBED = 1, MLORA_PROF_SHRINK = 2,
