@@ -65,6 +65,8 @@ struct EpiParams {
     int part_ld = 0;                // pitch of a row of partials (multiple of 4)
     int V = 0, Vpad = 0;
     int64_t out_row_shift = 0;      // output row = row + out_row_shift (chunk buffers)
+    int64_t out_rows = 0;           // EPI_LMFWD (kept logits) / EPI_LMDZ: rows of out0's buffer;
+                                    // > 0 lets the CTA-pair engine write out0 by TMA stores
     const float* gv = nullptr;      // EPI_LMDZ: dL/dl per padded row
     const float* lse = nullptr;     // EPI_LMDZ: log-sum-exp per padded row
     // adapter gradients
@@ -199,12 +201,61 @@ __device__ __forceinline__ void epi_row_begin(EpiRowState& st) {
     st.found = 0;
 }
 
+// EPI_LMFWD's running statistics of one row over the chunk's 32 columns
+// C[row][col0 .. col0+31]: the maximum and the sum of exp(x - max) over the
+// columns < V (rescaled as the maximum grows), and the target's logit.
+__device__ __forceinline__ void lmfwd_stats(const EpiParams& ep, int64_t row, int col0, const float* acc,
+                                            EpiRowState& st) {
+    const float LOG2E = 1.4426950408889634f;
+    int t = ep.tgt[row];
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        bool ok = (col0 + j) < ep.V;
+        cm = fmaxf(cm, ok ? acc[j] : -INFINITY);
+        if (col0 + j == t) { st.zt = acc[j]; st.found = 1; }
+    }
+    float mn = fmaxf(st.m, cm);
+    if (mn > -INFINITY) {
+        float sc = exp2f((st.m - mn) * LOG2E);
+        float sum = 0.f;
+        float mb = mn * LOG2E;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            sum += ((col0 + j) < ep.V) ? exp2f(fmaf(acc[j], LOG2E, -mb)) : 0.f;
+        st.s = st.s * sc + sum;
+        st.m = mn;
+    }
+}
+
+// EPI_LMDZ's values of one chunk: dz = g (onehot(y) - exp(z - lse)) for the
+// columns < V, 0 beyond.  The same arithmetic, in the same order, as the dz
+// pass over kept fp32 logits: the recomputed accumulator is bitwise the
+// forward's, so both LM-head backward modes give the same dz.
+__device__ __forceinline__ void lmdz_values(const EpiParams& ep, int64_t row, int col0, const float* acc,
+                                            float* o) {
+    const float LOG2E = 1.4426950408889634f;
+    const float gr = ep.gv[row];
+    if (gr == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0.f;
+    } else {
+        const float lb = ep.lse[row] * LOG2E;
+        const int y = ep.tgt[row];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int v = col0 + j;
+            const float pr = exp2f(fmaf(acc[j], LOG2E, -lb));
+            o[j] = v < ep.V ? gr * ((v == y ? 1.f : 0.f) - pr) : 0.f;
+        }
+    }
+}
+
 // acc holds C[row][col0 .. col0+31].  `row` is the global output row (padded
 // token row in dense mode, output-feature row in grouped mode).
 template <typename T>
 __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int col0, int adapter,
                                           float* acc, EpiRowState& st) {
-    const float LOG2E = 1.4426950408889634f;
     switch (ep.kind) {
     case EPI_SILU: {
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
@@ -282,45 +333,11 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     case EPI_LMFWD: {
         if (ep.out0 && col0 < ep.Vpad)     // keep the logits (fp32) for the backward
             store32_stream(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
-        int t = ep.tgt[row];
-        float cm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            bool ok = (col0 + j) < ep.V;
-            cm = fmaxf(cm, ok ? acc[j] : -INFINITY);
-            if (col0 + j == t) { st.zt = acc[j]; st.found = 1; }
-        }
-        float mn = fmaxf(st.m, cm);
-        if (mn > -INFINITY) {
-            float sc = exp2f((st.m - mn) * LOG2E);
-            float sum = 0.f;
-            float mb = mn * LOG2E;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                sum += ((col0 + j) < ep.V) ? exp2f(fmaf(acc[j], LOG2E, -mb)) : 0.f;
-            st.s = st.s * sc + sum;
-            st.m = mn;
-        }
+        lmfwd_stats(ep, row, col0, acc, st);
     } break;
     case EPI_LMDZ: {
-        // The same arithmetic, in the same order, as the dz pass over kept fp32
-        // logits: the recomputed accumulator is bitwise the forward's, so both
-        // LM-head backward modes give the same dz.
-        const float gr = ep.gv[row];
         float o[32];
-        if (gr == 0.f) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0.f;
-        } else {
-            const float lb = ep.lse[row] * LOG2E;
-            const int y = ep.tgt[row];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int v = col0 + j;
-                const float pr = exp2f(fmaf(acc[j], LOG2E, -lb));
-                o[j] = v < ep.V ? gr * ((v == y ? 1.f : 0.f) - pr) : 0.f;
-            }
-        }
+        lmdz_values(ep, row, col0, acc, o);
         store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, o);
     } break;
     case EPI_SHRINK_SEL: {

@@ -150,8 +150,85 @@ __device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t
     }
 }
 
+// Staged-store epilogue of the LM head (OST = 4: the forward's kept fp32
+// logits, with the row's log-sum-exp statistics; OST = 2: the recompute
+// GEMM's bf16 dz).  Each thread still owns one row, but instead of writing
+// its 32 columns as eight (fp32) or four (bf16) 16-byte pieces of one row --
+// 32 rows per warp store, each piece a partial sector at the L2 -- the warp
+// writes the 32 x 32 chunk into a staging box in shared memory and one lane
+// stores the box with TMA, whole 128- or 64-byte row segments.  Two boxes
+// per warp alternate, so the box of chunk c is refilled only after the TMA
+// store of chunk c - 2 has read it (wait_group.read 1).
+//   fp32 box: rows of 128 B, 128-byte swizzle (16-byte piece j of row r at
+//             piece j ^ (r & 7));  bf16 box: rows of 64 B, 64-byte swizzle
+//             (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor map's
+//             swizzle and keep each quarter-warp's st.shared.v4 on distinct
+//             banks.
+// `row_ok` is uniform over the warp here (whole tiles, M a multiple of 128);
+// y0 is the warp's first output row, `nbox` counts the warp's boxes.
+template <int OST>
+__device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensorMap* cmap, int64_t row,
+                                             int col0, const uint32_t (&r)[32], EpiRowState& st, uint32_t stg,
+                                             uint32_t& nbox, int y0) {
+    const int lane = threadIdx.x & 31;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    const uint32_t box = stg + (nbox & 1u) * (uint32_t)(32 * 32 * OST);
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    if (OST == 4) {
+        lmfwd_stats(p.ep, row, col0, v, st);
+        const uint32_t rb = box + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(rb + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    } else {
+        float o[32];
+        lmdz_values(p.ep, row, col0, v, o);
+        const uint32_t rb = box + lane * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(rb + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(o[8 * j], o[8 * j + 1]),
+                         pack_bf16x2(o[8 * j + 2], o[8 * j + 3]), pack_bf16x2(o[8 * j + 4], o[8 * j + 5]),
+                         pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
+    }
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(cmap, box, col0, y0);
+        bulk_commit();
+    }
+    ++nbox;
+}
+
+template <int BN, int OST>
+__device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const CUtensorMap* cmap, uint32_t tbase,
+                                                    int64_t row, bool row_ok, int col_base, int nt, uint32_t stg,
+                                                    uint32_t& nbox, int y0) {
+    static_assert((BN / 32) % 2 == 0, "chunks are processed in pairs");
+    if (!row_ok) return;
+    EpiRowState st;
+    epi_row_begin(st);
+    uint32_t ra[32], rb[32];
+    tmem_ld32(tbase, ra);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ch += 2) {
+        tmem_ld_wait();
+        tmem_ld32(tbase + (ch + 1) * 32, rb);
+        if (col_base + ch * 32 < p.N) staged_chunk<OST>(p, cmap, row, col_base + ch * 32, ra, st, stg, nbox, y0);
+        tmem_ld_wait();
+        if (ch + 2 < BN / 32) tmem_ld32(tbase + (ch + 2) * 32, ra);
+        if (col_base + (ch + 1) * 32 < p.N)
+            staged_chunk<OST>(p, cmap, row, col_base + (ch + 1) * 32, rb, st, stg, nbox, y0);
+    }
+    epi_row_end(p.ep, row, nt, st);
+}
+
 struct TcMaps {
     CUtensorMap A, B, Ax, Bx;
+    CUtensorMap C;     // output of the staged-store epilogues (32 x 32 boxes)
 };
 
 struct TileCoord {
@@ -453,15 +530,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // the accumulator on the leader's "tmem empty" barrier.  Used for GEMMs whose
 // B operand is shared by all rows (the LM head); the per-adapter GEMMs keep
 // the single-CTA kernel.
-template <int BN, int STAGES, int NUM_ACC, int SUB>
+// OST: 0, the epilogue stores straight from registers; 4 or 2, it writes its
+// output (fp32 or bf16) through two 32 x 32 staging boxes per epilogue warp
+// and TMA stores (see epilogue_row_staged).
+template <int BN, int STAGES, int NUM_ACC, int SUB, int OST = 0>
 struct SmemLayoutPair {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (BN / 2) * BK * 2;
     static constexpr int SUB_BYTES = A_BYTES + B_BYTES;   // one 64-wide K block: A rows, then B rows
     static constexpr int STAGE_BYTES = SUB * SUB_BYTES;   // a stage holds SUB consecutive K blocks
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BOX_BYTES = 32 * 32 * OST;        // one staging box
+    static constexpr int STG_OFF = TILES_BYTES;            // 1024-aligned (swizzled boxes)
+    static constexpr int STG_BYTES = 4 * 2 * BOX_BYTES;    // 4 epilogue warps x 2 boxes
     static constexpr int SCHED = 4;                     // tile-index ring depth
-    static constexpr int BAR_OFF = TILES_BYTES;
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * SCHED;
     static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int MISC_OFF = SLOT_OFF + SCHED * 4;
@@ -560,10 +643,11 @@ __device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_l
     return true;
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false>
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int OST = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, OST>;
+    static_assert(OST == 0 || (!MERGE && BN == 256), "staged stores: the LM head's 256-wide tiles");
     static_assert(SL::SCHED == 4, "sched_take assumes a 4-slot ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -843,6 +927,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
+        const uint32_t stg = sbase + SL::STG_OFF + (uint32_t)(warp - 2) * 2u * SL::BOX_BYTES;
+        uint32_t nbox = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         int sslot = 0;
@@ -873,6 +959,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool tile_ok = (my_mt - p.mt_base) < cnt && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
             if (MERGE) epilogue_row_merge<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0);
+            else if (OST) epilogue_row_staged<BN, OST>(p, &maps.C, tbase, row, tile_ok, c.nt * BN, c.nt, stg, nbox,
+                                                       (int)((int64_t)my_mt * BM + 32 * q + p.ep.out_row_shift));
             else epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
             tc_fence_before();
             __syncwarp();
@@ -882,6 +970,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
         }
+        if (OST && lane == 0) bulk_wait_all();   // the staged stores are written before the CTA exits
     }
 
     tc_fence_before();
@@ -957,9 +1046,27 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
     return cudaGetLastError();
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false>
+// Tensor map of a staged-store output: [rows x cols] of fp32 (esize 4, 128-byte
+// swizzle) or bf16 (esize 2, 64-byte swizzle), row pitch ld elements, 32 x 32
+// boxes.  TMA stores need a 16-byte aligned base and pitch.
+bool encode_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t ld, int esize) {
+    if (!ptr || reinterpret_cast<uintptr_t>(ptr) % 16 || (ld * esize) % 16 || rows <= 0 || cols <= 0 ||
+        rows >= (1LL << 31) || cols >= (1LL << 31))
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * esize)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          esize == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int OST = 0>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB>;
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, OST>;
     TcMaps maps;
     auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
         if (!operand_ok(op)) return false;
@@ -977,9 +1084,18 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         maps.Ax = maps.A;
         maps.Bx = maps.B;
     }
+    if (OST) {
+        // the staged-store epilogue writes whole 32-row boxes: whole row tiles,
+        // and the lowest output row (mt_base's first row) may not be negative
+        if (p.M % BM || p.ep.out_rows <= 0 || (int64_t)p.mt_base * BM + p.ep.out_row_shift < 0 ||
+            !encode_out(&maps.C, p.ep.out0, p.ep.out_rows, p.ep.Vpad, p.ep.ld0, OST))
+            return cudaErrorInvalidValue;
+    } else {
+        maps.C = maps.A;
+    }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, OST>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1003,7 +1119,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     cfg.numAttrs = 1;
     cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);   // fresh tile counter
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE>, maps, p, status, dbg);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, OST>, maps, p, status, dbg);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1056,8 +1172,15 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
     }
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
-    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
+    if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter) {
+        // the LM head's big outputs (kept fp32 logits, recomputed bf16 dz) leave
+        // through shared memory and TMA stores when the caller gave their rows
+        if (p.ep.kind == EPI_LMFWD && p.ep.out0 && p.ep.out_rows > 0)
+            return launch_pair<256, 3, 2, 2, false, 4>(p, s, num_sms, status, nullptr);
+        if (p.ep.kind == EPI_LMDZ && p.ep.out_rows > 0)
+            return launch_pair<256, 3, 2, 2, false, 2>(p, s, num_sms, status, nullptr);
         return launch_pair<256, 3, 2, 2>(p, s, num_sms, status, nullptr);
+    }
     return launch_bn<256, 4>(p, s, num_sms, status);
 }
 

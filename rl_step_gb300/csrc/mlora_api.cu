@@ -706,6 +706,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
                 p.ep.kind = EPI_LMDZ; p.ep.tgt = h->tgt_pad; p.ep.gv = h->gvec; p.ep.lse = h->lse;
                 p.ep.V = V; p.ep.Vpad = h->Vpad;
                 p.ep.out0 = h->dz[0]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+                p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
                 if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
             }
             GemmParams p = dh_params(c0, cnt, h->dz[0]);
@@ -745,6 +746,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
             p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
             p.ep.out0 = h->zbuf[buf]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+            p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
         }
         {

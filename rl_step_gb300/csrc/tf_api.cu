@@ -813,6 +813,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
                 GemmParams p = lm_fwd_params(c0, cnt);
                 p.ep.kind = EPI_LMDZ; p.ep.gv = h->gvec; p.ep.lse = h->lse;
                 p.ep.out0 = h->dz[0]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+                p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
                 if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_DZ))) return rc;
             }
             GemmParams p = dh_params(c0, cnt, h->dz[0]);
@@ -837,6 +838,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         {
             GemmParams p = lm_fwd_params(c0, cnt);
             p.ep.out0 = h->zbuf[buf]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
+            p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_FWD))) return rc;
         }
         {
