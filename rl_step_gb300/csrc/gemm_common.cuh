@@ -67,6 +67,7 @@ struct EpiParams {
     int64_t out_row_shift = 0;      // output row = row + out_row_shift (chunk buffers)
     int64_t out_rows = 0;           // EPI_LMFWD (kept logits) / EPI_LMDZ: rows of out0's buffer;
                                     // > 0 lets the CTA-pair engine write out0 by TMA stores
+                                    // (the other staged kinds write M rows)
     const float* gv = nullptr;      // EPI_LMDZ: dL/dl per padded row
     const float* lse = nullptr;     // EPI_LMDZ: log-sum-exp per padded row
     // adapter gradients
@@ -251,6 +252,24 @@ __device__ __forceinline__ void lmdz_values(const EpiParams& ep, int64_t row, in
     }
 }
 
+// EPI_SILU's second output: a = silu(acc)
+__device__ __forceinline__ void silu_values(const float* acc, float* a) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = acc[j] * sigmoidf_(acc[j]);
+}
+
+// EPI_DSILU: u (the saved pre-activation) becomes dL/du = acc * silu'(u).
+// Hardware reciprocal, as in EPI_DSWIGLU: with the IEEE division this
+// epilogue, not the tensor core, set the W2-backward GEMM's pace (16 % slower
+// in a same-box comparison); the forward SiLU keeps it.
+__device__ __forceinline__ void dsilu_values(const float* acc, float* u) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float s = __fdividef(1.0f, 1.0f + __expf(-u[j]));
+        u[j] = acc[j] * (s * (1.f + u[j] * (1.f - s)));
+    }
+}
+
 // acc holds C[row][col0 .. col0+31].  `row` is the global output row (padded
 // token row in dense mode, output-feature row in grouped mode).
 template <typename T>
@@ -260,8 +279,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     case EPI_SILU: {
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
         float a[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = acc[j] * sigmoidf_(acc[j]);
+        silu_values(acc, a);
         store32<T>(reinterpret_cast<T*>(ep.out1) + row * ep.ld1 + col0, a);
     } break;
     case EPI_RESID: {
@@ -314,14 +332,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     case EPI_DSILU: {
         float u[32];
         load32<T>(reinterpret_cast<const T*>(ep.aux) + row * ep.ld_aux + col0, u);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            // hardware reciprocal, as in EPI_DSWIGLU: with the IEEE division this
-            // epilogue, not the tensor core, set the W2-backward GEMM's pace (16 %
-            // slower in a same-box comparison); the forward SiLU keeps it
-            const float s = __fdividef(1.0f, 1.0f + __expf(-u[j]));
-            u[j] = acc[j] * (s * (1.f + u[j] * (1.f - s)));
-        }
+        dsilu_values(acc, u);
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, u);
     } break;
     case EPI_SHRINK: {

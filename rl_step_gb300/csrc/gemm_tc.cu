@@ -150,63 +150,127 @@ __device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t
     }
 }
 
-// Staged-store epilogue of the LM head (OST = 4: the forward's kept fp32
-// logits, with the row's log-sum-exp statistics; OST = 2: the recompute
-// GEMM's bf16 dz).  Each thread still owns one row, but instead of writing
-// its 32 columns as eight (fp32) or four (bf16) 16-byte pieces of one row --
-// 32 rows per warp store, each piece a partial sector at the L2 -- the warp
-// writes the 32 x 32 chunk into a staging box in shared memory and one lane
-// stores the box with TMA, whole 128- or 64-byte row segments.  Two boxes
-// per warp alternate, so the box of chunk c is refilled only after the TMA
-// store of chunk c - 2 has read it (wait_group.read 1).
-//   fp32 box: rows of 128 B, 128-byte swizzle (16-byte piece j of row r at
-//             piece j ^ (r & 7));  bf16 box: rows of 64 B, 64-byte swizzle
-//             (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor map's
-//             swizzle and keep each quarter-warp's st.shared.v4 on distinct
-//             banks.
-// `row_ok` is uniform over the warp here (whole tiles, M a multiple of 128);
-// y0 is the warp's first output row, `nbox` counts the warp's boxes.
-template <int OST>
-__device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensorMap* cmap, int64_t row,
-                                             int col0, const uint32_t (&r)[32], EpiRowState& st, uint32_t stg,
-                                             uint32_t& nbox, int y0) {
+// Staged-store epilogues.  Each epilogue thread owns one row of the tile; a
+// direct store writes the row's 32 columns of a chunk as 16-byte pieces, so
+// one warp store instruction touches 32 rows, each piece a partial sector at
+// the L2, and the load/store unit that also issues the producer's TMA copies
+// and the MMA thread's tcgen05 instructions is busy for 32 wavefronts.  An
+// ablation of the W1 forward GEMM (16,384 tokens, 8B widths) read the tensor
+// pipe 88 % active without its epilogue's stores and math, 81 % with the
+// math alone and 76 % with both.  Here the warp writes each 32 x 32 chunk of
+// an output into a box in shared memory (st.shared.v4, conflict-free) and
+// one lane writes the box out with a TMA store: whole 64- or 128-byte row
+// segments.  The arithmetic is epi_chunk's, helper for helper.
+//   SK_LMFWD  kept fp32 logits (box F -> map C) + the row's log-sum-exp state
+//   SK_LMDZ   recomputed bf16 dz (box 0 -> map C)
+//   SK_SILU   u = acc (box 0 -> map C) and act = silu(acc) (box 1 -> map D)
+//   SK_DSILU  du = acc * silu'(u), u read directly (box 0 -> map C)
+//   SK_RESID  h32 += acc (box F -> map D), its bf16 copy (box 0 -> map C)
+// Boxes: fp32 32 x 32 with 128-byte rows and 128-byte swizzle (16-byte piece
+// j of row r at piece j ^ (r & 7)); bf16 32 x 32 with 64-byte rows and
+// 64-byte swizzle (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor
+// maps' swizzle and put each quarter-warp's st.shared.v4 on distinct banks.
+// A warp owns NBUF sets of boxes; the set of chunk c is refilled once the
+// TMA stores of chunk c - NBUF have read it (one bulk group per chunk).
+enum { SK_NONE = 0, SK_LMFWD = 1, SK_LMDZ = 2, SK_SILU = 3, SK_DSILU = 4, SK_RESID = 5 };
+
+template <int SK>
+struct StagedCfg {
+    static constexpr bool F32 = SK == SK_LMFWD || SK == SK_RESID;      // an fp32 box, first in the set
+    static constexpr int N16 = SK == SK_SILU ? 2 : (SK == SK_LMFWD ? 0 : 1);   // bf16 boxes after it
+    static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;
+    static constexpr int NBUF = SK == SK_NONE ? 0 : (SET_BYTES <= 4096 ? 2 : 1);
+    static constexpr int WARP_BYTES = NBUF * SET_BYTES;              // a multiple of 1024
+};
+
+__device__ __forceinline__ void box_row_f32(uint32_t box, int lane, const float* v) {
+    const uint32_t rb = box + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(rb + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                     __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+}
+
+__device__ __forceinline__ void box_row_bf16(uint32_t box, int lane, const float* v) {
+    const uint32_t rb = box + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(rb + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                     pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                     pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+}
+
+// One chunk C[row][col0 .. col0+31] of a staged epilogue.  `stg` is the
+// warp's staging area, y0 its first output row, `nbox` counts its chunks.
+template <int SK>
+__device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensorMap* mc, const CUtensorMap* md,
+                                             int64_t row, int col0, const uint32_t (&r)[32], EpiRowState& st,
+                                             uint32_t stg, uint32_t& nbox, int y0) {
+    using CF = StagedCfg<SK>;
     const int lane = threadIdx.x & 31;
+    const EpiParams& ep = p.ep;
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-    const uint32_t box = stg + (nbox & 1u) * (uint32_t)(32 * 32 * OST);
-    if (lane == 0) bulk_wait_read<1>();
+    // the directly read operand first, so its latency overlaps the wait below
+    if (SK == SK_DSILU) {
+        float u[32];
+        load32<bf16>(reinterpret_cast<const bf16*>(ep.aux) + row * ep.ld_aux + col0, u);
+        dsilu_values(v, u);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = u[j];
+    } else if (SK == SK_RESID) {
+        float h[32];
+        load32<float>(ep.f32 + row * ep.ldf + col0, h);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += h[j];
+    }
+    const uint32_t set = stg + (nbox % (uint32_t)CF::NBUF) * (uint32_t)CF::SET_BYTES;
+    const uint32_t b16 = set + (CF::F32 ? 4096u : 0u);
+    if (lane == 0) bulk_wait_read<CF::NBUF - 1>();
     __syncwarp();
-    if (OST == 4) {
-        lmfwd_stats(p.ep, row, col0, v, st);
-        const uint32_t rb = box + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            st_shared_v4(rb + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-    } else {
+    if (SK == SK_LMFWD) {
+        lmfwd_stats(ep, row, col0, v, st);
+        box_row_f32(set, lane, v);
+    } else if (SK == SK_LMDZ) {
         float o[32];
-        lmdz_values(p.ep, row, col0, v, o);
-        const uint32_t rb = box + lane * 64;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            st_shared_v4(rb + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(o[8 * j], o[8 * j + 1]),
-                         pack_bf16x2(o[8 * j + 2], o[8 * j + 3]), pack_bf16x2(o[8 * j + 4], o[8 * j + 5]),
-                         pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
+        lmdz_values(ep, row, col0, v, o);
+        box_row_bf16(b16, lane, o);
+    } else if (SK == SK_SILU) {
+        box_row_bf16(b16, lane, v);
+        float a[32];
+        silu_values(v, a);
+        box_row_bf16(b16 + 2048, lane, a);
+    } else if (SK == SK_DSILU) {
+        box_row_bf16(b16, lane, v);
+    } else {   // SK_RESID
+        box_row_f32(set, lane, v);
+        if (ep.out0) box_row_bf16(b16, lane, v);
     }
     fence_async_shared();
     __syncwarp();
     if (lane == 0) {
-        tma_store_2d(cmap, box, col0, y0);
+        if (SK == SK_LMFWD) tma_store_2d(mc, set, col0, y0);
+        if (SK == SK_LMDZ || SK == SK_DSILU) tma_store_2d(mc, b16, col0, y0);
+        if (SK == SK_SILU) {
+            tma_store_2d(mc, b16, col0, y0);
+            tma_store_2d(md, b16 + 2048, col0, y0);
+        }
+        if (SK == SK_RESID) {
+            tma_store_2d(md, set, col0, y0);
+            if (ep.out0) tma_store_2d(mc, b16, col0, y0);
+        }
         bulk_commit();
     }
     ++nbox;
 }
 
-template <int BN, int OST>
-__device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const CUtensorMap* cmap, uint32_t tbase,
-                                                    int64_t row, bool row_ok, int col_base, int nt, uint32_t stg,
-                                                    uint32_t& nbox, int y0) {
+// The staged epilogue of one thread's row; `row_ok` is uniform over the warp
+// here (whole row tiles: M is a multiple of 128).
+template <int BN, int SK>
+__device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const CUtensorMap* mc,
+                                                    const CUtensorMap* md, uint32_t tbase, int64_t row, bool row_ok,
+                                                    int col_base, int nt, uint32_t stg, uint32_t& nbox, int y0) {
     static_assert((BN / 32) % 2 == 0, "chunks are processed in pairs");
     if (!row_ok) return;
     EpiRowState st;
@@ -217,18 +281,19 @@ __device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const C
     for (int ch = 0; ch < BN / 32; ch += 2) {
         tmem_ld_wait();
         tmem_ld32(tbase + (ch + 1) * 32, rb);
-        if (col_base + ch * 32 < p.N) staged_chunk<OST>(p, cmap, row, col_base + ch * 32, ra, st, stg, nbox, y0);
+        if (col_base + ch * 32 < p.N)
+            staged_chunk<SK>(p, mc, md, row, col_base + ch * 32, ra, st, stg, nbox, y0);
         tmem_ld_wait();
         if (ch + 2 < BN / 32) tmem_ld32(tbase + (ch + 2) * 32, ra);
         if (col_base + (ch + 1) * 32 < p.N)
-            staged_chunk<OST>(p, cmap, row, col_base + (ch + 1) * 32, rb, st, stg, nbox, y0);
+            staged_chunk<SK>(p, mc, md, row, col_base + (ch + 1) * 32, rb, st, stg, nbox, y0);
     }
     epi_row_end(p.ep, row, nt, st);
 }
 
 struct TcMaps {
     CUtensorMap A, B, Ax, Bx;
-    CUtensorMap C;     // output of the staged-store epilogues (32 x 32 boxes)
+    CUtensorMap C, D;  // outputs of the staged-store epilogues (32 x 32 boxes)
 };
 
 struct TileCoord {
@@ -530,19 +595,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // the accumulator on the leader's "tmem empty" barrier.  Used for GEMMs whose
 // B operand is shared by all rows (the LM head); the per-adapter GEMMs keep
 // the single-CTA kernel.
-// OST: 0, the epilogue stores straight from registers; 4 or 2, it writes its
-// output (fp32 or bf16) through two 32 x 32 staging boxes per epilogue warp
-// and TMA stores (see epilogue_row_staged).
-template <int BN, int STAGES, int NUM_ACC, int SUB, int OST = 0>
+// SK: the staged-store epilogue kind (SK_NONE: stores straight from
+// registers); its four epilogue warps' staging boxes follow the stages.
+template <int BN, int STAGES, int NUM_ACC, int SUB, int SK = SK_NONE>
 struct SmemLayoutPair {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (BN / 2) * BK * 2;
     static constexpr int SUB_BYTES = A_BYTES + B_BYTES;   // one 64-wide K block: A rows, then B rows
     static constexpr int STAGE_BYTES = SUB * SUB_BYTES;   // a stage holds SUB consecutive K blocks
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int BOX_BYTES = 32 * 32 * OST;        // one staging box
+    static constexpr int STG_WARP = StagedCfg<SK>::WARP_BYTES;
     static constexpr int STG_OFF = TILES_BYTES;            // 1024-aligned (swizzled boxes)
-    static constexpr int STG_BYTES = 4 * 2 * BOX_BYTES;    // 4 epilogue warps x 2 boxes
+    static constexpr int STG_BYTES = 4 * STG_WARP;         // 4 epilogue warps
     static constexpr int SCHED = 4;                     // tile-index ring depth
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * SCHED;
@@ -643,11 +707,11 @@ __device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_l
     return true;
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int OST = 0>
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int SK = SK_NONE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, OST>;
-    static_assert(OST == 0 || (!MERGE && BN == 256), "staged stores: the LM head's 256-wide tiles");
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, SK>;
+    static_assert(SK == SK_NONE || (!MERGE && BN == 256), "staged stores: 256-wide tiles");
     static_assert(SL::SCHED == 4, "sched_take assumes a 4-slot ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -927,7 +991,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
-        const uint32_t stg = sbase + SL::STG_OFF + (uint32_t)(warp - 2) * 2u * SL::BOX_BYTES;
+        const uint32_t stg = sbase + SL::STG_OFF + (uint32_t)(warp - 2) * (uint32_t)SL::STG_WARP;
         uint32_t nbox = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -959,8 +1023,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool tile_ok = (my_mt - p.mt_base) < cnt && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
             if (MERGE) epilogue_row_merge<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0);
-            else if (OST) epilogue_row_staged<BN, OST>(p, &maps.C, tbase, row, tile_ok, c.nt * BN, c.nt, stg, nbox,
-                                                       (int)((int64_t)my_mt * BM + 32 * q + p.ep.out_row_shift));
+            else if (SK != SK_NONE)
+                epilogue_row_staged<BN, SK>(p, &maps.C, &maps.D, tbase, row, tile_ok, c.nt * BN, c.nt, stg, nbox,
+                                            (int)((int64_t)my_mt * BM + 32 * q + p.ep.out_row_shift));
             else epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
             tc_fence_before();
             __syncwarp();
@@ -970,7 +1035,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
         }
-        if (OST && lane == 0) bulk_wait_all();   // the staged stores are written before the CTA exits
+        if (SK != SK_NONE && lane == 0) bulk_wait_all();   // staged stores written before the CTA exits
     }
 
     tc_fence_before();
@@ -1064,9 +1129,57 @@ bool encode_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t l
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int OST = 0>
+bool out_aligned(const void* ptr, int64_t ld, int esize) {
+    return ptr && reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && (ld * esize) % 16 == 0;
+}
+
+// The staged-store kind of a CTA-pair launch, or SK_NONE: whole row tiles
+// (M a multiple of 128) and outputs a TMA store can address.
+int staged_kind(const GemmParams& p) {
+    if (p.M % BM) return SK_NONE;
+    const EpiParams& e = p.ep;
+    switch (e.kind) {
+    case EPI_LMFWD:
+        return e.out0 && e.out_rows > 0 && out_aligned(e.out0, e.ld0, 4) ? SK_LMFWD : SK_NONE;
+    case EPI_LMDZ:
+        return e.out_rows > 0 && out_aligned(e.out0, e.ld0, 2) ? SK_LMDZ : SK_NONE;
+    case EPI_SILU:
+        return out_aligned(e.out0, e.ld0, 2) && out_aligned(e.out1, e.ld1, 2) ? SK_SILU : SK_NONE;
+    case EPI_DSILU:
+        return out_aligned(e.out0, e.ld0, 2) ? SK_DSILU : SK_NONE;
+    case EPI_RESID:
+        return out_aligned(e.f32, e.ldf, 4) && (!e.out0 || out_aligned(e.out0, e.ld0, 2)) ? SK_RESID : SK_NONE;
+    default:
+        return SK_NONE;
+    }
+}
+
+// Output maps of a staged kind (the box layouts of staged_chunk).
+template <int SK>
+bool encode_staged(TcMaps& maps, const GemmParams& p) {
+    const EpiParams& e = p.ep;
+    switch (SK) {
+    case SK_LMFWD:
+        return encode_out(&maps.C, e.out0, e.out_rows, e.Vpad, e.ld0, 4);
+    case SK_LMDZ:
+        return encode_out(&maps.C, e.out0, e.out_rows, e.Vpad, e.ld0, 2);
+    case SK_SILU:
+        return encode_out(&maps.C, e.out0, p.M, p.N, e.ld0, 2) && encode_out(&maps.D, e.out1, p.M, p.N, e.ld1, 2);
+    case SK_DSILU:
+        return encode_out(&maps.C, e.out0, p.M, p.N, e.ld0, 2);
+    case SK_RESID:
+        if (!encode_out(&maps.D, e.f32, p.M, p.N, e.ldf, 4)) return false;
+        if (e.out0) return encode_out(&maps.C, e.out0, p.M, p.N, e.ld0, 2);
+        maps.C = maps.D;
+        return true;
+    default:
+        return true;
+    }
+}
+
+template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int SK = SK_NONE>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* status, int* dbg) {
-    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, OST>;
+    using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, SK>;
     TcMaps maps;
     auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
         if (!operand_ok(op)) return false;
@@ -1084,18 +1197,18 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         maps.Ax = maps.A;
         maps.Bx = maps.B;
     }
-    if (OST) {
+    if (SK != SK_NONE) {
         // the staged-store epilogue writes whole 32-row boxes: whole row tiles,
         // and the lowest output row (mt_base's first row) may not be negative
-        if (p.M % BM || p.ep.out_rows <= 0 || (int64_t)p.mt_base * BM + p.ep.out_row_shift < 0 ||
-            !encode_out(&maps.C, p.ep.out0, p.ep.out_rows, p.ep.Vpad, p.ep.ld0, OST))
+        if (p.M % BM || (int64_t)p.mt_base * BM + p.ep.out_row_shift < 0 || !encode_staged<SK>(maps, p))
             return cudaErrorInvalidValue;
     } else {
         maps.C = maps.A;
+        maps.D = maps.A;
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, OST>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, SK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1119,7 +1232,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     cfg.numAttrs = 1;
     cudaError_t e = cudaMemsetAsync(p.tile_counter, 0, sizeof(int), s);   // fresh tile counter
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, OST>, maps, p, status, dbg);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN, STAGES, NUM_ACC, SUB, MERGE, SK>, maps, p, status, dbg);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1173,13 +1286,15 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
     // main B shared by every row: 256 x 256 tiles on CTA pairs (the per-adapter
     // K extension, if any, is split per row half inside the kernel)
     if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter) {
-        // the LM head's big outputs (kept fp32 logits, recomputed bf16 dz) leave
-        // through shared memory and TMA stores when the caller gave their rows
-        if (p.ep.kind == EPI_LMFWD && p.ep.out0 && p.ep.out_rows > 0)
-            return launch_pair<256, 3, 2, 2, false, 4>(p, s, num_sms, status, nullptr);
-        if (p.ep.kind == EPI_LMDZ && p.ep.out_rows > 0)
-            return launch_pair<256, 3, 2, 2, false, 2>(p, s, num_sms, status, nullptr);
-        return launch_pair<256, 3, 2, 2>(p, s, num_sms, status, nullptr);
+        // outputs leave through shared memory and TMA stores where they can
+        switch (staged_kind(p)) {
+        case SK_LMFWD: return launch_pair<256, 3, 2, 2, false, SK_LMFWD>(p, s, num_sms, status, nullptr);
+        case SK_LMDZ: return launch_pair<256, 3, 2, 2, false, SK_LMDZ>(p, s, num_sms, status, nullptr);
+        case SK_SILU: return launch_pair<256, 3, 2, 2, false, SK_SILU>(p, s, num_sms, status, nullptr);
+        case SK_DSILU: return launch_pair<256, 3, 2, 2, false, SK_DSILU>(p, s, num_sms, status, nullptr);
+        case SK_RESID: return launch_pair<256, 3, 2, 2, false, SK_RESID>(p, s, num_sms, status, nullptr);
+        default: return launch_pair<256, 3, 2, 2>(p, s, num_sms, status, nullptr);
+        }
     }
     return launch_bn<256, 4>(p, s, num_sms, status);
 }
