@@ -179,8 +179,8 @@ struct StagedCfg {
     static constexpr bool F32 = SK == SK_LMFWD || SK == SK_RESID;      // an fp32 box, first in the set
     static constexpr int N16 = SK == SK_SILU ? 2 : (SK == SK_LMFWD ? 0 : 1);   // bf16 boxes after it
     static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;
-    static constexpr int NBUF = SK == SK_NONE ? 0 : (SET_BYTES <= 4096 ? 2 : 1);
-    static constexpr int WARP_BYTES = NBUF * SET_BYTES;              // a multiple of 1024
+    static constexpr int NBUF = SET_BYTES <= 4096 ? 2 : 1;
+    static constexpr int WARP_BYTES = SK == SK_NONE ? 0 : NBUF * SET_BYTES;   // a multiple of 1024
 };
 
 __device__ __forceinline__ void box_row_f32(uint32_t box, int lane, const float* v) {
@@ -250,15 +250,18 @@ __device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensor
     fence_async_shared();
     __syncwarp();
     if (lane == 0) {
-        if (SK == SK_LMFWD) tma_store_2d(mc, set, col0, y0);
-        if (SK == SK_LMDZ || SK == SK_DSILU) tma_store_2d(mc, b16, col0, y0);
+        // written once here and read by a later launch: evict-first in L2, so
+        // that the outputs do not displace the operand tiles the GEMM re-reads
+        const uint64_t pol = l2_policy_evict_first();
+        if (SK == SK_LMFWD) tma_store_2d_hint(mc, set, col0, y0, pol);
+        if (SK == SK_LMDZ || SK == SK_DSILU) tma_store_2d_hint(mc, b16, col0, y0, pol);
         if (SK == SK_SILU) {
-            tma_store_2d(mc, b16, col0, y0);
-            tma_store_2d(md, b16 + 2048, col0, y0);
+            tma_store_2d_hint(mc, b16, col0, y0, pol);
+            tma_store_2d_hint(md, b16 + 2048, col0, y0, pol);
         }
         if (SK == SK_RESID) {
-            tma_store_2d(md, set, col0, y0);
-            if (ep.out0) tma_store_2d(mc, b16, col0, y0);
+            tma_store_2d_hint(md, set, col0, y0, pol);
+            if (ep.out0) tma_store_2d_hint(mc, b16, col0, y0, pol);
         }
         bulk_commit();
     }
@@ -1022,11 +1025,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = (int64_t)my_mt * BM + 32 * q + lane;
             const bool tile_ok = (my_mt - p.mt_base) < cnt && row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-            if (MERGE) epilogue_row_merge<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0);
-            else if (SK != SK_NONE)
+            if constexpr (MERGE) {
+                epilogue_row_merge<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0);
+            } else if constexpr (SK != SK_NONE) {
                 epilogue_row_staged<BN, SK>(p, &maps.C, &maps.D, tbase, row, tile_ok, c.nt * BN, c.nt, stg, nbox,
                                             (int)((int64_t)my_mt * BM + 32 * q + p.ep.out_row_shift));
-            else epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
+            } else {
+                epilogue_row<BN>(p, tbase, row, tile_ok, c.nt * BN, rank ? c.a1 : c.a0, c.nt);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
