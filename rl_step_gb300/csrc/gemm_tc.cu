@@ -172,16 +172,24 @@ __device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t
 // maps' swizzle and put each quarter-warp's st.shared.v4 on distinct banks.
 // A warp owns NBUF sets of boxes; the set of chunk c is refilled once the
 // TMA stores of chunk c - NBUF have read it (one bulk group per chunk).
-enum { SK_NONE = 0, SK_LMFWD = 1, SK_LMDZ = 2, SK_SILU = 3, SK_DSILU = 4, SK_RESID = 5 };
+//   SK_MERGE  the export merge (see merge_tile): W boxes loaded by TMA one
+//             tile ahead, out = bf16(W + gamma acc) in place, stored by TMA
+enum { SK_NONE = 0, SK_LMFWD = 1, SK_LMDZ = 2, SK_SILU = 3, SK_DSILU = 4, SK_RESID = 5, SK_MERGE = 6 };
 
 template <int SK>
 struct StagedCfg {
     static constexpr bool F32 = SK == SK_LMFWD || SK == SK_RESID;      // an fp32 box, first in the set
-    static constexpr int N16 = SK == SK_SILU ? 2 : (SK == SK_LMFWD ? 0 : 1);   // bf16 boxes after it
-    static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;
-    static constexpr int NBUF = SET_BYTES <= 4096 ? 2 : 1;
+    static constexpr int N16 = SK == SK_MERGE ? 4 : (SK == SK_SILU ? 2 : (SK == SK_LMFWD ? 0 : 1));
+    static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;     // bf16 boxes after it
+    static constexpr int NBUF = (SET_BYTES <= 4096 || SK == SK_MERGE) ? 2 : 1;
     static constexpr int WARP_BYTES = SK == SK_NONE ? 0 : NBUF * SET_BYTES;   // a multiple of 1024
+    // epilogue warps per CTA: one per TMEM lane quadrant, two (each half of
+    // the tile's columns) for the merge, whose epilogue is its whole time
+    static constexpr int EPI_WARPS = SK == SK_MERGE ? 8 : 4;
 };
+
+template <int SK>
+constexpr int pair_threads() { return 64 + 32 * StagedCfg<SK>::EPI_WARPS; }
 
 __device__ __forceinline__ void box_row_f32(uint32_t box, int lane, const float* v) {
     const uint32_t rb = box + lane * 128;
@@ -292,6 +300,44 @@ __device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const C
             staged_chunk<SK>(p, mc, md, row, col_base + (ch + 1) * 32, rb, st, stg, nbox, y0);
     }
     epi_row_end(p.ep, row, nt, st);
+}
+
+// The export merge's chunks of one warp (SK_MERGE): W's 32 x 32 bf16 boxes
+// of this warp's rows sit in shared memory (64-byte swizzle, as in
+// box_row_bf16); each thread turns its row into bf16(W + gamma acc) in place,
+// the arithmetic of epi_chunk's EPI_MERGE (one fmaf, one rounding).
+__device__ __forceinline__ void merge_tile(uint32_t tbase, uint32_t set, int lane, int n, float gm) {
+    uint32_t ra[32], rb[32];
+    tmem_ld32(tbase, ra);
+    auto chunk = [&](int ch, const uint32_t (&r)[32]) {
+        const uint32_t rowb = set + (uint32_t)ch * 2048u + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t a = rowb + ((j ^ ((lane >> 1) & 3)) << 4);
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(a));
+            const uint32_t wv[4] = {w0, w1, w2, w3};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+                o[e] = pack_bf16x2(fmaf(gm, __uint_as_float(r[8 * j + 2 * e]), f.x),
+                                   fmaf(gm, __uint_as_float(r[8 * j + 2 * e + 1]), f.y));
+            }
+            st_shared_v4(a, o[0], o[1], o[2], o[3]);
+        }
+    };
+#pragma unroll 1
+    for (int ch = 0; ch < n; ch += 2) {
+        tmem_ld_wait();
+        if (ch + 1 < n) tmem_ld32(tbase + (ch + 1) * 32, rb);
+        chunk(ch, ra);
+        if (ch + 1 >= n) break;
+        tmem_ld_wait();
+        if (ch + 2 < n) tmem_ld32(tbase + (ch + 2) * 32, ra);
+        chunk(ch + 1, rb);
+    }
+    tmem_ld_wait();
 }
 
 struct TcMaps {
@@ -609,10 +655,10 @@ struct SmemLayoutPair {
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr int STG_WARP = StagedCfg<SK>::WARP_BYTES;
     static constexpr int STG_OFF = TILES_BYTES;            // 1024-aligned (swizzled boxes)
-    static constexpr int STG_BYTES = 4 * STG_WARP;         // 4 epilogue warps
+    static constexpr int STG_BYTES = StagedCfg<SK>::EPI_WARPS * STG_WARP;
     static constexpr int SCHED = 4;                     // tile-index ring depth
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * SCHED;
+    static constexpr int NBARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * SCHED + 2 * StagedCfg<SK>::EPI_WARPS;
     static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int MISC_OFF = SLOT_OFF + SCHED * 4;
     static constexpr int TOTAL = MISC_OFF + 16 + 1024;
@@ -711,10 +757,11 @@ __device__ __forceinline__ bool sched_take(uint32_t bar_sfull, uint32_t sempty_l
 }
 
 template <int BN, int STAGES, int NUM_ACC, int SUB, bool MERGE = false, int SK = SK_NONE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(pair_threads<SK>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status, int* dbg) {
     using SL = SmemLayoutPair<BN, STAGES, NUM_ACC, SUB, SK>;
     static_assert(SK == SK_NONE || (!MERGE && BN == 256), "staged stores: 256-wide tiles");
+    static_assert(SK != SK_MERGE || (NUM_ACC == 2 && SUB == 1), "merge: two accumulators, one-block stages");
     static_assert(SL::SCHED == 4, "sched_take assumes a 4-slot ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -726,6 +773,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_drain = bar_tempty + NUM_ACC * 8;
     const uint32_t bar_sfull = bar_drain + 8;
     const uint32_t bar_sempty = bar_sfull + SL::SCHED * 8;
+    const uint32_t bar_epi = bar_sempty + SL::SCHED * 8;     // 2 per epilogue warp (the merge's W loads)
     volatile int* slots = reinterpret_cast<volatile int*>(smem + SL::SLOT_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC_OFF + 4);
@@ -750,13 +798,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < NUM_ACC; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
-            mbar_init(bar_tempty + 8 * b, 8);
+            mbar_init(bar_tempty + 8 * b, 2 * StagedCfg<SK>::EPI_WARPS);
         }
         mbar_init(bar_drain, 1);
         for (int s = 0; s < SL::SCHED; ++s) {
             mbar_init(bar_sfull + 8 * s, 1);
-            mbar_init(bar_sempty + 8 * s, 10);   // peer producer, leader MMA, 8 epilogue warps
+            // peer producer, leader MMA, both CTAs' epilogue warps
+            mbar_init(bar_sempty + 8 * s, 2 + 2 * StagedCfg<SK>::EPI_WARPS);
         }
+        for (int b = 0; b < 2 * StagedCfg<SK>::EPI_WARPS; ++b) mbar_init(bar_epi + 8 * b, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -991,6 +1041,114 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int dummy = 0;
             if (!mbar_wait(bar_drain, 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
         }
+    } else if constexpr (SK == SK_MERGE) {
+        // ------------------------------------------------------------ export-merge epilogue (both CTAs)
+        const int q = warp & 3;
+        const uint32_t stg = sbase + SL::STG_OFF + (uint32_t)(warp - 2) * (uint32_t)SL::STG_WARP;
+        const uint32_t wbar = bar_epi + (uint32_t)(warp - 2) * 16u;
+        const int cbase = ((warp - 2) >> 2) * (BN / 2);           // this warp's half of the columns
+        constexpr uint32_t SET = 4u * 2048u;                      // one tile's W boxes
+        const float gm = p.ep.gamma[0];
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int sslot = 0;
+        uint32_t sph = 0;
+        uint32_t wph = 0;      // bit s: parity of set s's barrier
+        uint32_t pend = 0;     // bit s: set s has W loads in flight not yet waited for
+        auto take = [&](int& t) -> bool {
+            bool ok = true;
+            t = -1;
+            if (lane == 0) ok = sched_take(bar_sfull, sempty_leader, slots, sslot, sph, leader, abort_flag, t);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            sslot = __shfl_sync(0xffffffffu, sslot, 0);
+            sph = __shfl_sync(0xffffffffu, sph, 0);
+            return ok;
+        };
+        // this warp's 32 rows of tile t: first output row, or -1 when it has none
+        auto warp_row0 = [&](const PairCoord& c) -> int {
+            const int my_mt = c.mt + (int)rank;
+            const int y0 = my_mt * BM + 32 * q;
+            return ((my_mt - p.mt_base) < cnt && y0 < p.M) ? y0 : -1;
+        };
+        auto nchunks = [&](const PairCoord& c) -> int {
+            const int left = p.N - c.nt * BN - cbase;
+            return left <= 0 ? 0 : (left >= BN / 2 ? BN / 64 : (left + 31) / 32);
+        };
+        // request tile t's W boxes (32 x 32 bf16 each) into set `set`
+        auto request = [&](int t, int set) -> int {
+            const PairCoord c = pair_coord<BN>(p, t, cnt);
+            const int y0 = warp_row0(c);
+            const int n = y0 < 0 ? 0 : nchunks(c);
+            if (n > 0) pend |= 1u << set;
+            if (n > 0 && lane == 0) {
+                const uint32_t bar = wbar + 8u * (uint32_t)set;
+                mbar_expect_tx(bar, (uint32_t)n * 2048u);
+                for (int ch = 0; ch < n; ++ch)
+                    tma_load_2d(stg + (uint32_t)set * SET + (uint32_t)ch * 2048u, &maps.D, bar,
+                                c.nt * BN + cbase + 32 * ch, y0);
+            }
+            return n;
+        };
+        int t = -1;
+        bool ok = take(t);
+        int n_cur = (ok && t >= 0) ? request(t, 0) : 0;
+        for (int i = 0; ok && t >= 0; ++i) {
+            const int set = i & 1;
+            int t_next = -1;
+            if (!(ok = take(t_next))) break;
+            int n_next = 0;
+            if (t_next >= 0) {
+                // the other set held tile i-1, whose stores must have read it
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                n_next = request(t_next, set ^ 1);
+            }
+            if (lane == 0) ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            tc_fence_after();
+            if (n_cur > 0) {
+                const PairCoord c = pair_coord<BN>(p, t, cnt);
+                const int y0 = warp_row0(c);
+                if (lane == 0) ok = mbar_wait(wbar + 8u * (uint32_t)set, (wph >> set) & 1u, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                wph ^= 1u << set;
+                pend &= ~(1u << set);
+                const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + cbase);
+                merge_tile(tbase, stg + (uint32_t)set * SET, lane, n_cur, gm);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint64_t pol = l2_policy_evict_first();
+                    for (int ch = 0; ch < n_cur; ++ch)
+                        tma_store_2d_hint(&maps.C, stg + (uint32_t)set * SET + (uint32_t)ch * 2048u,
+                                          c.nt * BN + cbase + 32 * ch, y0, pol);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(bar_tempty + 8 * acc);
+                else mbar_arrive_cluster(tempty_leader + 8 * acc);
+            }
+            if (++acc == NUM_ACC) { acc = 0; acc_phase ^= 1u; }
+            t = t_next;
+            n_cur = n_next;
+        }
+        if (!ok && lane == 0) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+        if (lane == 0) {
+            // W loads still in flight land before the CTA exits (bounded), stores are written
+            for (int set = 0; set < 2; ++set)
+                if (pend & (1u << set)) {
+                    int dummy = 0;
+                    if (!mbar_wait(wbar + 8u * (uint32_t)set, (wph >> set) & 1u, (volatile int*)&dummy))
+                        atomicOr(status, ST_TIMEOUT);
+                }
+            bulk_wait_all();
+        }
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
@@ -1160,6 +1318,13 @@ int staged_kind(const GemmParams& p) {
     }
 }
 
+// The export merge's staged form: whole 32-row warp slices (M a multiple of
+// 32), W and the output addressable by TMA, one adapter for every tile.
+bool merge_staged(const GemmParams& p) {
+    const EpiParams& e = p.ep;
+    return p.M % 32 == 0 && !p.tile_ad && out_aligned(e.aux, e.ld_aux, 2) && out_aligned(e.out0, e.ld0, 2);
+}
+
 // Output maps of a staged kind (the box layouts of staged_chunk).
 template <int SK>
 bool encode_staged(TcMaps& maps, const GemmParams& p) {
@@ -1178,6 +1343,9 @@ bool encode_staged(TcMaps& maps, const GemmParams& p) {
         if (e.out0) return encode_out(&maps.C, e.out0, p.M, p.N, e.ld0, 2);
         maps.C = maps.D;
         return true;
+    case SK_MERGE:
+        return encode_out(&maps.D, const_cast<void*>(e.aux), p.M, p.N, e.ld_aux, 2) &&
+               encode_out(&maps.C, e.out0, p.M, p.N, e.ld0, 2);
     default:
         return true;
     }
@@ -1204,9 +1372,11 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
         maps.Bx = maps.B;
     }
     if (SK != SK_NONE) {
-        // the staged-store epilogue writes whole 32-row boxes: whole row tiles,
-        // and the lowest output row (mt_base's first row) may not be negative
-        if (p.M % BM || (int64_t)p.mt_base * BM + p.ep.out_row_shift < 0 || !encode_staged<SK>(maps, p))
+        // the staged-store epilogue writes whole 32-row boxes: whole row tiles
+        // (32-row warp slices for the merge), and the lowest output row
+        // (mt_base's first row) may not be negative
+        if (p.M % (SK == SK_MERGE ? 32 : BM) || (int64_t)p.mt_base * BM + p.ep.out_row_shift < 0 ||
+            !encode_staged<SK>(maps, p))
             return cudaErrorInvalidValue;
     } else {
         maps.C = maps.A;
@@ -1226,7 +1396,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, int num_sms, int* s
     if (upper < nclusters) nclusters = (int)upper;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * nclusters, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(pair_threads<SK>(), 1, 1);
     cfg.dynamicSmemBytes = SL::TOTAL;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1272,8 +1442,11 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
     if (!get_encode()) return cudaErrorNotSupported;
     if (p.ep.kind == EPI_MERGE) {
         if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8, true>(p, s, num_sms, status);
-        if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter)
+        if (!p.grouped && p.B.ad_rows == 0 && !p.A.mn_major && p.N >= 256 && p.tile_counter) {
+            // K is a few blocks: one-block stages, and W requested a tile ahead
+            if (merge_staged(p)) return launch_pair<256, 3, 2, 1, false, SK_MERGE>(p, s, num_sms, status, nullptr);
             return launch_pair<256, 3, 2, 2, true>(p, s, num_sms, status, nullptr);
+        }
         return launch_bn<256, 4, true>(p, s, num_sms, status);
     }
     if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8>(p, s, num_sms, status);

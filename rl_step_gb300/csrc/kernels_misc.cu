@@ -588,9 +588,56 @@ __global__ void merge_operands_kernel(const float* __restrict__ Bf, const float*
     }
 }
 
+// The bf16 operands eight elements per thread (one 16-byte store, 32-bit
+// index arithmetic), the same values as merge_operands_kernel: each group of
+// eight lies in one part of K (RP is a multiple of 8), and N % 8 == 0.
+__global__ void merge_operands_bf16x8_kernel(const float* __restrict__ Bf, const float* __restrict__ Af, int M,
+                                             int N, int r, bf16* __restrict__ Aop, bf16* __restrict__ Bop) {
+    constexpr int KP = 3 * RP, GK = KP / 8;
+    const int gn = N / 8;
+    const int ga = M * GK, gall = ga + KP * gn;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < gall; g += gridDim.x * blockDim.x) {
+        float x[8];
+        uint4 w;
+        if (g < ga) {
+            const int m = g / GK;
+            const int c0 = (g - m * GK) * 8, part = c0 / RP, j0 = c0 % RP;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = j0 + e < r ? Bf[(int64_t)m * r + j0 + e] : 0.f;
+                const float hi = __bfloat162float(__float2bfloat16_rn(v));
+                x[e] = part < 2 ? hi : v - hi;
+            }
+            w = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                           pack_bf16x2(x[6], x[7]));
+            *reinterpret_cast<uint4*>(Aop + (int64_t)m * KP + c0) = w;
+        } else {
+            const int q = g - ga;
+            const int c = q / gn, n0 = (q - c * gn) * 8, part = c / RP, j = c % RP;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = j < r ? Af[(int64_t)j * N + n0 + e] : 0.f;
+                const float hi = __bfloat162float(__float2bfloat16_rn(v));
+                x[e] = part == 1 ? v - hi : hi;
+            }
+            w = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                           pack_bf16x2(x[6], x[7]));
+            *reinterpret_cast<uint4*>(Bop + (int64_t)c * N + n0) = w;
+        }
+    }
+}
+
 template <typename T>
 void launch_merge_operands(const float* Bf, const float* Af, int M, int N, int r, T* Aop, T* Bop,
                            cudaStream_t s) {
+    if (sizeof(T) == 2 && N % 8 == 0 && (int64_t)(M + N) * 3 * RP / 8 < (1LL << 31)) {
+        const int groups = (M + N) * (3 * RP / 8);
+        int blocks = (groups + 255) / 256;
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        merge_operands_bf16x8_kernel<<<blocks, 256, 0, s>>>(Bf, Af, M, N, r, reinterpret_cast<bf16*>(Aop),
+                                                            reinterpret_cast<bf16*>(Bop));
+        return;
+    }
     merge_operands_kernel<T><<<152 * 8, 256, 0, s>>>(Bf, Af, M, N, r, Aop, Bop);
 }
 template void launch_merge_operands<float>(const float*, const float*, int, int, int, float*, float*,
