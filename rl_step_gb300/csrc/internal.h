@@ -8,6 +8,28 @@
 
 namespace mlk {
 
+// Row tiles per chunk of the LM-head backward.  By default the tiles split
+// into equal chunks (an even number each, for the CTA-pair GEMMs) of at most
+// nc_tiles.  When the batch needs several chunks and dh runs on the tensor-core
+// engine, each of whose dh tiles contracts the whole vocabulary (about 1.5 ms
+// at 151,936 x 4,096), every chunk but the last takes the largest size whose
+// dh tiles fill whole waves of the `clusters` CTA pairs: no chunk but the last
+// ends on a partly idle wave.  dh_ntiles is dh's column tiles per row pair
+// (0: no such rule).
+inline int lm_chunk_tiles(int mt_upper, int nc_tiles, int dh_ntiles, int clusters) {
+    const int n_chunks = (mt_upper + nc_tiles - 1) / nc_tiles;
+    int chunk = (mt_upper + n_chunks - 1) / n_chunks;
+    chunk = (chunk + 1) & ~1;
+    if (chunk > nc_tiles) chunk = nc_tiles;
+    if (n_chunks > 1 && dh_ntiles > 0 && clusters > 0) {
+        int a = dh_ntiles, b = clusters;
+        while (b) { const int t = a % b; a = b; b = t; }
+        const int step = 2 * (clusters / a);          // row tiles per whole number of waves
+        if (step <= nc_tiles) chunk = nc_tiles / step * step;
+    }
+    return chunk;
+}
+
 // Device allocation of every create call (cudaMalloc, with a test hook that
 // can make one chosen allocation fail).
 cudaError_t mlk_malloc(void** p, size_t bytes);

@@ -679,12 +679,10 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         }
         if (!backward) return MLORA_OK;
     }
-    // equal chunks (an even number of row tiles, for the CTA-pair GEMMs) of at
-    // most nc_tiles tiles: no small last chunk whose GEMMs fill a wave poorly
-    const int n_chunks = (mt_upper + h->nc_tiles - 1) / h->nc_tiles;
-    int chunk = (mt_upper + n_chunks - 1) / n_chunks;
-    chunk = (chunk + 1) & ~1;
-    if (chunk > h->nc_tiles) chunk = h->nc_tiles;
+    // chunks of at most nc_tiles row tiles, sized so that dh fills whole waves
+    // (dh on the tensor-core engine: 256 x 512 tiles at the vocabulary's K)
+    const int dh_nt = sizeof(T) != 2 ? 0 : (h->Vpad >= 65536 && d % 512 == 0 ? d / 512 : (d + 255) / 256);
+    const int chunk = lm_chunk_tiles(mt_upper, h->nc_tiles, dh_nt, h->num_sms / 2);
     const int nch = (mt_upper + chunk - 1) / chunk;
     auto dh_params = [&](int c0, int cnt, const void* dzb) {
         GemmParams p = dense_params(h, mt_upper, d, h->Vpad);

@@ -787,10 +787,10 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         }
         if (!backward) return MLORA_OK;
     }
-    const int n_chunks = (mt_upper + h->nc_tiles - 1) / h->nc_tiles;
-    int chunk = (mt_upper + n_chunks - 1) / n_chunks;
-    chunk = (chunk + 1) & ~1;
-    if (chunk > h->nc_tiles) chunk = h->nc_tiles;
+    // chunks of at most nc_tiles row tiles, sized so that dh fills whole waves
+    // (dh: 256 x 512 tiles at the vocabulary's K)
+    const int dh_nt = h->Vpad >= 65536 && d % 512 == 0 ? d / 512 : (d + 255) / 256;
+    const int chunk = lm_chunk_tiles(mt_upper, h->nc_tiles, dh_nt, h->num_sms / 2);
     const int nch = (mt_upper + chunk - 1) / chunk;
     auto chunk_rows = [&](int i, int& c0, int& cnt) {
         c0 = i * chunk;
