@@ -145,19 +145,6 @@ __device__ __forceinline__ bool ring_get_warp(uint32_t full, uint32_t empty, con
     return ok != 0;
 }
 
-// Store 32 consecutive bf16 values (a 64-byte piece of a K-major row) into a
-// 128-byte-swizzled operand block: `blk` is the block's smem address, row r,
-// 16-byte chunks c0..c0+3 of the row.
-__device__ __forceinline__ void st_swizzled32(uint32_t blk, int r, int c0, const uint32_t (&w)[16]) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const uint32_t addr = blk + r * 128 + (((c0 + u) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]),
-                     "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
-                     : "memory");
-    }
-}
-
 // Descriptors are built once per product and moved by additions to their
 // start-address field (bits 0-13, address >> 4): shared-memory addresses stay
 // below 2^18, so the field never carries.  The one issuing thread then spends
@@ -170,8 +157,8 @@ constexpr uint32_t BLK_STEP = BLK >> 4;
 // kb (64 rows) at +512 kb, 16-row K step at +128 kk, MN halves 16 KB apart.
 __device__ __forceinline__ uint64_t mndesc(uint32_t base) { return sdesc(base, 2 * 8192, 1024); }
 
-// 128 x 128 x 128 products: D (+)= A B^T with A, B both K-major (two 64-wide
-// K blocks each), or A K-major and B the MN-major view of a row-major tile.
+// 128 x 128 x 128 product: D (+)= A B^T with A, B both K-major (two 64-wide
+// K blocks each).
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, bool acc) {
     const uint32_t id = idesc_bf16(128, 0, 0, 128);
     const uint64_t ad = kdesc(a), bd = kdesc(b);
@@ -181,15 +168,6 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a, uint32_t b, bool 
         for (int kk = 0; kk < 4; ++kk)
             umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + kb * BLK_STEP + 2 * kk, id,
                       (acc || kb || kk) ? 1u : 0u);
-}
-__device__ __forceinline__ void mma_kmn(uint32_t d, uint32_t a, uint32_t b, bool acc) {
-    const uint32_t id = idesc_bf16(128, 0, 1, 128);
-    const uint64_t ad = kdesc(a), bd = mndesc(b);
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + 512 * kb + 128 * kk, id, (acc || kb || kk) ? 1u : 0u);
 }
 
 // Load a 128-row x 128-column bf16 tile of a row-major matrix as two
@@ -632,7 +610,8 @@ struct KvSmem {
     static constexpr int Q0 = 4 * BLK;           // stage s: Q at Q0 + 4 BLK s, dO 2 BLK after
     static constexpr int VEC0 = 12 * BLK;        // stage s: lse[128] (log2 units), D[128], seq_start[128]
     static constexpr int BAR = VEC0 + 2 * 3 * 512;
-    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 7, PT_DONE = 9, ACC_FULL = 11,
+    // (slots 9-10 are spare)
+    enum { KV_FULL = 0, QD_FULL = 1, QD_EMPTY = 3, ST_FULL = 5, P_FULL = 7, SPARE = 9, ACC_FULL = 11,
            DRAIN = 12, KV_EMPTY = 13, ACC_FREE = 14, SCHED_FULL = 15, SCHED_EMPTY = 15 + RING,
            NBARS = 15 + 2 * RING };
     static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
@@ -650,17 +629,6 @@ __device__ __forceinline__ void mma_kk64(uint32_t d, uint32_t a, uint32_t b, int
         for (int kk = 0; kk < 4; ++kk)
             umma_bf16(d, ad + kb * BLK_STEP + 2 * kk, bd + kb * BLK_STEP + 2 * kk, id, (kb || kk) ? 1u : 0u);
 }
-// D (+)= A B^T, M = 128, N = 128, K = 64: A (bf16 pairs) in TMEM columns
-// a_tmem .. a_tmem + 31, B rows 64 s .. 64 s + 63 of a row-major smem tile
-// read MN-major.
-__device__ __forceinline__ void mma_t64mn(uint32_t d, uint32_t a_tmem, uint32_t b, int s, bool acc) {
-    const uint32_t id = idesc_bf16(128, 0, 1, 128);
-    const uint64_t bd = mndesc(b) + 512 * s;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_ts(d, a_tmem + 8 * kk, bd + 128 * kk, id, (acc || kk) ? 1u : 0u);
-}
-
 // Key-side work item: key tile kt of key/value head g; the query tiles
 // kt .. kt + nqt - 1 are those whose first row starts its sequence at or
 // before this tile's last key, taken for every query head of the group.
@@ -685,7 +653,9 @@ __device__ __forceinline__ KvItem kv_item(const AttnParams& p, int item, int mt_
 // phases follow running counts of query tiles and halves.  The next item's
 // K / V load starts once the current item's last scores are issued, and its
 // first products overlap the read-out of the current dK / dV.
-// The same with A in two 16-column pieces: K rows 0-31 (bf16 pairs) at
+// D (+)= A B^T, M = 128, N = 128, K = 64: B rows 64 s .. 64 s + 63 of a
+// row-major smem tile read MN-major; A (bf16 pairs) in TMEM in two 16-column
+// pieces: K rows 0-31 (bf16 pairs) at
 // a_tmem .. a_tmem + 15 and K rows 32-63 at a_tmem + 32 .. a_tmem + 47, as the
 // two softmax warpgroups write them (each over the columns it has read).
 __device__ __forceinline__ void mma_t64mn_split(uint32_t d, uint32_t a_tmem, uint32_t b, int s, bool acc) {
@@ -802,11 +772,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 // half m: query tile gn0 + m / 2 in stage (gn0 + m / 2) & 1, rows 64 (m & 1) ..,
                 // TMEM buffer m & 1 (gm is even)
                 auto issue_s = [&](int m) -> bool {
-                    const uint32_t M = gm + m, N = gn0 + (m >> 1);
+                    const uint32_t N = gn0 + (m >> 1);
                     const int b = m & 1;
                     const uint32_t st = sb + SL::Q0 + (N & 1) * 4 * BLK;
                     if (b == 0 && !mbar_wait(bar(SL::QD_FULL + (N & 1)), (N >> 1) & 1u, abort_flag)) return false;
-                    if (M >= 2 && !mbar_wait(bar(SL::PT_DONE + b), ((M >> 1) - 1) & 1u, abort_flag)) return false;
+                    // buffer b last held half m - 2's P^T / dS^T, read by its dV / dK
+                    // products, which this thread issued before: the tensor core runs
+                    // one thread's MMAs in issue order, so no wait is needed here
                     tc_fence_after();
                     mma_kk64(tmem + 64 * b, sb + SL::K, st, b);
                     mma_kk64(tmem + 128 + 64 * b, sb + SL::V, st + 2 * BLK, b);
@@ -831,7 +803,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     tc_fence_after();
                     mma_t64mn_split(tmem + 256, tmem + 64 * b, st + 2 * BLK, b, m > 0);
                     mma_t64mn_split(tmem + 384, tmem + 128 + 64 * b, st, b, m > 0);
-                    umma_commit(bar(SL::PT_DONE + b));
                     if (b == 1) umma_commit(bar(SL::QD_EMPTY + (N & 1)));
                 }
                 if (!ok) break;
@@ -985,7 +956,8 @@ struct QSmem {
     static constexpr int DO = 2 * BLK;
     static constexpr int K0 = 4 * BLK;          // stage s: K at K0 + 4 BLK s, V 2 BLK after
     static constexpr int BAR = 12 * BLK;
-    enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, DS_FULL = 7, DS_DONE = 9, ACC_FULL = 11,
+    // (slots 9-10 are spare)
+    enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 3, S_FULL = 5, DS_FULL = 7, SPARE = 9, ACC_FULL = 11,
            DRAIN = 12, Q_EMPTY = 13, ACC_FREE = 14, SCHED_FULL = 15, SCHED_EMPTY = 15 + RING,
            NBARS = 15 + 2 * RING };
     static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
@@ -1106,11 +1078,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 // half m: key tile gj0 + m / 2 in stage (gj0 + m / 2) & 1, keys 64 (m & 1) ..,
                 // TMEM buffer m & 1 (gm is even)
                 auto issue_s = [&](int m) -> bool {
-                    const uint32_t M = gm + m, J = gj0 + (m >> 1);
+                    const uint32_t J = gj0 + (m >> 1);
                     const int b = m & 1;
                     const uint32_t st = sb + SL::K0 + (J & 1) * 4 * BLK;
                     if (b == 0 && !mbar_wait(bar(SL::KV_FULL + (J & 1)), (J >> 1) & 1u, abort_flag)) return false;
-                    if (M >= 2 && !mbar_wait(bar(SL::DS_DONE + b), ((M >> 1) - 1) & 1u, abort_flag)) return false;
+                    // buffer b last held half m - 2's dS, read by its dQ product, issued
+                    // before by this thread: in-order on the tensor core, no wait
                     tc_fence_after();
                     mma_kk64(tmem + 64 * b, sb + SL::Q, st, b);
                     mma_kk64(tmem + 128 + 64 * b, sb + SL::DO, st + 2 * BLK, b);
@@ -1134,7 +1107,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     }
                     tc_fence_after();
                     mma_t64mn_split(tmem + 256, tmem + 64 * b, st, b, m > 0);
-                    umma_commit(bar(SL::DS_DONE + b));
                     if (b == 1) umma_commit(bar(SL::KV_EMPTY + (J & 1)));
                 }
                 if (!ok) break;
