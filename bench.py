@@ -9,7 +9,8 @@ and the per-adapter Adam update.  Default workload: Qwen3-8B widths
 traffic, 65,536 tokens in sequences of 512-2048 tokens, PPO clip 0.2.
 
 The LM-head backward has two modes (mlora_set_lm_backward): "keep_logits"
-(each chunk's fp32 logits kept from the forward; the headline by default,
+(each chunk's logits kept from the forward as fp16 exp(z - tile max) beside
+the tile maxima; the headline by default,
 --lm-backward) and "recompute" (a second GEMM recomputes each chunk's
 logits; the library's default).  Both are timed; `lm_backward` reports the
 step time and device memory of each.
@@ -271,9 +272,10 @@ def lora_hbm_bytes(cfg, b):
 
 
 def lm_dz_bytes(cfg, b):
-    """Bytes the LM-head dz pass must move: per token its fp32 logits read
-    (4 B x V) and its bf16 dz row written (2 B x V)."""
-    return len(b["tokens"]) * cfg.vocab * 6.0
+    """Bytes the LM-head dz pass must move: per token its kept logits read and
+    its dz row written -- on the bf16 engine the fp16 e = exp(z - tile max)
+    (2 B x V) and bf16 dz (2 B x V), on the fp32 one fp32 logits and dz."""
+    return len(b["tokens"]) * cfg.vocab * (4.0 if cfg.dtype == "bf16" else 8.0)
 
 
 def run_ours(args, rank, world):
@@ -477,8 +479,9 @@ def run_ours(args, rank, world):
         v["frac_of_bf16_peak"] = fl["total"] / (v["ms_per_step"] * 1e-3) / 1e12 / \
             load_peaks()[0]["bf16_tflops"]
     lm_modes["note"] = ("recompute: a second LM-head GEMM per chunk (2 N V d executed FLOPs, not "
-                        "credited) and one dz chunk buffer; keep_logits: fp32 logits of each chunk "
-                        "kept from the forward, dz by an elementwise pass on a side stream")
+                        "credited) and one dz chunk buffer; keep_logits: each chunk's logits kept from "
+                        "the forward (fp16 exp(z - tile max) on the bf16 engine), dz by an "
+                        "elementwise pass on a side stream")
 
     # ---- rows beyond the step (outside the timed region) ---------------------
     extras = None if args.no_extras else measure_next_rows(m, h, cfg, b, dev, stream)

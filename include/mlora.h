@@ -15,8 +15,8 @@
  * never stored whole).  The LM-head backward runs in chunks of at most 16,384
  * rows and has two modes (mlora_set_lm_backward): by default it recomputes
  * each chunk's logits with a second GEMM, as that section describes; on
- * request it instead keeps each chunk's fp32 logits from the forward in a
- * bounded buffer and reads them back.
+ * request it instead keeps each chunk's logits from the forward in a bounded
+ * buffer and reads them back.
  *
  * Conventions for every entry point:
  *  - Return value: MLORA_OK (0) or a negative MLORA_E_* code; the message of
@@ -375,14 +375,17 @@ int mlora_set_deterministic(mlora_t* h, int32_t on);
  *     dz = g (onehot(y) - softmax(z)) into a bf16 chunk buffer, then
  *     dh = dz Wout.  Extra device memory: one dz chunk buffer
  *     (16,384 x Vpad base-dtype elements, 5 GB at V = 151,936 in bf16).
- *   MLORA_LM_KEEP_LOGITS: the forward GEMM of each chunk also stores its fp32
+ *   MLORA_LM_KEEP_LOGITS: the forward GEMM of each chunk also stores its
  *     logits; an elementwise pass turns them into dz on a side stream while
  *     the next chunk's GEMMs run.  Saves the recompute GEMM (2 N V d FLOPs per
- *     step) for two fp32 logit chunk buffers and a second dz buffer (25 GB
- *     more at V = 151,936 in bf16).
+ *     step) for two kept-logit chunk buffers and a second dz buffer (15 GB
+ *     more at V = 151,936 in bf16).  A bf16 handle keeps, per 256-column
+ *     tile of a row, e = exp(z - m) in fp16 with the tile's maximum m (a
+ *     float per row and tile), and forms dz = g (onehot(y) - e exp(m - lse));
+ *     an fp32 handle keeps the fp32 logits.
  * Both modes give bitwise the same logprobs, losses and gradients: the
  * recomputed accumulator is the forward's, and dz is formed by the same
- * arithmetic.  Selecting KEEP_LOGITS allocates its buffers (E_NOMEM if they do
+ * arithmetic (on a bf16 handle the recompute epilogue forms the same fp16 e).  Selecting KEEP_LOGITS allocates its buffers (E_NOMEM if they do
  * not fit; the handle then stays in RECOMPUTE); selecting RECOMPUTE frees
  * them.  Synchronises the device.  Errors: E_ARG (NULL handle, unknown mode),
  * E_NOMEM, E_CUDA. */

@@ -146,9 +146,10 @@ int mlora_tf_check_status(mlora_tf_t* h, void* stream);
 /* LM-head backward mode, as mlora_set_lm_backward (MLORA_LM_RECOMPUTE, the
  * default of a new handle, or MLORA_LM_KEEP_LOGITS; Tinker API Implementation
  * on TPUs, section 10.4): recompute each row chunk's logits with a second
- * GEMM whose epilogue forms dz, or keep the forward's fp32 logits of each
- * chunk (two 16,384 x Vpad fp32 buffers and a second bf16 dz buffer, allocated
- * when selected, freed when left).  Both give bitwise the same results.
+ * GEMM whose epilogue forms dz, or keep the forward's logits of each chunk as
+ * fp16 e = exp(z - m) against each 256-column tile's maximum m (two 16,384 x
+ * Vpad fp16 buffers and a second bf16 dz buffer, allocated when selected,
+ * freed when left); dz = g (onehot(y) - e exp(m - lse)) in both modes.  Both give bitwise the same results.
  * Synchronises the device.  Errors: E_ARG, E_NOMEM (the handle then stays in
  * the recompute mode), E_CUDA. */
 int mlora_tf_set_lm_backward(mlora_tf_t* h, int32_t mode);

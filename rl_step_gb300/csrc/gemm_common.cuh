@@ -4,6 +4,8 @@
 // output row and 32 consecutive output columns held by one thread.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace mlk {
@@ -70,6 +72,10 @@ struct EpiParams {
                                     // (the other staged kinds write M rows)
     const float* gv = nullptr;      // EPI_LMDZ: dL/dl per padded row
     const float* lse = nullptr;     // EPI_LMDZ: log-sum-exp per padded row
+    float* mt = nullptr;            // EPI_LMFWD (written, if set) / EPI_LMDZ (read, bf16 engine):
+                                    // the row's max over each partial tile, [rows][part_ld]
+    int lm_bn = 0;                  // columns per log-sum-exp partial tile
+    int e16 = 0;                    // EPI_LMFWD: out0 keeps fp16 e = exp(z - tile max), not fp32 z
     // adapter gradients
     float* grad = nullptr;
     const int64_t* grad_off = nullptr;  // per adapter element offset of this tensor
@@ -145,6 +151,21 @@ __device__ __forceinline__ void store32_stream(float* dst, const float* v) {
     for (int q = 0; q < 8; ++q) __stcs(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
 }
 
+// 32 consecutive values as fp16 (round to nearest), evict-first stores
+__device__ __forceinline__ void store32_half(__half* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            __half2 h = __floats2half2_rn(v[8 * q + 2 * u], v[8 * q + 2 * u + 1]);
+            w[u] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        __stcs(d4 + q, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
 // first 16 of the values, 16 consecutive elements (32 bytes bf16, 64 bytes fp32)
 template <typename T> __device__ __forceinline__ void store16v(T* dst, const float* v);
 template <> __device__ __forceinline__ void store16v<bf16>(bf16* dst, const float* v) {
@@ -202,37 +223,52 @@ __device__ __forceinline__ void epi_row_begin(EpiRowState& st) {
     st.found = 0;
 }
 
-// EPI_LMFWD's running statistics of one row over the chunk's 32 columns
-// C[row][col0 .. col0+31]: the maximum and the sum of exp(x - max) over the
-// columns < V (rescaled as the maximum grows), and the target's logit.
-__device__ __forceinline__ void lmfwd_stats(const EpiParams& ep, int64_t row, int col0, const float* acc,
-                                            EpiRowState& st) {
-    const float LOG2E = 1.4426950408889634f;
-    int t = ep.tgt[row];
+// EPI_LMFWD, per partial tile of a row: the tile's maximum m over the columns
+// < V is taken first (lm_chunk_max over the tile's chunks, before the first
+// lmfwd_stats); then each column's e = exp(z - m), their sum s (the tile's
+// log-sum-exp partial is m + log s) and the target's logit.  The kept-logits
+// LM-head backward of the bf16 engine keeps e in fp16 beside m.
+__device__ __forceinline__ float lm_chunk_max(const EpiParams& ep, int col0, const float* acc) {
     float cm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        bool ok = (col0 + j) < ep.V;
-        cm = fmaxf(cm, ok ? acc[j] : -INFINITY);
-        if (col0 + j == t) { st.zt = acc[j]; st.found = 1; }
-    }
-    float mn = fmaxf(st.m, cm);
-    if (mn > -INFINITY) {
-        float sc = exp2f((st.m - mn) * LOG2E);
-        float sum = 0.f;
-        float mb = mn * LOG2E;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            sum += ((col0 + j) < ep.V) ? exp2f(fmaf(acc[j], LOG2E, -mb)) : 0.f;
-        st.s = st.s * sc + sum;
-        st.m = mn;
-    }
+    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, (col0 + j) < ep.V ? acc[j] : -INFINITY);
+    return cm;
 }
 
-// EPI_LMDZ's values of one chunk: dz = g (onehot(y) - exp(z - lse)) for the
-// columns < V, 0 beyond.  The same arithmetic, in the same order, as the dz
-// pass over kept fp32 logits: the recomputed accumulator is bitwise the
-// forward's, so both LM-head backward modes give the same dz.
+__device__ __forceinline__ void lmfwd_stats(const EpiParams& ep, int64_t row, int col0, const float* acc,
+                                            EpiRowState& st, float* e) {
+    const float LOG2E = 1.4426950408889634f;
+    const int t = ep.tgt[row];
+    const bool fin = st.m > -INFINITY;
+    const float mb = st.m * LOG2E;
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        e[j] = (fin && (col0 + j) < ep.V) ? exp2f(fmaf(acc[j], LOG2E, -mb)) : 0.f;
+        sum += e[j];
+        if (col0 + j == t) { st.zt = acc[j]; st.found = 1; }
+    }
+    st.s += sum;
+}
+
+// exp(m - lse) in the kept form's dz = g (onehot - e exp(m - lse)): one
+// expression for the dz pass and the recompute epilogue
+__device__ __forceinline__ float lm_tile_scale(float m, float lse) {
+    return exp2f((m - lse) * 1.4426950408889634f);
+}
+
+// dz of one column from its kept fp16 e: g (onehot - e c), the product and
+// the difference in one explicit fma so that every caller rounds alike
+__device__ __forceinline__ float lm_dz_from_e(float g, bool is_target, float e, float c) {
+    return g * fmaf(-e, c, is_target ? 1.f : 0.f);
+}
+
+// EPI_LMDZ's values of one chunk, for the columns < V (0 beyond).  bf16
+// engine (E16): e = fp16(exp(z - m)) against the forward's tile maximum m,
+// then dz = g (onehot - e exp(m - lse)) -- the kept form's arithmetic, so the
+// recomputed accumulator (bitwise the forward's) gives the kept-logits dz
+// pass's values.  Otherwise dz = g (onehot - exp(z - lse)), the fp32 dz pass's.
+template <bool E16>
 __device__ __forceinline__ void lmdz_values(const EpiParams& ep, int64_t row, int col0, const float* acc,
                                             float* o) {
     const float LOG2E = 1.4426950408889634f;
@@ -240,9 +276,21 @@ __device__ __forceinline__ void lmdz_values(const EpiParams& ep, int64_t row, in
     if (gr == 0.f) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = 0.f;
+        return;
+    }
+    const int y = ep.tgt[row];
+    if (E16) {
+        const float m = ep.mt[row * ep.part_ld + col0 / ep.lm_bn];
+        const float c = lm_tile_scale(m, ep.lse[row]);
+        const float mb = m * LOG2E;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int v = col0 + j;
+            const float e = __half2float(__float2half_rn(exp2f(fmaf(acc[j], LOG2E, -mb))));
+            o[j] = v < ep.V ? lm_dz_from_e(gr, v == y, e, c) : 0.f;
+        }
     } else {
         const float lb = ep.lse[row] * LOG2E;
-        const int y = ep.tgt[row];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int v = col0 + j;
@@ -342,13 +390,16 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
         store32<T>(reinterpret_cast<T*>(ep.out0) + row * ep.ld0 + col0, acc);
     } break;
     case EPI_LMFWD: {
-        if (ep.out0 && col0 < ep.Vpad)     // keep the logits (fp32) for the backward
-            store32_stream(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
-        lmfwd_stats(ep, row, col0, acc, st);
+        float e[32];
+        lmfwd_stats(ep, row, col0, acc, st, e);
+        if (ep.out0 && col0 < ep.Vpad) {   // keep the logits for the backward (or the sampler)
+            if (ep.e16) store32_half(reinterpret_cast<__half*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, e);
+            else store32_stream(reinterpret_cast<float*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, acc);
+        }
     } break;
     case EPI_LMDZ: {
         float o[32];
-        lmdz_values(ep, row, col0, acc, o);
+        lmdz_values<std::is_same<T, bf16>::value>(ep, row, col0, acc, o);
         store32<T>(reinterpret_cast<T*>(ep.out0) + (row + ep.out_row_shift) * ep.ld0 + col0, o);
     } break;
     case EPI_SHRINK_SEL: {
@@ -404,6 +455,7 @@ __device__ __forceinline__ void epi_row_end(const EpiParams& ep, int64_t row, in
                                             const EpiRowState& st) {
     if (ep.kind == EPI_LMFWD) {
         ep.part[row * ep.part_ld + ntile] = st.s > 0.f ? st.m + __logf(st.s) : -INFINITY;
+        if (ep.mt) ep.mt[row * ep.part_ld + ntile] = st.m;
         if (st.found) ep.zt[row] = st.zt;
     }
 }

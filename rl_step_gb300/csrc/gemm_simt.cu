@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(128) simt_gemm_kernel(GemmParams p) {
     if (row >= p.M) return;
     EpiRowState st;
     epi_row_begin(st);
+    // the log-sum-exp partial tile is this block's 32 columns: its maximum first
+    if (p.ep.kind == EPI_LMFWD) st.m = lm_chunk_max(p.ep, (int)n0, acc);
     epi_chunk<T>(p.ep, row, (int)n0, adapter, acc, st);
     epi_row_end(p.ep, row, nt, st);
 }

@@ -70,6 +70,32 @@ __device__ __forceinline__ void load_tile_b(uint32_t dst, const CUtensorMap* map
     }
 }
 
+// EPI_LMFWD's first pass over a finished accumulator row: the maximum over the
+// tile's columns < V, read from TMEM 32 columns at a time (the next chunk in
+// flight while one is reduced).
+template <int BN>
+__device__ __forceinline__ float lm_tile_max(const GemmParams& p, uint32_t tbase, int col_base) {
+    float m = -INFINITY;
+    uint32_t ra[32], rb[32];
+    auto red = [&](const uint32_t (&r)[32], int ch) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        if (col_base + ch * 32 < p.N) m = fmaxf(m, lm_chunk_max(p.ep, col_base + ch * 32, v));
+    };
+    tmem_ld32(tbase, ra);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ch += 2) {
+        tmem_ld_wait();
+        tmem_ld32(tbase + (ch + 1) * 32, rb);
+        red(ra, ch);
+        tmem_ld_wait();
+        if (ch + 2 < BN / 32) tmem_ld32(tbase + (ch + 2) * 32, ra);
+        red(rb, ch + 1);
+    }
+    return m;
+}
+
 // Epilogue of one finished accumulator for one thread's row: BN columns in
 // chunks of 32.  The TMEM read of chunk c+1 is issued before chunk c is
 // processed, so the load latency overlaps the epilogue arithmetic.
@@ -79,6 +105,7 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, uint32_t tbase
     static_assert((BN / 32) % 2 == 0, "chunks are processed in pairs");
     EpiRowState st;
     epi_row_begin(st);
+    if (p.ep.kind == EPI_LMFWD && row_ok) st.m = lm_tile_max<BN>(p, tbase, col_base);
     uint32_t ra[32], rb[32];
     tmem_ld32(tbase, ra);
 #pragma unroll 1
@@ -161,14 +188,15 @@ __device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t
 // an output into a box in shared memory (st.shared.v4, conflict-free) and
 // one lane writes the box out with a TMA store: whole 64- or 128-byte row
 // segments.  The arithmetic is epi_chunk's, helper for helper.
-//   SK_LMFWD  kept fp32 logits (box F -> map C) + the row's log-sum-exp state
+//   SK_LMFWD  kept fp16 e = exp(z - tile max) (box 0 -> map C) + the row's
+//             log-sum-exp state
 //   SK_LMDZ   recomputed bf16 dz (box 0 -> map C)
 //   SK_SILU   u = acc (box 0 -> map C) and act = silu(acc) (box 1 -> map D)
 //   SK_DSILU  du = acc * silu'(u), u read directly (box 0 -> map C)
 //   SK_RESID  h32 += acc (box F -> map D), its bf16 copy (box 0 -> map C)
 // Boxes: fp32 32 x 32 with 128-byte rows and 128-byte swizzle (16-byte piece
-// j of row r at piece j ^ (r & 7)); bf16 32 x 32 with 64-byte rows and
-// 64-byte swizzle (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor
+// j of row r at piece j ^ (r & 7)); bf16 (or fp16) 32 x 32 with 64-byte rows
+// and 64-byte swizzle (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor
 // maps' swizzle and put each quarter-warp's st.shared.v4 on distinct banks.
 // A warp owns NBUF sets of boxes; the set of chunk c is refilled once the
 // TMA stores of chunk c - NBUF have read it (one bulk group per chunk).
@@ -178,14 +206,17 @@ enum { SK_NONE = 0, SK_LMFWD = 1, SK_LMDZ = 2, SK_SILU = 3, SK_DSILU = 4, SK_RES
 
 template <int SK>
 struct StagedCfg {
-    static constexpr bool F32 = SK == SK_LMFWD || SK == SK_RESID;      // an fp32 box, first in the set
-    static constexpr int N16 = SK == SK_MERGE ? 4 : (SK == SK_SILU ? 2 : (SK == SK_LMFWD ? 0 : 1));
-    static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;     // bf16 boxes after it
+    static constexpr bool F32 = SK == SK_RESID;                          // an fp32 box, first in the set
+    static constexpr int N16 = SK == SK_MERGE ? 4 : (SK == SK_SILU ? 2 : 1);   // 16-bit boxes after it
+    static constexpr int SET_BYTES = (F32 ? 4096 : 0) + 2048 * N16;
     static constexpr int NBUF = (SET_BYTES <= 4096 || SK == SK_MERGE) ? 2 : 1;
     static constexpr int WARP_BYTES = SK == SK_NONE ? 0 : NBUF * SET_BYTES;   // a multiple of 1024
     // epilogue warps per CTA: one per TMEM lane quadrant, two (each half of
     // the tile's columns) for the merge, whose epilogue is its whole time
     static constexpr int EPI_WARPS = SK == SK_MERGE ? 8 : 4;
+    // every box staged_chunk / merge_tile addresses lies inside the warp's area
+    static_assert(SK == SK_NONE || (SET_BYTES >= 2048 && WARP_BYTES >= SET_BYTES && WARP_BYTES % 1024 == 0),
+                  "a staged kind needs room for its boxes");
 };
 
 template <int SK>
@@ -197,6 +228,20 @@ __device__ __forceinline__ void box_row_f32(uint32_t box, int lane, const float*
     for (int j = 0; j < 8; ++j)
         st_shared_v4(rb + ((j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
                      __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+}
+
+__device__ __forceinline__ void box_row_half(uint32_t box, int lane, const float* v) {
+    const uint32_t rb = box + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            __half2 h = __floats2half2_rn(v[8 * j + 2 * u], v[8 * j + 2 * u + 1]);
+            w[u] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st_shared_v4(rb + ((j ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+    }
 }
 
 __device__ __forceinline__ void box_row_bf16(uint32_t box, int lane, const float* v) {
@@ -238,11 +283,12 @@ __device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensor
     if (lane == 0) bulk_wait_read<CF::NBUF - 1>();
     __syncwarp();
     if (SK == SK_LMFWD) {
-        lmfwd_stats(ep, row, col0, v, st);
-        box_row_f32(set, lane, v);
+        float e[32];
+        lmfwd_stats(ep, row, col0, v, st, e);
+        box_row_half(b16, lane, e);
     } else if (SK == SK_LMDZ) {
         float o[32];
-        lmdz_values(ep, row, col0, v, o);
+        lmdz_values<true>(ep, row, col0, v, o);
         box_row_bf16(b16, lane, o);
     } else if (SK == SK_SILU) {
         box_row_bf16(b16, lane, v);
@@ -261,8 +307,7 @@ __device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensor
         // written once here and read by a later launch: evict-first in L2, so
         // that the outputs do not displace the operand tiles the GEMM re-reads
         const uint64_t pol = l2_policy_evict_first();
-        if (SK == SK_LMFWD) tma_store_2d_hint(mc, set, col0, y0, pol);
-        if (SK == SK_LMDZ || SK == SK_DSILU) tma_store_2d_hint(mc, b16, col0, y0, pol);
+        if (SK == SK_LMFWD || SK == SK_LMDZ || SK == SK_DSILU) tma_store_2d_hint(mc, b16, col0, y0, pol);
         if (SK == SK_SILU) {
             tma_store_2d_hint(mc, b16, col0, y0, pol);
             tma_store_2d_hint(md, b16 + 2048, col0, y0, pol);
@@ -286,6 +331,7 @@ __device__ __forceinline__ void epilogue_row_staged(const GemmParams& p, const C
     if (!row_ok) return;
     EpiRowState st;
     epi_row_begin(st);
+    if (SK == SK_LMFWD) st.m = lm_tile_max<BN>(p, tbase, col_base);
     uint32_t ra[32], rb[32];
     tmem_ld32(tbase, ra);
 #pragma unroll 1
@@ -662,6 +708,8 @@ struct SmemLayoutPair {
     static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int MISC_OFF = SLOT_OFF + SCHED * 4;
     static constexpr int TOTAL = MISC_OFF + 16 + 1024;
+    static_assert(TOTAL <= 232448, "dynamic shared memory of one CTA");
+    static_assert(STG_BYTES == StagedCfg<SK>::EPI_WARPS * StagedCfg<SK>::WARP_BYTES, "staging area");
 };
 
 struct PairCoord {
@@ -1278,7 +1326,7 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
 // Tensor map of a staged-store output: [rows x cols] of fp32 (esize 4, 128-byte
 // swizzle) or bf16 (esize 2, 64-byte swizzle), row pitch ld elements, 32 x 32
 // boxes.  TMA stores need a 16-byte aligned base and pitch.
-bool encode_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t ld, int esize) {
+bool encode_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t ld, int esize, bool half = false) {
     if (!ptr || reinterpret_cast<uintptr_t>(ptr) % 16 || (ld * esize) % 16 || rows <= 0 || cols <= 0 ||
         rows >= (1LL << 31) || cols >= (1LL << 31))
         return false;
@@ -1286,7 +1334,9 @@ bool encode_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t l
     cuuint64_t strides[1] = {(cuuint64_t)(ld * esize)};
     cuuint32_t box[2] = {32, 32};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const CUtensorMapDataType dt = esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (half ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    CUresult r = g_encode(m, dt, 2,
                           ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           esize == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1304,7 +1354,7 @@ int staged_kind(const GemmParams& p) {
     const EpiParams& e = p.ep;
     switch (e.kind) {
     case EPI_LMFWD:
-        return e.out0 && e.out_rows > 0 && out_aligned(e.out0, e.ld0, 4) ? SK_LMFWD : SK_NONE;
+        return e.out0 && e.e16 && e.out_rows > 0 && out_aligned(e.out0, e.ld0, 2) ? SK_LMFWD : SK_NONE;
     case EPI_LMDZ:
         return e.out_rows > 0 && out_aligned(e.out0, e.ld0, 2) ? SK_LMDZ : SK_NONE;
     case EPI_SILU:
@@ -1331,7 +1381,7 @@ bool encode_staged(TcMaps& maps, const GemmParams& p) {
     const EpiParams& e = p.ep;
     switch (SK) {
     case SK_LMFWD:
-        return encode_out(&maps.C, e.out0, e.out_rows, e.Vpad, e.ld0, 4);
+        return encode_out(&maps.C, e.out0, e.out_rows, e.Vpad, e.ld0, 2, true);
     case SK_LMDZ:
         return encode_out(&maps.C, e.out0, e.out_rows, e.Vpad, e.ld0, 2);
     case SK_SILU:

@@ -142,6 +142,11 @@ void launch_combine_loss(const LossArgs& la, const float* part, int n_nt, int pa
 template <typename T>
 void launch_lm_dz(const float* z, T* dz, int64_t ld, int V, int Vpad, const float* g, const float* lse,
                   const int* tgt, const int* meta, int row0, int nrows, cudaStream_t s);
+// dz of the bf16 engine's LM head from the kept fp16 e = exp(z - tile max)
+// and the tile maxima mt [rows][part_ld], one chunk of padded rows
+void launch_lm_dz_e16(const __half* e, bf16* dz, int64_t ld, int V, int Vpad, const float* mt, int part_ld,
+                      int lm_bn, const float* g, const float* lse, const int* tgt, const int* meta, int row0,
+                      int nrows, cudaStream_t s);
 void launch_loss_reduce(const double* val_row, const int* pad_off, int n_ad, double* loss_out,
                         cudaStream_t s);
 

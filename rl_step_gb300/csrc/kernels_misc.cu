@@ -315,6 +315,52 @@ template void launch_lm_dz<float>(const float*, float*, int64_t, int, int, const
 template void launch_lm_dz<bf16>(const float*, bf16*, int64_t, int, int, const float*, const float*,
                                  const int*, const int*, int, int, cudaStream_t);
 
+// dz of the bf16 engine's kept-logits LM-head backward from the kept fp16
+// e = exp(z - m) and the rows' tile maxima m: dz = g (onehot - e exp(m - lse)),
+// 16 columns per thread (a partial tile holds whole groups of 16).  The
+// recompute epilogue (lmdz_values<true>) forms the same values.
+__global__ void __launch_bounds__(256) lm_dz_e16_kernel(const __half* __restrict__ e, bf16* __restrict__ dz,
+                                                        int64_t ld, int V, int Vpad, const float* __restrict__ mt,
+                                                        int part_ld, int lm_bn, const float* __restrict__ g,
+                                                        const float* __restrict__ lse, const int* __restrict__ tgt,
+                                                        const int* __restrict__ meta, int row0, int nrows) {
+    const int r = blockIdx.y;
+    const int p = row0 + r;
+    if (r >= nrows || p >= meta[0] * TILE_M) return;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 16;
+    if (c >= Vpad) return;
+    const float gr = g[p];
+    float d[16];
+    if (gr == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) d[j] = 0.f;
+    } else {
+        const uint4* ep = reinterpret_cast<const uint4*>(e + (int64_t)r * ld + c);
+        const uint4 q0 = __ldcs(ep), q1 = __ldcs(ep + 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const int nt_last = (V - 1) / lm_bn;
+        const int nt = c / lm_bn < nt_last ? c / lm_bn : nt_last;   // columns >= V give 0 below
+        const float cc = lm_tile_scale(mt[(int64_t)p * part_ld + nt], lse[p]);
+        const int y = tgt[p];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+            const int v = c + 2 * u;
+            d[2 * u] = v < V ? lm_dz_from_e(gr, v == y, f.x, cc) : 0.f;
+            d[2 * u + 1] = v + 1 < V ? lm_dz_from_e(gr, v + 1 == y, f.y, cc) : 0.f;
+        }
+    }
+    store16<bf16>(dz + (int64_t)r * ld + c, d);
+}
+
+void launch_lm_dz_e16(const __half* e, bf16* dz, int64_t ld, int V, int Vpad, const float* mt, int part_ld,
+                      int lm_bn, const float* g, const float* lse, const int* tgt, const int* meta, int row0,
+                      int nrows, cudaStream_t s) {
+    if (nrows <= 0) return;
+    dim3 grid((unsigned)((Vpad / 16 + 255) / 256), (unsigned)nrows);
+    lm_dz_e16_kernel<<<grid, 256, 0, s>>>(e, dz, ld, V, Vpad, mt, part_ld, lm_bn, g, lse, tgt, meta, row0, nrows);
+}
+
 // Per-adapter loss: sum of its rows' loss values, in row order.
 __global__ void loss_reduce_kernel(const double* val_row, const int* pad_off, int n_ad, double* loss_out) {
     const int a = blockIdx.x;

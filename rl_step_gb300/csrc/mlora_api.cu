@@ -86,6 +86,7 @@ struct mlora {
     // LM head
     int lm_bn = 32, n_nt = 0, part_ld = 0, nc_tiles = 0;
     float* part = nullptr;
+    float* mt = nullptr;                // per row and partial tile: the tile's logit maximum
     float *zt = nullptr, *lse = nullptr, *gvec = nullptr;
     int* tgt_pad = nullptr;
     // LM-head backward (mlora_set_lm_backward).  Recompute: dz[0] only.  Kept
@@ -93,7 +94,8 @@ struct mlora {
     // on `side` beside the next chunk's GEMMs.
     int lm_keep = 0;
     void* dz[2] = {nullptr, nullptr};   // dz of a chunk of rows (base dtype)
-    float* zbuf[2] = {nullptr, nullptr};  // fp32 logits of a chunk of rows
+    void* zbuf[2] = {nullptr, nullptr};   // kept logits of a chunk of rows: fp16 e = exp(z - tile
+                                          // max) on the bf16 engine, fp32 z on the fp32 one
     cudaStream_t side = nullptr;
     cudaEvent_t ev_comb[2] = {}, ev_dz[2] = {}, ev_dh[2] = {};
     double* val_row = nullptr;          // per padded row loss value
@@ -381,6 +383,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         // LM head: partials, per-row scalars, and the bounded dz chunk buffer of
         // the recompute mode (the kept-logits mode adds its buffers on request)
         ALLOC(h->part, (size_t)MP * h->part_ld);
+        ALLOC(h->mt, (size_t)MP * h->part_ld);
         ALLOC(h->zt, MP); ALLOC(h->lse, MP); ALLOC(h->gvec, MP);
         ALLOC(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 128 ? h->max_tiles : 128;   // chunks of up to 16,384 rows
@@ -473,6 +476,7 @@ extern "C" int mlora_create(const mlora_config* cfg, const mlora_init* init, mlo
         CUDA_TRY_OUT(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
         CUDA_TRY_OUT(cudaMemset(h->status, 0, sizeof(int)));
         CUDA_TRY_OUT(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
+        CUDA_TRY_OUT(cudaMemset(h->mt, 0, sizeof(float) * (size_t)MP * h->part_ld));
         if (h->dtype == MLORA_BF16)
             launch_shadow_sync<bf16>(n_ad, h->ad_off, h->ranks_d, L, d, f, h->n_params, h->P, h->shadow, s);
         else
@@ -656,7 +660,8 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
     // walks the rows in chunks: by default each chunk's logits are recomputed
     // by a second GEMM whose epilogue writes dz = g (onehot - softmax) into the
     // chunk buffer, then dh = dz Wout; in the kept-logits mode the forward GEMM
-    // of each chunk also stores its fp32 logits and an elementwise pass forms dz.
+    // of each chunk also stores its logits (the bf16 engine: fp16 e = exp(z -
+    // tile max), beside the tile maxima) and an elementwise pass forms dz.
     if (!backward || !h->lm_keep) {
         {
             GemmParams p = dense_params(h, mt_upper, V, d);
@@ -664,6 +669,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.B = op_kmajor(h->Wout, V, d);
             p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
             p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
+            p.ep.mt = h->mt; p.ep.lm_bn = h->lm_bn;
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
         }
         {
@@ -703,6 +709,7 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
                 p.B = op_kmajor(h->Wout, V, d);
                 p.ep.kind = EPI_LMDZ; p.ep.tgt = h->tgt_pad; p.ep.gv = h->gvec; p.ep.lse = h->lse;
                 p.ep.V = V; p.ep.Vpad = h->Vpad;
+                p.ep.mt = h->mt; p.ep.part_ld = h->part_ld; p.ep.lm_bn = h->lm_bn;
                 p.ep.out0 = h->dz[0]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
                 p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
                 if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_DZ))) return rc;
@@ -743,8 +750,10 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
             p.B = op_kmajor(h->Wout, V, d);
             p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
             p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
+            p.ep.mt = h->mt; p.ep.lm_bn = h->lm_bn;
             p.ep.out0 = h->zbuf[buf]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
             p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
+            p.ep.e16 = sizeof(T) == 2;      // the bf16 engine keeps fp16 e; the fp32 one fp32 z
             if ((rc = run_gemm<T>(h, p, s, MLORA_PROF_LM_FWD))) return rc;
         }
         {
@@ -758,8 +767,14 @@ static int step_impl(mlora_t* h, const mlora_batch* b, const LossArgs& la, float
         if (i >= 2) CUDA_TRY(cudaStreamWaitEvent(h->side, h->ev_dh[buf], 0));
         {
             ProfScope ps(h, h->side, MLORA_PROF_LM_DZ);
-            launch_lm_dz<T>(h->zbuf[buf], reinterpret_cast<T*>(h->dz[buf]), h->Vpad, V, h->Vpad, h->gvec, h->lse,
-                            h->tgt_pad, h->rb.meta, c0 * TILE_M, cnt * TILE_M, h->side);
+            if constexpr (sizeof(T) == 2)
+                launch_lm_dz_e16(reinterpret_cast<const __half*>(h->zbuf[buf]), reinterpret_cast<bf16*>(h->dz[buf]),
+                                 h->Vpad, V, h->Vpad, h->mt, h->part_ld, h->lm_bn, h->gvec, h->lse, h->tgt_pad,
+                                 h->rb.meta, c0 * TILE_M, cnt * TILE_M, h->side);
+            else
+                launch_lm_dz<T>(reinterpret_cast<const float*>(h->zbuf[buf]), reinterpret_cast<T*>(h->dz[buf]),
+                                h->Vpad, V, h->Vpad, h->gvec, h->lse, h->tgt_pad, h->rb.meta, c0 * TILE_M,
+                                cnt * TILE_M, h->side);
             ++h->launches;
         }
         CUDA_TRY(cudaEventRecord(h->ev_dz[buf], h->side));
@@ -1196,17 +1211,18 @@ extern "C" int mlora_set_lm_backward(mlora_t* h, int32_t mode) {
     const size_t rows = (size_t)h->nc_tiles * TILE_M;
     if (mode == MLORA_LM_RECOMPUTE) {
         dfree(h, &h->dz[1]);
-        for (int b = 0; b < 2; ++b) dfree(h, reinterpret_cast<void**>(&h->zbuf[b]));
+        for (int b = 0; b < 2; ++b) dfree(h, &h->zbuf[b]);
         h->lm_keep = 0;
         return MLORA_OK;
     }
     int rc = dalloc(h, &h->dz[1], rows * h->Vpad * h->esize);
-    for (int b = 0; b < 2 && rc == MLORA_OK; ++b) rc = dalloc_t(h, &h->zbuf[b], rows * h->Vpad);
+    const size_t zes = h->esize == 2 ? 2 : 4;   // fp16 e on the bf16 engine, fp32 logits otherwise
+    for (int b = 0; b < 2 && rc == MLORA_OK; ++b) rc = dalloc(h, &h->zbuf[b], rows * h->Vpad * zes);
     if (rc == MLORA_OK && cudaMemset(h->dz[1], 0, rows * h->Vpad * h->esize) != cudaSuccess)
         rc = fail(MLORA_E_CUDA, "cudaMemset of a dz chunk buffer failed");
     if (rc != MLORA_OK) {
         dfree(h, &h->dz[1]);
-        for (int b = 0; b < 2; ++b) dfree(h, reinterpret_cast<void**>(&h->zbuf[b]));
+        for (int b = 0; b < 2; ++b) dfree(h, &h->zbuf[b]);
         return rc;
     }
     h->lm_keep = 1;

@@ -103,7 +103,8 @@ struct mlora_tf {
     // kept logits (dz[0..1], zbuf[0..1], allocated when selected)
     int lm_keep = 0;
     bf16* dz[2] = {nullptr, nullptr};
-    float* zbuf[2] = {nullptr, nullptr};
+    __half* zbuf[2] = {nullptr, nullptr};   // kept fp16 e = exp(z - tile max) of a chunk of rows
+    float* mt = nullptr;                    // per row and partial tile: the tile's logit maximum
     cudaStream_t side = nullptr;
     cudaEvent_t ev_comb[2] = {}, ev_dz[2] = {}, ev_dh[2] = {};
     double* val_row = nullptr;
@@ -392,6 +393,7 @@ extern "C" int mlora_tf_create(const mlora_tf_config* cfg, const mlora_tf_init* 
         TA(h->dqkv, MP * h->Nqkv); TA(h->embed_bf, MP * d);
         TA(h->DT, (size_t)h->nh * MP);
         TA(h->part, (size_t)MP * h->part_ld);
+        TA(h->mt, (size_t)MP * h->part_ld);
         TA(h->zt, MP); TA(h->lse, MP); TA(h->gvec, MP); TA(h->tgt_pad, MP);
         h->nc_tiles = h->max_tiles < 128 ? h->max_tiles : 128;
         TA(h->dz[0], (size_t)h->nc_tiles * TILE_M * h->Vpad);   // the kept-logits mode adds its buffers
@@ -502,6 +504,7 @@ extern "C" int mlora_tf_create(const mlora_tf_config* cfg, const mlora_tf_init* 
              TF_CUDA(cudaMemset(h->nonfinite, 0, sizeof(int) * n_ad));
              TF_CUDA(cudaMemset(h->status, 0, sizeof(int)));
              TF_CUDA(cudaMemset(h->part, 0, sizeof(float) * (size_t)MP * h->part_ld));
+             TF_CUDA(cudaMemset(h->mt, 0, sizeof(float) * (size_t)MP * h->part_ld));
              TF_CUDA(cudaMemset(h->dz[0], 0, (size_t)h->nc_tiles * TILE_M * h->Vpad * B2));
              launch_tf_adam(n_ad, h->ad_off, h->ranks_d, h->n_params, h->adam_tab, h->P, h->G, h->M, h->Vm, 0.f, 0.f,
                             0.f, 0.f, 0.f, h->mirror, 1, h->num_sms, s);
@@ -760,7 +763,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
     // walks the rows in chunks and by default recomputes each chunk's logits
     // with a second GEMM whose epilogue writes dz = g (onehot - softmax), then
     // dxf = dz Wout.  In the kept-logits mode the forward GEMM of each chunk
-    // also stores its fp32 logits and the dz pass of chunk i runs on the side
+    // also stores fp16 e = exp(z - tile max) and the dz pass of chunk i runs on the side
     // stream beside chunk i+1's GEMMs (as in the MLP model's step).
     auto lm_fwd_params = [&](int c0, int cnt) {
         GemmParams p = tf_dense(h, mt_upper, V, d);
@@ -769,6 +772,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         p.B = opnd(h->Wout, V, d, d, 0);
         p.ep.kind = EPI_LMFWD; p.ep.part = h->part; p.ep.zt = h->zt; p.ep.tgt = h->tgt_pad;
         p.ep.part_ld = h->part_ld; p.ep.V = V; p.ep.Vpad = h->Vpad;
+        p.ep.mt = h->mt; p.ep.lm_bn = 256;     // the partials' tile width (n_nt above)
         return p;
     };
     if (!backward || !h->lm_keep) {
@@ -839,6 +843,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
             GemmParams p = lm_fwd_params(c0, cnt);
             p.ep.out0 = h->zbuf[buf]; p.ep.ld0 = h->Vpad; p.ep.out_row_shift = -(int64_t)c0 * TILE_M;
             p.ep.out_rows = (int64_t)h->nc_tiles * TILE_M;
+            p.ep.e16 = 1;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_LM_FWD))) return rc;
         }
         {
@@ -852,8 +857,8 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         if (i >= 2) TF_CUDA(cudaStreamWaitEvent(h->side, h->ev_dh[buf], 0));
         {
             TfProf ps(h, h->side, MLORA_TF_PROF_LM_DZ);
-            launch_lm_dz<bf16>(h->zbuf[buf], h->dz[buf], h->Vpad, V, h->Vpad, h->gvec, h->lse, h->tgt_pad, h->rb.meta,
-                               c0 * TILE_M, cnt * TILE_M, h->side);
+            launch_lm_dz_e16(h->zbuf[buf], h->dz[buf], h->Vpad, V, h->Vpad, h->mt, h->part_ld, 256, h->gvec,
+                             h->lse, h->tgt_pad, h->rb.meta, c0 * TILE_M, cnt * TILE_M, h->side);
             ++h->launches;
         }
         TF_CUDA(cudaEventRecord(h->ev_dz[buf], h->side));

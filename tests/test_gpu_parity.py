@@ -153,8 +153,9 @@ def test_lm_backward_modes_bitwise_equal(dtype):
     accumulator is the forward's and dz is formed by the same arithmetic), over
     a batch of three LM-head chunks.  Deterministic mode makes the gradient
     reductions themselves repeatable (by default they meet in fp32 atomics in
-    arrival order).  The recompute handle holds less memory: no fp32 logit
-    chunks and one dz chunk buffer instead of two."""
+    arrival order).  The recompute handle holds less memory: no kept-logit
+    chunks (fp16 e = exp(z - tile max) on the bf16 engine, fp32 logits on the
+    fp32 one) and one dz chunk buffer instead of two."""
     import rl_step_gb300 as m
     over = {"d_model": 256, "d_ffn": 512, "vocab": 1000} if dtype == "bf16" else \
         {"d_model": 64, "d_ffn": 128, "vocab": 520, "dtype": "fp32"}
@@ -185,7 +186,8 @@ def test_lm_backward_modes_bitwise_equal(dtype):
     tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
     assert tiles > 2 * 128                               # three LM-head chunks
     rows, vpad = 128 * 128, (cfg.vocab + 63) // 64 * 64
-    assert bytes_k - bytes_r == rows * vpad * (es + 2 * 4)
+    zes = 2 if cfg.dtype == "bf16" else 4                # kept fp16 e (bf16 engine) or fp32 logits
+    assert bytes_k - bytes_r == rows * vpad * (es + 2 * zes)
 
 
 def test_lm_backward_mode_switch_frees_and_rejects():

@@ -181,7 +181,8 @@ def test_lm_backward_modes_agree_over_three_chunks():
     """Recomputing each LM-head chunk's logits and keeping them give bitwise
     the same logprobs and losses, and the same gradients up to the arrival
     order of the fp32 gradient atomics, on a batch of three LM-head chunks; the
-    kept-logits mode holds two fp32 logit chunks and a second dz chunk more."""
+    kept-logits mode holds two chunks of fp16 e = exp(z - tile max) and a
+    second dz chunk more."""
     import rl_step_gb300.transformer as t
     cfg = wt.get_tf_config("tf_small")
     base, ad = wt.make_tf_base_weights(cfg), wt.make_tf_adapters(cfg)
@@ -202,7 +203,7 @@ def test_lm_backward_modes_agree_over_three_chunks():
     tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
     assert tiles > 256
     vpad = (cfg.vocab + 63) // 64 * 64
-    assert by_k - by_r == 128 * 128 * vpad * (2 + 2 * 4)
+    assert by_k - by_r == 128 * 128 * vpad * (2 + 2 * 2)          # a dz chunk, two fp16 e chunks
 
 
 @pytest.mark.parametrize("kind", ["ppo", "custom"])
