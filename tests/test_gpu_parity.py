@@ -146,19 +146,22 @@ def test_step_parity(name, n, overrides, lm):
     assert g_after == 0.0                            # gradients consumed
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "bf16_wide", "fp32"])
 def test_lm_backward_modes_bitwise_equal(dtype):
     """Recomputing each chunk's logits and keeping them from the forward give
     bitwise the same logprobs, losses and gradients (the recompute GEMM's
     accumulator is the forward's and dz is formed by the same arithmetic), over
-    a batch of three LM-head chunks.  Deterministic mode makes the gradient
-    reductions themselves repeatable (by default they meet in fp32 atomics in
-    arrival order).  The recompute handle holds less memory: no kept-logit
-    chunks (fp16 e = exp(z - tile max) on the bf16 engine, fp32 logits on the
-    fp32 one) and one dz chunk buffer instead of two."""
+    a batch of three LM-head chunks; "bf16_wide" (V = 65,536, d = 512) runs dh
+    on its 256 x 512 tiles and the forward on the full-size tile layout of the
+    kept fp16 e.  Deterministic mode makes the gradient reductions themselves
+    repeatable (by default they meet in fp32 atomics in arrival order).  The
+    recompute handle holds less memory: no kept-logit chunks (fp16 e = exp(z -
+    tile max) on the bf16 engine, fp32 logits on the fp32 one) and one dz chunk
+    buffer instead of two."""
     import rl_step_gb300 as m
-    over = {"d_model": 256, "d_ffn": 512, "vocab": 1000} if dtype == "bf16" else \
-        {"d_model": 64, "d_ffn": 128, "vocab": 520, "dtype": "fp32"}
+    over = {"bf16": {"d_model": 256, "d_ffn": 512, "vocab": 1000},
+            "bf16_wide": {"d_model": 512, "d_ffn": 1024, "vocab": 65536},
+            "fp32": {"d_model": 64, "d_ffn": 128, "vocab": 520, "dtype": "fp32"}}[dtype]
     cfg = wl.get_config("qwen3_8b_ppo", **over)
     base = wl.make_base_weights(cfg)
     ad = wl.make_adapters(cfg)
