@@ -118,6 +118,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.first = 0
         self.thread = None
 
     def start(self):
@@ -136,6 +137,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self):
+        """The timed region starts: later summaries use the samples from here on
+        (and the one just before, so that a short region has one)."""
+        self.first = max(0, len(self.lines) - 1)
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -148,7 +154,7 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        for ln in self.lines[self.first:]:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -339,13 +345,6 @@ def run_ours(args, rank, world):
         m.mlora_optim_step(h, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
                            weight_decay=cfg.weight_decay, skipped_out=skipped)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    status = m.mlora_check_status(h)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
-
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
@@ -366,12 +365,22 @@ def run_ours(args, rank, world):
         return e0.elapsed_time(e1)
 
     # ---- device-timed region (no instrumentation) ----------------------------
-    launches0 = h.kernel_launches
+    # The clock sampler starts first; the warm-up steps then run right before
+    # the timed ones, so the timed steps follow steps as in training, not an
+    # idle GPU (whose power controller overshoots on the first busy second).
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = m.mlora_check_status(h)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    launches0 = h.kernel_launches
     barrier()
     torch.cuda.synchronize()
+    clocks.mark()
     ms = timed_steps(args.steps)
     barrier()
     clk = clocks.stop()
