@@ -437,7 +437,9 @@ def run_ours(args, rank, world):
         t_e2e = max_over_ranks(time.perf_counter() - t0, dev)
         e2e = {"value": job_throughput(N, args.steps, world, 1e3 * t_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": 1e3 * t_e2e / args.steps}
+               "ms_per_step": 1e3 * t_e2e / args.steps,
+               "note": ("timed after the headline and per-class loops, so later in the SM clock's "
+                        "rise over the first seconds of load; the copies cost well under 1 % of a step")}
 
     # ---- tokens whose dL/dl is non-zero (from this run's logprobs) ----------
     nz_g = count_nonzero_g(cfg, b, lp_out.cpu().numpy(),
