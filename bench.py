@@ -83,6 +83,10 @@ def parse_args():
                     help="override the transformer row's vocabulary (profiling; not a bench value)")
     ap.add_argument("--tf-layers", type=int, default=None,
                     help="override the transformer row's layer count (profiling; not a bench value)")
+    ap.add_argument("--tf-attn-bwd", default="stored_ds", choices=["stored_ds", "recompute"],
+                    help="attention backward of the transformer row's timed loop: dS blocks stored "
+                         "for the workload's longest sequence, or S and dP recomputed on the query "
+                         "side (the other mode's per-class times are reported too)")
     ap.add_argument("--deterministic", action="store_true",
                     help="batch-invariant mode: one gradient chunk per adapter")
     ap.add_argument("--lm-backward", default="keep_logits", choices=["keep_logits", "recompute"],
@@ -670,6 +674,10 @@ def measure_transformer_row(args, dev, stream, peaks):
     h = t.tf_create(cfg.vocab, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.n_layers, cfg.ranks,
                     cfg.alphas, N, dbase, A, B, rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
     t.tf_set_lm_backward(h, args.lm_backward)     # the MLP step's mode
+    # stored dS blocks: sequences of at most the workload's longest (2,048 tokens)
+    attn_seq = {"stored_ds": cfg.seq_hi, "recompute": 0}
+    t.tf_set_attention_backward(h, attn_seq[args.tf_attn_bwd])
+    mode_bytes = {args.tf_attn_bwd: h.device_bytes}
     torch.cuda.synchronize()
     del dbase, A, B
     torch.cuda.empty_cache()
@@ -691,21 +699,34 @@ def measure_transformer_row(args, dev, stream, peaks):
     if t.tf_check_status(h) != 0:
         raise RuntimeError("transformer row: device status after warm-up")
     K = max(1, min(args.steps, 5))
-    t.tf_profile_read(h, reset=True)
-    t.tf_profile_enable(h, True)
+
+    def timed(profile):
+        """ms per step over K steps; with per-launch events (per-class times) when profile."""
+        t.tf_profile_read(h, reset=True)
+        t.tf_profile_enable(h, profile)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t.tf_profile_enable(h, False)
+        if t.tf_check_status(h) != 0:
+            raise RuntimeError("transformer row: device status in the timed region")
+        return e0.elapsed_time(e1) / K, t.tf_profile_read(h, reset=True)
+
     launches0 = h.kernel_launches
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t.tf_profile_enable(h, False)
-    prof = t.tf_profile_read(h, reset=True)
+    ms, _ = timed(False)                 # the row's step time: no per-launch events
     launches = (h.kernel_launches - launches0) / K
-    if t.tf_check_status(h) != 0:
-        raise RuntimeError("transformer row: device status in the timed region")
-    ms = e0.elapsed_time(e1) / K
+    ms_prof, prof = timed(True)          # per-class times, a second loop
+    device_bytes = h.device_bytes
+    # the other attention backward mode: per-class times of its own loop
+    other = "recompute" if args.tf_attn_bwd == "stored_ds" else "stored_ds"
+    t.tf_set_attention_backward(h, attn_seq[other])
+    mode_bytes[other] = h.device_bytes
+    step()
+    torch.cuda.synchronize()
+    ms_other, prof_other = timed(True)
     fl = tf_flop_model(cfg, b)
     peak_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     kern = {c: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for c, v in prof.items() if v[1] > 0}
@@ -715,6 +736,15 @@ def measure_transformer_row(args, dev, stream, peaks):
         return (flops / (tms * 1e-3) / 1e12) if tms > 0 else None
     att_f, att_b = rate(fl["attn_fwd"], ("attn_fwd",)), rate(fl["attn_bwd"], ("attn_bwd",))
     gemm = rate(fl["proj_lm"], TF_TC_CLASSES)
+    attn_modes = {}
+    for mode, (msm, pr) in ((args.tf_attn_bwd, (ms_prof, prof)), (other, (ms_other, prof_other))):
+        tb = pr["attn_bwd"][0] / K
+        attn_modes[mode] = {"attn_bwd_ms_per_step": tb,
+                            "bwd_tflops": fl["attn_bwd"] / (tb * 1e-3) / 1e12 if tb > 0 else None,
+                            "bwd_frac": fl["attn_bwd"] / (tb * 1e-3) / 1e12 / peak_tc if tb > 0 else None,
+                            "step_ms_with_per_launch_events": msm,
+                            "max_seq_len": attn_seq[mode],
+                            "device_bytes": mode_bytes[mode]}
     row = {
         "workload": cfg.description + (f" (override {over})" if over else ""),
         "tokens": N, "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
@@ -725,10 +755,14 @@ def measure_transformer_row(args, dev, stream, peaks):
                       "fwd_frac": att_f / peak_tc if att_f else None,
                       "bwd_frac": att_b / peak_tc if att_b else None,
                       "bound": "tensor", "unit": "TFLOP/s (algorithmic, causal pairs only; backward "
-                                                "includes its rowsum pass, the S recompute is not credited)"},
+                                                "includes its rowsum pass; the recompute mode's second S "
+                                                "and dP are not credited)",
+                      "backward_mode": args.tf_attn_bwd, "backward_modes": attn_modes},
         "projection_and_lm_gemms": {"tflops": gemm, "frac": gemm / peak_tc if gemm else None},
         "kernels": kern, "gpu_launches_per_step": launches,
-        "device_bytes": h.device_bytes, "lm_backward": args.lm_backward,
+        "device_bytes": device_bytes, "lm_backward": args.lm_backward,
+        "timing": "step time from a loop without per-launch events; per-class times from a second loop "
+                  "with them",
     }
     del h
     torch.cuda.empty_cache()

@@ -154,6 +154,23 @@ int mlora_tf_check_status(mlora_tf_t* h, void* stream);
  * the recompute mode), E_CUDA. */
 int mlora_tf_set_lm_backward(mlora_tf_t* h, int32_t mode);
 
+/* Attention backward mode (the pages fix only what the backward computes,
+ * the gradients of causal attention; this choice of kernels has no
+ * counterpart there).  max_seq_len = 0 (the default of a new handle): the
+ * query-side kernel recomputes S = Q K^T and dP = dO V^T to form dS and dQ.
+ * max_seq_len > 0: the key-side kernel also stores every 128 x 128 block of
+ * dS it forms (bf16, the values its dK product reads) and the query side
+ * computes dQ = dS K from them, without recomputing; the handle then holds
+ * max_tokens-padded/128 x (ceil((S-1)/128) + 1) x n_heads blocks of 32 KB,
+ * S = min(max_seq_len, max_tokens), allocated here and freed when the mode
+ * is left, and positions must be below S: a token at a larger position is a
+ * range error (MLORA_E_RANGE; it is treated as a one-token sequence).  The
+ * two modes sum dQ in different orders, so their dQ agree to rounding, not
+ * bit for bit; dK and dV are the same.  Synchronises the device.  Errors:
+ * E_ARG (max_seq_len < 0, or a layout past 2^31 rows), E_NOMEM (the handle
+ * is then in the recompute mode), E_CUDA. */
+int mlora_tf_set_attention_backward(mlora_tf_t* h, int32_t max_seq_len);
+
 /* Per-kernel-class timing, as mlora_profile_enable / mlora_profile_read, with
  * the classes below (arrays of MLORA_TF_PROF_CLASSES entries). */
 enum {

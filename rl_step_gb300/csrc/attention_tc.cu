@@ -41,6 +41,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 struct AttnMaps {
     CUtensorMap rows128;   // qkv, boxes of 64 columns x 128 rows
     CUtensorMap do128;     // dO [P x n_heads*128], boxes of 64 x 128 (backward only)
+    CUtensorMap ds128;     // stored dS blocks [blocks*128 x 128], boxes of 64 x 128 (stored mode only)
 };
 
 struct AttnParams {
@@ -59,6 +60,8 @@ struct AttnParams {
     const float* DT;       // [n_heads x ld_t]
     bf16* dqkv;            // [P x ld_qkv]: dQ, dK, dV in the columns of q, k, v
     int* counter;          // item counter of the persistent kernels (zeroed before each launch)
+    bf16* ds;              // stored dS blocks (null: the query side recomputes them), see AttnArgs
+    int ktc;               // key tiles per query tile in the stored layout
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -842,6 +845,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const uint32_t M = gm + m, N = gn0 + n;
                 const int s = N & 1;
                 const int q0 = (it.kt + n % it.nqt) * TB;
+                // stored mode: this thread's 32 dS values of the half, row r of block
+                // (query tile, key tile, head), columns 64 b + 32 wg ..
+                bf16* dsp = nullptr;
+                if (p.ds) {
+                    const int qt = it.kt + n % it.nqt, hq = it.g * grp + n / it.nqt;
+                    if (qt - it.kt < p.ktc)
+                        dsp = p.ds + (((int64_t)qt * p.ktc + (qt - it.kt)) * p.n_heads + hq) * (TB * TB) +
+                              (int64_t)r * TB + 64 * b + 32 * wg;
+                    else if (lane == 0)
+                        raise_status(status, ST_RANGE);
+                }
                 const float* lse_s = reinterpret_cast<const float*>(smem + SL::VEC0 + s * 1536);
                 const float* D_s = lse_s + 128;
                 const int* ss_s = reinterpret_cast<const int*>(lse_s + 256);
@@ -894,6 +908,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     }
                     tmem_st16(cs, wp);           // over this warpgroup's columns, already read
                     tmem_st16(cd, wd);
+                    if (dsp) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dsp);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            d4[u] = make_uint4(wd[4 * u], wd[4 * u + 1], wd[4 * u + 2], wd[4 * u + 3]);
+                    }
                 };
                 if (whole) write_pd(std::false_type{});
                 else write_pd(std::true_type{});
@@ -1211,6 +1231,227 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ----------------------------------------------------------------------------
+// Backward, query side from stored dS.  When the key-side kernel has written
+// every dS block (128 key rows x 128 query columns, bf16, the values its dK
+// product reads), dQ = scale sum_kt dS_kt K_kt is a plain product chain: no
+// scores, no softmax.  Work item = (128-row query tile qt, query head h); its
+// key tiles are the 128-aligned tiles kt = floor(seq_start / 128) .. qt (the
+// key-side kernel's tiles; keys before the sequence start carry dS = 0).  Per
+// key tile one stage holds the dS block (A, read MN-major: queries are its
+// contiguous columns) and the K tile (B, read MN-major: head columns), and
+// the MMA thread adds the 128 x 128 x 128 product into one of two TMEM
+// accumulators, so the read-out of one item overlaps the next item's
+// products.  Warps: 0 loads, 1 issues the MMAs, 2-5 read dQ out (one query
+// row per thread, TMEM lane quarter = warp % 4).
+// ----------------------------------------------------------------------------
+constexpr int QS_STAGES = 3;
+constexpr int QS_THREADS = 192;
+
+struct QsSmem {
+    static constexpr int ST0 = 0;                 // stage s: dS block at ST0 + 4 BLK s, K tile 2 BLK after
+    static constexpr int BAR = QS_STAGES * 4 * BLK;
+    enum { FULL = 0, EMPTY = QS_STAGES, ACC_FULL = 2 * QS_STAGES, ACC_FREE = 2 * QS_STAGES + 2,
+           DRAIN = 2 * QS_STAGES + 4, SCHED_FULL = 2 * QS_STAGES + 5, SCHED_EMPTY = SCHED_FULL + RING,
+           NBARS = SCHED_EMPTY + RING };
+    static constexpr int MISC = BAR + NBARS * 8;     // TMEM base, abort flag, then the item ring
+    static constexpr int TOTAL = MISC + 32 + 1024;
+};
+static_assert(QsSmem::TOTAL <= 232448, "dynamic shared memory of one CTA");
+
+// Query-side item over stored blocks: query tile qt of head h, key tiles
+// kt0 .. qt (at most ktc of them; more would mean a sequence longer than the
+// stored layout holds, which the row metadata rules out).
+struct QsItem {
+    int qt, h, kt0, nt;
+};
+
+__device__ __forceinline__ QsItem qs_item(const AttnParams& p, int item) {
+    QsItem it;
+    it.qt = item / p.n_heads;
+    it.h = item % p.n_heads;
+    it.kt0 = p.seq_start[it.qt * TB] / TB;
+    if (it.qt - it.kt0 >= p.ktc) it.kt0 = it.qt - p.ktc + 1;
+    it.nt = it.qt - it.kt0 + 1;
+    return it;
+}
+
+// dQ (+)= dS K: M = 128 queries, N = 128 head columns, K = 128 keys; both
+// operands MN-major tiles of 128 rows (keys) x 128 columns.
+__device__ __forceinline__ void mma_dsk(uint32_t d, uint32_t ds, uint32_t k, bool acc) {
+    const uint32_t id = idesc_bf16(128, 1, 1, 128);
+    const uint64_t ad = mndesc(ds), bd = mndesc(k);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, ad + 512 * kb + 128 * kk, bd + 512 * kb + 128 * kk, id, (acc || kb || kk) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(QS_THREADS, 1)
+    attn_bwd_q_stored_kernel(const __grid_constant__ AttnMaps maps, const AttnParams p, int n_items, int* status) {
+    using SL = QsSmem;
+    const int mt_valid = *p.meta < p.max_tiles ? *p.meta : p.max_tiles;
+    auto valid = [&](int item) -> bool { return item >= 0 && item < n_items && item / p.n_heads < mt_valid; };
+    if (blockIdx.x >= mt_valid * p.n_heads) return;   // more CTAs than items
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + SL::BAR + 8 * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = p.n_heads / p.n_kv;
+
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + SL::MISC + 16);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QS_STAGES; ++i) {
+            mbar_init(bar(SL::FULL + i), 1);
+            mbar_init(bar(SL::EMPTY + i), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(SL::ACC_FULL + a), 1);
+            mbar_init(bar(SL::ACC_FREE + a), 4);      // the four read-out warps
+        }
+        mbar_init(bar(SL::DRAIN), 1);
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(bar(SL::SCHED_FULL + i), 1);
+            mbar_init(bar(SL::SCHED_EMPTY + i), 5);   // MMA thread, four read-out warps
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+        tma_prefetch_desc(&maps.rows128);
+        tma_prefetch_desc(&maps.ds128);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;   // accumulator a at columns 128 a
+    int dummy = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int last[QS_STAGES];
+            for (int s = 0; s < QS_STAGES; ++s) last[s] = -1;
+            uint32_t gj = 0;                           // blocks loaded by this CTA
+            RingPos rp;
+            while (ok) {
+                int item = atomicAdd(p.counter, 1);
+                if (!valid(item)) item = -1;
+                if (!ring_put(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const QsItem it = qs_item(p, item);
+                if (p.seq_start[it.qt * TB] / TB != it.kt0) raise_status(status, ST_RANGE);
+                const int kcol = (p.n_heads + it.h / grp) * HD;
+                for (int j = 0; j < it.nt; ++j, ++gj) {
+                    const int s = (int)(gj % QS_STAGES);
+                    const uint32_t sp = (gj / QS_STAGES) & 1u;
+                    if (!mbar_wait(bar(SL::EMPTY + s), sp ^ 1u, abort_flag)) { ok = false; break; }
+                    const int kt = it.kt0 + j;
+                    const int64_t blk = ((int64_t)it.qt * p.ktc + (it.qt - kt)) * p.n_heads + it.h;
+                    const uint32_t fb = bar(SL::FULL + s), st = sb + SL::ST0 + s * 4 * BLK;
+                    mbar_expect_tx(fb, 4 * BLK);
+                    load_tile128(st, &maps.ds128, fb, 0, (int)(blk * TB));
+                    load_tile128(st + 2 * BLK, &maps.rows128, fb, kcol, kt * TB);
+                    last[s] = (int)sp;
+                }
+            }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            bool dr = true;                            // our copies have landed
+            for (int s = 0; s < QS_STAGES; ++s)
+                if (last[s] >= 0) dr &= mbar_wait(bar(SL::FULL + s), (uint32_t)last[s], (volatile int*)&dummy);
+            if (!dr) atomicOr(status, ST_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t gj = 0, nit = 0;                  // blocks and items consumed
+            RingPos rp;
+            while (ok) {
+                int item;
+                if (!ring_get(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (item < 0) break;
+                const int nt = qs_item(p, item).nt;
+                const int a = nit & 1;
+                // the read-out of this accumulator's previous item is done
+                if (nit >= 2 && !mbar_wait(bar(SL::ACC_FREE + a), ((nit >> 1) - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                for (int j = 0; j < nt; ++j, ++gj) {
+                    const int s = (int)(gj % QS_STAGES);
+                    if (!mbar_wait(bar(SL::FULL + s), (gj / QS_STAGES) & 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t st = sb + SL::ST0 + s * 4 * BLK;
+                    mma_dsk(tmem + 128 * a, st, st + 2 * BLK, j > 0);
+                    umma_commit(bar(SL::EMPTY + s));
+                }
+                if (!ok) break;
+                umma_commit(bar(SL::ACC_FULL + a));
+                ++nit;
+            }
+            if (!ok) { atomicOr(status, ST_TIMEOUT); *abort_flag = 1; }
+            umma_commit(bar(SL::DRAIN));
+            if (!mbar_wait(bar(SL::DRAIN), 0, (volatile int*)&dummy)) atomicOr(status, ST_TIMEOUT);
+        }
+    } else {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        bool ok = true;
+        uint32_t ra[32];
+        uint32_t nit = 0;
+        RingPos rp;
+        while (ok) {
+            int item;
+            if (!ring_get_warp(bar(SL::SCHED_FULL), bar(SL::SCHED_EMPTY), ring, rp, item, abort_flag, lane)) {
+                ok = false;
+                break;
+            }
+            if (item < 0) break;
+            const QsItem it = qs_item(p, item);
+            const int a = nit & 1;
+            if (!warp_wait(bar(SL::ACC_FULL + a), (nit >> 1) & 1u, abort_flag, lane)) { ok = false; break; }
+            tc_fence_after();
+            bf16* row = p.dqkv + (int64_t)(it.qt * TB + r) * p.ld_qkv + it.h * HD;
+            float v[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld32(tl + 128 * a + 32 * c, ra);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]) * p.scale;
+                store32<bf16>(row + 32 * c, v);
+            }
+            // this accumulator has been read: a later item's products may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SL::ACC_FREE + a));
+            ++nit;
+        }
+        if (!ok && lane == 0) {
+            atomicOr(status, ST_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
 // D[h][p] = sum_c dO[p][h*128 + c] O[p][h*128 + c]: 16 threads per (row, head),
 // 8 elements each.
 __global__ void attn_rowdot_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, int n_heads,
@@ -1265,6 +1506,12 @@ bool make_maps(AttnMaps& m, const AttnArgs& a) {
     } else {
         m.do128 = m.rows128;
     }
+    if (a.ds) {
+        const int64_t rows = (int64_t)(a.max_rows / TB) * a.ktc * a.n_heads * TB;
+        if (a.ktc < 1 || rows > INT32_MAX || !tc_encode_bf16(&m.ds128, a.ds, rows, TB, TB, 64, TB)) return false;
+    } else {
+        m.ds128 = m.rows128;
+    }
     return true;
 }
 
@@ -1284,6 +1531,8 @@ AttnParams make_params(const AttnArgs& a) {
     p.DT = a.DT;
     p.dqkv = a.dqkv;
     p.counter = a.counter;
+    p.ds = a.ds;
+    p.ktc = a.ktc;
     return p;
 }
 
@@ -1313,6 +1562,9 @@ cudaError_t launch_attention_bwd(const AttnArgs& a, int* status, cudaStream_t s)
     e = launch_attn_persistent(attn_bwd_kv_kernel, KvSmem::TOTAL, BWD_THREADS, maps, p, p.max_tiles * a.n_kv,
                                a.num_sms, status, s);
     if (e != cudaSuccess) return e;
+    if (a.ds)   // dQ from the dS blocks the key side stored
+        return launch_attn_persistent(attn_bwd_q_stored_kernel, QsSmem::TOTAL, QS_THREADS, maps, p,
+                                      p.max_tiles * a.n_heads, a.num_sms, status, s);
     return launch_attn_persistent(attn_bwd_q_kernel, QSmem::TOTAL, BWD_THREADS, maps, p, p.max_tiles * a.n_heads,
                                   a.num_sms, status, s);
 }

@@ -63,6 +63,13 @@ struct AttnArgs {
     bf16* dqkv = nullptr;          // backward: dL/d(q, k, v), same layout as qkv
     int num_sms = 0;               // persistent kernels: one CTA per SM
     int* counter = nullptr;        // device int: their work-item counter
+    // backward with stored dS blocks (null: the query side recomputes S and dP):
+    // [max_rows/128 x ktc x n_heads] blocks of 128 key rows x 128 query columns,
+    // block (query tile qt, key tile kt, head h) at (qt ktc + qt - kt) n_heads + h;
+    // every query tile sees at most ktc key tiles (sequences of at most
+    // 128 (ktc - 1) + 1 rows)
+    bf16* ds = nullptr;
+    int ktc = 0;
 };
 cudaError_t launch_attention_fwd(const AttnArgs& a, int* status, cudaStream_t s);
 // rowsum kernel, key-side (dK, dV) kernel, query-side (dQ) kernel

@@ -105,6 +105,12 @@ struct mlora_tf {
     bf16* dz[2] = {nullptr, nullptr};
     __half* zbuf[2] = {nullptr, nullptr};   // kept fp16 e = exp(z - tile max) of a chunk of rows
     float* mt = nullptr;                    // per row and partial tile: the tile's logit maximum
+    // attention backward (mlora_tf_set_attention_backward): the query side
+    // recomputes S and dP (attn_ds null), or reads the dS blocks the key side
+    // stores for sequences of at most attn_max_seq tokens (attn_ktc key tiles
+    // per query tile)
+    bf16* attn_ds = nullptr;
+    int attn_ktc = 0, attn_max_seq = 0;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_comb[2] = {}, ev_dz[2] = {}, ev_dh[2] = {};
     double* val_row = nullptr;
@@ -705,8 +711,10 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         TfProf ps(h, s, MLORA_TF_PROF_ROUTING);
         launch_routing(b->adapter_ids, N, n_ad, h->rb, backward ? h->touched : nullptr, h->status, s, &h->launches,
                        GRAD_CHUNK);
+        // positions bound the sequence lengths the stored dS layout holds
         launch_tf_rows(h->rb.perm_pad, h->rb.meta, h->rb.tile_ad, h->rb.pad_off, b->positions, b->adapter_ids,
-                       (int)h->max_tokens, mp, h->pos_pad, h->seq_start, h->status, s);
+                       h->attn_ds ? h->attn_max_seq : (int)h->max_tokens, mp, h->pos_pad, h->seq_start, h->status,
+                       s);
         ++h->launches;
     }
     {
@@ -903,7 +911,10 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         if ((rc = proj_grads(h, G_O, MLORA_TF_O, l, mp, h->dhb, h->vo[l], h->o[l], s))) return rc;
         {
             TfProf ps(h, s, MLORA_TF_PROF_ATTN_BWD);
-            const cudaError_t e = launch_attention_bwd(attn_args(h, l, mp), h->status, s);
+            AttnArgs aa = attn_args(h, l, mp);
+            aa.ds = h->attn_ds;
+            aa.ktc = h->attn_ktc;
+            const cudaError_t e = launch_attention_bwd(aa, h->status, s);
             if (e != cudaSuccess) return tfail(MLORA_E_CUDA, "attention backward launch: %s", cudaGetErrorString(e));
             h->launches += 3;
         }
@@ -1079,6 +1090,30 @@ extern "C" int mlora_tf_set_lm_backward(mlora_tf_t* h, int32_t mode) {
         return rc;
     }
     h->lm_keep = 1;
+    return MLORA_OK;
+}
+
+extern "C" int mlora_tf_set_attention_backward(mlora_tf_t* h, int32_t max_seq_len) {
+    if (!h) return tfail(MLORA_E_ARG, "NULL handle");
+    if (max_seq_len < 0) return tfail(MLORA_E_ARG, "max_seq_len %d < 0", max_seq_len);
+    const int S = (int64_t)max_seq_len > h->max_tokens ? (int)h->max_tokens : max_seq_len;
+    const int ktc = S > 0 ? (S - 1 + 127) / 128 + 1 : 0;   // key tiles one query tile can see
+    if (S > 0 && h->attn_ds && ktc == h->attn_ktc) {
+        h->attn_max_seq = S;
+        return MLORA_OK;
+    }
+    TF_CUDA(cudaDeviceSynchronize());   // no queued step may still use the buffer
+    tf_free(h, reinterpret_cast<void**>(&h->attn_ds));
+    h->attn_ktc = 0;
+    h->attn_max_seq = 0;
+    if (S == 0) return MLORA_OK;
+    const int64_t blocks = (h->max_pad / 128) * (int64_t)ktc * h->nh;
+    if (blocks * 128 > INT32_MAX)
+        return tfail(MLORA_E_ARG, "stored attention blocks for %d-token sequences exceed the layout's range", S);
+    const int rc = tf_alloc_t(h, &h->attn_ds, (size_t)blocks * 128 * 128);
+    if (rc != MLORA_OK) return rc;
+    h->attn_ktc = ktc;
+    h->attn_max_seq = S;
     return MLORA_OK;
 }
 

@@ -18,7 +18,8 @@ from . import LOSS_KINDS, _Adam, _check, _LossInputs, _ptr, _stream, load_librar
 
 __all__ = ["PROJ", "TF_PROF_CLASSES", "TfHandle", "tf_create", "tf_destroy", "tf_forward",
            "tf_forward_backward", "tf_forward_backward_custom", "tf_optim_step", "tf_read_adapter",
-           "tf_get_steps", "tf_check_status", "tf_profile_enable", "tf_profile_read", "tf_set_lm_backward"]
+           "tf_get_steps", "tf_check_status", "tf_profile_enable", "tf_profile_read", "tf_set_lm_backward",
+           "tf_set_attention_backward"]
 
 PROJ = ("q", "k", "v", "o", "gate", "up", "down")
 HEAD_DIM = 128
@@ -64,6 +65,7 @@ _SIGNATURES = {
     "mlora_tf_check_status": (c_int32, [c_void_p, c_void_p]),
     "mlora_tf_profile_enable": (c_int32, [c_void_p, c_int32]),
     "mlora_tf_set_lm_backward": (c_int32, [c_void_p, c_int32]),
+    "mlora_tf_set_attention_backward": (c_int32, [c_void_p, c_int32]),
     "mlora_tf_profile_read": (c_int32, [c_void_p, POINTER(c_double), POINTER(c_int64), c_int32]),
     "mlora_tf_kernel_launches": (c_int64, [c_void_p]),
     "mlora_tf_device_bytes": (c_int64, [c_void_p]),
@@ -252,6 +254,12 @@ def tf_set_lm_backward(h: TfHandle, mode: str):
     """LM-head backward mode: "recompute" (default) or "keep_logits"."""
     from . import LM_BACKWARD_MODES
     _check(_lib().mlora_tf_set_lm_backward(h.ptr, LM_BACKWARD_MODES[mode]))
+
+
+def tf_set_attention_backward(h: TfHandle, max_seq_len: int):
+    """0: the query side recomputes S and dP (default); > 0: dS blocks are
+    stored for sequences of at most max_seq_len tokens."""
+    _check(_lib().mlora_tf_set_attention_backward(h.ptr, int(max_seq_len)))
 
 
 def tf_profile_enable(h: TfHandle, on: bool = True):

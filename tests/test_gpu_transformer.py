@@ -46,7 +46,7 @@ def _lib():
     __graft_entry__.build()
 
 
-def _make(cfg, base, ad, max_tokens, lm=None):
+def _make(cfg, base, ad, max_tokens, lm=None, attn=0):
     import rl_step_gb300.transformer as t
     dbase = {"E": dev(base["E"]), "Wout": dev(base["Wout"]), "final_norm": dev(base["final_norm"]),
              "attn_norm": [dev(g) for g in base["attn_norm"]], "mlp_norm": [dev(g) for g in base["mlp_norm"]],
@@ -58,6 +58,8 @@ def _make(cfg, base, ad, max_tokens, lm=None):
                     rms_eps=cfg.rms_eps)
     if lm is not None:
         t.tf_set_lm_backward(h, lm)
+    if attn:
+        t.tf_set_attention_backward(h, attn)
     return h
 
 
@@ -149,11 +151,11 @@ def test_forward_matches_oracle(small):
     assert np.isfinite(lp).all() and err <= LP_TOL, err
 
 
-def _step_and_adam(prob, kind, lm=None):
+def _step_and_adam(prob, kind, lm=None, attn=0):
     import rl_step_gb300.transformer as t
     cfg, base, ad, b, lp0 = prob
     s = lp0 + b["sampler_noise"]
-    h = _make(cfg, base, ad, len(b["tokens"]), lm)
+    h = _make(cfg, base, ad, len(b["tokens"]), lm, attn)
     o = _oracle(cfg, base, ad)
     lp, loss = _gpu_step(h, b, kind, s)
     ref = _oracle_step(o, b, kind, s)
@@ -211,6 +213,48 @@ def test_sharp_attention_step_matches_oracle(sharp, kind):
     _step_and_adam(sharp, kind)
 
 
+# The stored-dS attention backward: the key side stores every dS block and the
+# query side forms dQ = dS K from them.  tf_small's sequences are at most 300
+# tokens long (a query tile then sees at most four key tiles).
+SEQ_HI_SMALL = 300
+
+
+@pytest.mark.parametrize("prob", ["small", "sharp"])
+@pytest.mark.parametrize("kind", ["ppo", "cross_entropy", "custom"])
+def test_stored_ds_step_matches_oracle(request, prob, kind):
+    _step_and_adam(request.getfixturevalue(prob), kind, attn=SEQ_HI_SMALL)
+
+
+def test_attention_backward_modes_agree_and_bound_positions(small):
+    """Both attention backward modes give the same logprobs and losses bit for
+    bit (the forward is shared) and gradients equal to rounding (dQ is summed in
+    another order); the stored mode holds max_tiles x ktc x n_heads blocks of
+    32 KB more, and a position past its sequence bound is a range error."""
+    import rl_step_gb300.transformer as t
+    cfg, base, ad, b, _ = small
+    N = len(b["tokens"])
+    res = {}
+    for attn in (0, SEQ_HI_SMALL):
+        h = _make(cfg, base, ad, N, attn=attn)
+        lp, loss = t.tf_forward_backward(h, *_dargs(b), "cross_entropy", weights=dev(b["weights"]))
+        assert t.tf_check_status(h) == 0
+        g = {(a, l, p, fac): t.tf_read_adapter(h, a, l, p, fac, "grad").cpu().numpy()
+             for a in range(cfg.n_adapters) for l in range(cfg.n_layers) for p in t.PROJ for fac in ("A", "B")}
+        res[attn] = (lp.cpu().numpy(), loss.cpu().numpy(), g, h.device_bytes)
+        if attn:
+            long_seq = _layout(cfg, [SEQ_HI_SMALL + 5, 3], [0, 1], 11)
+            t.tf_forward_backward(h, *_dargs(long_seq), "cross_entropy", weights=dev(long_seq["weights"]))
+            assert t.tf_check_status(h) == -2
+            assert t.tf_check_status(h) == 0
+        del h
+    (lp_r, loss_r, g_r, by_r), (lp_s, loss_s, g_s, by_s) = res[0], res[SEQ_HI_SMALL]
+    assert np.array_equal(lp_r, lp_s) and np.array_equal(loss_r, loss_s)
+    assert max(rel_fro(g_s[k], g_r[k]) for k in g_r) <= 1e-2
+    max_tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
+    ktc = -(-(SEQ_HI_SMALL - 1) // 128) + 1
+    assert by_s - by_r == max_tiles * ktc * cfg.n_heads * 128 * 128 * 2
+
+
 def test_sharp_attention_forward_matches_oracle(sharp):
     import rl_step_gb300.transformer as t
     cfg, base, ad, b, lp0 = sharp
@@ -248,11 +292,12 @@ def _layout(cfg, lens, ads, seed):
     ([1], [2]),                                                # a single token
     ([129, 127, 1, 255, 2, 130], [0, 0, 0, 2, 2, 1]),          # ragged tiles, several per tile
 ])
-def test_edge_layouts_match_oracle(small, lens, ads):
+@pytest.mark.parametrize("attn", [0, SEQ_HI_SMALL])
+def test_edge_layouts_match_oracle(small, lens, ads, attn):
     import rl_step_gb300.transformer as t
     cfg, base, ad, _, _ = small
     b = _layout(cfg, lens, ads, sum(lens))
-    h = _make(cfg, base, ad, 1024)
+    h = _make(cfg, base, ad, 1024, attn=attn)
     o = _oracle(cfg, base, ad)
     lp, _ = _gpu_step(h, b, "cross_entropy", None)
     ref = _oracle_step(o, b, "cross_entropy", None)

@@ -48,8 +48,10 @@ def _lib():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("lm", ["keep_logits", "recompute"])
-def test_full_size_prefix_parity_and_gradient_isolation(lm):
+@pytest.mark.parametrize("lm,attn", [("keep_logits", 0), ("recompute", 0), ("keep_logits", 2048)])
+def test_full_size_prefix_parity_and_gradient_isolation(lm, attn):
+    """attn = 2048: the benchmark's attention backward, dS blocks stored for
+    sequences of up to 2,048 tokens (the workload's longest)."""
     import rl_step_gb300.transformer as t
     cfg = wt.get_tf_config("qwen3_8b_tf_ppo")
     base = wt.make_tf_base_weights(cfg)
@@ -63,7 +65,7 @@ def test_full_size_prefix_parity_and_gradient_isolation(lm):
     w[rows] = 1.0
     assert (b["positions"][rows] == np.tile(np.arange(PREFIX), len(chosen))).all()
 
-    h = _make(cfg, base, ad, N, lm)
+    h = _make(cfg, base, ad, N, lm, attn)
     args = [dev(b[k]) for k in ("tokens", "targets", "positions", "adapter_ids")]
     lp, _ = t.tf_forward_backward(h, *args, "cross_entropy", weights=dev(w))
     assert t.tf_check_status(h) == 0
