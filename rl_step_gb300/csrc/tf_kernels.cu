@@ -110,9 +110,67 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const float* __restric
     }
 }
 
+// One-pass forms for d <= 512 NV: one block of 128 threads per row, thread t
+// holding the row's float4 chunks t + 128 i (i < NV) in registers, so each
+// input row is read from memory once.  (With one warp per row the second
+// loop's re-read of x misses L2 whenever the rows in flight, ~16 KB each,
+// outgrow it.)  The row's sum of squares: per-thread partials in chunk
+// order, a warp tree, then the four warps' sums in warp order.
+constexpr int NORM_THREADS = 128;
+
+__device__ __forceinline__ float block128_sum(float v, float* part) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_row_kernel(const float* __restrict__ x,
+                                                                       const bf16* __restrict__ g, int d, float eps,
+                                                                       const int* __restrict__ meta,
+                                                                       bf16* __restrict__ y, float* __restrict__ rstd,
+                                                                       float* __restrict__ snap) {
+    __shared__ float part[NORM_THREADS / 32];
+    const int64_t p = blockIdx.x;
+    if (p >= (int64_t)meta[0] * TILE_M) return;
+    const int n4 = d >> 2;
+    const float4* xr = reinterpret_cast<const float4*>(x + p * d);
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = threadIdx.x + NORM_THREADS * i;
+        if (c < n4) {
+            v[i] = xr[c];
+            ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        }
+    }
+    const float r = rsqrtf(block128_sum(ss, part) / (float)d + eps);
+    if (threadIdx.x == 0) rstd[p] = r;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = threadIdx.x + NORM_THREADS * i;
+        if (c < n4) {
+            if (snap) reinterpret_cast<float4*>(snap + p * d)[c] = v[i];
+            float gv[4];
+            load4_bf16(g + 4 * c, gv);
+            uint2 w;
+            w.x = pack_bf16x2(v[i].x * r * gv[0], v[i].y * r * gv[1]);
+            w.y = pack_bf16x2(v[i].z * r * gv[2], v[i].w * r * gv[3]);
+            reinterpret_cast<uint2*>(y + p * d)[c] = w;
+        }
+    }
+}
+
 void launch_rmsnorm_fwd(const float* x, const bf16* g, int d, float eps, const int* meta, int max_rows, bf16* y,
                         float* rstd, float* snap, cudaStream_t s) {
-    rmsnorm_fwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+    if (d <= 512 * 8)
+        rmsnorm_fwd_row_kernel<8><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+    else if (d <= 512 * 16)
+        rmsnorm_fwd_row_kernel<16><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+    else
+        rmsnorm_fwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
 }
 
 // dx = rstd (g dy) - x rstd^3 mean(x g dy);  dh (+)= dx;  dhb = bf16(dh).
@@ -155,9 +213,67 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
     }
 }
 
+// One-pass backward (d <= 512 NV): dy and x of the row held in registers.
+template <int NV>
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_row_kernel(const float* __restrict__ dy,
+                                                                       const float* __restrict__ x,
+                                                                       const bf16* __restrict__ g,
+                                                                       const float* __restrict__ rstd, int d,
+                                                                       const int* __restrict__ meta, int accumulate,
+                                                                       float* __restrict__ dh, bf16* __restrict__ dhb) {
+    __shared__ float part[NORM_THREADS / 32];
+    const int64_t p = blockIdx.x;
+    if (p >= (int64_t)meta[0] * TILE_M) return;
+    const int n4 = d >> 2;
+    const float4* dyr = reinterpret_cast<const float4*>(dy + p * d);
+    const float4* xr = reinterpret_cast<const float4*>(x + p * d);
+    float4 a[NV], b[NV];
+    float c = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int k = threadIdx.x + NORM_THREADS * i;
+        if (k < n4) {
+            a[i] = dyr[k];
+            b[i] = xr[k];
+            float gv[4];
+            load4_bf16(g + 4 * k, gv);
+            c += a[i].x * gv[0] * b[i].x + a[i].y * gv[1] * b[i].y + a[i].z * gv[2] * b[i].z +
+                 a[i].w * gv[3] * b[i].w;
+        }
+    }
+    c = block128_sum(c, part) / (float)d;
+    const float r = rstd[p];
+    const float r3c = r * r * r * c;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int k = threadIdx.x + NORM_THREADS * i;
+        if (k < n4) {
+            float gv[4];
+            load4_bf16(g + 4 * k, gv);
+            float4 o = make_float4(r * gv[0] * a[i].x - b[i].x * r3c, r * gv[1] * a[i].y - b[i].y * r3c,
+                                   r * gv[2] * a[i].z - b[i].z * r3c, r * gv[3] * a[i].w - b[i].w * r3c);
+            float4* hp = reinterpret_cast<float4*>(dh + p * d) + k;
+            if (accumulate) {
+                const float4 h = *hp;
+                o.x += h.x; o.y += h.y; o.z += h.z; o.w += h.w;
+            }
+            *hp = o;
+            uint2 w;
+            w.x = pack_bf16x2(o.x, o.y);
+            w.y = pack_bf16x2(o.z, o.w);
+            reinterpret_cast<uint2*>(dhb + p * d)[k] = w;
+        }
+    }
+}
+
 void launch_rmsnorm_bwd(const float* dy, const float* x, const bf16* g, const float* rstd, int d, const int* meta,
                         int max_rows, int accumulate, float* dh, bf16* dhb, cudaStream_t s) {
-    rmsnorm_bwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(dy, x, g, rstd, d, meta, accumulate, dh, dhb);
+    if (d <= 512 * 8)
+        rmsnorm_bwd_row_kernel<8><<<max_rows, NORM_THREADS, 0, s>>>(dy, x, g, rstd, d, meta, accumulate, dh, dhb);
+    else if (d <= 512 * 16)
+        rmsnorm_bwd_row_kernel<16><<<max_rows, NORM_THREADS, 0, s>>>(dy, x, g, rstd, d, meta, accumulate, dh, dhb);
+    else
+        rmsnorm_bwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(dy, x, g, rstd, d, meta, accumulate, dh, dhb);
 }
 
 // ----------------------------------------------------------------------------
