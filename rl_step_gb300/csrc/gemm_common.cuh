@@ -26,7 +26,7 @@ struct GemmOperand {
 
 enum EpiKind : int {
     EPI_SILU = 0,     // out0 = u = acc ; out1 = silu(acc)                     (T)
-    EPI_RESID = 1,    // f32 += acc ; out0 = T(f32)                             (residual h / dh)
+    EPI_RESID = 1,    // f32 = (f32_in or f32) + acc ; out0 = T(f32)            (residual h / dh)
     EPI_STORE2 = 2,   // f32 = acc ; out0 = T(acc)                              (dh of the LM head)
     EPI_DSILU = 3,    // out0 = T(acc * silu'(aux))                             (du)
     EPI_SHRINK = 4,   // out0 = T(gamma[a] * acc)                               (LoRA shrink)
@@ -57,6 +57,7 @@ struct EpiParams {
     int64_t ld0 = 0, ld1 = 0;
     float* f32 = nullptr;
     int64_t ldf = 0;
+    const float* f32_in = nullptr;  // EPI_RESID: the residual read, pitch ldf (null: f32 itself)
     const void* aux = nullptr;
     int64_t ld_aux = 0;
     const float* gamma = nullptr;   // per adapter
@@ -333,7 +334,7 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     case EPI_RESID: {
         float* hp = ep.f32 + row * ep.ldf + col0;
         float h[32];
-        load32<float>(hp, h);
+        load32<float>(ep.f32_in ? ep.f32_in + row * ep.ldf + col0 : hp, h);
 #pragma unroll
         for (int j = 0; j < 32; ++j) h[j] += acc[j];
         store32<float>(hp, h);

@@ -193,7 +193,7 @@ __device__ __forceinline__ void epilogue_row_merge(const GemmParams& p, uint32_t
 //   SK_LMDZ   recomputed bf16 dz (box 0 -> map C)
 //   SK_SILU   u = acc (box 0 -> map C) and act = silu(acc) (box 1 -> map D)
 //   SK_DSILU  du = acc * silu'(u), u read directly (box 0 -> map C)
-//   SK_RESID  h32 += acc (box F -> map D), its bf16 copy (box 0 -> map C)
+//   SK_RESID  h32 = (f32_in or h32) + acc (box F -> map D), its bf16 copy (box 0 -> map C)
 // Boxes: fp32 32 x 32 with 128-byte rows and 128-byte swizzle (16-byte piece
 // j of row r at piece j ^ (r & 7)); bf16 (or fp16) 32 x 32 with 64-byte rows
 // and 64-byte swizzle (piece j at j ^ ((r >> 1) & 3)).  Both match the tensor
@@ -274,7 +274,7 @@ __device__ __forceinline__ void staged_chunk(const GemmParams& p, const CUtensor
         for (int j = 0; j < 32; ++j) v[j] = u[j];
     } else if (SK == SK_RESID) {
         float h[32];
-        load32<float>(ep.f32 + row * ep.ldf + col0, h);
+        load32<float>((ep.f32_in ? ep.f32_in : ep.f32) + row * ep.ldf + col0, h);
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] += h[j];
     }

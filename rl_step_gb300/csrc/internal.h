@@ -97,7 +97,7 @@ void launch_tf_rows(const int* perm_pad, const int* meta, const int* tile_ad, co
                     const int* positions, const int* adapter_ids, int max_pos, int max_rows, int* pos_pad,
                     int* seq_start, int* status, cudaStream_t s);
 void launch_rmsnorm_fwd(const float* x, const bf16* g, int d, float eps, const int* meta, int max_rows, bf16* y,
-                        float* rstd, float* snap, cudaStream_t s);
+                        float* rstd, cudaStream_t s);
 void launch_rmsnorm_bwd(const float* dy, const float* x, const bf16* g, const float* rstd, int d, const int* meta,
                         int max_rows, int accumulate, float* dh, bf16* dhb, cudaStream_t s);
 void launch_rope(bf16* buf, int64_t ld, int col0, int n_heads, const int* pos_pad, const float2* cs,

@@ -659,9 +659,9 @@ int proj_grads(mlora_tf_t* h, int g, int proj, int l, int mp, const bf16* dy, co
     return tf_grad(h, mp, in, opnd(x, MP, in, in, 1), opnd(h->wbuf + RP * sub, MP, RP, kx, 1), l, proj, 0, 1, 0, 0, s);
 }
 
-int tf_norm_fwd(mlora_tf_t* h, const bf16* gain, bf16* y, float* rstd, float* snap, int mp, cudaStream_t s) {
+int tf_norm_fwd(mlora_tf_t* h, const float* x, const bf16* gain, bf16* y, float* rstd, int mp, cudaStream_t s) {
     TfProf ps(h, s, MLORA_TF_PROF_NORM);
-    launch_rmsnorm_fwd(h->h32, gain, h->d, h->eps, h->rb.meta, mp, y, rstd, snap, s);
+    launch_rmsnorm_fwd(x, gain, h->d, h->eps, h->rb.meta, mp, y, rstd, s);
     ++h->launches;
     return MLORA_OK;
 }
@@ -717,15 +717,25 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
                        s);
         ++h->launches;
     }
+    // The fp32 residual stream.  With a backward to follow, every value that
+    // feeds an RMSNorm is kept: the residual GEMMs read one version and write
+    // the next (embedding -> snap1[0] -> snap2[0] -> snap1[1] ... -> snapf),
+    // so the norms' backward finds its inputs without a copy; a forward alone
+    // updates h32 in place.
+    float* cur = backward ? h->snap1[0] : h->h32;
+    auto resid_to = [&](float* next, GemmParams& p) {
+        p.ep.kind = EPI_RESID; p.ep.f32 = next; p.ep.f32_in = cur; p.ep.ldf = d;
+        cur = next;
+    };
     {
         TfProf ps(h, s, MLORA_TF_PROF_EMBED);
-        launch_embed<bf16>(h->rb.perm_pad, h->rb.meta, mp, b->tokens, b->targets, h->E, V, d, h->embed_bf, h->h32,
+        launch_embed<bf16>(h->rb.perm_pad, h->rb.meta, mp, b->tokens, b->targets, h->E, V, d, h->embed_bf, cur,
                            h->tgt_pad, h->status, s);
         ++h->launches;
     }
     for (int l = 0; l < L; ++l) {
         // attention sub-block
-        if ((rc = tf_norm_fwd(h, h->gattn[l], h->x1[l], h->rstd1[l], backward ? h->snap1[l] : nullptr, mp, s))) return rc;
+        if ((rc = tf_norm_fwd(h, cur, h->gattn[l], h->x1[l], h->rstd1[l], mp, s))) return rc;
         if ((rc = shrink_fwd(h, G_QKV, l, h->x1[l], h->vqkv[l], mt_upper, s))) return rc;
         {
             GemmParams p = proj_fwd(h, G_QKV, l, h->x1[l], h->vqkv[l], mt_upper);
@@ -746,11 +756,11 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         if ((rc = shrink_fwd(h, G_O, l, h->o[l], h->vo[l], mt_upper, s))) return rc;
         {
             GemmParams p = proj_fwd(h, G_O, l, h->o[l], h->vo[l], mt_upper);
-            p.ep.kind = EPI_RESID; p.ep.f32 = h->h32; p.ep.ldf = d;
+            resid_to(backward ? h->snap2[l] : cur, p);
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_O))) return rc;
         }
         // MLP sub-block
-        if ((rc = tf_norm_fwd(h, h->gmlp[l], h->x2[l], h->rstd2[l], backward ? h->snap2[l] : nullptr, mp, s))) return rc;
+        if ((rc = tf_norm_fwd(h, cur, h->gmlp[l], h->x2[l], h->rstd2[l], mp, s))) return rc;
         if ((rc = shrink_fwd(h, G_GU, l, h->x2[l], h->vgu[l], mt_upper, s))) return rc;
         {
             GemmParams p = proj_fwd(h, G_GU, l, h->x2[l], h->vgu[l], mt_upper);
@@ -760,11 +770,11 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
         if ((rc = shrink_fwd(h, G_D, l, h->act[l], h->vd[l], mt_upper, s))) return rc;
         {
             GemmParams p = proj_fwd(h, G_D, l, h->act[l], h->vd[l], mt_upper);
-            p.ep.kind = EPI_RESID; p.ep.f32 = h->h32; p.ep.ldf = d;
+            resid_to(!backward ? cur : (l + 1 < L ? h->snap1[l + 1] : h->snapf), p);
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_DOWN))) return rc;
         }
     }
-    if ((rc = tf_norm_fwd(h, h->gfinal, h->xf, h->rstdf, backward ? h->snapf : nullptr, mp, s))) return rc;
+    if ((rc = tf_norm_fwd(h, cur, h->gfinal, h->xf, h->rstdf, mp, s))) return rc;
 
     // LM head (Tinker API Implementation on TPUs, section 10.3-10.4): per-tile
     // log-sum-exp partials and the target logit over all rows; the backward

@@ -54,8 +54,7 @@ void launch_tf_rows(const int* perm_pad, const int* meta, const int* tile_ad, co
 
 // ----------------------------------------------------------------------------
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one warp per row (d % 128 == 0).
-// Writes y (bf16), 1/rms per row, and optionally a copy of x (the backward's
-// input).  Rows past the valid tiles are skipped.
+// Writes y (bf16) and 1/rms per row.  Rows past the valid tiles are skipped.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -83,8 +82,7 @@ __device__ __forceinline__ void load8_bf16(const bf16* p, float (&v)[8]) {
 
 __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const float* __restrict__ x, const bf16* __restrict__ g,
                                                           int d, float eps, const int* __restrict__ meta,
-                                                          bf16* __restrict__ y, float* __restrict__ rstd,
-                                                          float* __restrict__ snap) {
+                                                          bf16* __restrict__ y, float* __restrict__ rstd) {
     const int rows = meta[0] * TILE_M;
     const int lane = threadIdx.x & 31;
     const int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -94,7 +92,6 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const float* __restric
     for (int c = lane * 4; c < d; c += 128) {
         const float4 v = *reinterpret_cast<const float4*>(xr + c);
         ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        if (snap) *reinterpret_cast<float4*>(snap + p * d + c) = v;
     }
     ss = warp_sum(ss);
     const float r = rsqrtf(ss / (float)d + eps);
@@ -129,8 +126,7 @@ template <int NV>
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_row_kernel(const float* __restrict__ x,
                                                                        const bf16* __restrict__ g, int d, float eps,
                                                                        const int* __restrict__ meta,
-                                                                       bf16* __restrict__ y, float* __restrict__ rstd,
-                                                                       float* __restrict__ snap) {
+                                                                       bf16* __restrict__ y, float* __restrict__ rstd) {
     __shared__ float part[NORM_THREADS / 32];
     const int64_t p = blockIdx.x;
     if (p >= (int64_t)meta[0] * TILE_M) return;
@@ -152,7 +148,6 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_row_kernel(const flo
     for (int i = 0; i < NV; ++i) {
         const int c = threadIdx.x + NORM_THREADS * i;
         if (c < n4) {
-            if (snap) reinterpret_cast<float4*>(snap + p * d)[c] = v[i];
             float gv[4];
             load4_bf16(g + 4 * c, gv);
             uint2 w;
@@ -164,13 +159,13 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_row_kernel(const flo
 }
 
 void launch_rmsnorm_fwd(const float* x, const bf16* g, int d, float eps, const int* meta, int max_rows, bf16* y,
-                        float* rstd, float* snap, cudaStream_t s) {
+                        float* rstd, cudaStream_t s) {
     if (d <= 512 * 8)
-        rmsnorm_fwd_row_kernel<8><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+        rmsnorm_fwd_row_kernel<8><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd);
     else if (d <= 512 * 16)
-        rmsnorm_fwd_row_kernel<16><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+        rmsnorm_fwd_row_kernel<16><<<max_rows, NORM_THREADS, 0, s>>>(x, g, d, eps, meta, y, rstd);
     else
-        rmsnorm_fwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(x, g, d, eps, meta, y, rstd, snap);
+        rmsnorm_fwd_kernel<<<(max_rows + 7) / 8, 256, 0, s>>>(x, g, d, eps, meta, y, rstd);
 }
 
 // dx = rstd (g dy) - x rstd^3 mean(x g dy);  dh (+)= dx;  dhb = bf16(dh).
