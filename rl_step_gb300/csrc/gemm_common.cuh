@@ -86,6 +86,10 @@ struct EpiParams {
     int grad_ilv = 0;               // > 0: rows interleave two tensors in blocks of grad_ilv;
     int grad_sub = 0;               //      only rows of block parity grad_sub are accumulated,
                                     //      at row (row / (2 ilv)) ilv + row % ilv
+    int grad_sub_stride = 0;        // > 0: several tensors side by side in N, RP columns each;
+                                    //      column block s is tensor s, whose per-adapter offsets
+                                    //      are grad_off + s grad_sub_stride; with grad_ilv, the
+                                    //      rows of block parity s go to tensor s (the rest skipped)
     int* nonfinite = nullptr;       // per adapter flag
     const int* row_slot = nullptr;  // sampler: adapter slot per row (-1: none)
 };
@@ -421,9 +425,14 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int64_t row, int 
     } break;
     case EPI_GRAD: {
         int r = ep.ranks[adapter];
-        float* base = ep.grad + ep.grad_off[adapter];
+        int sub = ep.grad_sub;
+        if (ep.grad_sub_stride) {       // column block -> tensor
+            sub = col0 / RP;
+            col0 -= sub * RP;
+        }
+        float* base = ep.grad + ep.grad_off[(int64_t)sub * ep.grad_sub_stride + adapter];
         if (ep.grad_ilv) {
-            if ((int)((row / ep.grad_ilv) & 1) != ep.grad_sub) break;
+            if ((int)((row / ep.grad_ilv) & 1) != sub) break;
             row = (row / (2 * ep.grad_ilv)) * ep.grad_ilv + row % ep.grad_ilv;
         }
         bool bad = false;

@@ -615,11 +615,14 @@ GemmParams proj_bwd(mlora_tf_t* h, int g, int l, const bf16* dy, int mt_upper) {
     return p;
 }
 
-// grad[a] (+)= X_seg^T Y_seg over each adapter's token chunks (fp32 atomics)
+// grad[a] (+)= X_seg^T Y_seg over each adapter's token chunks (fp32 atomics).
+// ncols > RP: Y holds the factors of consecutive projections proj, proj + 1, ..
+// side by side (RP columns each), and one pass over X feeds all of them.
 int tf_grad(mlora_tf_t* h, int mp, int Dout, GemmOperand X, GemmOperand Y, int l, int proj, int factor, int trans,
-            int ilv, int sub, cudaStream_t s) {
+            int ilv, int sub, cudaStream_t s, int ncols = RP) {
     GemmParams p;
-    p.M = Dout; p.N = RP; p.K = 0;
+    p.M = Dout; p.N = ncols; p.K = 0;
+    p.force_bn64 = ncols <= RP;   // several members: one 256-column tile reads each X block once
     p.grouped = 1;
     p.chunks = h->rb.chunks;
     p.nchunks_dev = h->rb.meta + 1;
@@ -635,28 +638,38 @@ int tf_grad(mlora_tf_t* h, int mp, int Dout, GemmOperand X, GemmOperand Y, int l
     p.ep.grad_M = Dout;
     p.ep.grad_ilv = ilv;
     p.ep.grad_sub = sub;
+    // the next projection's offsets: the same factor, one projection on
+    p.ep.grad_sub_stride = ncols > RP ? 2 * h->n_ad : 0;
     p.ep.nonfinite = h->nonfinite;
     return tf_gemm(h, p, s, MLORA_TF_PROF_GRAD);
 }
 
-// Gradients of projection `proj` (member `sub` of group g): dB += dy_sub^T v_sub
-// (v includes gamma), dA += w_sub^T x.  dy [rows x N_g], v / w [rows x kx].
-int proj_grads(mlora_tf_t* h, int g, int proj, int l, int mp, const bf16* dy, const bf16* v, const bf16* x,
-               cudaStream_t s) {
-    const int kx = GROUP_KX[g], N = h->gN[g], sub = SUB_OF[proj];
+// Gradients of group g's projections: dB_p += dy_p^T v_p (v includes gamma),
+// dA_p += w_p^T x.  dy [rows x N_g], v / w [rows x kx], the members' factors
+// side by side.  Every dA of a group reads the group's input x once (one
+// reduction over all members' w); gate and up also share one pass over the
+// interleaved d gate|up (rows of block parity s to member s); q, k and v
+// read their own column slices of dq|dk|dv.
+int group_grads(mlora_tf_t* h, int g, int l, int mp, const bf16* dy, const bf16* v, const bf16* x, cudaStream_t s) {
+    static constexpr int FIRST[NGROUPS] = {MLORA_TF_Q, MLORA_TF_O, MLORA_TF_GATE, MLORA_TF_DOWN};
+    const int kx = GROUP_KX[g], N = h->gN[g], in = h->gIn[g], first = FIRST[g];
     const int64_t MP = h->max_pad;
-    int out, in;
-    proj_shape(h, proj, &out, &in);
     int rc;
-    const GemmOperand vY = opnd(v + RP * sub, MP, RP, kx, 1);
-    if (g == G_GU) {   // rows of dy interleave gate and up
-        rc = tf_grad(h, mp, N, opnd(dy, MP, N, N, 1), vY, l, proj, 1, 0, GU_ILV, sub, s);
+    if (g == G_GU) {
+        rc = tf_grad(h, mp, N, opnd(dy, MP, N, N, 1), opnd(v, MP, kx, kx, 1), l, first, 1, 0, GU_ILV, 0, s, kx);
     } else {
-        const int off = (proj == MLORA_TF_K) ? h->Q : (proj == MLORA_TF_V ? h->Q + h->KV : 0);
-        rc = tf_grad(h, mp, out, opnd(dy + off, MP, out, N, 1), vY, l, proj, 1, 0, 0, 0, s);
+        rc = MLORA_OK;
+        for (int sub = 0; sub * RP < kx && rc == MLORA_OK; ++sub) {
+            const int proj = first + sub;
+            int out, in_p;
+            proj_shape(h, proj, &out, &in_p);
+            const int off = (proj == MLORA_TF_K) ? h->Q : (proj == MLORA_TF_V ? h->Q + h->KV : 0);
+            rc = tf_grad(h, mp, out, opnd(dy + off, MP, out, N, 1), opnd(v + RP * sub, MP, RP, kx, 1), l, proj, 1,
+                         0, 0, 0, s);
+        }
     }
     if (rc) return rc;
-    return tf_grad(h, mp, in, opnd(x, MP, in, in, 1), opnd(h->wbuf + RP * sub, MP, RP, kx, 1), l, proj, 0, 1, 0, 0, s);
+    return tf_grad(h, mp, in, opnd(x, MP, in, in, 1), opnd(h->wbuf, MP, kx, kx, 1), l, first, 0, 1, 0, 0, s, kx);
 }
 
 int tf_norm_fwd(mlora_tf_t* h, const float* x, const bf16* gain, bf16* y, float* rstd, int mp, cudaStream_t s) {
@@ -901,15 +914,14 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
             p.ep.kind = EPI_DSWIGLU; p.ep.aux = h->gu[l]; p.ep.ld_aux = 2 * f; p.ep.out0 = h->dgu; p.ep.ld0 = 2 * f;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_DOWN_BWD))) return rc;
         }
-        if ((rc = proj_grads(h, G_D, MLORA_TF_DOWN, l, mp, h->dhb, h->vd[l], h->act[l], s))) return rc;
+        if ((rc = group_grads(h, G_D, l, mp, h->dhb, h->vd[l], h->act[l], s))) return rc;
         if ((rc = shrink_bwd(h, G_GU, l, h->dgu, mt_upper, s))) return rc;
         {
             GemmParams p = proj_bwd(h, G_GU, l, h->dgu, mt_upper);
             p.ep.kind = EPI_F32; p.ep.f32 = h->dxn32; p.ep.ldf = d;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_GATEUP_BWD))) return rc;
         }
-        if ((rc = proj_grads(h, G_GU, MLORA_TF_GATE, l, mp, h->dgu, h->vgu[l], h->x2[l], s))) return rc;
-        if ((rc = proj_grads(h, G_GU, MLORA_TF_UP, l, mp, h->dgu, h->vgu[l], h->x2[l], s))) return rc;
+        if ((rc = group_grads(h, G_GU, l, mp, h->dgu, h->vgu[l], h->x2[l], s))) return rc;
         if ((rc = tf_norm_bwd(h, h->snap2[l], h->gmlp[l], h->rstd2[l], 1, mp, s))) return rc;
         // h_mid = h_in + P_o(attention(rope(P_q x), rope(P_k x), P_v x))
         if ((rc = shrink_bwd(h, G_O, l, h->dhb, mt_upper, s))) return rc;
@@ -918,7 +930,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
             p.ep.kind = EPI_STORE; p.ep.out0 = h->dO; p.ep.ld0 = h->Q;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_O_BWD))) return rc;
         }
-        if ((rc = proj_grads(h, G_O, MLORA_TF_O, l, mp, h->dhb, h->vo[l], h->o[l], s))) return rc;
+        if ((rc = group_grads(h, G_O, l, mp, h->dhb, h->vo[l], h->o[l], s))) return rc;
         {
             TfProf ps(h, s, MLORA_TF_PROF_ATTN_BWD);
             AttnArgs aa = attn_args(h, l, mp);
@@ -939,8 +951,7 @@ int tf_step(mlora_tf_t* h, const mlora_tf_batch* b, const LossArgs& la, float* l
             p.ep.kind = EPI_F32; p.ep.f32 = h->dxn32; p.ep.ldf = d;
             if ((rc = tf_gemm(h, p, s, MLORA_TF_PROF_QKV_BWD))) return rc;
         }
-        for (int pj = MLORA_TF_Q; pj <= MLORA_TF_V; ++pj)
-            if ((rc = proj_grads(h, G_QKV, pj, l, mp, h->dqkv, h->vqkv[l], h->x1[l], s))) return rc;
+        if ((rc = group_grads(h, G_QKV, l, mp, h->dqkv, h->vqkv[l], h->x1[l], s))) return rc;
         if ((rc = tf_norm_bwd(h, h->snap1[l], h->gattn[l], h->rstd1[l], 1, mp, s))) return rc;
     }
     return MLORA_OK;
