@@ -196,7 +196,7 @@ __device__ __forceinline__ void load_tile128(uint32_t dst, const CUtensorMap* ma
 // MMAs, 3-6 and 7-10 are the softmax warpgroups of the two heads (one query
 // row per thread; warp w reads TMEM lanes 32 (w % 4) ..).  Per key tile j and
 // head h:  S_h = Q_h K_j^T into TMEM; the warpgroup reads the score row into
-// registers, takes its max, and writes P_h = exp(S_h - m) in bf16 back into
+// registers (one tensor-memory read of its 128 columns), takes its max, and writes P_h = exp(S_h - m) in bf16 back into
 // the first 64 columns of S_h; O_h += P_h V_j reads P_h from TMEM.  The MMA
 // thread issues head h's P V and right after it head h's next S (over the
 // same columns: the tensor core runs one thread's MMAs in issue order), so
@@ -466,78 +466,61 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 // the whole tile takes the unmasked copy of the loops
                 const int lo = ss - key0, hi = i - key0;
                 const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= TB - 1);
-                // pass 1: the row max of the raw scores (the scale is positive, so
-                // scaling the max equals the max of the scaled scores), reading the
-                // row from TMEM 32 columns at a time, the next chunk in flight
-                float mx = -INFINITY;
-                {
-                    uint32_t ca[32], cb[32];
-                    auto chunk_max = [&](const uint32_t (&cur)[32], int c, auto masked) {
+                // the score row, read from TMEM once into registers
+                uint32_t s0[32], s1[32], s2[32], s3[32];
+                tmem_ld32(tS, s0);
+                tmem_ld32(tS + 32, s1);
+                tmem_ld32(tS + 64, s2);
+                tmem_ld32(tS + 96, s3);
+                tmem_ld_wait_regs(s0);
+                tmem_ld_wait_regs(s1);
+                tmem_ld_wait_regs(s2);
+                tmem_ld_wait_regs(s3);
+                float mx = -INFINITY, alpha = 1.f, rs = 0.f;
+                bool raise = false;
+                // the row max of the raw scores (the scale is positive, so scaling the
+                // max equals the max of the scaled scores)
+                auto chunk_max = [&](const uint32_t (&cur)[32], int c, auto masked) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int idx = 32 * c + e;
-                            const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                            mx = fmaxf(mx, v ? __uint_as_float(cur[e]) : -INFINITY);
-                        }
-                    };
-                    auto pass = [&](auto masked) {
-                        tmem_ld32(tS, ca);
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld32(tS + 32, cb);
-                        chunk_max(ca, 0, masked);
-                        tmem_ld_wait_regs(cb);
-                        tmem_ld32(tS + 64, ca);
-                        chunk_max(cb, 1, masked);
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld32(tS + 96, cb);
-                        chunk_max(ca, 2, masked);
-                        tmem_ld_wait_regs(cb);
-                        chunk_max(cb, 3, masked);
-                    };
-                    if (whole) pass(std::false_type{});
-                    else pass(std::true_type{});
-                }
-                mx *= sc;
-                const bool raise = mx > m_run + RESCALE_LOG2;
-                const float alpha = raise ? ex2_ftz(m_run - mx) : 1.f;
-                if (raise) m_run = mx;
-                // pass 2: P = exp2(scale s - m) in bf16, written over the first 64
-                // columns of S_h (bf16 pairs) after the chunk that held them is read
-                float rs = 0.f;
-                {
-                    uint32_t ca[32], cb[32];
-                    auto chunk_p = [&](const uint32_t (&cur)[32], int c, auto masked) {
-                        uint32_t w[16];
+                    for (int e = 0; e < 32; ++e) {
+                        const int idx = 32 * c + e;
+                        const bool v = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                        mx = fmaxf(mx, v ? __uint_as_float(cur[e]) : -INFINITY);
+                    }
+                };
+                // P = exp2(scale s - m) in bf16, written over the first 64 columns of
+                // S_h (bf16 pairs): the whole row is already in registers
+                auto chunk_p = [&](const uint32_t (&cur)[32], int c, auto masked) {
+                    uint32_t w[16];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int idx = 32 * c + e;
-                            const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
-                            const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
-                            // masked entries give exp2(-inf) = 0: no branch around the exponential
-                            const float p0 = ex2_ftz(v0 ? fmaf(__uint_as_float(cur[e]), sc, -m_run) : -INFINITY);
-                            const float p1 = ex2_ftz(v1 ? fmaf(__uint_as_float(cur[e + 1]), sc, -m_run) : -INFINITY);
-                            rs += p0 + p1;
-                            w[e >> 1] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16(tS + 16 * c, w);     // keys 32 c .. 32 c + 31
-                    };
-                    auto pass = [&](auto masked) {
-                        tmem_ld32(tS, ca);
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld32(tS + 32, cb);
-                        chunk_p(ca, 0, masked);        // writes columns 0-15: chunk 0, already read
-                        tmem_ld_wait_regs(cb);
-                        tmem_ld32(tS + 64, ca);
-                        chunk_p(cb, 1, masked);        // columns 16-31: chunk 0
-                        tmem_ld_wait_regs(ca);
-                        tmem_ld32(tS + 96, cb);
-                        chunk_p(ca, 2, masked);        // columns 32-47: chunk 1
-                        tmem_ld_wait_regs(cb);
-                        chunk_p(cb, 3, masked);        // columns 48-63: chunk 1
-                    };
-                    if (whole) pass(std::false_type{});
-                    else pass(std::true_type{});
-                }
+                    for (int e = 0; e < 32; e += 2) {
+                        const int idx = 32 * c + e;
+                        const bool v0 = !decltype(masked)::value || ((idx >= lo) & (idx <= hi));
+                        const bool v1 = !decltype(masked)::value || ((idx + 1 >= lo) & (idx + 1 <= hi));
+                        // masked entries give exp2(-inf) = 0: no branch around the exponential
+                        const float p0 = ex2_ftz(v0 ? fmaf(__uint_as_float(cur[e]), sc, -m_run) : -INFINITY);
+                        const float p1 = ex2_ftz(v1 ? fmaf(__uint_as_float(cur[e + 1]), sc, -m_run) : -INFINITY);
+                        rs += p0 + p1;
+                        w[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + 16 * c, w);     // keys 32 c .. 32 c + 31
+                };
+                auto row = [&](auto masked) {
+                    chunk_max(s0, 0, masked);
+                    chunk_max(s1, 1, masked);
+                    chunk_max(s2, 2, masked);
+                    chunk_max(s3, 3, masked);
+                    mx *= sc;
+                    raise = mx > m_run + RESCALE_LOG2;
+                    alpha = raise ? ex2_ftz(m_run - mx) : 1.f;
+                    if (raise) m_run = mx;
+                    chunk_p(s0, 0, masked);
+                    chunk_p(s1, 1, masked);
+                    chunk_p(s2, 2, masked);
+                    chunk_p(s3, 3, masked);
+                };
+                if (whole) row(std::false_type{});
+                else row(std::true_type{});
                 // a raised max rescales O_h before this tile's P V accumulates into it
                 if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
