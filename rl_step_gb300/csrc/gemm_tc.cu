@@ -455,11 +455,12 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int t) {
     return c;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int SUB = 1>
 struct SmemLayout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SUB_BYTES = A_BYTES + B_BYTES;         // one 64-wide K block: A rows, then B rows
+    static constexpr int STAGE_BYTES = SUB * SUB_BYTES;         // a stage holds up to SUB consecutive K blocks
     static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = TILES_BYTES;                 // full[S], empty[S], tfull[2], tempty[2], drain
     static constexpr int NBARS = 2 * STAGES + 5;
@@ -468,11 +469,13 @@ struct SmemLayout {
 };
 
 // MERGE selects the export-merge epilogue (a separate instantiation, so the
-// other GEMMs keep their register allocation).
-template <int BN, int STAGES, bool MERGE = false>
+// other GEMMs keep their register allocation).  SUB: K blocks per stage (the
+// main blocks and the extension's are grouped separately; a group's last
+// stage may hold fewer), so that each barrier hand-off moves SUB blocks.
+template <int BN, int STAGES, bool MERGE = false, int SUB = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, const GemmParams p, int* status) {
-    using SL = SmemLayout<BN, STAGES>;
+    using SL = SmemLayout<BN, STAGES, SUB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -532,29 +535,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int m0 = c.mt * BM;
                 const int n0 = c.nt * BN;
                 const int withhold = (blockIdx.x == 0 && t == 0) ? p.test_withhold_kb : -1;
-                for (int kb = 0; kb < c.nkb && ok; ++kb) {
+                for (int kb = 0; kb < c.nkb && ok; kb += SUB) {
+                    const int cnt = c.nkb - kb < SUB ? c.nkb - kb : SUB;
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (kb == withhold) {   // test hook: this stage is never filled
+                    if (withhold >= kb && withhold < kb + cnt) {   // test hook: this stage is never filled
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                         continue;
                     }
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    mbar_expect_tx(fb, SL::STAGE_BYTES);
-                    const int k = c.k0 + kb * BK;
-                    load_tile_a<BM>(sa, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), false);
-                    load_tile_b<BN>(sa + SL::A_BYTES, &maps.B, fb, p.B, n0, k, c.adapter, false);
+                    mbar_expect_tx(fb, cnt * SL::SUB_BYTES);
+                    for (int u = 0; u < cnt; ++u) {
+                        const int k = c.k0 + (kb + u) * BK;
+                        const uint32_t su = sa + u * SL::SUB_BYTES;
+                        load_tile_a<BM>(su, &maps.A, fb, p.A, m0, k, (int)(m0 + p.A.row_shift), false);
+                        load_tile_b<BN>(su + SL::A_BYTES, &maps.B, fb, p.B, n0, k, c.adapter, false);
+                    }
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                for (int kb = 0; kb < c.nkbx && ok; ++kb) {
+                for (int kb = 0; kb < c.nkbx && ok; kb += SUB) {
+                    const int cnt = c.nkbx - kb < SUB ? c.nkbx - kb : SUB;
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t fb = bar_full + 8 * stage;
                     const uint32_t sa = sbase + stage * SL::STAGE_BYTES;
-                    mbar_expect_tx(fb, SL::STAGE_BYTES);
-                    const int k = kb * BK;
-                    load_tile_a<BM>(sa, &maps.Ax, fb, p.Ax, m0, k, (int)(m0 + p.Ax.row_shift), false);
-                    load_tile_b<BN>(sa + SL::A_BYTES, &maps.Bx, fb, p.Bx, n0, k, c.adapter, false);
+                    mbar_expect_tx(fb, cnt * SL::SUB_BYTES);
+                    for (int u = 0; u < cnt; ++u) {
+                        const int k = (kb + u) * BK;
+                        const uint32_t su = sa + u * SL::SUB_BYTES;
+                        load_tile_a<BM>(su, &maps.Ax, fb, p.Ax, m0, k, (int)(m0 + p.Ax.row_shift), false);
+                        load_tile_b<BN>(su + SL::A_BYTES, &maps.Bx, fb, p.Bx, n0, k, c.adapter, false);
+                    }
                     issued[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -595,40 +606,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t ax_step = p.Ax.mn_major ? (2048 >> 4) : (32 >> 4);
             const uint32_t bx_step = p.Bx.mn_major ? (2048 >> 4) : (32 >> 4);
             constexpr uint32_t STAGE_STEP = SL::STAGE_BYTES >> 4;
+            constexpr uint32_t SUB_STEP = SL::SUB_BYTES >> 4;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileCoord c = tile_coord<BN>(p, t);
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < c.nkb; ++kb) {
+                for (int kb = 0; kb < c.nkb; kb += SUB) {
+                    const int cnt = c.nkb - kb < SUB ? c.nkb - kb : SUB;
                     if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
                         !mbar_wait(bar_full + 8 * stage, phase, abort_flag, full_limit)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP);
-                    const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP);
-                    umma_bf16(d_tmem, ad, bd, id_main, kb > 0 ? 1u : 0u);
+                    for (int u = 0; u < cnt; ++u) {
+                        const uint64_t ad = a0 + (uint64_t)(stage * STAGE_STEP + u * SUB_STEP);
+                        const uint64_t bd = b0 + (uint64_t)(stage * STAGE_STEP + u * SUB_STEP);
+                        umma_bf16(d_tmem, ad, bd, id_main, (kb + u) > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 1; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + kk * a_step, bd + kk * b_step, id_main, 1u);
+                        for (int kk = 1; kk < BK / 16; ++kk)
+                            umma_bf16(d_tmem, ad + kk * a_step, bd + kk * b_step, id_main, 1u);
+                    }
                     umma_commit(bar_empty + 8 * stage);     // frees the stage when the MMAs finish
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                for (int kb = 0; kb < c.nkbx && ok; ++kb) {
+                for (int kb = 0; kb < c.nkbx && ok; kb += SUB) {
+                    const int cnt = c.nkbx - kb < SUB ? c.nkbx - kb : SUB;
                     if (!mbar_try_wait(bar_full + 8 * stage, phase) &&
                         !mbar_wait(bar_full + 8 * stage, phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = ax0 + (uint64_t)(stage * STAGE_STEP);
-                    const uint64_t bd = bx0 + (uint64_t)(stage * STAGE_STEP);
-                    umma_bf16(d_tmem, ad, bd, id_ext, (c.nkb > 0 || kb > 0) ? 1u : 0u);
+                    for (int u = 0; u < cnt; ++u) {
+                        const uint64_t ad = ax0 + (uint64_t)(stage * STAGE_STEP + u * SUB_STEP);
+                        const uint64_t bd = bx0 + (uint64_t)(stage * STAGE_STEP + u * SUB_STEP);
+                        umma_bf16(d_tmem, ad, bd, id_ext, (c.nkb > 0 || kb + u > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 1; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + kk * ax_step, bd + kk * bx_step, id_ext, 1u);
+                        for (int kk = 1; kk < BK / 16; ++kk)
+                            umma_bf16(d_tmem, ad + kk * ax_step, bd + kk * bx_step, id_ext, 1u);
+                    }
                     umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -1291,9 +1309,9 @@ bool operand_ok(const GemmOperand& op) {
            op.cols > 0 && op.rows < (1LL << 31) && op.cols < (1LL << 31);
 }
 
-template <int BN, int STAGES, bool MERGE = false>
+template <int BN, int STAGES, bool MERGE = false, int SUB = 1>
 cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* status) {
-    using SL = SmemLayout<BN, STAGES>;
+    using SL = SmemLayout<BN, STAGES, SUB>;
     TcMaps maps;
     auto enc = [&](CUtensorMap* m, const GemmOperand& op, int rows_mn) -> bool {
         if (!operand_ok(op)) return false;
@@ -1309,7 +1327,7 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, MERGE>,
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, MERGE, SUB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SL::TOTAL);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1319,7 +1337,7 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s, int num_sms, int* sta
                               : (int64_t)p.mt_count * n_nt;
     if (upper <= 0) return cudaSuccess;
     int grid = (int)(upper < num_sms ? upper : num_sms);
-    tc_gemm_kernel<BN, STAGES, MERGE><<<grid, NUM_THREADS, SL::TOTAL, s>>>(maps, p, status);
+    tc_gemm_kernel<BN, STAGES, MERGE, SUB><<<grid, NUM_THREADS, SL::TOTAL, s>>>(maps, p, status);
     return cudaGetLastError();
 }
 
@@ -1499,7 +1517,8 @@ cudaError_t launch_tc_gemm(const GemmParams& p, cudaStream_t s, int num_sms, int
         }
         return launch_bn<256, 4, true>(p, s, num_sms, status);
     }
-    if (p.N <= 64 || p.force_bn64) return launch_bn<64, 8>(p, s, num_sms, status);
+    // 128 x 64 tiles: two K blocks per stage, four stages
+    if (p.N <= 64 || p.force_bn64) return launch_bn<64, 4, false, 2>(p, s, num_sms, status);
     // a very long contraction (the LM head's dh, K = the vocabulary): 256 x 512
     // tiles, so the 76 clusters' tiles in flight read the A band about half as
     // often; one accumulator, whose unhidden epilogue is ~1 % of a tile here.
