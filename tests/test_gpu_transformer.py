@@ -246,6 +246,15 @@ def test_attention_backward_modes_agree_and_bound_positions(small):
             t.tf_forward_backward(h, *_dargs(long_seq), "cross_entropy", weights=dev(long_seq["weights"]))
             assert t.tf_check_status(h) == -2
             assert t.tf_check_status(h) == 0
+            stored_bytes = h.device_bytes
+            import rl_step_gb300 as m
+            with pytest.raises(m.MLoRAError):
+                t.tf_set_attention_backward(h, -1)
+            assert h.device_bytes == stored_bytes           # a rejected call changes nothing
+            t.tf_set_attention_backward(h, 0)               # back to recomputing: the blocks are freed
+            res["left"] = h.device_bytes
+            t.tf_forward_backward(h, *_dargs(long_seq), "cross_entropy", weights=dev(long_seq["weights"]))
+            assert t.tf_check_status(h) == 0                # positions are bounded by max_tokens again
         del h
     (lp_r, loss_r, g_r, by_r), (lp_s, loss_s, g_s, by_s) = res[0], res[SEQ_HI_SMALL]
     assert np.array_equal(lp_r, lp_s) and np.array_equal(loss_r, loss_s)
@@ -253,6 +262,7 @@ def test_attention_backward_modes_agree_and_bound_positions(small):
     max_tiles = -(-(N + 127 * min(N, cfg.n_adapters)) // 128)
     ktc = -(-(SEQ_HI_SMALL - 1) // 128) + 1
     assert by_s - by_r == max_tiles * ktc * cfg.n_heads * 128 * 128 * 2
+    assert res["left"] == by_r
 
 
 def test_sharp_attention_forward_matches_oracle(sharp):
